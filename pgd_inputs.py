@@ -1,0 +1,141 @@
+"""Seeded synthetic workloads for paged grouped-query decode attention.
+
+This module serves both the CUDA path and the oracle with the same inputs.
+It holds none of the method's arithmetic: it draws contexts, assigns pool
+pages to rows, and fills tensors with seeded random values.  Slot
+computation, the append, and attention itself live only in the two
+implementations under test.
+
+Workload shapes follow the model cards of the "Nest" zoo: Qwen2.5-0.5B
+(14 query / 2 kv heads, head_dim 64), gpt-oss-20b (64 / 8, head_dim 64,
+per-head sink logits, 128-position sliding window on alternating layers),
+Mistral-7B-v0.3 (32 / 8, head_dim 128).  Pages hold 64 positions.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+import torch
+
+PAGE_SIZE = 64
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    rows: int
+    q_heads: int
+    kv_heads: int
+    head_dim: int
+    ctx_lo: int          # row contexts (positions attended before the window) ~ U[ctx_lo, ctx_hi]
+    ctx_hi: int
+    window: int = 0      # <= 0: full causal attention
+    sinks: bool = False
+    pool_pages: int | None = None   # None: pages needed + 10 % slack
+    page_size: int = PAGE_SIZE
+
+    @property
+    def group(self) -> int:
+        return self.q_heads // self.kv_heads
+
+    @property
+    def max_pages_per_row(self) -> int:
+        return math.ceil(self.ctx_hi / self.page_size)
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+    def replace(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+
+# The five single-layer workloads; the first finishes in the oracle in
+# seconds, the last is the large serving batch (tens of GB of pool).
+WORKLOADS = {
+    "qwen_small": Workload("qwen_small", rows=4, q_heads=14, kv_heads=2, head_dim=64,
+                           ctx_lo=1, ctx_hi=300, pool_pages=32),
+    "qwen_serve": Workload("qwen_serve", rows=64, q_heads=14, kv_heads=2, head_dim=64,
+                           ctx_lo=129, ctx_hi=640),
+    "gptoss_full": Workload("gptoss_full", rows=64, q_heads=64, kv_heads=8, head_dim=64,
+                            ctx_lo=512, ctx_hi=4096, sinks=True),
+    "gptoss_sliding": Workload("gptoss_sliding", rows=128, q_heads=64, kv_heads=8,
+                               head_dim=64, ctx_lo=1, ctx_hi=32768, window=128, sinks=True),
+    "mistral_serve": Workload("mistral_serve", rows=256, q_heads=32, kv_heads=8,
+                              head_dim=128, ctx_lo=1024, ctx_hi=32768),
+}
+
+
+@dataclasses.dataclass
+class PageLayout:
+    contexts: np.ndarray     # int64 [R]; row b's new token sits at contexts[b] - 1
+    positions: np.ndarray    # int32 [R]
+    table: np.ndarray        # int32 [R, max_pages_per_row]; unused entries 0
+    num_pages: int
+    pages_used: int
+
+
+def draw_layout(wl: Workload, seed: int) -> PageLayout:
+    """Contexts ~ U[ctx_lo, ctx_hi]; each row gets ceil(context / page_size)
+    distinct pages taken in order from a random permutation of the pool, so
+    tables are shuffled and no two rows share a page."""
+    rng = np.random.default_rng(seed)
+    contexts = rng.integers(wl.ctx_lo, wl.ctx_hi + 1, size=wl.rows).astype(np.int64)
+    need = [math.ceil(int(c) / wl.page_size) for c in contexts]
+    used = int(sum(need))
+    num_pages = wl.pool_pages if wl.pool_pages is not None else max(1, math.ceil(used * 1.1))
+    if used > num_pages:
+        raise ValueError(f"{wl.name}: rows need {used} pages, pool holds {num_pages}")
+    order = rng.permutation(num_pages).astype(np.int32)
+    table = np.zeros((wl.rows, wl.max_pages_per_row), dtype=np.int32)
+    taken = 0
+    for b, k in enumerate(need):
+        table[b, :k] = order[taken:taken + k]
+        taken += k
+    positions = (contexts - 1).astype(np.int32)
+    return PageLayout(contexts, positions, table, num_pages, used)
+
+
+@dataclasses.dataclass
+class Batch:
+    wl: Workload
+    layout: PageLayout
+    q: torch.Tensor          # bf16 [R, Hq, D]
+    k_new: torch.Tensor      # bf16 [R, Hkv, D]
+    v_new: torch.Tensor      # bf16 [R, Hkv, D]
+    k_pool: torch.Tensor     # bf16, flat, num_pages * Hkv * page_size * D values
+    v_pool: torch.Tensor
+    sinks: torch.Tensor | None   # fp32 [Hq]
+    table: torch.Tensor      # int32 [R, max_pages]
+    positions: torch.Tensor  # int32 [R]
+
+
+def make_batch(wl: Workload, seed: int, device: str | torch.device = "cpu") -> Batch:
+    """q, k, v and pool contents ~ N(0, 1) in bf16, sinks ~ N(0, 1) in fp32,
+    all from one seeded torch generator on ``device``."""
+    layout = draw_layout(wl, seed)
+    device = torch.device(device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+
+    def normal(*shape, dtype=torch.bfloat16):
+        return torch.randn(*shape, generator=gen, device=device, dtype=dtype)
+
+    pool_len = layout.num_pages * wl.kv_heads * wl.page_size * wl.head_dim
+    q = normal(wl.rows, wl.q_heads, wl.head_dim)
+    k_new = normal(wl.rows, wl.kv_heads, wl.head_dim)
+    v_new = normal(wl.rows, wl.kv_heads, wl.head_dim)
+    k_pool = normal(pool_len)
+    v_pool = normal(pool_len)
+    sinks = normal(wl.q_heads, dtype=torch.float32) if wl.sinks else None
+    table = torch.from_numpy(layout.table).to(device)
+    positions = torch.from_numpy(layout.positions).to(device)
+    return Batch(wl, layout, q, k_new, v_new, k_pool, v_pool, sinks, table, positions)
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    """The uint16 bit patterns of a bf16 tensor, as a host numpy array."""
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+

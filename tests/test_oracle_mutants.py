@@ -1,0 +1,52 @@
+"""The oracle's pins must catch plausible mistakes.  Each case plants one
+mistake in a copy of the oracle's C source (on the CPU, in a temporary
+directory), builds it, and runs the pin suite against that build in a
+subprocess: the suite has to fail."""
+import os
+import subprocess
+import sys
+import tempfile
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "pgd_oracle.c")
+
+MUTANTS = {
+    "sink_scaled": ("double sink = job->sinks ? (double)job->sinks[h] : -INFINITY;",
+                    "double sink = job->sinks ? job->scale * (double)job->sinks[h] : -INFINITY;"),
+    "group_modulo": ("int g = h / group;", "int g = h % job->kv_heads;"),
+    "window_off_by_one": ("if (window > 0 && n - window + 1 > 0) lo = n - window + 1;",
+                          "if (window > 0 && n - window > 0) lo = n - window;"),
+    "sink_not_in_denominator": ("double z = (sink == -INFINITY) ? 0.0 : exp(sink - m);",
+                                "double z = 0.0;"),
+    "unscaled_scores": ("score[j] = scale * dot;", "score[j] = dot;"),
+    "max_without_sink": ("double m = m_real > sink ? m_real : sink;", "double m = m_real;"),
+    "slot_uses_quotient": ("slots[b] = (int64_t)page * page_size + n % page_size;",
+                           "slots[b] = (int64_t)page * page_size + n / page_size;"),
+    "gather_wrong_page_index": ("int64_t page_index = s / page_size;",
+                                "int64_t page_index = s % page_size;"),
+    "page_major_heads_swapped": (
+        "return ((page * kv_heads + kv_head) * page_size + in_page) * head_dim + d;",
+        "return ((kv_head * kv_heads + page) * page_size + in_page) * head_dim + d;"),
+    "value_from_key": ("const uint16_t* vj = v + (int64_t)(lo + j) * head_dim;",
+                       "const uint16_t* vj = k + (int64_t)(lo + j) * head_dim;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found once"
+    with tempfile.TemporaryDirectory() as tmp:
+        c = os.path.join(tmp, "mutant.c")
+        so = os.path.join(tmp, "libmutant.so")
+        open(c, "w").write(src.replace(old, new))
+        subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", so, c,
+                        "-lm"], check=True)
+        env = dict(os.environ, PGD_ORACLE_LIB=so)
+        run = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                              os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                             cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert run.returncode != 0, f"mutant {name} passed every pin:\n{run.stdout[-2000:]}"
