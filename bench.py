@@ -1,0 +1,461 @@
+"""Benchmark of the paged GQA decode step (KV append + split decode + combine).
+
+Default workload: the Mistral-7B-v0.3-shaped serving batch (256 rows, 32 query
+/ 8 kv heads, head_dim 128, contexts ~ U[1024, 32768], 64-position pages in
+one shuffled pool of ~18 GB per K and V), the largest of the five workloads.
+One step = one append of each row's new K/V at its page slot, then grouped
+decode attention of every row over its pages.  Inputs are resident in HBM and
+much larger than L2 (129 MB), so no flush is needed between steps; smaller
+workloads (--workload) are timed step by step with a 1 GiB L2 flush between
+steps, outside the timed spans.
+
+Prints one JSON line.  `value` is achieved HBM GB/s of the whole step over
+all ranks (algorithmic bytes: every attended K/V row read once, q read, out
+written, the append's read and write); `row_tokens_per_s` is rows decoded per
+second.  `--impl reference` times the fp64 CPU oracle on the host's cores on
+a bounded sample of the same workload instead.
+
+Multi-GPU: one process per GPU under torchrun; rows are independent, so each
+rank decodes its own batch (weak scaling) and no collective touches the data
+path; the ranks only meet at the barriers around the timed region.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from pgd_inputs import WORKLOADS, Workload, bf16_bits, make_batch  # noqa: E402
+
+METRIC = "paged decode attention: achieved HBM GB/s (% of GB300 peak); row-tokens/s"
+DEFAULT_WORKLOAD = "mistral_serve"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2 ** 20
+
+
+# --------------------------------------------------------------------------- bytes
+
+
+def algorithmic_bytes(wl: Workload, positions: np.ndarray) -> dict:
+    """Bytes one step must move at least once.  K/V: every attended (position,
+    kv head) row of K and of V, read once.  q read and out written once.  The
+    append reads k_new and v_new and writes them into the pool.  Sinks, the
+    table and positions are negligible and not counted.  Attended positions
+    per active row: min(window, n + 1) with a window, n + 1 without."""
+    n = positions.astype(np.int64)
+    active = n >= 0
+    attended = np.where(active, n + 1, 0)
+    if wl.window > 0:
+        attended = np.minimum(attended, wl.window)
+    row_bytes = 2 * wl.kv_heads * wl.head_dim * 2
+    kv = int(attended.sum()) * row_bytes
+    q_out = 2 * len(n) * wl.q_heads * wl.head_dim * 2
+    append = 2 * int(active.sum()) * row_bytes
+    return {"kv": kv, "q_out": q_out, "decode": kv + q_out, "append": append,
+            "step": kv + q_out + append}
+
+
+def describe(wl: Workload) -> str:
+    win = f"window {wl.window}" if wl.window > 0 else "full window"
+    sink = "fp32 sinks" if wl.sinks else "no sink"
+    return (f"{wl.name}: {wl.rows} rows, {wl.q_heads}q/{wl.kv_heads}kv, d{wl.head_dim}, "
+            f"ctx U[{wl.ctx_lo},{wl.ctx_hi}], page {wl.page_size}, {sink}, {win}")
+
+
+# --------------------------------------------------------------------------- env
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    if world == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, world: int, device) -> float:
+    if world == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+def measured_peak() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples; only those taken inside
+    the timed region (by their timestamps) are summarised."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device: torch.device):
+        try:
+            self.gpu = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+        except Exception:
+            self.gpu = str(device.index)
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+            except (ValueError, IndexError):
+                continue
+        inside = [r for r in rows if self.t0 is not None and self.t0 <= r[0] <= self.t1 + 0.1]
+        use = inside or rows
+        if not use:
+            return None
+        reasons = sorted({n for r in use for n, f in zip(self.NAMES, r[3]) if f.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in use),
+                "sm_max_mhz": max(r[2] for r in use), "reasons": reasons,
+                "samples": len(use), "in_timed_region": bool(inside)}
+
+
+def kernel_traffic(source_digest: str, workload: str):
+    """DRAM bytes per decode call (split + combine) from the committed ncu
+    summary, if it was taken on the current kernel sources and this
+    workload; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_digest") != source_digest or rec.get("workload") != workload:
+        return None
+    return rec.get("decode_bytes_per_launch")
+
+
+def source_digest() -> str:
+    csrc = os.path.join(ROOT, "paged_gqa_decode_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+# --------------------------------------------------------------------------- oracle timing
+
+
+def oracle_rows_timing(batch, rows, window, nthreads=None) -> float:
+    """Seconds the oracle takes for append + decode of `rows` of the batch."""
+    from tests.oracle_side import oracle_step, snapshot_rows
+    host = snapshot_rows(batch, rows)
+    t0 = time.perf_counter()
+    oracle_step(batch, host, window=window, sinks=batch.sinks, scale=batch.wl.scale,
+                nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(batch, target_s: float = 12.0) -> dict:
+    import oracle
+    wl = batch.wl
+    pos = batch.layout.positions
+    order = np.random.default_rng(0).permutation(wl.rows)
+    count = min(4, wl.rows)
+    elapsed = oracle_rows_timing(batch, order[:count], wl.window)
+    if elapsed < target_s and count < wl.rows:
+        count = int(min(wl.rows, max(count + 1, count * target_s / max(elapsed, 1e-3))))
+        elapsed = oracle_rows_timing(batch, order[:count], wl.window)
+    rows = order[:count]
+    by = algorithmic_bytes(wl, pos[rows])
+    return {"value": by["step"] / elapsed / 1e9, "unit": "GB/s", "cores": oracle.default_threads(),
+            "kind": "oracle",
+            "row_tokens_per_s": count / elapsed,
+            "sample": f"{count} of {wl.rows} rows of {wl.name} (seeded choice), append + decode, "
+                      f"{elapsed:.2f} s"}
+
+
+# --------------------------------------------------------------------------- arms
+
+
+def run_reference(args, wl: Workload):
+    """The oracle as it stands, on the host's cores: each step is a bounded
+    sample (a few rows) of the workload."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    batch = make_batch(wl, seed=1000 + list(WORKLOADS).index(wl.name), device="cpu"
+                       if not torch.cuda.is_available() else "cuda:0")
+    pos = batch.layout.positions
+    order = np.random.default_rng(0).permutation(wl.rows)
+    rows_per_step = args.reference_rows
+    times, total_bytes, total_rows = [], 0, 0
+    for step in range(args.warmup + args.steps):
+        rows = order[(step * rows_per_step) % wl.rows:][:rows_per_step]
+        if len(rows) < rows_per_step:
+            rows = order[:rows_per_step]
+        t = oracle_rows_timing(batch, rows, wl.window)
+        if step >= args.warmup:
+            times.append(t)
+            total_bytes += algorithmic_bytes(wl, pos[rows])["step"]
+            total_rows += len(rows)
+    elapsed = sum(times)
+    value = total_bytes / elapsed / 1e9
+    sample = f"{rows_per_step} rows of {wl.name} per step (seeded), append + decode"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * elapsed / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe(wl), "rows_per_step": rows_per_step},
+        "row_tokens_per_s": total_rows / elapsed,
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.default_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_pgd(args, wl: Workload):
+    import paged_gqa_decode_gb300 as pgd
+    world, rank, local = dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    init_dist(world, "nccl")
+    seed = 1000 + list(WORKLOADS).index(wl.name) + 7919 * rank
+    batch = make_batch(wl, seed=seed, device=device)
+    lay = batch.layout
+    dims = pgd.make_dims(rows=wl.rows, num_q_heads=wl.q_heads, num_kv_heads=wl.kv_heads,
+                         head_dim=wl.head_dim, num_pages=lay.num_pages,
+                         max_pages_per_row=batch.table.shape[1])
+    ws = torch.empty(max(16, pgd.paged_decode_workspace_bytes(dims, args.pages_per_split)),
+                     dtype=torch.uint8, device=device)
+    out = torch.empty_like(batch.q)
+    stream = torch.cuda.current_stream()
+    by = algorithmic_bytes(wl, lay.positions)
+    flush = None
+    if by["step"] < 4 * L2_BYTES:
+        flush = torch.empty(2 ** 30, dtype=torch.uint8, device=device)
+
+    def append():
+        pgd.kv_append_paged(batch.k_new, batch.v_new, batch.table, batch.positions,
+                            batch.k_pool, batch.v_pool)
+
+    def decode():
+        pgd.paged_decode_attention(batch.q, batch.k_pool, batch.v_pool, batch.table,
+                                   batch.positions, batch.sinks, wl.window, wl.scale,
+                                   num_kv_heads=wl.kv_heads, out=out, workspace=ws,
+                                   pages_per_split=args.pages_per_split)
+
+    for _ in range(args.warmup):
+        append()
+        decode()
+    status = pgd.get_device_error()
+    if status != pgd.OK:
+        raise RuntimeError(f"device error during warm-up: {pgd.status_string(status)}")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(device)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.mark_start()
+    for i in range(args.steps):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        append()
+        ev[i][1].record(stream)
+        decode()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_end()
+    barrier(world)
+    clk = clocks.stop()
+    status = pgd.get_device_error()
+    if status != pgd.OK:
+        raise RuntimeError(f"device error in the timed region: {pgd.status_string(status)}")
+    append_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
+    decode_ms = sum(e[1].elapsed_time(e[2]) for e in ev)
+    step_ms = append_ms + decode_ms if flush is not None else ev[0][0].elapsed_time(ev[-1][2])
+    step_ms = max_over_ranks(step_ms, world, device)
+    decode_ms = max_over_ranks(decode_ms, world, device)
+    total_bytes = sum_over_ranks(by["step"] * args.steps, world, device)
+    total_rows = sum_over_ranks(wl.rows * args.steps, world, device)
+    value = total_bytes / (step_ms * 1e-3) / 1e9
+
+    # End to end through the public API with host buffers: per step the
+    # inputs go host -> device from pinned memory, the output comes back.
+    host_in = {k: getattr(batch, k).cpu().pin_memory() for k in ("q", "k_new", "v_new")}
+    host_in["table"] = batch.table.cpu().pin_memory()
+    host_in["positions"] = batch.positions.cpu().pin_memory()
+    if batch.sinks is not None:
+        host_in["sinks"] = batch.sinks.cpu().pin_memory()
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for k, t in host_in.items():
+            getattr(batch, k).copy_(t, non_blocking=True)
+        append()
+        decode()
+        host_out.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = 0.0
+    if flush is None:
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1)
+    else:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            e0.record(stream)
+            e2e_step()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            e2e_ms += e0.elapsed_time(e1)
+    barrier(world)
+    e2e_ms = max_over_ranks(e2e_ms, world, device)
+    e2e_value = total_bytes / (e2e_ms * 1e-3) / 1e9
+
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peak()
+    decode_s = decode_ms * 1e-3 / args.steps
+    achieved = by["decode"] / decode_s / 1e9
+    digest = source_digest()
+    traffic = kernel_traffic(digest, wl.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "storage_dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": describe(wl), "rows_per_gpu": wl.rows,
+                   "pool_pages_per_gpu": lay.num_pages,
+                   "pool_gb_per_gpu": 2 * lay.num_pages * wl.kv_heads * 64 * wl.head_dim * 2 / 1e9,
+                   "l2": "inputs larger than L2" if flush is None else "1 GiB L2 flush between steps",
+                   "pages_per_split": args.pages_per_split or "auto",
+                   "parallelism": f"replicas over rows x{world}"},
+        "row_tokens_per_s": total_rows / (step_ms * 1e-3),
+        "pct_of_nominal_8tbs": 100.0 * value / world / NOMINAL_HBM_GBS,
+        "pct_of_measured_peak": 100.0 * value / world / peak,
+        "append_ms_per_step": append_ms / args.steps,
+        "decode_ms_per_step": decode_ms / args.steps,
+        "bytes_per_step_per_gpu": by,
+        "roofline": {"bound": "hbm", "kernel": "paged_decode (split + combine kernels)",
+                     "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": achieved / peak,
+                     "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
+                     "traffic": traffic, "algorithmic_bytes_per_launch": by["decode"]},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+        "kernel_source_digest": digest,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(batch)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["pgd", "reference"], default="pgd")
+    ap.add_argument("--workload", choices=list(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--pages-per-split", type=int, default=0)
+    ap.add_argument("--reference-rows", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    wl = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_pgd(args, wl)
+    world, _, _ = dist_env()
+    if world > 1 and torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

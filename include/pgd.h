@@ -1,0 +1,161 @@
+/*
+ * pgd.h -- C ABI of libpgd: paged grouped-query decode attention for GB300
+ * (sm_103a), with an optional per-head attention-sink logit and an optional
+ * sliding window.
+ *
+ * One serving step of a continuous batch: every row b has one new token at
+ * position positions[b].  Its key and value are appended to a pool of
+ * 64-position pages at the place the row's page table gives, then the row's
+ * query heads attend over the row's pages up to and including that position.
+ *
+ * Operation definitions (model-card pages of the "Nest" zoo):
+ *   - Mistral 7B Instruct v0.3, src/attention.linnet,
+ *     GroupedQueryAttention.decode_paged, and README "Entries" (decode_paged):
+ *     page_slots(table, positions), write_tokens into the pool, then
+ *     paged_attention(q, cache_k, cache_v, table, positions, rsqrt(head_dim)).
+ *   - GPT-OSS 20B, README "Attention sinks": one learned logit per query head
+ *     joins the scores as an extra key and is dropped after the softmax, so it
+ *     adds exp(sink - m) to the softmax denominator only.
+ *   - GPT-OSS 20B, src/attention.linnet, SinkAttention.decode_rows: key s is
+ *     seen by the query at position n when s <= n and s > n - window.
+ *   - GPT-OSS 20B, README (grouped sink_attention): query head h reads kv head
+ *     h / (num_q_heads / num_kv_heads); K/V are never copied per query head.
+ *
+ * Conventions for every entry point:
+ *   - All pointers except `dims`, `opts` and the result of
+ *     pgd_status_string are DEVICE pointers owned by the caller.  The library
+ *     allocates no memory; scratch is the caller's `workspace`.
+ *   - bf16 tensors are passed as raw 16-bit storage.  Every bf16 pointer and
+ *     the workspace must be 16-byte aligned.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream).  Arguments are validated on the host before anything
+ *     is launched; a non-zero return means nothing was enqueued.
+ *   - Row b is inactive when positions[b] < 0: nothing is appended for it and
+ *     its output is zero.
+ *   - Bad table entries or positions found on the device do not fault: the
+ *     affected row is skipped (its output zero) and a sticky device error
+ *     word is set, which pgd_get_device_error reads and clears.
+ */
+#ifndef PGD_H_
+#define PGD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define PGD_API __attribute__((visibility("default")))
+#else
+#define PGD_API
+#endif
+
+/* Same handle as cudaStream_t. */
+typedef struct CUstream_st* pgd_stream_t;
+
+/* Status codes. */
+enum {
+  PGD_OK = 0,
+  PGD_EINVAL = 1,          /* NULL pointer, bad shape, misaligned pointer */
+  PGD_EUNSUPPORTED = 2,    /* head_dim not 64/128, page_size not 64, group > 8 */
+  PGD_ECUDA = 3,           /* a CUDA runtime or driver call failed */
+  PGD_EDEVICE_BOUNDS = 4,  /* device: table entry or position out of range */
+  PGD_EDEVICE_TIMEOUT = 5, /* device: a pipeline wait gave up (bounded waits) */
+  PGD_EWORKSPACE = 6       /* workspace smaller than pgd_paged_decode_workspace_bytes */
+};
+
+/* Pool layouts.  In both, the 64 x head_dim values of one (page, kv head)
+ * form one contiguous tile, so a page tile is read with a single copy. */
+enum {
+  PGD_PAGE_MAJOR = 0, /* [num_pages][num_kv_heads][64][head_dim] */
+  PGD_HEAD_MAJOR = 1  /* [num_kv_heads][num_pages * 64][head_dim]: the pages'
+                         own cache_k[0] layout, [KvHeads, MaxSeq, D] */
+};
+
+typedef struct {
+  int32_t rows;              /* R >= 0 rows of the continuous batch */
+  int32_t num_q_heads;       /* Hq > 0 */
+  int32_t num_kv_heads;      /* Hkv > 0, Hq % Hkv == 0, Hq / Hkv <= 8 */
+  int32_t head_dim;          /* D: 64 or 128 */
+  int32_t page_size;         /* positions per page: must be 64 */
+  int32_t num_pages;         /* pool capacity in pages, >= 1 */
+  int32_t max_pages_per_row; /* table row stride (entries per row), >= 1 */
+  int32_t layout;            /* PGD_PAGE_MAJOR or PGD_HEAD_MAJOR */
+} pgd_dims;
+
+/* Optional tuning of the decode launch; pass NULL for the defaults.  The same
+ * options must be passed to pgd_paged_decode_workspace_bytes and to
+ * pgd_paged_decode_attention. */
+typedef struct {
+  int32_t pages_per_split; /* pages one CTA streams; 0 = chosen from dims and
+                              the device's SM count */
+} pgd_decode_options;
+
+/*
+ * kv_append_paged -- page_slots + write_tokens.
+ *   k_new, v_new  bf16 [R][Hkv][D]: the new token's key and value per row.
+ *   table         int32 [R][max_pages_per_row]: row b's pages in order.
+ *   positions     int32 [R]: the new token's 0-based position (< 0: inactive).
+ *   k_pool,v_pool bf16 pools in dims->layout, num_pages pages each.
+ * Row b's token is written at position positions[b] % 64 of page
+ * table[b][positions[b] / 64], for every kv head.  Two active rows must not
+ * name the same slot (the result would be either row's value).
+ * Device errors: positions[b] / 64 >= max_pages_per_row, or a table entry
+ * outside [0, num_pages): nothing is written for that row and
+ * PGD_EDEVICE_BOUNDS is recorded.
+ */
+PGD_API int pgd_kv_append_paged(const pgd_dims* dims, const void* k_new, const void* v_new,
+                        const int32_t* table, const int32_t* positions, void* k_pool,
+                        void* v_pool, pgd_stream_t stream);
+
+/*
+ * Bytes of device workspace pgd_paged_decode_attention needs for these dims
+ * and options on the current device: split partials (m, l and an unnormalised
+ * fp32 accumulator per row, query head and split).  0 if dims are invalid.
+ */
+PGD_API size_t pgd_paged_decode_workspace_bytes(const pgd_dims* dims, const pgd_decode_options* opts);
+
+/*
+ * paged_decode_attention -- paged_attention with an optional sink and window.
+ *   q          bf16 [R][Hq][D]: queries (rope already applied).
+ *   k_pool, v_pool  the pools, holding each active row's positions
+ *              0..positions[b] (append first: the new token attends to itself).
+ *   table, positions  as for pgd_kv_append_paged.
+ *   sinks      fp32 [Hq] sink logits (score space: not multiplied by scale),
+ *              or NULL for none.
+ *   window     > 0: row b attends to positions (n - window, n];
+ *              <= 0: full causal attention over 0..n.
+ *   scale      score scale, normally 1 / sqrt(D).
+ *   out        bf16 [R][Hq][D], rounded to nearest even from fp32.
+ *   workspace  >= pgd_paged_decode_workspace_bytes(dims, opts) bytes.
+ * Query head h of row b uses kv head h / (Hq / Hkv).  For each row and head,
+ * m = max(max_j s_j, sink), out = sum_j e^(s_j - m) v_j /
+ * (sum_j e^(s_j - m) + e^(sink - m)) with s_j = scale * q . k_j, in fp32.
+ * Device errors: as for pgd_kv_append_paged (for any attended page), plus
+ * PGD_EDEVICE_TIMEOUT if a pipeline wait exceeded its limit; affected rows
+ * or splits contribute zero.
+ */
+PGD_API int pgd_paged_decode_attention(const pgd_dims* dims, const void* q, const void* k_pool,
+                               const void* v_pool, const int32_t* table,
+                               const int32_t* positions, const float* sinks, int32_t window,
+                               float scale, void* out, void* workspace, size_t workspace_bytes,
+                               const pgd_decode_options* opts, pgd_stream_t stream);
+
+/* Synchronises `stream`, then returns and clears the sticky device error word
+ * of the current device (PGD_OK if none).  Returns PGD_ECUDA if the
+ * synchronisation itself failed. */
+PGD_API int pgd_get_device_error(pgd_stream_t stream);
+
+/* A static, human-readable name for a status code. */
+PGD_API const char* pgd_status_string(int status);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+PGD_API int pgd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PGD_H_ */

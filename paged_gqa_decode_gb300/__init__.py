@@ -1,0 +1,214 @@
+"""Paged grouped-query decode attention for GB300 (sm_103a).
+
+A thin binding over libpgd's C ABI (include/pgd.h): it turns torch tensors
+into device pointers, sizes and the current CUDA stream, and nothing else.
+Every step of the computation runs in the library's CUDA kernels; there is
+no CPU or PyTorch fallback, and every call fails loudly if the library is
+missing or the tensors are not on a CUDA device.
+
+Entry points (same names as the C ABI, without the ``pgd_`` prefix):
+
+- ``kv_append_paged``: write each row's new key and value at its page slot.
+- ``paged_decode_attention``: grouped-query decode attention of each row over
+  its pages, with optional per-head sink logits and sliding window.
+- ``paged_decode_workspace_bytes``, ``get_device_error``.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+PAGE_SIZE = 64
+PAGE_MAJOR = 0
+HEAD_MAJOR = 1
+
+OK, EINVAL, EUNSUPPORTED, ECUDA, EDEVICE_BOUNDS, EDEVICE_TIMEOUT, EWORKSPACE = range(7)
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libpgd.so")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class PgdError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_int32) for name in (
+        "rows", "num_q_heads", "num_kv_heads", "head_dim", "page_size", "num_pages",
+        "max_pages_per_row", "layout")]
+
+
+class DecodeOptions(ctypes.Structure):
+    _fields_ = [("pages_per_split", ctypes.c_int32)]
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Loads libpgd.so (built by ``paged_gqa_decode_gb300.build``); raises if absent."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = path or LIB_PATH
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"libpgd is not built ({path} missing): run "
+                    "`python -c 'import __graft_entry__ as g; g.build()'`")
+            lib = ctypes.CDLL(path)
+            vp, i32 = ctypes.c_void_p, ctypes.c_int32
+            dims_p = ctypes.POINTER(Dims)
+            opts_p = ctypes.POINTER(DecodeOptions)
+            lib.pgd_kv_append_paged.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, vp]
+            lib.pgd_kv_append_paged.restype = ctypes.c_int
+            lib.pgd_paged_decode_workspace_bytes.argtypes = [dims_p, opts_p]
+            lib.pgd_paged_decode_workspace_bytes.restype = ctypes.c_size_t
+            lib.pgd_paged_decode_attention.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, i32,
+                                                      ctypes.c_float, vp, vp, ctypes.c_size_t,
+                                                      opts_p, vp]
+            lib.pgd_paged_decode_attention.restype = ctypes.c_int
+            lib.pgd_get_device_error.argtypes = [vp]
+            lib.pgd_get_device_error.restype = ctypes.c_int
+            lib.pgd_status_string.argtypes = [ctypes.c_int]
+            lib.pgd_status_string.restype = ctypes.c_char_p
+            lib.pgd_version.argtypes = []
+            lib.pgd_version.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load_library().pgd_status_string(status).decode()
+
+
+def _stream_handle(stream: torch.cuda.Stream | None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _check_cuda(*tensors: torch.Tensor | None) -> torch.device:
+    device = None
+    for t in tensors:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("paged_gqa_decode_gb300 runs on CUDA tensors only")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+        if device is None:
+            device = t.device
+        elif t.device != device:
+            raise ValueError("all tensors must be on one device")
+    return device
+
+
+def _dtype(t: torch.Tensor, dtype: torch.dtype, name: str) -> None:
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def make_dims(*, rows: int, num_q_heads: int, num_kv_heads: int, head_dim: int, num_pages: int,
+              max_pages_per_row: int, layout: int = PAGE_MAJOR) -> Dims:
+    return Dims(rows, num_q_heads, num_kv_heads, head_dim, PAGE_SIZE, num_pages,
+                max_pages_per_row, layout)
+
+
+def _pool_pages(pool: torch.Tensor, kv_heads: int, head_dim: int) -> int:
+    per_page = kv_heads * PAGE_SIZE * head_dim
+    if pool.numel() % per_page:
+        raise ValueError(f"pool of {pool.numel()} values is not a whole number of pages")
+    return pool.numel() // per_page
+
+
+def kv_append_paged(k_new: torch.Tensor, v_new: torch.Tensor, table: torch.Tensor,
+                    positions: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor, *,
+                    layout: int = PAGE_MAJOR, stream: torch.cuda.Stream | None = None) -> None:
+    """Writes k_new/v_new (bf16 [R, Hkv, D]) into the pools at each row's slot:
+    position positions[b] % 64 of page table[b][positions[b] // 64]."""
+    dev = _check_cuda(k_new, v_new, table, positions, k_pool, v_pool)
+    for t, n in ((k_new, "k_new"), (v_new, "v_new"), (k_pool, "k_pool"), (v_pool, "v_pool")):
+        _dtype(t, torch.bfloat16, n)
+    _dtype(table, torch.int32, "table")
+    _dtype(positions, torch.int32, "positions")
+    rows, hkv, d = k_new.shape
+    if v_new.shape != k_new.shape or positions.shape != (rows,) or table.dim() != 2 \
+            or table.shape[0] != rows or k_pool.shape != v_pool.shape:
+        raise ValueError("inconsistent shapes")
+    dims = make_dims(rows=rows, num_q_heads=hkv, num_kv_heads=hkv, head_dim=d,
+                     num_pages=_pool_pages(k_pool, hkv, d), max_pages_per_row=table.shape[1],
+                     layout=layout)
+    with torch.cuda.device(dev):
+        rc = load_library().pgd_kv_append_paged(
+            ctypes.byref(dims), _ptr(k_new), _ptr(v_new), _ptr(table), _ptr(positions),
+            _ptr(k_pool), _ptr(v_pool), _stream_handle(stream))
+    if rc != OK:
+        raise PgdError(rc, "kv_append_paged")
+
+
+def paged_decode_workspace_bytes(dims: Dims, pages_per_split: int = 0) -> int:
+    opts = DecodeOptions(pages_per_split)
+    return load_library().pgd_paged_decode_workspace_bytes(ctypes.byref(dims), ctypes.byref(opts))
+
+
+def paged_decode_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                           table: torch.Tensor, positions: torch.Tensor,
+                           sinks: torch.Tensor | None = None, window: int = 0,
+                           scale: float | None = None, *, num_kv_heads: int,
+                           layout: int = PAGE_MAJOR, out: torch.Tensor | None = None,
+                           workspace: torch.Tensor | None = None, pages_per_split: int = 0,
+                           stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Grouped-query decode attention of each row over its pages.
+
+    q: bf16 [R, Hq, D]; pools: bf16 with num_kv_heads kv heads in ``layout``;
+    table: int32 [R, max_pages]; positions: int32 [R]; sinks: fp32 [Hq] or
+    None; window <= 0 for full attention.  Returns bf16 [R, Hq, D]."""
+    dev = _check_cuda(q, k_pool, v_pool, table, positions, sinks, out, workspace)
+    _dtype(q, torch.bfloat16, "q")
+    _dtype(k_pool, torch.bfloat16, "k_pool")
+    _dtype(v_pool, torch.bfloat16, "v_pool")
+    _dtype(table, torch.int32, "table")
+    _dtype(positions, torch.int32, "positions")
+    if sinks is not None:
+        _dtype(sinks, torch.float32, "sinks")
+    rows, hq, d = q.shape
+    if positions.shape != (rows,) or table.dim() != 2 or table.shape[0] != rows \
+            or k_pool.shape != v_pool.shape or (sinks is not None and sinks.shape != (hq,)):
+        raise ValueError("inconsistent shapes")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dims = make_dims(rows=rows, num_q_heads=hq, num_kv_heads=num_kv_heads, head_dim=d,
+                     num_pages=_pool_pages(k_pool, num_kv_heads, d),
+                     max_pages_per_row=table.shape[1], layout=layout)
+    opts = DecodeOptions(pages_per_split)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        if out is None:
+            out = torch.empty_like(q)
+        elif out.shape != q.shape or out.dtype != torch.bfloat16:
+            raise ValueError("out must be bf16 shaped like q")
+        need = lib.pgd_paged_decode_workspace_bytes(ctypes.byref(dims), ctypes.byref(opts))
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        rc = lib.pgd_paged_decode_attention(
+            ctypes.byref(dims), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(table),
+            _ptr(positions), _ptr(sinks), int(window), float(scale), _ptr(out), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), ctypes.byref(opts),
+            _stream_handle(stream))
+    if rc != OK:
+        raise PgdError(rc, "paged_decode_attention")
+    return out
+
+
+def get_device_error(stream: torch.cuda.Stream | None = None) -> int:
+    """Synchronises the stream and returns (and clears) the device error word."""
+    return load_library().pgd_get_device_error(_stream_handle(stream))

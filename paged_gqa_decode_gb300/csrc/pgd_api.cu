@@ -1,0 +1,263 @@
+// Host side of the C ABI declared in include/pgd.h: argument validation,
+// launch planning (pages per split), TMA descriptor encoding and launches.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "pgd.h"
+#include "pgd_internal.h"
+
+namespace pgd {
+
+// The sticky device error word of each device that loads the library.
+__device__ unsigned int g_device_error = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kPageSize = 64;
+constexpr int kMaxPagesPerSplit = 64;
+
+struct DeviceInfo {
+  std::once_flag once;
+  cudaError_t status = cudaSuccess;
+  int sm_count = 0;
+  unsigned int* err = nullptr;  // device address of g_device_error
+};
+DeviceInfo g_devices[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+int current_device(DeviceInfo** info) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PGD_ECUDA;
+  DeviceInfo& d = g_devices[dev];
+  std::call_once(d.once, [&] {
+    d.status = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (d.status == cudaSuccess)
+      d.status = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.err), g_device_error);
+  });
+  if (d.status != cudaSuccess) return PGD_ECUDA;
+  *info = &d;
+  return PGD_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_dims(const pgd_dims* d) {
+  if (!d) return PGD_EINVAL;
+  if (d->rows < 0 || d->num_q_heads <= 0 || d->num_kv_heads <= 0 || d->head_dim <= 0 ||
+      d->num_pages <= 0 || d->max_pages_per_row <= 0)
+    return PGD_EINVAL;
+  if (d->num_q_heads % d->num_kv_heads != 0) return PGD_EINVAL;
+  if (d->layout != PGD_PAGE_MAJOR && d->layout != PGD_HEAD_MAJOR) return PGD_EINVAL;
+  if (d->page_size != kPageSize) return PGD_EUNSUPPORTED;
+  if (d->head_dim != 64 && d->head_dim != 128) return PGD_EUNSUPPORTED;
+  if (padded_group(d->num_q_heads / d->num_kv_heads) == 0) return PGD_EUNSUPPORTED;
+  // Pool rows are addressed with 32-bit TMA coordinates; positions are int32.
+  if ((int64_t)d->num_pages * d->num_kv_heads * kPageSize >= (int64_t)INT32_MAX)
+    return PGD_EUNSUPPORTED;
+  if ((int64_t)d->max_pages_per_row * kPageSize > (int64_t)INT32_MAX) return PGD_EUNSUPPORTED;
+  return PGD_OK;
+}
+
+struct Plan {
+  int pages_per_split;
+  int max_splits;
+};
+
+// Pages per split: enough CTAs for several waves of 2 CTAs per SM when rows
+// are about half full, capped so one split is at most 64 pages.
+Plan make_plan(const pgd_dims* d, const pgd_decode_options* opts, int sm_count) {
+  Plan pl;
+  int pps = opts ? opts->pages_per_split : 0;
+  if (pps <= 0) {
+    const int64_t target = 4ll * 2 * (sm_count > 0 ? sm_count : 1);
+    const int64_t expected = (int64_t)d->rows * d->num_kv_heads *
+                             (d->max_pages_per_row > 1 ? d->max_pages_per_row / 2 : 1);
+    int64_t v = (expected + target - 1) / target;
+    pps = (int)(v < 1 ? 1 : (v > kMaxPagesPerSplit ? kMaxPagesPerSplit : v));
+  }
+  if (pps > d->max_pages_per_row) pps = d->max_pages_per_row;
+  pl.pages_per_split = pps;
+  pl.max_splits = (d->max_pages_per_row + pps - 1) / pps;
+  return pl;
+}
+
+size_t workspace_bytes(const pgd_dims* d, const Plan& pl) {
+  return (size_t)d->rows * d->num_q_heads * pl.max_splits * (d->head_dim + 2) * sizeof(float);
+}
+
+int encode_pool_map(CUtensorMap* map, const void* pool, const pgd_dims* d) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return PGD_ECUDA;
+  // The pool as a 2-D tensor: rows of head_dim bf16 values, one row per
+  // (page, kv head, position) in either layout.  A box is 64 rows x 64
+  // values (128 bytes): one page tile, or half of one when head_dim is 128.
+  const cuuint64_t rows = (cuuint64_t)d->num_pages * d->num_kv_heads * kPageSize;
+  const cuuint64_t dims[2] = {(cuuint64_t)d->head_dim, rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)d->head_dim * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)kPageSize};
+  const cuuint32_t elem[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims,
+                        strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PGD_OK : PGD_ECUDA;
+}
+
+}  // namespace
+
+int padded_group(int group) {
+  if (group == 1) return 1;
+  if (group == 2) return 2;
+  if (group >= 3 && group <= 4) return 4;
+  if (group >= 5 && group <= 8) return 8;
+  return 0;
+}
+
+}  // namespace pgd
+
+using namespace pgd;
+
+extern "C" {
+
+int pgd_kv_append_paged(const pgd_dims* dims, const void* k_new, const void* v_new,
+                        const int32_t* table, const int32_t* positions, void* k_pool,
+                        void* v_pool, pgd_stream_t stream) {
+  int rc = check_dims(dims);
+  if (rc != PGD_OK) return rc;
+  if (dims->rows == 0) return PGD_OK;
+  if (!k_new || !v_new || !table || !positions || !k_pool || !v_pool) return PGD_EINVAL;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool))
+    return PGD_EINVAL;
+  DeviceInfo* dev = nullptr;
+  if ((rc = current_device(&dev)) != PGD_OK) return rc;
+  AppendParams p;
+  p.k_new = static_cast<const uint16_t*>(k_new);
+  p.v_new = static_cast<const uint16_t*>(v_new);
+  p.table = table;
+  p.positions = positions;
+  p.k_pool = static_cast<uint16_t*>(k_pool);
+  p.v_pool = static_cast<uint16_t*>(v_pool);
+  p.err = dev->err;
+  p.rows = dims->rows;
+  p.hkv = dims->num_kv_heads;
+  p.head_dim = dims->head_dim;
+  p.maxp = dims->max_pages_per_row;
+  p.num_pages = dims->num_pages;
+  p.layout = dims->layout;
+  return launch_kv_append(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? PGD_OK
+                                                                                     : PGD_ECUDA;
+}
+
+size_t pgd_paged_decode_workspace_bytes(const pgd_dims* dims, const pgd_decode_options* opts) {
+  if (check_dims(dims) != PGD_OK) return 0;
+  DeviceInfo* dev = nullptr;
+  if (current_device(&dev) != PGD_OK) return 0;
+  return workspace_bytes(dims, make_plan(dims, opts, dev->sm_count));
+}
+
+int pgd_paged_decode_attention(const pgd_dims* dims, const void* q, const void* k_pool,
+                               const void* v_pool, const int32_t* table,
+                               const int32_t* positions, const float* sinks, int32_t window,
+                               float scale, void* out, void* workspace, size_t workspace_size,
+                               const pgd_decode_options* opts, pgd_stream_t stream) {
+  int rc = check_dims(dims);
+  if (rc != PGD_OK) return rc;
+  if (dims->rows == 0) return PGD_OK;
+  if (!q || !k_pool || !v_pool || !table || !positions || !out) return PGD_EINVAL;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
+    return PGD_EINVAL;
+  if (!std::isfinite(scale)) return PGD_EINVAL;
+  DeviceInfo* dev = nullptr;
+  if ((rc = current_device(&dev)) != PGD_OK) return rc;
+  const Plan pl = make_plan(dims, opts, dev->sm_count);
+  const size_t need = workspace_bytes(dims, pl);
+  if (workspace_size < need) return PGD_EWORKSPACE;
+  if (!workspace || !aligned16(workspace)) return PGD_EINVAL;
+
+  CUtensorMap k_map, v_map;
+  if ((rc = encode_pool_map(&k_map, k_pool, dims)) != PGD_OK) return rc;
+  if ((rc = encode_pool_map(&v_map, v_pool, dims)) != PGD_OK) return rc;
+
+  DecodeParams p;
+  p.q = static_cast<const uint16_t*>(q);
+  p.table = table;
+  p.positions = positions;
+  p.sinks = sinks;
+  p.out = static_cast<uint16_t*>(out);
+  const size_t acc_floats =
+      (size_t)dims->rows * dims->num_q_heads * pl.max_splits * dims->head_dim;
+  p.ws_acc = static_cast<float*>(workspace);
+  p.ws_ml = p.ws_acc + acc_floats;
+  p.err = dev->err;
+  p.rows = dims->rows;
+  p.hq = dims->num_q_heads;
+  p.hkv = dims->num_kv_heads;
+  p.group = dims->num_q_heads / dims->num_kv_heads;
+  p.maxp = dims->max_pages_per_row;
+  p.num_pages = dims->num_pages;
+  p.layout = dims->layout;
+  p.window = window > 0 ? window : 0;
+  p.pages_per_split = pl.pages_per_split;
+  p.max_splits = pl.max_splits;
+  p.q_scale_log2 = (float)((double)scale * 1.4426950408889634);
+
+  // With a window, a row spans at most ceil((window - 1) / 64) + 1 pages.
+  int grid_pages = dims->max_pages_per_row;
+  if (p.window > 0) {
+    const int64_t wp = ((int64_t)p.window + kPageSize - 2) / kPageSize + 1;
+    if (wp < grid_pages) grid_pages = (int)wp;
+  }
+  const int grid_splits = (grid_pages + pl.pages_per_split - 1) / pl.pages_per_split;
+
+  const int padded = padded_group(p.group);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = dims->head_dim == 64 ? launch_decode_d64(p, k_map, v_map, padded, grid_splits, st)
+                                       : launch_decode_d128(p, k_map, v_map, padded, grid_splits, st);
+  return e == cudaSuccess ? PGD_OK : PGD_ECUDA;
+}
+
+int pgd_get_device_error(pgd_stream_t stream) {
+  DeviceInfo* dev = nullptr;
+  int rc = current_device(&dev);
+  if (rc != PGD_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return PGD_ECUDA;
+  unsigned int word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_device_error, sizeof word) != cudaSuccess) return PGD_ECUDA;
+  const unsigned int zero = 0;
+  if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero) != cudaSuccess) return PGD_ECUDA;
+  return (int)word;
+}
+
+const char* pgd_status_string(int status) {
+  switch (status) {
+    case PGD_OK: return "ok";
+    case PGD_EINVAL: return "invalid argument";
+    case PGD_EUNSUPPORTED: return "unsupported shape";
+    case PGD_ECUDA: return "CUDA error";
+    case PGD_EDEVICE_BOUNDS: return "device: table entry or position out of range";
+    case PGD_EDEVICE_TIMEOUT: return "device: pipeline wait timed out";
+    case PGD_EWORKSPACE: return "workspace too small";
+    default: return "unknown status";
+  }
+}
+
+int pgd_version(void) { return 100; }
+
+}  // extern "C"

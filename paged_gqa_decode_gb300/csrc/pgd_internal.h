@@ -1,0 +1,52 @@
+// Launch parameters and launcher declarations shared by the host API
+// (pgd_api.cu) and the kernel translation units.  Not part of the C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pgd.h"
+
+namespace pgd {
+
+struct AppendParams {
+  const uint16_t* k_new;  // [R][Hkv][D] bf16
+  const uint16_t* v_new;
+  const int32_t* table;  // [R][maxp]
+  const int32_t* positions;
+  uint16_t* k_pool;
+  uint16_t* v_pool;
+  unsigned int* err;  // sticky device error word
+  int rows, hkv, head_dim, maxp, num_pages, layout;
+};
+
+struct DecodeParams {
+  const uint16_t* q;  // [R][Hq][D] bf16
+  const int32_t* table;
+  const int32_t* positions;
+  const float* sinks;  // [Hq] or nullptr
+  uint16_t* out;       // [R][Hq][D] bf16
+  float* ws_acc;       // [R][Hq][max_splits][D]
+  float* ws_ml;        // [R][Hq][max_splits][2]: (m, l), m in log2 units
+  unsigned int* err;
+  int rows, hq, hkv, group, maxp, num_pages, layout, window;
+  int pages_per_split;  // pages one split CTA streams
+  int max_splits;       // split stride of the workspace
+  float q_scale_log2;   // scale * log2(e): scores are kept in log2 units
+};
+
+// Padded query-group sizes that have a decode kernel instantiation.
+int padded_group(int group);  // 0 if unsupported
+
+cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
+
+// Split kernel + combine kernel for one (head_dim, padded group).
+cudaError_t launch_decode_d64(const DecodeParams& p, const CUtensorMap& k_map,
+                              const CUtensorMap& v_map, int padded, int grid_splits,
+                              cudaStream_t stream);
+cudaError_t launch_decode_d128(const DecodeParams& p, const CUtensorMap& k_map,
+                               const CUtensorMap& v_map, int padded, int grid_splits,
+                               cudaStream_t stream);
+
+}  // namespace pgd

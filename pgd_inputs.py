@@ -77,25 +77,39 @@ class PageLayout:
     pages_used: int
 
 
+def layout_from_contexts(wl: Workload, contexts, seed: int, num_pages: int | None = None,
+                         table: np.ndarray | None = None) -> PageLayout:
+    """Row b's new token sits at contexts[b] - 1 (a context <= 0 makes the row
+    inactive).  Unless a table is given, each row gets ceil(context /
+    page_size) distinct pages taken in order from a random permutation of the
+    pool, so tables are shuffled and no two rows share a page; unused table
+    entries are 0."""
+    rng = np.random.default_rng(seed)
+    contexts = np.asarray(contexts, dtype=np.int64)
+    need = [max(0, math.ceil(int(c) / wl.page_size)) for c in contexts]
+    used = int(sum(need))
+    if num_pages is None:
+        num_pages = wl.pool_pages if wl.pool_pages is not None else max(1, math.ceil(used * 1.1))
+    if table is None:
+        if used > num_pages:
+            raise ValueError(f"{wl.name}: rows need {used} pages, pool holds {num_pages}")
+        order = rng.permutation(num_pages).astype(np.int32)
+        width = max(wl.max_pages_per_row, max(need, default=1), 1)
+        table = np.zeros((len(contexts), width), dtype=np.int32)
+        taken = 0
+        for b, k in enumerate(need):
+            table[b, :k] = order[taken:taken + k]
+            taken += k
+    positions = np.where(contexts > 0, contexts - 1, -1).astype(np.int32)
+    return PageLayout(contexts, positions, np.ascontiguousarray(table, dtype=np.int32),
+                      int(num_pages), used)
+
+
 def draw_layout(wl: Workload, seed: int) -> PageLayout:
-    """Contexts ~ U[ctx_lo, ctx_hi]; each row gets ceil(context / page_size)
-    distinct pages taken in order from a random permutation of the pool, so
-    tables are shuffled and no two rows share a page."""
+    """Contexts ~ U[ctx_lo, ctx_hi], then pages as in layout_from_contexts."""
     rng = np.random.default_rng(seed)
     contexts = rng.integers(wl.ctx_lo, wl.ctx_hi + 1, size=wl.rows).astype(np.int64)
-    need = [math.ceil(int(c) / wl.page_size) for c in contexts]
-    used = int(sum(need))
-    num_pages = wl.pool_pages if wl.pool_pages is not None else max(1, math.ceil(used * 1.1))
-    if used > num_pages:
-        raise ValueError(f"{wl.name}: rows need {used} pages, pool holds {num_pages}")
-    order = rng.permutation(num_pages).astype(np.int32)
-    table = np.zeros((wl.rows, wl.max_pages_per_row), dtype=np.int32)
-    taken = 0
-    for b, k in enumerate(need):
-        table[b, :k] = order[taken:taken + k]
-        taken += k
-    positions = (contexts - 1).astype(np.int32)
-    return PageLayout(contexts, positions, table, num_pages, used)
+    return layout_from_contexts(wl, contexts, seed + 1)
 
 
 @dataclasses.dataclass
@@ -112,21 +126,23 @@ class Batch:
     positions: torch.Tensor  # int32 [R]
 
 
-def make_batch(wl: Workload, seed: int, device: str | torch.device = "cpu") -> Batch:
+def make_batch(wl: Workload, seed: int, device: str | torch.device = "cpu",
+               layout: PageLayout | None = None) -> Batch:
     """q, k, v and pool contents ~ N(0, 1) in bf16, sinks ~ N(0, 1) in fp32,
     all from one seeded torch generator on ``device``."""
-    layout = draw_layout(wl, seed)
+    layout = layout if layout is not None else draw_layout(wl, seed)
     device = torch.device(device)
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
+    rows = len(layout.positions)
 
     def normal(*shape, dtype=torch.bfloat16):
         return torch.randn(*shape, generator=gen, device=device, dtype=dtype)
 
     pool_len = layout.num_pages * wl.kv_heads * wl.page_size * wl.head_dim
-    q = normal(wl.rows, wl.q_heads, wl.head_dim)
-    k_new = normal(wl.rows, wl.kv_heads, wl.head_dim)
-    v_new = normal(wl.rows, wl.kv_heads, wl.head_dim)
+    q = normal(rows, wl.q_heads, wl.head_dim)
+    k_new = normal(rows, wl.kv_heads, wl.head_dim)
+    v_new = normal(rows, wl.kv_heads, wl.head_dim)
     k_pool = normal(pool_len)
     v_pool = normal(pool_len)
     sinks = normal(wl.q_heads, dtype=torch.float32) if wl.sinks else None

@@ -1,0 +1,296 @@
+"""GPU parity: libpgd (through its C ABI) against the fp64 oracle on the same
+seeded inputs.  Append indexing must be bit-exact; attention output must be
+within max abs 1e-2 and max rel 2e-2 (bf16 output, fp32 accumulation).
+
+Covers the five workloads (three checked on every row at full size, two at
+full size -- in the launch configuration the benchmark times -- on sampled
+rows), and the edge cases: contexts around page boundaries, window
+boundaries, group sizes 1..8 with padding, head_dim 64 and 128, sink of
+-inf / huge / none, shared and reversed page lists, inactive rows, both pool
+layouts, split sizes that force the combine kernel, poisoned (NaN) slots
+outside every attended set, device-side bounds errors, and CUDA graphs."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_gqa_decode_gb300 as pgd
+from pgd_inputs import WORKLOADS, Workload, bf16_bits, layout_from_contexts, make_batch
+from tests.parity import compare, gpu_step, oracle_step, snapshot_rows
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    yield
+    torch.cuda.synchronize()
+
+
+def run_and_check(batch, *, window=None, sinks="batch", layout=pgd.PAGE_MAJOR, rows=None,
+                  pages_per_split=0, what=""):
+    wl = batch.wl
+    window = wl.window if window is None else window
+    sinks = batch.sinks if isinstance(sinks, str) else sinks
+    rows = np.arange(len(batch.layout.positions)) if rows is None else np.asarray(rows)
+    host = snapshot_rows(batch, rows, layout)
+    got = gpu_step(batch, window=window, sinks=sinks, scale=wl.scale, layout=layout,
+                   pages_per_split=pages_per_split)
+    want, _, _ = oracle_step(batch, host, window=window, sinks=sinks, scale=wl.scale,
+                             layout=layout)
+    idx = torch.as_tensor(rows, device=got.device)
+    return compare(got.index_select(0, idx), want, what or wl.name)
+
+
+# ---------------------------------------------------------------------------
+# Append: bit-exact against the oracle's page_slots + write_tokens.
+
+
+@pytest.mark.parametrize("layout", [pgd.PAGE_MAJOR, pgd.HEAD_MAJOR])
+@pytest.mark.parametrize("hkv,d", [(2, 64), (8, 128), (3, 64), (1, 128)])
+def test_append_bit_exact(layout, hkv, d):
+    wl = Workload("append", rows=9, q_heads=hkv, kv_heads=hkv, head_dim=d, ctx_lo=1, ctx_hi=300)
+    contexts = [1, 64, 65, 128, 129, 300, 0, 63, 200]   # a 0 context is an inactive row
+    lay = layout_from_contexts(wl, contexts, seed=5, num_pages=40)
+    batch = make_batch(wl, seed=21, device=DEV, layout=lay)
+    k_host, v_host = bf16_bits(batch.k_pool).copy(), bf16_bits(batch.v_pool).copy()
+    pgd.kv_append_paged(batch.k_new, batch.v_new, batch.table, batch.positions, batch.k_pool,
+                        batch.v_pool, layout=layout)
+    assert pgd.get_device_error() == pgd.OK
+    slots = oracle.page_slots(lay.table, lay.positions, 64, lay.num_pages)
+    geo = dict(kv_heads=hkv, head_dim=d, page_size=64, num_pages=lay.num_pages, layout=layout)
+    oracle.write_tokens(k_host, bf16_bits(batch.k_new), slots, **geo)
+    oracle.write_tokens(v_host, bf16_bits(batch.v_new), slots, **geo)
+    assert np.array_equal(bf16_bits(batch.k_pool), k_host)
+    assert np.array_equal(bf16_bits(batch.v_pool), v_host)
+
+
+# ---------------------------------------------------------------------------
+# The five workloads.
+
+
+@pytest.mark.parametrize("name", ["qwen_small", "qwen_serve", "gptoss_full"])
+def test_workload_every_row(name):
+    wl = WORKLOADS[name]
+    batch = make_batch(wl, seed=1000 + list(WORKLOADS).index(name), device=DEV)
+    run_and_check(batch)
+
+
+@pytest.mark.parametrize("name,sample", [("gptoss_sliding", 32), ("mistral_serve", 6)])
+def test_workload_full_size_sampled_rows(name, sample):
+    """Full-size pool and batch, the benchmark's launch configuration; the
+    oracle checks a seeded sample of rows, always including the longest and
+    the shortest."""
+    wl = WORKLOADS[name]
+    batch = make_batch(wl, seed=1000 + list(WORKLOADS).index(name), device=DEV)
+    pos = batch.layout.positions
+    rng = np.random.default_rng(7)
+    rows = set(rng.choice(wl.rows, size=sample - 2, replace=False).tolist())
+    rows |= {int(np.argmax(pos)), int(np.argmin(pos))}
+    run_and_check(batch, rows=sorted(rows))
+    del batch
+    torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------
+# Edge cases.
+
+EDGE_CONTEXTS = [1, 2, 63, 64, 65, 127, 128, 129, 191, 192, 193, 255, 256, 257, 700]
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(14, 2, 64), (64, 8, 64), (32, 8, 128), (8, 8, 64),
+                                      (6, 3, 128), (12, 4, 64), (10, 2, 128), (16, 8, 128)])
+@pytest.mark.parametrize("window", [0, 1, 63, 64, 65, 128, 129])
+def test_edge_contexts_windows_groups(hq, hkv, d, window):
+    wl = Workload("edge", rows=len(EDGE_CONTEXTS), q_heads=hq, kv_heads=hkv, head_dim=d,
+                  ctx_lo=1, ctx_hi=700, sinks=True)
+    lay = layout_from_contexts(wl, EDGE_CONTEXTS, seed=hq + d + window)
+    batch = make_batch(wl, seed=31 + window, device=DEV, layout=lay)
+    run_and_check(batch, window=window, what=f"edge hq={hq} hkv={hkv} d={d} w={window}")
+
+
+@pytest.mark.parametrize("kind", ["none", "minus_inf", "huge", "mixed"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_sink_values(kind, d):
+    wl = Workload("sinks", rows=6, q_heads=8, kv_heads=2, head_dim=d, ctx_lo=1, ctx_hi=400)
+    lay = layout_from_contexts(wl, [1, 65, 130, 257, 400, 64], seed=3)
+    batch = make_batch(wl, seed=41, device=DEV, layout=lay)
+    sinks = {
+        "none": None,
+        "minus_inf": torch.full((8,), -math.inf, device=DEV),
+        "huge": torch.full((8,), 1e4, device=DEV),
+        "mixed": torch.tensor([1e4, -math.inf, 0.0, 3.0, -3.0, 30.0, -30.0, 1.5], device=DEV),
+    }[kind]
+    stats = run_and_check(batch, sinks=sinks, what=f"sink {kind}")
+    if kind == "huge":
+        assert stats["max_abs"] <= 1e-6
+
+
+@pytest.mark.parametrize("pps", [1, 2, 3, 5, 64])
+@pytest.mark.parametrize("window", [0, 100])
+def test_split_sizes_force_the_combine(pps, window):
+    wl = Workload("splits", rows=5, q_heads=16, kv_heads=4, head_dim=64, ctx_lo=1, ctx_hi=1500,
+                  sinks=True)
+    lay = layout_from_contexts(wl, [1500, 1, 640, 641, 1000], seed=9)
+    batch = make_batch(wl, seed=51, device=DEV, layout=lay)
+    run_and_check(batch, window=window, pages_per_split=pps, what=f"pps={pps}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_head_major_layout(d):
+    wl = Workload("headmajor", rows=7, q_heads=16, kv_heads=4, head_dim=d, ctx_lo=1, ctx_hi=900,
+                  sinks=True)
+    lay = layout_from_contexts(wl, [900, 1, 64, 65, 500, 129, 0], seed=11)
+    batch = make_batch(wl, seed=61, device=DEV, layout=lay)
+    run_and_check(batch, layout=pgd.HEAD_MAJOR, pages_per_split=3)
+
+
+def test_shared_prefix_and_reversed_pages():
+    """Rows 0 and 1 share their first three pages (a shared prefix) and
+    differ in the page holding the new token; row 2 lists its pages in
+    reverse pool order; row 3 is inactive and lists page 0."""
+    wl = Workload("shared", rows=4, q_heads=8, kv_heads=2, head_dim=64, ctx_lo=1, ctx_hi=256,
+                  sinks=True)
+    table = np.zeros((4, 4), dtype=np.int32)
+    table[0] = [5, 2, 7, 1]
+    table[1] = [5, 2, 7, 3]
+    table[2] = [11, 10, 9, 8]
+    contexts = [250, 230, 256, 0]
+    lay = layout_from_contexts(wl, contexts, seed=0, num_pages=12, table=table)
+    batch = make_batch(wl, seed=71, device=DEV, layout=lay)
+    run_and_check(batch, pages_per_split=1)
+
+
+def test_poisoned_slots_outside_attention_are_never_read():
+    """Every pool position no row attends to holds NaN: any read of it that
+    reached the result would show."""
+    wl = Workload("poison", rows=6, q_heads=8, kv_heads=2, head_dim=128, ctx_lo=1, ctx_hi=600,
+                  sinks=True)
+    window = 70
+    lay = layout_from_contexts(wl, [600, 1, 64, 65, 129, 300], seed=13)
+    batch = make_batch(wl, seed=81, device=DEV, layout=lay)
+    keep = np.zeros(lay.num_pages * 64, dtype=bool)
+    for b, n in enumerate(lay.positions):
+        for s in range(max(0, n - window + 1), n + 1):
+            keep[lay.table[b, s // 64] * 64 + s % 64] = True
+    nan_slots = torch.from_numpy(~keep).to(DEV)
+    for pool in (batch.k_pool, batch.v_pool):
+        view = pool.view(lay.num_pages, wl.kv_heads, 64, wl.head_dim)
+        mask = nan_slots.view(lay.num_pages, 1, 64, 1).expand_as(view)
+        view.masked_fill_(mask, float("nan"))
+    run_and_check(batch, window=window, pages_per_split=2)
+
+
+def test_inactive_rows_are_zero_and_untouched():
+    wl = Workload("inactive", rows=4, q_heads=4, kv_heads=1, head_dim=64, ctx_lo=1, ctx_hi=128)
+    lay = layout_from_contexts(wl, [0, 100, 0, 1], seed=17, num_pages=6)
+    batch = make_batch(wl, seed=91, device=DEV, layout=lay)
+    out = gpu_step(batch, window=0, sinks=None, scale=wl.scale)
+    assert torch.all(out[0] == 0) and torch.all(out[2] == 0)
+    assert torch.any(out[1] != 0)
+
+
+def test_zero_rows_is_a_no_op():
+    q = torch.empty(0, 8, 64, dtype=torch.bfloat16, device=DEV)
+    pool = torch.zeros(4 * 2 * 64 * 64, dtype=torch.bfloat16, device=DEV)
+    table = torch.zeros(0, 3, dtype=torch.int32, device=DEV)
+    pos = torch.zeros(0, dtype=torch.int32, device=DEV)
+    out = pgd.paged_decode_attention(q, pool, pool, table, pos, num_kv_heads=2)
+    assert out.shape == (0, 8, 64)
+
+
+# ---------------------------------------------------------------------------
+# Errors: caught on the host, or recorded on the device without a fault.
+
+
+def test_device_bounds_errors_do_not_fault():
+    wl = Workload("bounds", rows=3, q_heads=8, kv_heads=2, head_dim=64, ctx_lo=1, ctx_hi=200)
+    lay = layout_from_contexts(wl, [200, 100, 50], seed=19, num_pages=10)
+    batch = make_batch(wl, seed=101, device=DEV, layout=lay)
+    bad_table = batch.table.clone()
+    bad_table[1, 1] = 10 ** 6                      # row 1's last page: outside the pool
+    out = pgd.paged_decode_attention(batch.q, batch.k_pool, batch.v_pool, bad_table,
+                                     batch.positions, num_kv_heads=2)
+    assert pgd.get_device_error() == pgd.EDEVICE_BOUNDS
+    assert torch.all(out[1] == 0)
+    bad_pos = batch.positions.clone()
+    bad_pos[2] = 64 * batch.table.shape[1] + 5      # beyond the row's table
+    out = pgd.paged_decode_attention(batch.q, batch.k_pool, batch.v_pool, batch.table, bad_pos,
+                                     num_kv_heads=2, pages_per_split=1)
+    assert pgd.get_device_error() == pgd.EDEVICE_BOUNDS
+    assert torch.all(out[2] == 0)
+    before = batch.k_pool.clone()
+    pgd.kv_append_paged(batch.k_new, batch.v_new, bad_table, bad_pos, batch.k_pool, batch.v_pool)
+    assert pgd.get_device_error() == pgd.EDEVICE_BOUNDS
+    # rows 1 and 2 were skipped; row 0 was written
+    changed = (batch.k_pool != before).view(-1, 64 * 64).any(dim=1).nonzero().flatten()
+    assert changed.numel() == 2
+    # the context is still healthy: a valid step matches the oracle
+    batch2 = make_batch(wl, seed=102, device=DEV, layout=lay)
+    run_and_check(batch2)
+
+
+def test_host_validation():
+    q = torch.zeros(2, 8, 64, dtype=torch.bfloat16, device=DEV)
+    pool = torch.zeros(4 * 2 * 64 * 64, dtype=torch.bfloat16, device=DEV)
+    table = torch.zeros(2, 3, dtype=torch.int32, device=DEV)
+    pos = torch.zeros(2, dtype=torch.int32, device=DEV)
+    with pytest.raises(ValueError):
+        pgd.paged_decode_attention(q.float(), pool, pool, table, pos, num_kv_heads=2)
+    with pytest.raises(ValueError):
+        pgd.paged_decode_attention(q.cpu(), pool, pool, table, pos, num_kv_heads=2)
+    with pytest.raises(pgd.PgdError) as e:   # group of 16 has no kernel
+        pgd.paged_decode_attention(torch.zeros(2, 32, 64, dtype=torch.bfloat16, device=DEV),
+                                   pool, pool, table, pos, num_kv_heads=2)
+    assert e.value.status == pgd.EUNSUPPORTED
+    with pytest.raises(pgd.PgdError) as e:   # head_dim 96
+        pgd.paged_decode_attention(torch.zeros(2, 8, 96, dtype=torch.bfloat16, device=DEV),
+                                   torch.zeros(4 * 2 * 64 * 96, dtype=torch.bfloat16, device=DEV),
+                                   torch.zeros(4 * 2 * 64 * 96, dtype=torch.bfloat16, device=DEV),
+                                   table, pos, num_kv_heads=2)
+    assert e.value.status == pgd.EUNSUPPORTED
+    with pytest.raises(pgd.PgdError) as e:   # misaligned q
+        raw = torch.zeros(2 * 8 * 64 + 1, dtype=torch.bfloat16, device=DEV)
+        pgd.paged_decode_attention(raw[1:].view(2, 8, 64), pool, pool, table, pos,
+                                   num_kv_heads=2)
+    assert e.value.status == pgd.EINVAL
+    with pytest.raises(pgd.PgdError) as e:   # workspace too small
+        pgd.paged_decode_attention(q, pool, pool, table, pos, num_kv_heads=2,
+                                   workspace=torch.zeros(16, dtype=torch.uint8, device=DEV),
+                                   pages_per_split=1)
+    assert e.value.status == pgd.EWORKSPACE
+
+
+def test_cuda_graph_replay_matches_eager():
+    wl = WORKLOADS["qwen_serve"]
+    batch = make_batch(wl, seed=1001, device=DEV)
+    want = gpu_step(batch, window=0, sinks=None, scale=wl.scale).clone()
+    out = torch.empty_like(want)
+    dims = pgd.make_dims(rows=wl.rows, num_q_heads=wl.q_heads, num_kv_heads=wl.kv_heads,
+                         head_dim=wl.head_dim, num_pages=batch.layout.num_pages,
+                         max_pages_per_row=batch.table.shape[1])
+    ws = torch.empty(pgd.paged_decode_workspace_bytes(dims), dtype=torch.uint8, device=DEV)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):   # warm up on the capture stream
+        pgd.paged_decode_attention(batch.q, batch.k_pool, batch.v_pool, batch.table,
+                                   batch.positions, None, 0, wl.scale, num_kv_heads=wl.kv_heads,
+                                   out=out, workspace=ws)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        pgd.kv_append_paged(batch.k_new, batch.v_new, batch.table, batch.positions,
+                            batch.k_pool, batch.v_pool)
+        pgd.paged_decode_attention(batch.q, batch.k_pool, batch.v_pool, batch.table,
+                                   batch.positions, None, 0, wl.scale, num_kv_heads=wl.kv_heads,
+                                   out=out, workspace=ws)
+    out.zero_()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, want)
