@@ -16,8 +16,14 @@
 // each page's K and V tiles (64 x D bf16, contiguous in the pool) into a ring
 // of shared-memory stages with 2-D TMA loads (128-byte swizzle, completion
 // on an mbarrier); each page is read from HBM exactly once for all G query
-// heads that share the kv head.  Four consumer warps take whole pages in
-// turn, each keeping its own fp32 online-softmax state for the G heads:
+// heads that share the kv head.  Page i goes to stage i % kStages and to
+// consumer warp i % kWarps.  Because those two cycles differ, a warp could
+// reach a stage's barrier a full phase early; the producer therefore
+// publishes the page index it last issued into each stage (stage_seq), and a
+// consumer waits for its own page index there before it waits on the stage's
+// barrier, so every parity wait targets the barrier's current phase.  Four
+// consumer warps take whole pages in turn, each keeping its own fp32
+// online-softmax state for the G heads:
 //   - scores: lane r owns tile rows r and r + 32 and forms the full dot
 //     products against q (broadcast from shared memory), so no cross-lane
 //     reduction is needed for Q.K^T;
@@ -92,6 +98,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 2)
   uint64_t* full = reinterpret_cast<uint64_t*>(p_s + C::kPFloats);
   uint64_t* empty = full + C::kStages;
   __shared__ int abort_flag;
+  __shared__ int stage_seq[C::kStages];  // page index last issued into each stage
 
   // Every table entry this split reads must name a pool page.
   bool bad = false;
@@ -124,6 +131,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 2)
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      stage_seq[s] = -1;
     }
     mbar_init_fence();
     abort_flag = 0;
@@ -162,6 +170,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 2)
           tma_load_2d(st + bx * C::kBoxBytes, &k_map, bx * 64, y, &full[s]);
           tma_load_2d(st + C::kTileBytes + bx * C::kBoxBytes, &v_map, bx * 64, y, &full[s]);
         }
+        *reinterpret_cast<volatile int*>(&stage_seq[s]) = i;
         issued = i + 1;
       }
       // No copy may still be landing in shared memory when the CTA exits.
@@ -186,7 +195,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 2)
 
   for (int i = warp; i < npages; i += C::kWarps) {
     const int s = i % C::kStages;
-    if (!mbar_wait_bounded(&full[s], (i / C::kStages) & 1, p.err)) {
+    if (!wait_seq_bounded(&stage_seq[s], i, p.err) ||
+        !mbar_wait_bounded(&full[s], (i / C::kStages) & 1, p.err)) {
       abort_flag = 1;
       break;
     }

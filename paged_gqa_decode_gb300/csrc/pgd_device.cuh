@@ -79,6 +79,23 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// Waits until the shared word *seq equals `want` (written by another warp of
+// the CTA).  Returns false (and records PGD_EDEVICE_TIMEOUT) after
+// kWaitLimitNs.
+__device__ __forceinline__ bool wait_seq_bounded(const volatile int* seq, int want,
+                                                 unsigned int* err) {
+  if (*seq == want) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(20);
+    if (*seq == want) return true;
+    if ((it & 255u) == 0u && global_ns() - t0 > kWaitLimitNs) {
+      record_error(err, PGD_EDEVICE_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // 2-D tiled TMA load of one box into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int32_t x,
                                             int32_t y, uint64_t* bar) {
