@@ -221,23 +221,21 @@ def oracle_rows_timing(batch, rows, window, nthreads=None) -> float:
     return time.perf_counter() - t0
 
 
-def cpu_baseline(batch, target_s: float = 12.0) -> dict:
+def cpu_baseline(batch, max_rows: int = 256) -> dict:
+    """The oracle (append + decode) on up to `max_rows` seeded rows of the
+    batch, on all host cores."""
     import oracle
     wl = batch.wl
     pos = batch.layout.positions
     order = np.random.default_rng(0).permutation(wl.rows)
-    count = min(4, wl.rows)
-    elapsed = oracle_rows_timing(batch, order[:count], wl.window)
-    if elapsed < target_s and count < wl.rows:
-        count = int(min(wl.rows, max(count + 1, count * target_s / max(elapsed, 1e-3))))
-        elapsed = oracle_rows_timing(batch, order[:count], wl.window)
-    rows = order[:count]
+    rows = order[:min(max_rows, wl.rows)]
+    elapsed = oracle_rows_timing(batch, rows, wl.window)
     by = algorithmic_bytes(wl, pos[rows])
     return {"value": by["step"] / elapsed / 1e9, "unit": "GB/s", "cores": oracle.default_threads(),
             "kind": "oracle",
-            "row_tokens_per_s": count / elapsed,
-            "sample": f"{count} of {wl.rows} rows of {wl.name} (seeded choice), append + decode, "
-                      f"{elapsed:.2f} s"}
+            "row_tokens_per_s": len(rows) / elapsed,
+            "sample": f"{len(rows)} of {wl.rows} rows of {wl.name} (seeded choice), "
+                      f"append + decode, {elapsed:.2f} s"}
 
 
 # --------------------------------------------------------------------------- arms
@@ -442,12 +440,16 @@ def main():
     ap.add_argument("--impl", choices=["pgd", "reference"], default="pgd")
     ap.add_argument("--workload", choices=list(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--pages-per-split", type=int, default=0)
+    ap.add_argument("--rows", type=int, default=0,
+                    help="override the workload's row count (small profiling cases)")
     ap.add_argument("--reference-rows", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     wl = WORKLOADS[args.workload]
+    if args.rows > 0:
+        wl = wl.replace(rows=args.rows)
     if args.impl == "reference":
         run_reference(args, wl)
     else:
