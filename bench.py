@@ -86,6 +86,11 @@ def dist_env():
     return world, rank, local
 
 
+def rank_seed(wl: Workload, rank: int) -> int:
+    """Each rank decodes its own batch: the workload's seed offset by rank."""
+    return 1000 + list(WORKLOADS).index(wl.name) + 7919 * rank
+
+
 def init_dist(world: int, backend: str):
     if world > 1 and not torch.distributed.is_initialized():
         torch.distributed.init_process_group(backend=backend)
@@ -286,8 +291,7 @@ def run_pgd(args, wl: Workload):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     init_dist(world, "nccl")
-    seed = 1000 + list(WORKLOADS).index(wl.name) + 7919 * rank
-    batch = make_batch(wl, seed=seed, device=device)
+    batch = make_batch(wl, seed=rank_seed(wl, rank), device=device)
     lay = batch.layout
     dims = pgd.make_dims(rows=wl.rows, num_q_heads=wl.q_heads, num_kv_heads=wl.kv_heads,
                          head_dim=wl.head_dim, num_pages=lay.num_pages,
