@@ -63,7 +63,8 @@ enum {
   PGD_ECUDA = 3,           /* a CUDA runtime or driver call failed */
   PGD_EDEVICE_BOUNDS = 4,  /* device: table entry or position out of range */
   PGD_EDEVICE_TIMEOUT = 5, /* device: a pipeline wait gave up (bounded waits) */
-  PGD_EWORKSPACE = 6       /* workspace smaller than pgd_paged_decode_workspace_bytes */
+  PGD_EWORKSPACE = 6,      /* workspace smaller than pgd_paged_decode_workspace_bytes */
+  PGD_ESCRATCH_LIMIT = 7   /* problem needs more scratch than PGD_STATIC_SCRATCH_BYTES */
 };
 
 /* Pool layouts.  In both, the 64 x head_dim values of one (page, kv head)
@@ -142,6 +143,41 @@ PGD_API int pgd_paged_decode_attention(const pgd_dims* dims, const void* q, cons
                                const int32_t* positions, const float* sinks, int32_t window,
                                float scale, void* out, void* workspace, size_t workspace_bytes,
                                const pgd_decode_options* opts, pgd_stream_t stream);
+
+/* Size of the library's own device scratch buffer used by
+ * pgd_paged_decode_attention_static: 64 MiB on every device that loads the
+ * library, held until the process exits. */
+#define PGD_STATIC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/*
+ * paged_decode_attention_static -- pgd_paged_decode_attention for callers that
+ * cannot allocate device memory.  The model-card pages have no counterpart
+ * for this entry point: it exists for callers such as plugins hosted by a
+ * runtime that owns every device allocation, or code on a path where
+ * cudaMalloc/cudaFree (which can synchronise the whole device) are not
+ * allowed.  It takes the same arguments minus the workspace, and allocates
+ * nothing: the split partials go to a file-scope device array of
+ * PGD_STATIC_SCRATCH_BYTES inside the library.  The caller still owns q, the
+ * pools, table, positions, sinks and out.
+ *   - Returns PGD_ESCRATCH_LIMIT, with nothing launched, if these dims and
+ *     options need more than PGD_STATIC_SCRATCH_BYTES of partials (that is,
+ *     if pgd_paged_decode_workspace_bytes(dims, opts) exceeds it).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     outside any stream capture.
+ *   - Every call on a device shares the one array, which keeps whatever the
+ *     last call left there.  Nothing in it has to start at zero: every
+ *     partial a call reads was written earlier in the same call.  Calls whose
+ *     kernels can overlap on the GPU (different streams without ordering
+ *     between them) race on the array and give wrong results; serialise them.
+ * Results equal those of pgd_paged_decode_attention with the same options.
+ */
+PGD_API int pgd_paged_decode_attention_static(const pgd_dims* dims, const void* q,
+                                              const void* k_pool, const void* v_pool,
+                                              const int32_t* table, const int32_t* positions,
+                                              const float* sinks, int32_t window, float scale,
+                                              void* out, const pgd_decode_options* opts,
+                                              pgd_stream_t stream);
 
 /* Synchronises `stream`, then returns and clears the sticky device error word
  * of the current device (PGD_OK if none).  Returns PGD_ECUDA if the

@@ -254,6 +254,7 @@ const char* pgd_status_string(int status) {
     case PGD_EDEVICE_BOUNDS: return "device: table entry or position out of range";
     case PGD_EDEVICE_TIMEOUT: return "device: pipeline wait timed out";
     case PGD_EWORKSPACE: return "workspace too small";
+    case PGD_ESCRATCH_LIMIT: return "problem needs more than the library's static scratch";
     default: return "unknown status";
   }
 }
@@ -261,3 +262,47 @@ const char* pgd_status_string(int status) {
 int pgd_version(void) { return 100; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode without caller-provided workspace, for callers that cannot allocate
+// device memory.  The split partials live in this file-scope array (one per
+// device that loads the library, held until exit); the host needs its device
+// address, looked up once per device.
+
+namespace pgd {
+namespace {
+
+static __device__ __align__(256) unsigned char g_static_scratch[PGD_STATIC_SCRATCH_BYTES];
+
+struct StaticScratch {
+  std::once_flag once;
+  cudaError_t status = cudaSuccess;
+  void* ptr = nullptr;
+};
+StaticScratch g_static[kMaxDevices];
+
+}  // namespace
+}  // namespace pgd
+
+extern "C" int pgd_paged_decode_attention_static(const pgd_dims* dims, const void* q,
+                                                 const void* k_pool, const void* v_pool,
+                                                 const int32_t* table, const int32_t* positions,
+                                                 const float* sinks, int32_t window, float scale,
+                                                 void* out, const pgd_decode_options* opts,
+                                                 pgd_stream_t stream) {
+  int rc = check_dims(dims);
+  if (rc != PGD_OK) return rc;
+  if (dims->rows == 0) return PGD_OK;
+  const size_t need = pgd_paged_decode_workspace_bytes(dims, opts);
+  if (need == 0) return PGD_ECUDA;
+  if (need > PGD_STATIC_SCRATCH_BYTES) return PGD_ESCRATCH_LIMIT;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PGD_ECUDA;
+  StaticScratch& sc = g_static[dev];
+  std::call_once(sc.once, [&] {
+    sc.status = cudaGetSymbolAddress(&sc.ptr, g_static_scratch);
+  });
+  if (sc.status != cudaSuccess || sc.ptr == nullptr) return PGD_ECUDA;
+  return pgd_paged_decode_attention(dims, q, k_pool, v_pool, table, positions, sinks, window,
+                                    scale, out, sc.ptr, PGD_STATIC_SCRATCH_BYTES, opts, stream);
+}

@@ -28,7 +28,8 @@ def declared_symbols():
 def test_header_declares_the_entry_points():
     assert declared_symbols() == {
         "pgd_kv_append_paged", "pgd_paged_decode_workspace_bytes", "pgd_paged_decode_attention",
-        "pgd_get_device_error", "pgd_status_string", "pgd_version"}
+        "pgd_get_device_error", "pgd_status_string", "pgd_version",
+        "pgd_paged_decode_attention_static"}
 
 
 def test_library_exports_every_declared_symbol_and_nothing_else(lib):
@@ -46,7 +47,7 @@ def test_status_strings_and_version(lib):
     import paged_gqa_decode_gb300 as pgd
     so, _ = lib
     assert so.pgd_version() >= 100
-    for code in range(7):
+    for code in range(8):
         assert pgd.status_string(code) not in ("", "unknown status")
     assert pgd.status_string(99) == "unknown status"
 
