@@ -313,7 +313,8 @@ def run_pgd(args, wl: Workload):
         pgd.paged_decode_attention(batch.q, batch.k_pool, batch.v_pool, batch.table,
                                    batch.positions, batch.sinks, wl.window, wl.scale,
                                    num_kv_heads=wl.kv_heads, out=out, workspace=ws,
-                                   pages_per_split=args.pages_per_split)
+                                   pages_per_split=args.pages_per_split,
+                                   kernel={"auto": 0, "tensor": 1, "cuda": 2}[args.kernel])
 
     for _ in range(args.warmup):
         append()
@@ -413,6 +414,7 @@ def run_pgd(args, wl: Workload):
                    "pool_gb_per_gpu": 2 * lay.num_pages * wl.kv_heads * 64 * wl.head_dim * 2 / 1e9,
                    "l2": "inputs larger than L2" if flush is None else "1 GiB L2 flush between steps",
                    "pages_per_split": args.pages_per_split or "auto",
+                   "kernel": args.kernel,
                    "parallelism": f"replicas over rows x{world}"},
         "row_tokens_per_s": total_rows / (step_ms * 1e-3),
         "pct_of_nominal_8tbs": 100.0 * value / world / NOMINAL_HBM_GBS,
@@ -444,6 +446,8 @@ def main():
     ap.add_argument("--impl", choices=["pgd", "reference"], default="pgd")
     ap.add_argument("--workload", choices=list(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--pages-per-split", type=int, default=0)
+    ap.add_argument("--kernel", choices=["auto", "tensor", "cuda"], default="auto",
+                    help="decode kernel variant (tensor-core or CUDA-core products)")
     ap.add_argument("--rows", type=int, default=0,
                     help="override the workload's row count (small profiling cases)")
     ap.add_argument("--reference-rows", type=int, default=2)

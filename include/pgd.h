@@ -86,12 +86,21 @@ typedef struct {
   int32_t layout;            /* PGD_PAGE_MAJOR or PGD_HEAD_MAJOR */
 } pgd_dims;
 
+/* Decode kernel variants.  Both compute the same function; they differ in
+ * where the per-page Q.K^T and P.V products run. */
+enum {
+  PGD_KERNEL_AUTO = 0,        /* the tensor-core kernel */
+  PGD_KERNEL_TENSOR_CORE = 1, /* mma.sync bf16 products, fp32 accumulate */
+  PGD_KERNEL_CUDA_CORE = 2    /* fp32 FMA products on the CUDA cores */
+};
+
 /* Optional tuning of the decode launch; pass NULL for the defaults.  The same
  * options must be passed to pgd_paged_decode_workspace_bytes and to
  * pgd_paged_decode_attention. */
 typedef struct {
   int32_t pages_per_split; /* pages one CTA streams; 0 = chosen from dims and
                               the device's SM count */
+  int32_t kernel;          /* PGD_KERNEL_*; 0 = auto */
 } pgd_decode_options;
 
 /*

@@ -47,8 +47,11 @@ class Dims(ctypes.Structure):
         "max_pages_per_row", "layout")]
 
 
+KERNEL_AUTO, KERNEL_TENSOR_CORE, KERNEL_CUDA_CORE = range(3)
+
+
 class DecodeOptions(ctypes.Structure):
-    _fields_ = [("pages_per_split", ctypes.c_int32)]
+    _fields_ = [("pages_per_split", ctypes.c_int32), ("kernel", ctypes.c_int32)]
 
 
 def load_library(path: str | None = None) -> ctypes.CDLL:
@@ -156,7 +159,7 @@ def kv_append_paged(k_new: torch.Tensor, v_new: torch.Tensor, table: torch.Tenso
 
 
 def paged_decode_workspace_bytes(dims: Dims, pages_per_split: int = 0) -> int:
-    opts = DecodeOptions(pages_per_split)
+    opts = DecodeOptions(pages_per_split, KERNEL_AUTO)
     return load_library().pgd_paged_decode_workspace_bytes(ctypes.byref(dims), ctypes.byref(opts))
 
 
@@ -166,6 +169,7 @@ def paged_decode_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.
                            scale: float | None = None, *, num_kv_heads: int,
                            layout: int = PAGE_MAJOR, out: torch.Tensor | None = None,
                            workspace: torch.Tensor | None = None, pages_per_split: int = 0,
+                           kernel: int = KERNEL_AUTO,
                            stream: torch.cuda.Stream | None = None) -> torch.Tensor:
     """Grouped-query decode attention of each row over its pages.
 
@@ -189,7 +193,7 @@ def paged_decode_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.
     dims = make_dims(rows=rows, num_q_heads=hq, num_kv_heads=num_kv_heads, head_dim=d,
                      num_pages=_pool_pages(k_pool, num_kv_heads, d),
                      max_pages_per_row=table.shape[1], layout=layout)
-    opts = DecodeOptions(pages_per_split)
+    opts = DecodeOptions(pages_per_split, kernel)
     lib = load_library()
     with torch.cuda.device(dev):
         if out is None:

@@ -8,8 +8,8 @@
 // A = { s : s <= n, s > n - window (window > 0) },
 //   out = sum_{s in A} e^{x_s - m} v_s / (sum_{s in A} e^{x_s - m} + e^{sink_h - m}),
 // with x_s = scale * q_h . k_s and m = max(max_s x_s, sink_h).  The sink only
-// adds to the denominator.  Scores are carried in log2 units (q is
-// pre-multiplied by scale * log2 e), so every exponential is one ex2.
+// adds to the denominator.  Scores are carried in log2 units (multiplied by
+// scale * log2 e), so every exponential is one ex2.
 //
 // Split kernel: one CTA per (split, kv head, row).  A split is a run of
 // `pages_per_split` attended pages of one row.  One producer warp streams
@@ -21,24 +21,29 @@
 // reach a stage's barrier a full phase early; the producer therefore
 // publishes the page index it last issued into each stage (stage_seq), and a
 // consumer waits for its own page index there before it waits on the stage's
-// barrier, so every parity wait targets the barrier's current phase.  Four
-// consumer warps take whole pages in turn, each keeping its own fp32
-// online-softmax state for the G heads:
-//   - scores: lane r owns tile rows r and r + 32 and forms the full dot
-//     products against q (broadcast from shared memory), so no cross-lane
-//     reduction is needed for Q.K^T;
-//   - the page's max per head is one warp-shuffle max; the denominator stays
-//     a per-lane partial until the end of the split;
-//   - P.V: the probabilities go through a per-warp shared buffer and lane l
-//     owns D/32 output dims, accumulating over the page's valid rows.
-// At the end the four warps' states are merged through shared memory.  A row
-// with one split writes its output directly (sink included); otherwise the
-// split writes (m, l, acc) to the workspace and the combine kernel merges.
+// barrier, so every parity wait targets the barrier's current phase.
+//
+// Consumer warps take whole pages in turn, each keeping its own fp32
+// online-softmax state for the group's query heads.  Two consumers:
+//   - MmaConsumer (default, group <= 8): the page's 64 x G scores are
+//     S^T = K q^T on the tensor cores (mma.sync m16n8k16, bf16 in, fp32
+//     accumulate; K fragments by ldmatrix from the swizzled tile, q as
+//     register fragments, the group padded to 8 heads), the probabilities
+//     are re-packed in registers (a bf16x2 head and residual, transposed by
+//     movmatrix) as the B operand of O^T += V^T P^T (V fragments by
+//     ldmatrix.trans), so P.V keeps fp32-level accuracy.
+//   - ScalarConsumer: the same on CUDA cores (lane r owns tile rows r and
+//     r + 32 for the scores; lane l owns D/32 output dims for P.V).
+// At the end the warps' states are merged through shared memory.  A row with
+// one split writes its output directly (sink included); otherwise the split
+// writes (m, l, acc) to the workspace and the combine kernel merges.
 //
 // Pages wholly outside the window are never visited (the split range starts
-// at the window's first page); positions outside the window or past n inside
-// a visited page are masked to -inf before the softmax and skipped in P.V, so
-// their K/V values never reach the result.
+// at the window's first page).  Positions outside the window or past n inside
+// a visited page get a -inf score before the softmax; the scalar consumer
+// skips them in P.V and the MMA consumer zeroes their V rows in shared memory
+// first (a zero weight times a non-finite stale value would otherwise leak),
+// so nothing outside the attended set reaches the result.
 #pragma once
 
 #include <math.h>
@@ -49,30 +54,427 @@
 namespace pgd {
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kBoxBytes = kPage * 64 * 2;  // one TMA box: 64 rows x 128 bytes
 
+// ------------------------------------------------------------------ tensor-core helpers
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                              uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// d += a * b for one m16n8k16 tile, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two fp32 values as a bf16x2 word (round to nearest even), `lo` in bits 0-15.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// Transpose of an 8x8 b16 matrix held one bf16x2 per lane.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA) accesses of the same bytes.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ consumers
+
+// Tensor-core consumer: one warp, whole pages, group padded to 8 heads.
+// Fragment ownership (m16n8k16): lane = 4 * gid + tig.  Score tile t covers
+// page rows 16t..16t+15; the lane holds rows 16t + gid (+8) of heads 2tig and
+// 2tig + 1.  Output tile mt covers dims 16mt..16mt+15; the lane holds dims
+// 16mt + gid (+8) of the same two heads.
+template <int D>
+struct MmaConsumer {
+  static constexpr int kHeads = 8;
+  static constexpr int kSteps = D / 16;  // k-steps of Q.K^T and dim tiles of P.V
+  static constexpr int kSharedFloats = 0;
+
+  uint32_t qb[kSteps][2];  // q^T fragments (B operand), bf16x2
+  float o[kSteps][4];      // O^T accumulators
+  float m[2], l[2];        // running max (log2 units) and per-lane denominator
+  uint32_t off_k[4], off_v[4];
+  int gid, tig;
+  float c;
+
+  __device__ static void prepare_shared(float*, const DecodeParams&, int, int, int, int) {}
+
+  __device__ void init(const DecodeParams& p, int b, int h0, int lane, const float*) {
+    gid = lane >> 2;
+    tig = lane & 3;
+    c = p.q_scale_log2;
+    const bool live = gid < p.group;
+    const uint32_t* qrow =
+        reinterpret_cast<const uint32_t*>(p.q + ((size_t)b * p.hq + h0 + (live ? gid : 0)) * D);
+#pragma unroll
+    for (int kk = 0; kk < kSteps; ++kk) {
+      qb[kk][0] = live ? qrow[(16 * kk + 2 * tig) >> 1] : 0u;
+      qb[kk][1] = live ? qrow[(16 * kk + 8 + 2 * tig) >> 1] : 0u;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[kk][e] = 0.f;
+    }
+    m[0] = m[1] = -INFINITY;
+    l[0] = l[1] = 0.f;
+    // ldmatrix row addresses: lane supplies row (lane & 7) of matrix (lane >> 3).
+    // K (no transpose): matrix j holds rows +8*(j&1), 16-byte chunk +(j>>1).
+    // V (transpose):    matrix j holds rows +8*(j>>1), chunk +(j&1).
+    // Rows are 128-byte swizzled: chunk c of row r sits at chunk c ^ (r & 7).
+    const int j = lane >> 3, r = lane & 7;
+    const uint32_t row_k = ((j & 1) * 8 + r) * 128, x_k = (j >> 1) ^ r;
+    const uint32_t row_v = ((j >> 1) * 8 + r) * 128, x_v = (j & 1) ^ r;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      off_k[i] = row_k + ((x_k ^ (2 * i)) << 4);
+      off_v[i] = row_v + ((x_v ^ (2 * i)) << 4);
+    }
+  }
+
+  // One page: kt is the shared address of its K tile, vt_ptr its V tile,
+  // valid rows [rlo, rhi].  Returns true if it wrote zeros into the V tile.
+  __device__ bool page(uint32_t kt, unsigned char* vt_ptr, int rlo, int rhi, int lane) {
+    const uint32_t vt = smem_addr(vt_ptr);
+    float s[4][4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[t][e] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < kSteps; ++kk)
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(kt + (kk >> 2) * kBoxBytes + t * 2048 + off_k[kk & 3], a0, a1, a2, a3);
+        mma_bf16(s[t], a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+      }
+
+    const bool full = rlo == 0 && rhi == kPage - 1;
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int row = 16 * t + gid + ((e & 2) ? 8 : 0);
+        const float v = s[t][e] * c;
+        s[t][e] = (full || (row >= rlo && row <= rhi)) ? v : -INFINITY;
+      }
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      mx0 = fmaxf(mx0, fmaxf(s[t][0], s[t][2]));
+      mx1 = fmaxf(mx1, fmaxf(s[t][1], s[t][3]));
+    }
+#pragma unroll
+    for (int x = 4; x < 32; x <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, x));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, x));
+    }
+    const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+    const float ref0 = mn0 == -INFINITY ? 0.f : mn0;
+    const float ref1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float al0 = exp2_approx(m[0] - ref0), al1 = exp2_approx(m[1] - ref1);
+    float sum0 = 0.f, sum1 = 0.f;
+    // P as the B operand of P.V, split into a bf16 head and a bf16 residual
+    // (p = hi + lo to ~2^-17 relative) so the products keep fp32-level
+    // accuracy: one bf16 rounding of p alone would err by up to 2^-9 of
+    // sum_j p_j |v_j|, far more than an output near cancellation allows.
+    uint32_t pb[4][2], pl[4][2];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      s[t][0] = exp2_approx(s[t][0] - ref0);
+      s[t][1] = exp2_approx(s[t][1] - ref1);
+      s[t][2] = exp2_approx(s[t][2] - ref0);
+      s[t][3] = exp2_approx(s[t][3] - ref1);
+      sum0 += s[t][0] + s[t][2];
+      sum1 += s[t][1] + s[t][3];
+      // rows gid / gid + 8 of heads (2tig, 2tig+1), transposed into the
+      // B-operand layout (rows 2tig, 2tig+1 (+8) of head gid).
+      const uint32_t h01 = pack_bf16x2(s[t][0], s[t][1]);
+      const uint32_t h23 = pack_bf16x2(s[t][2], s[t][3]);
+      const uint32_t l01 = pack_bf16x2(s[t][0] - bf16_lo(h01), s[t][1] - bf16_hi(h01));
+      const uint32_t l23 = pack_bf16x2(s[t][2] - bf16_lo(h23), s[t][3] - bf16_hi(h23));
+      pb[t][0] = movmatrix_trans(h01);
+      pb[t][1] = movmatrix_trans(h23);
+      pl[t][0] = movmatrix_trans(l01);
+      pl[t][1] = movmatrix_trans(l23);
+    }
+    l[0] = fmaf(l[0], al0, sum0);
+    l[1] = fmaf(l[1], al1, sum1);
+    m[0] = mn0;
+    m[1] = mn1;
+#pragma unroll
+    for (int mt = 0; mt < kSteps; ++mt) {
+      o[mt][0] *= al0;
+      o[mt][1] *= al1;
+      o[mt][2] *= al0;
+      o[mt][3] *= al1;
+    }
+
+    if (!full) {  // zero the V rows outside [rlo, rhi]
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int row = lane + 32 * half;
+        if (row < rlo || row > rhi) {
+#pragma unroll
+          for (int bx = 0; bx < D / 64; ++bx)
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+              *reinterpret_cast<uint4*>(vt_ptr + bx * kBoxBytes + row * 128 + ch * 16) = z;
+        }
+      }
+      __syncwarp();
+    }
+
+#pragma unroll
+    for (int mt = 0; mt < kSteps; ++mt)
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_trans(vt + (mt >> 2) * kBoxBytes + t * 2048 + off_v[mt & 3], a0, a1, a2, a3);
+        mma_bf16(o[mt], a0, a1, a2, a3, pb[t][0], pb[t][1]);
+        mma_bf16(o[mt], a0, a1, a2, a3, pl[t][0], pl[t][1]);
+      }
+    return !full;
+  }
+
+  __device__ void finish() {
+#pragma unroll
+    for (int x = 4; x < 32; x <<= 1) {
+      l[0] += __shfl_xor_sync(0xffffffffu, l[0], x);
+      l[1] += __shfl_xor_sync(0xffffffffu, l[1], x);
+    }
+  }
+
+  // red: [warps][kHeads][D + 2] = (acc[D], m, l)
+  __device__ void store(float* red, int warp, int) const {
+#pragma unroll
+    for (int mt = 0; mt < kSteps; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int head = 2 * tig + (e & 1);
+        const int dim = 16 * mt + gid + ((e & 2) ? 8 : 0);
+        red[(warp * kHeads + head) * (D + 2) + dim] = o[mt][e];
+      }
+    if (gid == 0) {
+      float* r0 = red + (warp * kHeads + 2 * tig) * (D + 2);
+      float* r1 = r0 + (D + 2);
+      r0[D] = m[0];
+      r0[D + 1] = l[0];
+      r1[D] = m[1];
+      r1[D + 1] = l[1];
+    }
+  }
+};
+
+// CUDA-core consumer for a group padded to GP heads.
 template <int D, int GP>
+struct ScalarConsumer {
+  static constexpr int kHeads = GP;
+  static constexpr int kDims = D / 32;  // output dims per lane
+  // q (fp32, scaled to log2 units) and a per-warp probability buffer
+  static constexpr int kQFloats = GP * D;
+  static constexpr int kPFloatsPerWarp = kPage * GP;
+  static constexpr int kSharedFloats = kQFloats + 4 * kPFloatsPerWarp;
+
+  float m[GP], l[GP], acc[GP][kDims];
+  const float* q_s;
+  float* pw;
+
+  __device__ static void prepare_shared(float* shared, const DecodeParams& p, int b, int h0,
+                                        int tid, int nthreads) {
+    for (int e = tid; e < GP * D; e += nthreads) {
+      const int g = e / D, d = e % D;
+      float v = 0.f;
+      if (g < p.group) {
+        const uint16_t bits = p.q[((size_t)b * p.hq + h0 + g) * D + d];
+        v = __uint_as_float((uint32_t)bits << 16) * p.q_scale_log2;
+      }
+      shared[e] = v;
+    }
+  }
+
+  __device__ void init(const DecodeParams&, int, int, int, const float* shared) {
+    q_s = shared;
+    pw = const_cast<float*>(shared) + kQFloats;
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+      m[g] = -INFINITY;
+      l[g] = 0.f;
+#pragma unroll
+      for (int j = 0; j < kDims; ++j) acc[g][j] = 0.f;
+    }
+  }
+
+  __device__ void set_warp(int warp) { pw += warp * kPFloatsPerWarp; }
+
+  __device__ bool page(uint32_t, unsigned char* kt_ptr, int rlo, int rhi, int lane) {
+    const unsigned char* kt = kt_ptr;
+    const unsigned char* vt = kt_ptr + kPage * D * 2;
+    const int r0 = lane, r1 = lane + 32;
+    const int sw = lane & 7;
+    float s0[GP], s1[GP];
+#pragma unroll
+    for (int g = 0; g < GP; ++g) s0[g] = s1[g] = 0.f;
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) {
+      const unsigned char* box = kt + (c >> 3) * kBoxBytes;
+      const int chunk = ((c & 7) ^ sw) << 4;
+      const uint4 ka = *reinterpret_cast<const uint4*>(box + r0 * 128 + chunk);
+      const uint4 kb = *reinterpret_cast<const uint4*>(box + r1 * 128 + chunk);
+      const float fa[8] = {bf16_lo(ka.x), bf16_hi(ka.x), bf16_lo(ka.y), bf16_hi(ka.y),
+                           bf16_lo(ka.z), bf16_hi(ka.z), bf16_lo(ka.w), bf16_hi(ka.w)};
+      const float fb[8] = {bf16_lo(kb.x), bf16_hi(kb.x), bf16_lo(kb.y), bf16_hi(kb.y),
+                           bf16_lo(kb.z), bf16_hi(kb.z), bf16_lo(kb.w), bf16_hi(kb.w)};
+#pragma unroll
+      for (int g = 0; g < GP; ++g) {
+        const float4 qa = *reinterpret_cast<const float4*>(q_s + g * D + c * 8);
+        const float4 qc = *reinterpret_cast<const float4*>(q_s + g * D + c * 8 + 4);
+        const float qv[8] = {qa.x, qa.y, qa.z, qa.w, qc.x, qc.y, qc.z, qc.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          s0[g] = fmaf(qv[e], fa[e], s0[g]);
+          s1[g] = fmaf(qv[e], fb[e], s1[g]);
+        }
+      }
+    }
+    const bool ok0 = r0 >= rlo && r0 <= rhi;
+    const bool ok1 = r1 >= rlo && r1 <= rhi;
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+      const float a0 = ok0 ? s0[g] : -INFINITY;
+      const float a1 = ok1 ? s1[g] : -INFINITY;
+      const float mn = fmaxf(m[g], warp_max(fmaxf(a0, a1)));
+      const float alpha = exp2_approx(m[g] - mn);
+      const float p0 = exp2_approx(a0 - mn);
+      const float p1 = exp2_approx(a1 - mn);
+      l[g] = fmaf(l[g], alpha, p0 + p1);
+#pragma unroll
+      for (int j = 0; j < kDims; ++j) acc[g][j] *= alpha;
+      m[g] = mn;
+      s0[g] = p0;
+      s1[g] = p1;
+    }
+    if constexpr (GP % 4 == 0) {
+#pragma unroll
+      for (int g = 0; g < GP; g += 4) {
+        *reinterpret_cast<float4*>(pw + r0 * GP + g) =
+            make_float4(s0[g], s0[g + 1], s0[g + 2], s0[g + 3]);
+        *reinterpret_cast<float4*>(pw + r1 * GP + g) =
+            make_float4(s1[g], s1[g + 1], s1[g + 2], s1[g + 3]);
+      }
+    } else {
+#pragma unroll
+      for (int g = 0; g < GP; ++g) {
+        pw[r0 * GP + g] = s0[g];
+        pw[r1 * GP + g] = s1[g];
+      }
+    }
+    __syncwarp();
+    for (int r = rlo; r <= rhi; ++r) {
+      float pr[GP];
+      if constexpr (GP % 4 == 0) {
+#pragma unroll
+        for (int g = 0; g < GP; g += 4) {
+          const float4 t = *reinterpret_cast<const float4*>(pw + r * GP + g);
+          pr[g] = t.x;
+          pr[g + 1] = t.y;
+          pr[g + 2] = t.z;
+          pr[g + 3] = t.w;
+        }
+      } else {
+#pragma unroll
+        for (int g = 0; g < GP; ++g) pr[g] = pw[r * GP + g];
+      }
+      float vv[kDims];
+      if constexpr (D == 64) {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(
+            vt + r * 128 + ((((lane >> 2)) ^ (r & 7)) << 4) + (lane & 3) * 4);
+        vv[0] = bf16_lo(w);
+        vv[1] = bf16_hi(w);
+      } else {
+        const int l16 = lane & 15;
+        const uint2 w = *reinterpret_cast<const uint2*>(
+            vt + (lane >> 4) * kBoxBytes + r * 128 + (((l16 >> 1) ^ (r & 7)) << 4) +
+            (l16 & 1) * 8);
+        vv[0] = bf16_lo(w.x);
+        vv[1] = bf16_hi(w.x);
+        vv[2] = bf16_lo(w.y);
+        vv[3] = bf16_hi(w.y);
+      }
+#pragma unroll
+      for (int g = 0; g < GP; ++g)
+#pragma unroll
+        for (int j = 0; j < kDims; ++j) acc[g][j] = fmaf(pr[g], vv[j], acc[g][j]);
+    }
+    return false;
+  }
+
+  __device__ void finish() {
+#pragma unroll
+    for (int g = 0; g < GP; ++g) l[g] = warp_sum(l[g]);
+  }
+
+  __device__ void store(float* red, int warp, int lane) const {
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+      float* rw = red + (warp * GP + g) * (D + 2);
+#pragma unroll
+      for (int j = 0; j < kDims; ++j) rw[lane * kDims + j] = acc[g][j];
+      if (lane == 0) {
+        rw[D] = m[g];
+        rw[D + 1] = l[g];
+      }
+    }
+  }
+};
+
+// ------------------------------------------------------------------ split kernel
+
+template <int D, int STAGES, class Consumer>
 struct DecodeCfg {
   static constexpr int kWarps = 4;  // consumer warps
   static constexpr int kThreads = (kWarps + 1) * 32;
-  static constexpr int kBoxBytes = kPage * 64 * 2;  // 64 rows x 128 bytes
   static constexpr int kBoxes = D / 64;
   static constexpr int kTileBytes = kPage * D * 2;
   static constexpr int kStageBytes = 2 * kTileBytes;  // K tile then V tile
-  static constexpr int kStages = D == 128 ? 3 : 6;
-  static constexpr int kQFloats = GP * D;
-  static constexpr int kPFloats = kWarps * kPage * GP;
-  static constexpr int kDims = D / 32;  // output dims per lane
+  static constexpr int kStages = STAGES;
+  static constexpr int kHeads = Consumer::kHeads;
   static constexpr int kSmemBytes =
-      1024 + kStages * kStageBytes + (kQFloats + kPFloats) * 4 + 2 * kStages * 8;
-  static_assert(kWarps * GP * (D + 2) * 4 <= kStages * kStageBytes, "merge buffer");
+      1024 + kStages * kStageBytes + Consumer::kSharedFloats * 4 + 2 * kStages * 8;
+  static_assert(kWarps * kHeads * (D + 2) * 4 <= kStages * kStageBytes, "merge buffer");
   static_assert(D == 64 || D == 128, "head_dim");
 };
 
-template <int D, int GP>
-__global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 2)
+template <int D, int STAGES, class Consumer>
+__global__ void __launch_bounds__(DecodeCfg<D, STAGES, Consumer>::kThreads)
     paged_decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                               const __grid_constant__ CUtensorMap v_map, const DecodeParams p) {
-  using C = DecodeCfg<D, GP>;
+  using C = DecodeCfg<D, STAGES, Consumer>;
+  constexpr int GP = C::kHeads;
   const int split = blockIdx.x;
   const int kvh = blockIdx.y;
   const int b = blockIdx.z;
@@ -83,8 +485,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 2)
   const int n = p.positions[b];
   const RowSpan span = row_span(n, p.window);
   const int nsplit = (span.pages + p.pages_per_split - 1) / p.pages_per_split;
-  if (split >= nsplit) return;                 // inactive row, or past this row's splits
-  if (n / kPage >= p.maxp) return;              // reported (and zeroed) by the combine kernel
+  if (split >= nsplit) return;     // inactive row, or past this row's splits
+  if (n / kPage >= p.maxp) return;  // reported (and zeroed) by the combine kernel
   const int page0 = span.first_page + split * p.pages_per_split;
   const int npages = min(p.pages_per_split, span.pages - split * p.pages_per_split);
   const int h0 = kvh * p.group;
@@ -93,9 +495,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 2)
   extern __shared__ unsigned char smem_raw[];
   unsigned char* stages = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* q_s = reinterpret_cast<float*>(stages + C::kStages * C::kStageBytes);
-  float* p_s = q_s + C::kQFloats;
-  uint64_t* full = reinterpret_cast<uint64_t*>(p_s + C::kPFloats);
+  float* cshared = reinterpret_cast<float*>(stages + C::kStages * C::kStageBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(cshared + Consumer::kSharedFloats);
   uint64_t* empty = full + C::kStages;
   __shared__ int abort_flag;
   __shared__ int stage_seq[C::kStages];  // page index last issued into each stage
@@ -109,9 +510,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 2)
   bad = __syncthreads_or(bad);
   if (bad) {
     if (tid == 0) record_error(p.err, PGD_EDEVICE_BOUNDS);
-    for (int e = tid; e < GP * D; e += C::kThreads) {
+    for (int e = tid; e < p.group * D; e += C::kThreads) {
       const int g = e / D, d = e % D;
-      if (g >= p.group) continue;
       const size_t bh = (size_t)b * p.hq + h0 + g;
       if (nsplit == 1) {
         p.out[bh * D + d] = 0;
@@ -136,16 +536,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 2)
     mbar_init_fence();
     abort_flag = 0;
   }
-  // q for the G heads of this kv head, scaled into log2 units; padded heads are 0.
-  for (int e = tid; e < GP * D; e += C::kThreads) {
-    const int g = e / D, d = e % D;
-    float v = 0.f;
-    if (g < p.group) {
-      const uint16_t bits = p.q[((size_t)b * p.hq + h0 + g) * D + d];
-      v = __uint_as_float((uint32_t)bits << 16) * p.q_scale_log2;
-    }
-    q_s[e] = v;
-  }
+  Consumer::prepare_shared(cshared, p, b, h0, tid, C::kThreads);
   __syncthreads();
 
   // ---------------------------------------------------------------- producer
@@ -167,8 +558,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 2)
         mbar_arrive_expect_tx(&full[s], C::kStageBytes);
 #pragma unroll
         for (int bx = 0; bx < C::kBoxes; ++bx) {
-          tma_load_2d(st + bx * C::kBoxBytes, &k_map, bx * 64, y, &full[s]);
-          tma_load_2d(st + C::kTileBytes + bx * C::kBoxBytes, &v_map, bx * 64, y, &full[s]);
+          tma_load_2d(st + bx * kBoxBytes, &k_map, bx * 64, y, &full[s]);
+          tma_load_2d(st + C::kTileBytes + bx * kBoxBytes, &v_map, bx * 64, y, &full[s]);
         }
         *reinterpret_cast<volatile int*>(&stage_seq[s]) = i;
         issued = i + 1;
@@ -181,17 +572,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 2)
   }
 
   // ---------------------------------------------------------------- consumers
-  float m[GP], l[GP], acc[GP][C::kDims];
-#pragma unroll
-  for (int g = 0; g < GP; ++g) {
-    m[g] = -INFINITY;
-    l[g] = 0.f;
-#pragma unroll
-    for (int j = 0; j < C::kDims; ++j) acc[g][j] = 0.f;
-  }
-  float* pw = p_s + warp * kPage * GP;
-  const int r0 = lane, r1 = lane + 32;
-  const int sw = lane & 7;  // swizzle phase of rows r0 and r1
+  Consumer cons;
+  cons.init(p, b, h0, lane, cshared);
+  if constexpr (Consumer::kSharedFloats > 0) cons.set_warp(warp);
 
   for (int i = warp; i < npages; i += C::kWarps) {
     const int s = i % C::kStages;
@@ -200,138 +583,32 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 2)
       abort_flag = 1;
       break;
     }
-    const unsigned char* kt = stages + s * C::kStageBytes;
-    const unsigned char* vt = kt + C::kTileBytes;
+    unsigned char* kt = stages + s * C::kStageBytes;
     const int pos0 = (page0 + i) * kPage;
     const int rlo = max(span.lo - pos0, 0);
     const int rhi = min(n - pos0, kPage - 1);
-
-    // Scores for rows r0 and r1 against the G queries.
-    float s0[GP], s1[GP];
-#pragma unroll
-    for (int g = 0; g < GP; ++g) s0[g] = s1[g] = 0.f;
-#pragma unroll
-    for (int c = 0; c < D / 8; ++c) {
-      const unsigned char* box = kt + (c >> 3) * C::kBoxBytes;
-      const int chunk = ((c & 7) ^ sw) << 4;
-      const uint4 ka = *reinterpret_cast<const uint4*>(box + r0 * 128 + chunk);
-      const uint4 kb = *reinterpret_cast<const uint4*>(box + r1 * 128 + chunk);
-      const float fa[8] = {bf16_lo(ka.x), bf16_hi(ka.x), bf16_lo(ka.y), bf16_hi(ka.y),
-                           bf16_lo(ka.z), bf16_hi(ka.z), bf16_lo(ka.w), bf16_hi(ka.w)};
-      const float fb[8] = {bf16_lo(kb.x), bf16_hi(kb.x), bf16_lo(kb.y), bf16_hi(kb.y),
-                           bf16_lo(kb.z), bf16_hi(kb.z), bf16_lo(kb.w), bf16_hi(kb.w)};
-#pragma unroll
-      for (int g = 0; g < GP; ++g) {
-        const float4 qa = *reinterpret_cast<const float4*>(q_s + g * D + c * 8);
-        const float4 qb = *reinterpret_cast<const float4*>(q_s + g * D + c * 8 + 4);
-        const float qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          s0[g] = fmaf(qv[e], fa[e], s0[g]);
-          s1[g] = fmaf(qv[e], fb[e], s1[g]);
-        }
-      }
-    }
-    const bool ok0 = r0 >= rlo && r0 <= rhi;
-    const bool ok1 = r1 >= rlo && r1 <= rhi;
-
-    // Online softmax over this page (every visited page has a valid row, so
-    // the new running max is finite).
-#pragma unroll
-    for (int g = 0; g < GP; ++g) {
-      const float a0 = ok0 ? s0[g] : -INFINITY;
-      const float a1 = ok1 ? s1[g] : -INFINITY;
-      const float mn = fmaxf(m[g], warp_max(fmaxf(a0, a1)));
-      const float alpha = exp2_approx(m[g] - mn);
-      const float p0 = exp2_approx(a0 - mn);
-      const float p1 = exp2_approx(a1 - mn);
-      l[g] = fmaf(l[g], alpha, p0 + p1);
-#pragma unroll
-      for (int j = 0; j < C::kDims; ++j) acc[g][j] *= alpha;
-      m[g] = mn;
-      s0[g] = p0;
-      s1[g] = p1;
-    }
-    if constexpr (GP % 4 == 0) {
-#pragma unroll
-      for (int g = 0; g < GP; g += 4) {
-        *reinterpret_cast<float4*>(pw + r0 * GP + g) = make_float4(s0[g], s0[g + 1], s0[g + 2], s0[g + 3]);
-        *reinterpret_cast<float4*>(pw + r1 * GP + g) = make_float4(s1[g], s1[g + 1], s1[g + 2], s1[g + 3]);
-      }
-    } else {
-#pragma unroll
-      for (int g = 0; g < GP; ++g) {
-        pw[r0 * GP + g] = s0[g];
-        pw[r1 * GP + g] = s1[g];
-      }
-    }
-    __syncwarp();
-
-    // P.V over the page's valid rows; lane owns dims [kDims*lane, kDims*(lane+1)).
-    for (int r = rlo; r <= rhi; ++r) {
-      float pr[GP];
-      if constexpr (GP % 4 == 0) {
-#pragma unroll
-        for (int g = 0; g < GP; g += 4) {
-          const float4 t = *reinterpret_cast<const float4*>(pw + r * GP + g);
-          pr[g] = t.x;
-          pr[g + 1] = t.y;
-          pr[g + 2] = t.z;
-          pr[g + 3] = t.w;
-        }
-      } else {
-#pragma unroll
-        for (int g = 0; g < GP; ++g) pr[g] = pw[r * GP + g];
-      }
-      float vv[C::kDims];
-      if constexpr (D == 64) {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(
-            vt + r * 128 + ((((lane >> 2)) ^ (r & 7)) << 4) + (lane & 3) * 4);
-        vv[0] = bf16_lo(w);
-        vv[1] = bf16_hi(w);
-      } else {
-        const int l16 = lane & 15;
-        const uint2 w = *reinterpret_cast<const uint2*>(
-            vt + (lane >> 4) * C::kBoxBytes + r * 128 + (((l16 >> 1) ^ (r & 7)) << 4) +
-            (l16 & 1) * 8);
-        vv[0] = bf16_lo(w.x);
-        vv[1] = bf16_hi(w.x);
-        vv[2] = bf16_lo(w.y);
-        vv[3] = bf16_hi(w.y);
-      }
-#pragma unroll
-      for (int g = 0; g < GP; ++g)
-#pragma unroll
-        for (int j = 0; j < C::kDims; ++j) acc[g][j] = fmaf(pr[g], vv[j], acc[g][j]);
-    }
+    bool wrote;
+    if constexpr (Consumer::kSharedFloats > 0)
+      wrote = cons.page(0u, kt, rlo, rhi, lane);
+    else
+      wrote = cons.page(smem_addr(kt), kt + C::kTileBytes, rlo, rhi, lane);
+    if (wrote) fence_proxy_async_shared();
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
   }
-
-#pragma unroll
-  for (int g = 0; g < GP; ++g) l[g] = warp_sum(l[g]);
+  cons.finish();
 
   constexpr int kConsumers = C::kWarps * 32;
   named_sync(1, kConsumers);  // all pages consumed; the stages are free
   if (abort_flag) return;
 
-  // Merge the four warps' states through shared memory (aliasing the stages).
+  // Merge the warps' states through shared memory (aliasing the stages).
   float* red = reinterpret_cast<float*>(stages);  // [kWarps][GP][D + 2]
-#pragma unroll
-  for (int g = 0; g < GP; ++g) {
-    float* rw = red + (warp * GP + g) * (D + 2);
-#pragma unroll
-    for (int j = 0; j < C::kDims; ++j) rw[lane * C::kDims + j] = acc[g][j];
-    if (lane == 0) {
-      rw[D] = m[g];
-      rw[D + 1] = l[g];
-    }
-  }
+  cons.store(red, warp, lane);
   named_sync(1, kConsumers);
 
-  for (int e = tid; e < GP * D; e += kConsumers) {
+  for (int e = tid; e < p.group * D; e += kConsumers) {
     const int g = e / D, d = e % D;
-    if (g >= p.group) continue;
     float mx = -INFINITY;
 #pragma unroll
     for (int w = 0; w < C::kWarps; ++w) mx = fmaxf(mx, red[(w * GP + g) * (D + 2) + D]);
@@ -426,23 +703,42 @@ __global__ void __launch_bounds__(128) paged_decode_combine_kernel(const DecodeP
   for (int j = 0; j < kDims; ++j) o[j] = __bfloat16_as_ushort(__float2bfloat16_rn(res[j] * inv));
 }
 
-template <int D, int GP>
+template <int D, int STAGES, class Consumer>
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& k_map,
                           const CUtensorMap& v_map, int grid_splits, cudaStream_t stream) {
-  using C = DecodeCfg<D, GP>;
+  using C = DecodeCfg<D, STAGES, Consumer>;
   static_assert(C::kSmemBytes <= 227 * 1024, "shared memory");
-  cudaError_t e = cudaFuncSetAttribute(paged_decode_split_kernel<D, GP>,
+  cudaError_t e = cudaFuncSetAttribute(paged_decode_split_kernel<D, STAGES, Consumer>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
   if (p.rows == 0) return cudaSuccess;
   dim3 grid(grid_splits, p.hkv, p.rows);
-  paged_decode_split_kernel<D, GP><<<grid, C::kThreads, C::kSmemBytes, stream>>>(k_map, v_map, p);
+  paged_decode_split_kernel<D, STAGES, Consumer>
+      <<<grid, C::kThreads, C::kSmemBytes, stream>>>(k_map, v_map, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   dim3 cgrid((p.hq + 3) / 4, p.rows);
   paged_decode_combine_kernel<D><<<cgrid, 128, 0, stream>>>(p);
   return cudaGetLastError();
+}
+
+// Kernel choice for one head_dim: the tensor-core consumer unless the caller
+// asks for the CUDA-core one.
+template <int D>
+cudaError_t launch_decode_for_dim(const DecodeParams& p, const CUtensorMap& k_map,
+                                  const CUtensorMap& v_map, int padded, int kernel,
+                                  int grid_splits, cudaStream_t stream) {
+  constexpr int kStages = D == 128 ? 3 : 6;
+  if (kernel != PGD_KERNEL_CUDA_CORE)
+    return launch_decode<D, kStages, MmaConsumer<D>>(p, k_map, v_map, grid_splits, stream);
+  switch (padded) {
+    case 1: return launch_decode<D, kStages, ScalarConsumer<D, 1>>(p, k_map, v_map, grid_splits, stream);
+    case 2: return launch_decode<D, kStages, ScalarConsumer<D, 2>>(p, k_map, v_map, grid_splits, stream);
+    case 4: return launch_decode<D, kStages, ScalarConsumer<D, 4>>(p, k_map, v_map, grid_splits, stream);
+    case 8: return launch_decode<D, kStages, ScalarConsumer<D, 8>>(p, k_map, v_map, grid_splits, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace pgd

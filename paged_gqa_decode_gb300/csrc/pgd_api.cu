@@ -226,9 +226,12 @@ int pgd_paged_decode_attention(const pgd_dims* dims, const void* q, const void* 
   const int grid_splits = (grid_pages + pl.pages_per_split - 1) / pl.pages_per_split;
 
   const int padded = padded_group(p.group);
+  const int kernel = opts ? opts->kernel : PGD_KERNEL_AUTO;
+  if (kernel < PGD_KERNEL_AUTO || kernel > PGD_KERNEL_CUDA_CORE) return PGD_EINVAL;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = dims->head_dim == 64 ? launch_decode_d64(p, k_map, v_map, padded, grid_splits, st)
-                                       : launch_decode_d128(p, k_map, v_map, padded, grid_splits, st);
+  cudaError_t e =
+      dims->head_dim == 64 ? launch_decode_d64(p, k_map, v_map, padded, kernel, grid_splits, st)
+                           : launch_decode_d128(p, k_map, v_map, padded, kernel, grid_splits, st);
   return e == cudaSuccess ? PGD_OK : PGD_ECUDA;
 }
 

@@ -41,12 +41,13 @@ int padded_group(int group);  // 0 if unsupported
 
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
 
-// Split kernel + combine kernel for one (head_dim, padded group).
+// Split kernel + combine kernel for one head_dim; `padded` is the padded
+// group size, `kernel` a PGD_KERNEL_* choice.
 cudaError_t launch_decode_d64(const DecodeParams& p, const CUtensorMap& k_map,
-                              const CUtensorMap& v_map, int padded, int grid_splits,
+                              const CUtensorMap& v_map, int padded, int kernel, int grid_splits,
                               cudaStream_t stream);
 cudaError_t launch_decode_d128(const DecodeParams& p, const CUtensorMap& k_map,
-                               const CUtensorMap& v_map, int padded, int grid_splits,
+                               const CUtensorMap& v_map, int padded, int kernel, int grid_splits,
                                cudaStream_t stream);
 
 }  // namespace pgd

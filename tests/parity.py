@@ -18,14 +18,14 @@ REL_FLOOR = 1e-3
 
 
 def gpu_step(batch: Batch, *, window: int, sinks, scale: float, layout: int = pgd.PAGE_MAJOR,
-             pages_per_split: int = 0) -> torch.Tensor:
+             pages_per_split: int = 0, kernel: int = pgd.KERNEL_AUTO) -> torch.Tensor:
     wl = batch.wl
     pgd.kv_append_paged(batch.k_new, batch.v_new, batch.table, batch.positions, batch.k_pool,
                         batch.v_pool, layout=layout)
     out = pgd.paged_decode_attention(batch.q, batch.k_pool, batch.v_pool, batch.table,
                                      batch.positions, sinks, window, scale,
                                      num_kv_heads=wl.kv_heads, layout=layout,
-                                     pages_per_split=pages_per_split)
+                                     pages_per_split=pages_per_split, kernel=kernel)
     status = pgd.get_device_error()
     assert status == pgd.OK, pgd.status_string(status)
     return out

@@ -34,14 +34,14 @@ def _built():
 
 
 def run_and_check(batch, *, window=None, sinks="batch", layout=pgd.PAGE_MAJOR, rows=None,
-                  pages_per_split=0, what=""):
+                  pages_per_split=0, kernel=pgd.KERNEL_AUTO, what=""):
     wl = batch.wl
     window = wl.window if window is None else window
     sinks = batch.sinks if isinstance(sinks, str) else sinks
     rows = np.arange(len(batch.layout.positions)) if rows is None else np.asarray(rows)
     host = snapshot_rows(batch, rows, layout)
     got = gpu_step(batch, window=window, sinks=sinks, scale=wl.scale, layout=layout,
-                   pages_per_split=pages_per_split)
+                   pages_per_split=pages_per_split, kernel=kernel)
     want, _, _ = oracle_step(batch, host, window=window, sinks=sinks, scale=wl.scale,
                              layout=layout)
     idx = torch.as_tensor(rows, device=got.device)
@@ -113,6 +113,27 @@ def test_edge_contexts_windows_groups(hq, hkv, d, window):
     lay = layout_from_contexts(wl, EDGE_CONTEXTS, seed=hq + d + window)
     batch = make_batch(wl, seed=31 + window, device=DEV, layout=lay)
     run_and_check(batch, window=window, what=f"edge hq={hq} hkv={hkv} d={d} w={window}")
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(14, 2, 64), (64, 8, 64), (32, 8, 128), (8, 8, 128),
+                                      (6, 3, 64)])
+@pytest.mark.parametrize("window", [0, 65])
+def test_cuda_core_kernel(hq, hkv, d, window):
+    """The CUDA-core variant of the split kernel (selectable through the
+    decode options) against the oracle on the edge contexts."""
+    wl = Workload("edge_cc", rows=len(EDGE_CONTEXTS), q_heads=hq, kv_heads=hkv, head_dim=d,
+                  ctx_lo=1, ctx_hi=700, sinks=True)
+    lay = layout_from_contexts(wl, EDGE_CONTEXTS, seed=hq + d + window + 1)
+    batch = make_batch(wl, seed=37 + window, device=DEV, layout=lay)
+    run_and_check(batch, window=window, kernel=pgd.KERNEL_CUDA_CORE, pages_per_split=2,
+                  what=f"cuda-core hq={hq} d={d} w={window}")
+
+
+@pytest.mark.parametrize("name", ["gptoss_full", "qwen_serve"])
+def test_cuda_core_kernel_workloads(name):
+    wl = WORKLOADS[name]
+    batch = make_batch(wl, seed=1000 + list(WORKLOADS).index(name), device=DEV)
+    run_and_check(batch, kernel=pgd.KERNEL_CUDA_CORE)
 
 
 @pytest.mark.parametrize("kind", ["none", "minus_inf", "huge", "mixed"])
