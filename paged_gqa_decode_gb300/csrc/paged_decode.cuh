@@ -48,6 +48,8 @@
 
 #include <math.h>
 
+#include <atomic>
+
 #include "pgd_device.cuh"
 #include "pgd_internal.h"
 
@@ -708,10 +710,17 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& k_map,
                           const CUtensorMap& v_map, int grid_splits, cudaStream_t stream) {
   using C = DecodeCfg<D, STAGES, Consumer>;
   static_assert(C::kSmemBytes <= 227 * 1024, "shared memory");
-  cudaError_t e = cudaFuncSetAttribute(paged_decode_split_kernel<D, STAGES, Consumer>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::kSmemBytes);
+  // The shared-memory opt-in is per device; set it once on each.
+  static std::atomic<bool> configured[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(paged_decode_split_kernel<D, STAGES, Consumer>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured[dev].store(true, std::memory_order_release);
+  }
   if (p.rows == 0) return cudaSuccess;
   dim3 grid(grid_splits, p.hkv, p.rows);
   paged_decode_split_kernel<D, STAGES, Consumer>

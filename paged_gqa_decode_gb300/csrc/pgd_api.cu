@@ -94,7 +94,46 @@ size_t workspace_bytes(const pgd_dims* d, const Plan& pl) {
   return (size_t)d->rows * d->num_q_heads * pl.max_splits * (d->head_dim + 2) * sizeof(float);
 }
 
+int encode_pool_map_uncached(CUtensorMap* map, const void* pool, const pgd_dims* d);
+
+// Encoded pool descriptors are reused while the same pool is passed again: a
+// small per-process cache keyed by (device, address, pages, kv heads, dim).
+struct MapEntry {
+  int dev;
+  const void* pool;
+  int32_t num_pages, kv_heads, head_dim;
+  CUtensorMap map;
+};
+constexpr int kMapCache = 16;
+MapEntry g_maps[kMapCache];
+int g_map_count = 0, g_map_next = 0;
+std::mutex g_map_mutex;
+
 int encode_pool_map(CUtensorMap* map, const void* pool, const pgd_dims* d) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PGD_ECUDA;
+  {
+    std::lock_guard<std::mutex> lock(g_map_mutex);
+    for (int i = 0; i < g_map_count; ++i) {
+      const MapEntry& m = g_maps[i];
+      if (m.dev == dev && m.pool == pool && m.num_pages == d->num_pages &&
+          m.kv_heads == d->num_kv_heads && m.head_dim == d->head_dim) {
+        *map = m.map;
+        return PGD_OK;
+      }
+    }
+  }
+  const int rc = encode_pool_map_uncached(map, pool, d);
+  if (rc != PGD_OK) return rc;
+  std::lock_guard<std::mutex> lock(g_map_mutex);
+  MapEntry& slot = g_maps[g_map_next];
+  slot = MapEntry{dev, pool, d->num_pages, d->num_kv_heads, d->head_dim, *map};
+  g_map_next = (g_map_next + 1) % kMapCache;
+  if (g_map_count < kMapCache) ++g_map_count;
+  return PGD_OK;
+}
+
+int encode_pool_map_uncached(CUtensorMap* map, const void* pool, const pgd_dims* d) {
   std::call_once(g_encode_once, [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
