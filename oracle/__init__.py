@@ -63,8 +63,10 @@ def _load():
                                             p, p, p, i]
             lib.orc_decode_paged.argtypes = [i, i, i, i, i, i, i, i, p, p, p, p, p, p, i,
                                              ctypes.c_float, p, p, p, i]
+            lib.orc_prefill_paged.argtypes = [i, i, i, i, i, i, i, i, i, p, p, p, p, p, p, p,
+                                              i, ctypes.c_float, p, p, p, i]
             for fn in (lib.orc_page_slots, lib.orc_write_tokens, lib.orc_decode_rows,
-                       lib.orc_decode_paged):
+                       lib.orc_decode_paged, lib.orc_prefill_paged):
                 fn.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -163,4 +165,36 @@ def decode_paged(q, k_pool, v_pool, table, positions, *, kv_heads, page_size=64,
                                     _ptr(positions), _ptr(sinks), int(window), float(scale),
                                     _ptr(out), _ptr(lse), _ptr(lse_real),
                                     nthreads or default_threads()), "decode_paged")
+    return out, lse, lse_real
+
+
+def prefill_paged(q, k_pool, v_pool, table, rows, positions, *, kv_heads, page_size=64,
+                  num_pages, layout=PAGE_MAJOR, sinks=None, window=0, scale=None,
+                  nthreads=None):
+    """Paged prefill: token p (q uint16 [P, Hq, D]) attends over the pages of
+    table row rows[p] up to positions[p], within the window, sink in the
+    denominator.  Returns (out [P, Hq, D], lse [P, Hq], lse_real [P, Hq])."""
+    q = _c(q, np.uint16)
+    k_pool = _c(k_pool, np.uint16)
+    v_pool = _c(v_pool, np.uint16)
+    table = _c(table, np.int32)
+    rows = _c(rows, np.int32)
+    positions = _c(positions, np.int32)
+    sinks = None if sinks is None else _c(sinks, np.float32)
+    tokens, hq, d = q.shape
+    table_rows, max_pages = table.shape
+    if scale is None:
+        scale = 1.0 / float(np.sqrt(d))
+    expect = num_pages * kv_heads * page_size * d
+    if k_pool.size != expect or v_pool.size != expect:
+        raise ValueError(f"pool holds {k_pool.size} values, layout needs {expect}")
+    out = np.empty((tokens, hq, d), dtype=np.float64)
+    lse = np.empty((tokens, hq), dtype=np.float64)
+    lse_real = np.empty((tokens, hq), dtype=np.float64)
+    _check(_load().orc_prefill_paged(tokens, hq, kv_heads, d, page_size, num_pages, table_rows,
+                                     max_pages, layout, _ptr(q), _ptr(k_pool), _ptr(v_pool),
+                                     _ptr(table), _ptr(rows), _ptr(positions), _ptr(sinks),
+                                     int(window), float(scale), _ptr(out), _ptr(lse),
+                                     _ptr(lse_real), nthreads or default_threads()),
+           "prefill_paged")
     return out, lse, lse_real

@@ -26,6 +26,11 @@
  *  - GPT-OSS 20B, README (grouping of sink_attention): query heads are
  *    grouped by the key/value head they share, [B, KvHeads, G, Q, D], so
  *    query head h reads key/value head h / G.
+ *  - Mistral 7B Instruct v0.3, src/attention.linnet, prefill_paged and the
+ *    model's prefill_paged entry: packed prompt tokens are written at the
+ *    caller's slots, and token p attends over its row's pages
+ *    (table[rows[p]]) up to its position; GPT-OSS 20B, prefill_packed: the
+ *    same window and sinks apply to prompt tokens.
  *
  * Readings where the pages leave a step open (each also listed in the
  * design notes):
@@ -195,6 +200,9 @@ typedef struct {
   /* paged source */
   int paged, max_pages, page_size, num_pages, layout;
   const int32_t* table;
+  /* prefill: token b reads table row row_of[b] (of table_rows); NULL: row b */
+  const int32_t* row_of;
+  int table_rows;
   const uint16_t *k_pool, *v_pool;
   /* work distribution */
   int nthreads, thread;
@@ -217,6 +225,11 @@ static int run_row(job_t* job, int b) {
   uint16_t *k_buf = NULL, *v_buf = NULL;
   int64_t stride;
   if (job->paged) {
+    int trow = b;
+    if (job->row_of) {
+      trow = job->row_of[b];
+      if (trow < 0 || trow >= job->table_rows) return ORC_ERANGE;
+    }
     size_t count = (size_t)job->kv_heads * (size_t)(n + 1) * (size_t)d_head;
     k_buf = (uint16_t*)malloc(count * sizeof(uint16_t));
     v_buf = (uint16_t*)malloc(count * sizeof(uint16_t));
@@ -225,10 +238,10 @@ static int run_row(job_t* job, int b) {
       free(v_buf);
       return ORC_ENOMEM;
     }
-    int rc = gather_row(b, n, job->max_pages, job->kv_heads, d_head, job->page_size,
+    int rc = gather_row(trow, n, job->max_pages, job->kv_heads, d_head, job->page_size,
                         job->num_pages, job->layout, job->table, job->k_pool, k_buf);
     if (rc == ORC_OK)
-      rc = gather_row(b, n, job->max_pages, job->kv_heads, d_head, job->page_size,
+      rc = gather_row(trow, n, job->max_pages, job->kv_heads, d_head, job->page_size,
                       job->num_pages, job->layout, job->table, job->v_pool, v_buf);
     if (rc != ORC_OK) {
       free(k_buf);
@@ -378,5 +391,51 @@ int orc_decode_paged(int rows, int q_heads, int kv_heads, int head_dim, int page
   job.table = table;
   job.k_pool = k_pool;
   job.v_pool = v_pool;
+  return run_job(&job, nthreads);
+}
+
+/* Paged prefill (prefill_paged / paged_prefill_attention): P packed tokens;
+ * token p is position positions[p] of the request in table row rows[p]
+ * (table has table_rows rows of max_pages entries).  Its key and value were
+ * written at its slot beforehand (orc_write_tokens with the caller's
+ * slots), and its query attends over its row's pages up to and including
+ * its own position, within the window, with the sink in the denominator:
+ * exactly a decode step of row rows[p] at position positions[p].
+ *   q [P][q_heads][head_dim] bf16; out [P][q_heads][head_dim] double. */
+int orc_prefill_paged(int tokens, int q_heads, int kv_heads, int head_dim, int page_size,
+                      int num_pages, int table_rows, int max_pages, int layout,
+                      const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                      const int32_t* table, const int32_t* rows, const int32_t* positions,
+                      const float* sinks, int window, float scale, double* out, double* lse,
+                      double* lse_real, int nthreads) {
+  int rc = check_heads(tokens, q_heads, kv_heads, head_dim);
+  if (rc != ORC_OK) return rc;
+  if (page_size <= 0 || num_pages <= 0 || max_pages <= 0 || table_rows <= 0 || !rows)
+    return ORC_EINVAL;
+  if (layout != ORC_PAGE_MAJOR && layout != ORC_HEAD_MAJOR) return ORC_EINVAL;
+  job_t job;
+  memset(&job, 0, sizeof job);
+  job.rows = tokens;
+  job.q_heads = q_heads;
+  job.kv_heads = kv_heads;
+  job.head_dim = head_dim;
+  job.window = window;
+  job.scale = (double)scale;
+  job.q = q;
+  job.positions = positions;
+  job.sinks = sinks;
+  job.out = out;
+  job.lse = lse;
+  job.lse_real = lse_real;
+  job.paged = 1;
+  job.max_pages = max_pages;
+  job.page_size = page_size;
+  job.num_pages = num_pages;
+  job.layout = layout;
+  job.table = table;
+  job.k_pool = k_pool;
+  job.v_pool = v_pool;
+  job.row_of = rows;
+  job.table_rows = table_rows;
   return run_job(&job, nthreads);
 }

@@ -29,6 +29,7 @@ MUTANTS = {
     "page_major_heads_swapped": (
         "return ((page * kv_heads + kv_head) * page_size + in_page) * head_dim + d;",
         "return ((kv_head * kv_heads + page) * page_size + in_page) * head_dim + d;"),
+    "prefill_row_ignored": ("      trow = job->row_of[b];", "      trow = b;"),
     "value_from_key": ("const uint16_t* vj = v + (int64_t)(lo + j) * head_dim;",
                        "const uint16_t* vj = k + (int64_t)(lo + j) * head_dim;"),
 }

@@ -422,3 +422,115 @@ def test_append_skips_inactive_rows():
     tiles = pool.reshape(2, 64, 4)
     assert not tiles[0].any()
     assert (tiles[1, 5] == 0x3F80).all() and tiles[1].sum() == 4 * 0x3F80
+
+
+# ---------------------------------------------------------------------------
+# Paged prefill: packed prompt tokens, each a decode step of its own row.
+
+
+def _prefill_setup(seed, rows, hq, hkv, d, pages_per_row, page=64):
+    """A pool built by pure reshape from contiguous per-row caches (row b owns
+    pages b*k .. b*k+k-1, identity table)."""
+    length = pages_per_row * page
+    q_dummy, k, v, sinks = _contiguous_case(seed, rows, hq, hkv, d, length)
+    k_pool, per_row = _identity_page_major_pool(k, page)
+    v_pool, _ = _identity_page_major_pool(v, page)
+    table = np.arange(rows * per_row, dtype=np.int32).reshape(rows, per_row)
+    return k, v, sinks, k_pool, v_pool, table
+
+
+def test_prefill_one_token_per_row_is_decode():
+    rows, hq, hkv, d = 3, 8, 2, 16
+    k, v, sinks, k_pool, v_pool, table = _prefill_setup(20, rows, hq, hkv, d, 3)
+    gen = torch.Generator().manual_seed(21)
+    q = rand_bf16(gen, rows, hq, d)
+    positions = np.array([191, 70, 0], dtype=np.int32)
+    geo = dict(kv_heads=hkv, page_size=64, num_pages=table.size, sinks=sinks, window=40)
+    want = oracle.decode_paged(q, k_pool, v_pool, table, positions, **geo)
+    got = oracle.prefill_paged(q, k_pool, v_pool, table, np.arange(rows, dtype=np.int32),
+                               positions, **geo)
+    for a, b in zip(got, want):
+        np.testing.assert_array_equal(a, b)
+    # tokens may name rows in any order; each follows its own row's pages
+    perm = np.array([2, 0, 1], dtype=np.int32)
+    got = oracle.prefill_paged(q[perm], k_pool, v_pool, table, perm, positions[perm], **geo)
+    np.testing.assert_array_equal(got[0], want[0][perm])
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (4, 4)])
+def test_prefill_whole_prompt_equals_causal_sdpa(hq, hkv):
+    """A prompt of L tokens at positions 0..L-1 of one row, no sink and no
+    window: plain causal attention, checked against the library routine
+    with KV replicated per head."""
+    d, L = 16, 150
+    k, v, _, k_pool, v_pool, table = _prefill_setup(22, 1, hq, hkv, d, 3)
+    gen = torch.Generator().manual_seed(23)
+    q = rand_bf16(gen, L, hq, d)
+    positions = np.arange(L, dtype=np.int32)
+    scale = 0.25
+    out, _, _ = oracle.prefill_paged(q, k_pool, v_pool, table, np.zeros(L, dtype=np.int32),
+                                     positions, kv_heads=hkv, num_pages=table.size, scale=scale)
+    qt = torch.from_numpy(as_float(q)).permute(1, 0, 2)                  # [Hq, L, D]
+    kt = torch.from_numpy(as_float(k[0, :, :L])).repeat_interleave(hq // hkv, dim=0)
+    vt = torch.from_numpy(as_float(v[0, :, :L])).repeat_interleave(hq // hkv, dim=0)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, is_causal=True,
+                                                           scale=scale)
+    np.testing.assert_allclose(out, ref.permute(1, 0, 2).numpy(), rtol=1e-12, atol=1e-13)
+
+
+def test_prefill_with_sink_and_window_equals_k_plus_one_column():
+    rows, hq, hkv, d = 2, 6, 2, 8
+    k, v, sinks, k_pool, v_pool, table = _prefill_setup(24, rows, hq, hkv, d, 2)
+    gen = torch.Generator().manual_seed(25)
+    tokens = 12
+    q = rand_bf16(gen, tokens, hq, d)
+    token_rows = np.array([0] * 6 + [1] * 6, dtype=np.int32)
+    positions = np.array([60, 61, 62, 63, 64, 65, 0, 1, 2, 100, 101, 127], dtype=np.int32)
+    window, scale = 5, 0.375
+    out, _, _ = oracle.prefill_paged(q, k_pool, v_pool, table, token_rows, positions,
+                                     kv_heads=hkv, num_pages=table.size, sinks=sinks,
+                                     window=window, scale=scale)
+    for p in range(tokens):
+        r = token_rows[p]
+        for h in range(hq):
+            want = brute_force_k_plus_one(q[p, h], k[r, h // (hq // hkv)], v[r, h // (hq // hkv)],
+                                          int(positions[p]), window, scale, float(sinks[h]))
+            np.testing.assert_allclose(out[p, h], want, rtol=1e-12, atol=1e-14)
+
+
+def test_prefill_in_chunks_equals_one_pass():
+    """Writing a prompt's K/V and attending in two chunks gives the second
+    chunk the same result as one pass over the whole prompt."""
+    hq, hkv, d, L, cut = 4, 2, 8, 100, 37
+    gen = torch.Generator().manual_seed(26)
+    q = rand_bf16(gen, L, hq, d)
+    kv_k = rand_bf16(gen, L, hkv, d)
+    kv_v = rand_bf16(gen, L, hkv, d)
+    num_pages = 4
+    order = np.array([3, 0, 2, 1], dtype=np.int32)
+    table = order[None, :2].copy()
+    geo = dict(kv_heads=hkv, head_dim=d, page_size=64, num_pages=num_pages)
+
+    def run(chunks):
+        kp = np.zeros(num_pages * hkv * 64 * d, dtype=np.uint16)
+        vp = np.zeros_like(kp)
+        outs = []
+        for lo, hi in chunks:
+            pos = np.arange(lo, hi, dtype=np.int32)
+            rows = np.zeros(hi - lo, dtype=np.int32)
+            slots = np.array([table[0, s // 64] * 64 + s % 64 for s in pos], dtype=np.int64)
+            oracle.write_tokens(kp, kv_k[lo:hi], slots, **geo)
+            oracle.write_tokens(vp, kv_v[lo:hi], slots, **geo)
+            outs.append(oracle.prefill_paged(q[lo:hi], kp, vp, table, rows, pos, kv_heads=hkv,
+                                             num_pages=num_pages)[0])
+        return np.concatenate(outs)
+
+    np.testing.assert_array_equal(run([(0, cut), (cut, L)]), run([(0, L)]))
+
+
+def test_prefill_rejects_rows_outside_the_table():
+    k, v, sinks, k_pool, v_pool, table = _prefill_setup(27, 2, 4, 2, 8, 1)
+    q = np.zeros((1, 4, 8), dtype=np.uint16)
+    with pytest.raises(ValueError):
+        oracle.prefill_paged(q, k_pool, v_pool, table, np.array([2], dtype=np.int32),
+                             np.array([3], dtype=np.int32), kv_heads=2, num_pages=table.size)
