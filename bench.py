@@ -461,13 +461,116 @@ def run_pgd(args, wl: Workload):
     print(json.dumps(line), flush=True)
 
 
+def prefill_work(wl, b) -> dict:
+    """Algorithmic work of one prefill step.  Bytes: per row, the K/V of the
+    union of its tokens' attended positions, read once; q read, out written;
+    the tokens' K/V read and written into the pool.  FLOPs: per token and
+    query head, 2 * D for each attended key in Q.K^T and again in P.V."""
+    pos = b.positions_np.astype(np.int64)
+    lo = np.maximum(pos - wl.window + 1, 0) if wl.window > 0 else np.zeros_like(pos)
+    attended = pos - lo + 1
+    row_bytes = 2 * wl.kv_heads * wl.head_dim * 2
+    kv = 0
+    for r in np.unique(b.rows_np):
+        sel = b.rows_np == r
+        kv += int(pos[sel].max() - lo[sel].min() + 1) * row_bytes
+    tokens = len(pos)
+    q_out = 2 * tokens * wl.q_heads * wl.head_dim * 2
+    writes = 2 * tokens * row_bytes
+    flops = int(attended.sum()) * wl.q_heads * wl.head_dim * 4
+    return {"kv": kv, "q_out": q_out, "writes": writes, "bytes": kv + q_out + writes,
+            "flops": flops, "tokens": tokens}
+
+
+def measured_tensor_peak() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
+def run_prefill(args, wl):
+    """Prefill step: page_slots + kv_write_slots + paged_prefill_attention over
+    the packed chunks (one GPU)."""
+    import paged_gqa_decode_gb300 as pgd
+    from pgd_inputs import PREFILL_WORKLOADS, make_prefill_batch
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    b = make_prefill_batch(wl, 2000 + list(PREFILL_WORKLOADS).index(wl.name), device)
+    work = prefill_work(wl, b)
+    opts = dict(num_kv_heads=wl.kv_heads, pages_per_split=args.pages_per_split,
+                kernel={"auto": 0, "tensor": 1, "cuda": 2}[args.kernel])
+    out = torch.empty_like(b.q)
+    dims = pgd.make_dims(rows=work["tokens"], num_q_heads=wl.q_heads, num_kv_heads=wl.kv_heads,
+                         head_dim=wl.head_dim, num_pages=b.num_pages,
+                         max_pages_per_row=b.table.shape[1])
+    ws = torch.empty(max(16, pgd.paged_decode_workspace_bytes(dims, args.pages_per_split)),
+                     dtype=torch.uint8, device=device)
+    slots = torch.empty(work["tokens"], dtype=torch.int32, device=device)
+
+    def step():
+        s_ = pgd.page_slots(b.table, b.positions, b.rows, num_pages=b.num_pages)
+        pgd.kv_write_slots(b.k_new, b.v_new, s_, b.k_pool, b.v_pool)
+        pgd.paged_prefill_attention(b.q, b.k_pool, b.v_pool, b.table, b.rows, b.positions,
+                                    b.sinks, wl.window, wl.scale, out=out, workspace=ws, **opts)
+
+    for _ in range(args.warmup):
+        step()
+    assert pgd.get_device_error() == pgd.OK
+    flush = torch.empty(2 ** 30, dtype=torch.uint8, device=device)
+    e = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        e[i][0].record(stream)
+        step()
+        e[i][1].record(stream)
+    torch.cuda.synchronize()
+    assert pgd.get_device_error() == pgd.OK
+    ms = sum(a.elapsed_time(z) for a, z in e) / args.steps
+    del slots
+    hbm, hbm_kind = measured_peak()
+    tf, tf_kind = measured_tensor_peak()
+    gbs = work["bytes"] / (ms * 1e-3) / 1e9
+    tflops = work["flops"] / (ms * 1e-3) / 1e12
+    bound = "tensor" if work["flops"] / (tf * 1e12) > work["bytes"] / (hbm * 1e9) else "hbm"
+    line = {
+        "metric": "paged prefill attention: tokens/s (achieved GB/s, TFLOP/s)",
+        "value": work["tokens"] / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "dtype": "f32", "storage_dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{wl.name}: {wl.rows} rows, {wl.q_heads}q/{wl.kv_heads}kv, "
+                               f"d{wl.head_dim}, prefix U[{wl.prefix_lo},{wl.prefix_hi}], "
+                               f"chunk {wl.chunk}, window {wl.window}, sinks {wl.sinks}",
+                   "tokens": work["tokens"], "l2": "1 GiB L2 flush between steps",
+                   "kernel": args.kernel},
+        "gbs": gbs, "tflops": tflops,
+        "roofline": {"bound": bound,
+                     "achieved": tflops if bound == "tensor" else gbs,
+                     "peak": tf if bound == "tensor" else hbm,
+                     "peak_kind": tf_kind if bound == "tensor" else hbm_kind,
+                     "unit": "TFLOP/s" if bound == "tensor" else "GB/s",
+                     "frac": tflops / tf if bound == "tensor" else gbs / hbm},
+        "work": work,
+        "gpu_launches": 4 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["pgd", "reference"], default="pgd")
-    ap.add_argument("--workload", choices=list(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--path", choices=["decode", "prefill"], default="decode",
+                    help="decode step (default) or packed prefill chunks")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    help=f"decode: {', '.join(WORKLOADS)}; prefill: mistral_prefill, "
+                         "gptoss_prefill_sliding")
     ap.add_argument("--pages-per-split", type=int, default=0)
     ap.add_argument("--kernel", choices=["auto", "tensor", "cuda"], default="auto",
                     help="decode kernel variant (tensor-core or CUDA-core products)")
@@ -478,6 +581,16 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.path == "prefill":
+        from pgd_inputs import PREFILL_WORKLOADS
+        name = args.workload if args.workload in PREFILL_WORKLOADS else "mistral_prefill"
+        wl = PREFILL_WORKLOADS[name]
+        if args.rows > 0:
+            wl = wl.replace(rows=args.rows)
+        run_prefill(args, wl)
+        return
+    if args.workload not in WORKLOADS:
+        ap.error(f"unknown decode workload {args.workload}")
     wl = WORKLOADS[args.workload]
     if args.rows > 0:
         wl = wl.replace(rows=args.rows)

@@ -121,6 +121,36 @@ PGD_API int pgd_kv_append_paged(const pgd_dims* dims, const void* k_new, const v
                         void* v_pool, pgd_stream_t stream);
 
 /*
+ * page_slots -- the pool position of each token (Mistral 7B Instruct v0.3
+ * model files, src/attention.linnet, decode_paged: page_slots(table,
+ * positions); README "Entries": row b's positions lie in the pages table[b]
+ * lists): slots[p] = table[r][n / 64] * 64 + n % 64 with n = positions[p]
+ * and r = rows[p] (rows NULL: r = p).  n < 0 gives -1.
+ *   dims->rows   number of tokens P; dims->max_pages_per_row the table width.
+ *   table_rows   rows of `table` (ignored when rows is NULL: P rows).
+ * Device errors: n / 64 beyond the table, r outside the table, or a listed
+ * page outside the pool -> slots[p] = -1 and PGD_EDEVICE_BOUNDS recorded.
+ */
+PGD_API int pgd_page_slots(const pgd_dims* dims, int32_t table_rows, const int32_t* table,
+                           const int32_t* rows, const int32_t* positions, int32_t* slots,
+                           pgd_stream_t stream);
+
+/*
+ * kv_write_slots -- prefill's write_tokens at caller-given places (Mistral 7B
+ * Instruct v0.3 model files, src/attention.linnet, prefill_paged: each
+ * packed prompt token is written at its place in the pool, `slots`).
+ *   dims->rows    P tokens; dims->max_pages_per_row is not used.
+ *   k_new, v_new  bf16 [P][Hkv][D].
+ *   slots         int32 [P]: pool position slot = page * 64 + offset, the
+ *                 same numbering page_slots produces; < 0: padding, skipped.
+ * Device errors: slot / 64 >= num_pages -> nothing written for that token,
+ * PGD_EDEVICE_BOUNDS recorded.
+ */
+PGD_API int pgd_kv_write_slots(const pgd_dims* dims, const void* k_new, const void* v_new,
+                               const int32_t* slots, void* k_pool, void* v_pool,
+                               pgd_stream_t stream);
+
+/*
  * Bytes of device workspace pgd_paged_decode_attention needs for these dims
  * and options on the current device: split partials (m, l and an unnormalised
  * fp32 accumulator per row, query head and split).  0 if dims are invalid.
@@ -152,6 +182,34 @@ PGD_API int pgd_paged_decode_attention(const pgd_dims* dims, const void* q, cons
                                const int32_t* positions, const float* sinks, int32_t window,
                                float scale, void* out, void* workspace, size_t workspace_bytes,
                                const pgd_decode_options* opts, pgd_stream_t stream);
+
+/*
+ * paged_prefill_attention -- packed prompt tokens over their rows' pages
+ * (Mistral 7B Instruct v0.3 model files, src/attention.linnet,
+ * prefill_paged / step_paged and the model's prefill_paged entry; window and
+ * sinks as GPT-OSS 20B prefill_packed).  Token p is position positions[p]
+ * of the request in table row rows[p]; its query attends over that row's
+ * pages up to and including positions[p], within the window, with the sink
+ * in the denominator -- the same function as a decode step of that row.
+ * Write the tokens' keys and values first (pgd_kv_write_slots).
+ *   dims->rows    P tokens; dims->max_pages_per_row is the table width.
+ *   table_rows    rows of `table` (int32 [table_rows][max_pages_per_row]).
+ *   q, out        bf16 [P][Hq][D]; rows, positions int32 [P].
+ *   Others as for pgd_paged_decode_attention; the workspace size is
+ *   pgd_paged_decode_workspace_bytes(dims, opts) with dims->rows = P.
+ * step_paged (prompts and one decode step per row in one pass) is one call
+ * over the concatenation: the step of row b is a token with rows = b at its
+ * step position.
+ * Device errors: rows[p] outside [0, table_rows), plus those of
+ * pgd_paged_decode_attention; the token's output is zero.
+ */
+PGD_API int pgd_paged_prefill_attention(const pgd_dims* dims, int32_t table_rows, const void* q,
+                                        const void* k_pool, const void* v_pool,
+                                        const int32_t* table, const int32_t* rows,
+                                        const int32_t* positions, const float* sinks,
+                                        int32_t window, float scale, void* out, void* workspace,
+                                        size_t workspace_bytes, const pgd_decode_options* opts,
+                                        pgd_stream_t stream);
 
 /* Size of the library's own device scratch buffer used by
  * pgd_paged_decode_attention_static: 64 MiB on every device that loads the

@@ -11,6 +11,8 @@ Entry points (same names as the C ABI, without the ``pgd_`` prefix):
 - ``kv_append_paged``: write each row's new key and value at its page slot.
 - ``paged_decode_attention``: grouped-query decode attention of each row over
   its pages, with optional per-head sink logits and sliding window.
+- ``page_slots``, ``kv_write_slots``, ``paged_prefill_attention``: packed
+  prompt tokens (prefill) and prompts plus decode steps in one pass.
 - ``paged_decode_workspace_bytes``, ``get_device_error``.
 """
 from __future__ import annotations
@@ -70,6 +72,14 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             opts_p = ctypes.POINTER(DecodeOptions)
             lib.pgd_kv_append_paged.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, vp]
             lib.pgd_kv_append_paged.restype = ctypes.c_int
+            lib.pgd_page_slots.argtypes = [dims_p, i32, vp, vp, vp, vp, vp]
+            lib.pgd_page_slots.restype = ctypes.c_int
+            lib.pgd_kv_write_slots.argtypes = [dims_p, vp, vp, vp, vp, vp, vp]
+            lib.pgd_kv_write_slots.restype = ctypes.c_int
+            lib.pgd_paged_prefill_attention.argtypes = [dims_p, i32, vp, vp, vp, vp, vp, vp, vp,
+                                                       i32, ctypes.c_float, vp, vp,
+                                                       ctypes.c_size_t, opts_p, vp]
+            lib.pgd_paged_prefill_attention.restype = ctypes.c_int
             lib.pgd_paged_decode_workspace_bytes.argtypes = [dims_p, opts_p]
             lib.pgd_paged_decode_workspace_bytes.restype = ctypes.c_size_t
             lib.pgd_paged_decode_attention.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, i32,
@@ -210,6 +220,102 @@ def paged_decode_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.
             _stream_handle(stream))
     if rc != OK:
         raise PgdError(rc, "paged_decode_attention")
+    return out
+
+
+def page_slots(table: torch.Tensor, positions: torch.Tensor, rows: torch.Tensor | None = None, *,
+               num_pages: int, stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Pool position of each token: table[r][n // 64] * 64 + n % 64 with
+    n = positions[p], r = rows[p] (rows None: r = p); -1 for n < 0."""
+    dev = _check_cuda(table, positions, rows)
+    _dtype(table, torch.int32, "table")
+    _dtype(positions, torch.int32, "positions")
+    if rows is not None:
+        _dtype(rows, torch.int32, "rows")
+        if rows.shape != positions.shape:
+            raise ValueError("rows and positions must have one entry per token")
+    elif table.shape[0] != positions.shape[0]:
+        raise ValueError("without rows, the table needs one row per token")
+    tokens = positions.shape[0]
+    dims = make_dims(rows=tokens, num_q_heads=1, num_kv_heads=1, head_dim=64,
+                     num_pages=num_pages, max_pages_per_row=table.shape[1])
+    with torch.cuda.device(dev):
+        slots = torch.empty(tokens, dtype=torch.int32, device=dev)
+        rc = load_library().pgd_page_slots(ctypes.byref(dims), table.shape[0], _ptr(table),
+                                           _ptr(rows), _ptr(positions), _ptr(slots),
+                                           _stream_handle(stream))
+    if rc != OK:
+        raise PgdError(rc, "page_slots")
+    return slots
+
+
+def kv_write_slots(k_new: torch.Tensor, v_new: torch.Tensor, slots: torch.Tensor,
+                   k_pool: torch.Tensor, v_pool: torch.Tensor, *, layout: int = PAGE_MAJOR,
+                   stream: torch.cuda.Stream | None = None) -> None:
+    """Writes token p's key and value (bf16 [P, Hkv, D]) at pool position slots[p]."""
+    dev = _check_cuda(k_new, v_new, slots, k_pool, v_pool)
+    for t, n in ((k_new, "k_new"), (v_new, "v_new"), (k_pool, "k_pool"), (v_pool, "v_pool")):
+        _dtype(t, torch.bfloat16, n)
+    _dtype(slots, torch.int32, "slots")
+    tokens, hkv, d = k_new.shape
+    if v_new.shape != k_new.shape or slots.shape != (tokens,) or k_pool.shape != v_pool.shape:
+        raise ValueError("inconsistent shapes")
+    dims = make_dims(rows=tokens, num_q_heads=hkv, num_kv_heads=hkv, head_dim=d,
+                     num_pages=_pool_pages(k_pool, hkv, d), max_pages_per_row=1, layout=layout)
+    with torch.cuda.device(dev):
+        rc = load_library().pgd_kv_write_slots(ctypes.byref(dims), _ptr(k_new), _ptr(v_new),
+                                               _ptr(slots), _ptr(k_pool), _ptr(v_pool),
+                                               _stream_handle(stream))
+    if rc != OK:
+        raise PgdError(rc, "kv_write_slots")
+
+
+def paged_prefill_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                            table: torch.Tensor, rows: torch.Tensor, positions: torch.Tensor,
+                            sinks: torch.Tensor | None = None, window: int = 0,
+                            scale: float | None = None, *, num_kv_heads: int,
+                            layout: int = PAGE_MAJOR, out: torch.Tensor | None = None,
+                            workspace: torch.Tensor | None = None, pages_per_split: int = 0,
+                            kernel: int = KERNEL_AUTO,
+                            stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Packed prompt tokens: token p (q bf16 [P, Hq, D]) attends over table row
+    rows[p]'s pages up to positions[p].  Prompts and decode steps can share one
+    call (a step of row b is a token with rows[p] = b).  Returns bf16 [P, Hq, D]."""
+    dev = _check_cuda(q, k_pool, v_pool, table, rows, positions, sinks, out, workspace)
+    _dtype(q, torch.bfloat16, "q")
+    _dtype(k_pool, torch.bfloat16, "k_pool")
+    _dtype(v_pool, torch.bfloat16, "v_pool")
+    _dtype(table, torch.int32, "table")
+    _dtype(rows, torch.int32, "rows")
+    _dtype(positions, torch.int32, "positions")
+    if sinks is not None:
+        _dtype(sinks, torch.float32, "sinks")
+    tokens, hq, d = q.shape
+    if positions.shape != (tokens,) or rows.shape != (tokens,) or table.dim() != 2 \
+            or k_pool.shape != v_pool.shape or (sinks is not None and sinks.shape != (hq,)):
+        raise ValueError("inconsistent shapes")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dims = make_dims(rows=tokens, num_q_heads=hq, num_kv_heads=num_kv_heads, head_dim=d,
+                     num_pages=_pool_pages(k_pool, num_kv_heads, d),
+                     max_pages_per_row=table.shape[1], layout=layout)
+    opts = DecodeOptions(pages_per_split, kernel)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        if out is None:
+            out = torch.empty_like(q)
+        elif out.shape != q.shape or out.dtype != torch.bfloat16:
+            raise ValueError("out must be bf16 shaped like q")
+        need = lib.pgd_paged_decode_workspace_bytes(ctypes.byref(dims), ctypes.byref(opts))
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        rc = lib.pgd_paged_prefill_attention(
+            ctypes.byref(dims), table.shape[0], _ptr(q), _ptr(k_pool), _ptr(v_pool),
+            _ptr(table), _ptr(rows), _ptr(positions), _ptr(sinks), int(window), float(scale),
+            _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+            ctypes.byref(opts), _stream_handle(stream))
+    if rc != OK:
+        raise PgdError(rc, "paged_prefill_attention")
     return out
 
 

@@ -489,10 +489,12 @@ __global__ void __launch_bounds__(DecodeCfg<D, STAGES, Consumer>::kThreads)
   const int nsplit = (span.pages + p.pages_per_split - 1) / p.pages_per_split;
   if (split >= nsplit) return;     // inactive row, or past this row's splits
   if (n / kPage >= p.maxp) return;  // reported (and zeroed) by the combine kernel
+  const int table_row = p.row_of ? p.row_of[b] : b;
+  if (p.row_of && (table_row < 0 || table_row >= p.table_rows)) return;  // likewise
   const int page0 = span.first_page + split * p.pages_per_split;
   const int npages = min(p.pages_per_split, span.pages - split * p.pages_per_split);
   const int h0 = kvh * p.group;
-  const int32_t* trow = p.table + (size_t)b * p.maxp + page0;
+  const int32_t* trow = p.table + (size_t)table_row * p.maxp + page0;
 
   extern __shared__ unsigned char smem_raw[];
   unsigned char* stages = reinterpret_cast<unsigned char*>(
@@ -643,8 +645,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, STAGES, Consumer>::kThreads)
 // Merges the split partials of rows with two or more splits and folds in the
 // sink: M = max(max_i m_i, sink), L = sum_i l_i 2^(m_i - M) + 2^(sink - M),
 // out = sum_i acc_i 2^(m_i - M) / L.  Also zeroes inactive rows, rows whose
-// position lies beyond their table (recording PGD_EDEVICE_BOUNDS) and rows
-// with a split skipped for a bad table entry (marked l < 0).
+// position lies beyond their table or whose table row is out of range
+// (recording PGD_EDEVICE_BOUNDS) and rows with a split skipped for a bad
+// table entry (marked l < 0).
 // One warp per (row, query head); lane l owns dims [D/32 * l, D/32 * (l + 1)).
 template <int D>
 __global__ void __launch_bounds__(128) paged_decode_combine_kernel(const DecodeParams p) {
@@ -656,7 +659,9 @@ __global__ void __launch_bounds__(128) paged_decode_combine_kernel(const DecodeP
   const size_t bh = (size_t)b * p.hq + h;
   uint16_t* o = p.out + bh * D + lane * kDims;
   const int n = p.positions[b];
-  const bool beyond = n >= 0 && n / kPage >= p.maxp;
+  const int table_row = p.row_of ? p.row_of[b] : b;
+  const bool beyond = n >= 0 && (n / kPage >= p.maxp ||
+                                 (p.row_of && (table_row < 0 || table_row >= p.table_rows)));
   if (n < 0 || beyond) {
     if (beyond && h == 0 && lane == 0) record_error(p.err, PGD_EDEVICE_BOUNDS);
 #pragma unroll

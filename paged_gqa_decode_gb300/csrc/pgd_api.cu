@@ -174,13 +174,14 @@ using namespace pgd;
 
 extern "C" {
 
-int pgd_kv_append_paged(const pgd_dims* dims, const void* k_new, const void* v_new,
-                        const int32_t* table, const int32_t* positions, void* k_pool,
-                        void* v_pool, pgd_stream_t stream) {
+static int append_impl(const pgd_dims* dims, const void* k_new, const void* v_new,
+                       const int32_t* table, const int32_t* positions, const int32_t* slots,
+                       void* k_pool, void* v_pool, pgd_stream_t stream) {
   int rc = check_dims(dims);
   if (rc != PGD_OK) return rc;
   if (dims->rows == 0) return PGD_OK;
-  if (!k_new || !v_new || !table || !positions || !k_pool || !v_pool) return PGD_EINVAL;
+  if (!k_new || !v_new || !k_pool || !v_pool) return PGD_EINVAL;
+  if (slots == nullptr && (!table || !positions)) return PGD_EINVAL;
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool))
     return PGD_EINVAL;
   DeviceInfo* dev = nullptr;
@@ -190,6 +191,7 @@ int pgd_kv_append_paged(const pgd_dims* dims, const void* k_new, const void* v_n
   p.v_new = static_cast<const uint16_t*>(v_new);
   p.table = table;
   p.positions = positions;
+  p.slots = slots;
   p.k_pool = static_cast<uint16_t*>(k_pool);
   p.v_pool = static_cast<uint16_t*>(v_pool);
   p.err = dev->err;
@@ -203,6 +205,45 @@ int pgd_kv_append_paged(const pgd_dims* dims, const void* k_new, const void* v_n
                                                                                      : PGD_ECUDA;
 }
 
+int pgd_kv_append_paged(const pgd_dims* dims, const void* k_new, const void* v_new,
+                        const int32_t* table, const int32_t* positions, void* k_pool,
+                        void* v_pool, pgd_stream_t stream) {
+  return append_impl(dims, k_new, v_new, table, positions, nullptr, k_pool, v_pool, stream);
+}
+
+int pgd_page_slots(const pgd_dims* dims, int32_t table_rows, const int32_t* table,
+                   const int32_t* rows, const int32_t* positions, int32_t* slots,
+                   pgd_stream_t stream) {
+  int rc = check_dims(dims);
+  if (rc != PGD_OK) return rc;
+  if (dims->rows == 0) return PGD_OK;
+  if (!table || !positions || !slots) return PGD_EINVAL;
+  if (rows != nullptr && table_rows <= 0) return PGD_EINVAL;
+  if ((int64_t)dims->num_pages * kPageSize > (int64_t)INT32_MAX) return PGD_EUNSUPPORTED;
+  DeviceInfo* dev = nullptr;
+  if ((rc = current_device(&dev)) != PGD_OK) return rc;
+  SlotParams p;
+  p.table = table;
+  p.row_of = rows;
+  p.positions = positions;
+  p.slots = slots;
+  p.err = dev->err;
+  p.tokens = dims->rows;
+  p.table_rows = rows ? table_rows : dims->rows;
+  p.maxp = dims->max_pages_per_row;
+  p.num_pages = dims->num_pages;
+  return launch_page_slots(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? PGD_OK
+                                                                                     : PGD_ECUDA;
+}
+
+int pgd_kv_write_slots(const pgd_dims* dims, const void* k_new, const void* v_new,
+                       const int32_t* slots, void* k_pool, void* v_pool, pgd_stream_t stream) {
+  const int rc = check_dims(dims);
+  if (rc != PGD_OK) return rc;
+  if (dims->rows > 0 && !slots) return PGD_EINVAL;
+  return append_impl(dims, k_new, v_new, nullptr, nullptr, slots, k_pool, v_pool, stream);
+}
+
 size_t pgd_paged_decode_workspace_bytes(const pgd_dims* dims, const pgd_decode_options* opts) {
   if (check_dims(dims) != PGD_OK) return 0;
   DeviceInfo* dev = nullptr;
@@ -210,15 +251,17 @@ size_t pgd_paged_decode_workspace_bytes(const pgd_dims* dims, const pgd_decode_o
   return workspace_bytes(dims, make_plan(dims, opts, dev->sm_count));
 }
 
-int pgd_paged_decode_attention(const pgd_dims* dims, const void* q, const void* k_pool,
-                               const void* v_pool, const int32_t* table,
-                               const int32_t* positions, const float* sinks, int32_t window,
-                               float scale, void* out, void* workspace, size_t workspace_size,
-                               const pgd_decode_options* opts, pgd_stream_t stream) {
+static int decode_impl(const pgd_dims* dims, int32_t table_rows, const int32_t* row_of,
+                       const void* q, const void* k_pool, const void* v_pool,
+                       const int32_t* table, const int32_t* positions, const float* sinks,
+                       int32_t window, float scale, void* out, void* workspace,
+                       size_t workspace_size, const pgd_decode_options* opts,
+                       pgd_stream_t stream) {
   int rc = check_dims(dims);
   if (rc != PGD_OK) return rc;
   if (dims->rows == 0) return PGD_OK;
   if (!q || !k_pool || !v_pool || !table || !positions || !out) return PGD_EINVAL;
+  if (row_of != nullptr && table_rows <= 0) return PGD_EINVAL;
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
     return PGD_EINVAL;
   if (!std::isfinite(scale)) return PGD_EINVAL;
@@ -237,6 +280,8 @@ int pgd_paged_decode_attention(const pgd_dims* dims, const void* q, const void* 
   p.q = static_cast<const uint16_t*>(q);
   p.table = table;
   p.positions = positions;
+  p.row_of = row_of;
+  p.table_rows = table_rows;
   p.sinks = sinks;
   p.out = static_cast<uint16_t*>(out);
   const size_t acc_floats =
@@ -272,6 +317,28 @@ int pgd_paged_decode_attention(const pgd_dims* dims, const void* q, const void* 
       dims->head_dim == 64 ? launch_decode_d64(p, k_map, v_map, padded, kernel, grid_splits, st)
                            : launch_decode_d128(p, k_map, v_map, padded, kernel, grid_splits, st);
   return e == cudaSuccess ? PGD_OK : PGD_ECUDA;
+}
+
+int pgd_paged_decode_attention(const pgd_dims* dims, const void* q, const void* k_pool,
+                               const void* v_pool, const int32_t* table,
+                               const int32_t* positions, const float* sinks, int32_t window,
+                               float scale, void* out, void* workspace, size_t workspace_size,
+                               const pgd_decode_options* opts, pgd_stream_t stream) {
+  return decode_impl(dims, dims ? dims->rows : 0, nullptr, q, k_pool, v_pool, table, positions,
+                     sinks, window, scale, out, workspace, workspace_size, opts, stream);
+}
+
+int pgd_paged_prefill_attention(const pgd_dims* dims, int32_t table_rows, const void* q,
+                                const void* k_pool, const void* v_pool, const int32_t* table,
+                                const int32_t* rows, const int32_t* positions,
+                                const float* sinks, int32_t window, float scale, void* out,
+                                void* workspace, size_t workspace_size,
+                                const pgd_decode_options* opts, pgd_stream_t stream) {
+  const int rc = check_dims(dims);
+  if (rc != PGD_OK) return rc;
+  if (dims->rows > 0 && !rows) return PGD_EINVAL;
+  return decode_impl(dims, table_rows, rows, q, k_pool, v_pool, table, positions, sinks, window,
+                     scale, out, workspace, workspace_size, opts, stream);
 }
 
 int pgd_get_device_error(pgd_stream_t stream) {

@@ -15,6 +15,7 @@ struct AppendParams {
   const uint16_t* v_new;
   const int32_t* table;  // [R][maxp]
   const int32_t* positions;
+  const int32_t* slots;  // prefill: explicit pool positions (table unused); else nullptr
   uint16_t* k_pool;
   uint16_t* v_pool;
   unsigned int* err;  // sticky device error word
@@ -25,6 +26,8 @@ struct DecodeParams {
   const uint16_t* q;  // [R][Hq][D] bf16
   const int32_t* table;
   const int32_t* positions;
+  const int32_t* row_of;  // prefill: table row of each token (nullptr: row b)
+  int table_rows;         // rows of the table when row_of is given
   const float* sinks;  // [Hq] or nullptr
   uint16_t* out;       // [R][Hq][D] bf16
   float* ws_acc;       // [R][Hq][max_splits][D]
@@ -40,6 +43,16 @@ struct DecodeParams {
 int padded_group(int group);  // 0 if unsupported
 
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
+
+struct SlotParams {
+  const int32_t* table;
+  const int32_t* row_of;  // nullptr: token p uses table row p
+  const int32_t* positions;
+  int32_t* slots;
+  unsigned int* err;
+  int tokens, table_rows, maxp, num_pages;
+};
+cudaError_t launch_page_slots(const SlotParams& p, cudaStream_t stream);
 
 // Split kernel + combine kernel for one head_dim; `padded` is the padded
 // group size, `kernel` a PGD_KERNEL_* choice.

@@ -155,3 +155,102 @@ def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """The uint16 bit patterns of a bf16 tensor, as a host numpy array."""
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
 
+
+
+# ---------------------------------------------------------------------------
+# Prefill: packed prompt chunks over the paged pool.
+
+@dataclasses.dataclass(frozen=True)
+class PrefillWorkload:
+    """`rows` requests, each with `prefix` positions already cached
+    (~ U[prefix_lo, prefix_hi]) and a chunk of `chunk` new prompt tokens;
+    the chunks are packed end to end into one pass of rows * chunk tokens."""
+    name: str
+    rows: int
+    q_heads: int
+    kv_heads: int
+    head_dim: int
+    prefix_lo: int
+    prefix_hi: int
+    chunk: int
+    window: int = 0
+    sinks: bool = False
+    page_size: int = PAGE_SIZE
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+    @property
+    def max_pages_per_row(self) -> int:
+        return math.ceil((self.prefix_hi + self.chunk) / self.page_size)
+
+    def replace(self, **kw) -> "PrefillWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+PREFILL_WORKLOADS = {
+    "mistral_prefill": PrefillWorkload("mistral_prefill", rows=8, q_heads=32, kv_heads=8,
+                                       head_dim=128, prefix_lo=0, prefix_hi=8192, chunk=512),
+    "gptoss_prefill_sliding": PrefillWorkload("gptoss_prefill_sliding", rows=8, q_heads=64,
+                                              kv_heads=8, head_dim=64, prefix_lo=0,
+                                              prefix_hi=8192, chunk=256, window=128,
+                                              sinks=True),
+}
+
+
+@dataclasses.dataclass
+class PrefillBatch:
+    wl: PrefillWorkload
+    prefix: np.ndarray       # int64 [R] cached positions before each chunk
+    table_np: np.ndarray     # int32 [R, max_pages]
+    rows_np: np.ndarray      # int32 [P] table row of each packed token
+    positions_np: np.ndarray  # int32 [P]
+    num_pages: int
+    q: torch.Tensor          # bf16 [P, Hq, D]
+    k_new: torch.Tensor      # bf16 [P, Hkv, D]
+    v_new: torch.Tensor
+    k_pool: torch.Tensor
+    v_pool: torch.Tensor
+    sinks: torch.Tensor | None
+    table: torch.Tensor
+    rows: torch.Tensor
+    positions: torch.Tensor
+
+
+def make_prefill_batch(wl: PrefillWorkload, seed: int, device: str | torch.device = "cpu",
+                       prefix=None, chunks=None) -> PrefillBatch:
+    """Prefix lengths ~ U[prefix_lo, prefix_hi] (or given); row r's chunk is
+    positions prefix[r] .. prefix[r] + chunk[r] - 1, packed row after row.
+    Pages per row cover prefix + chunk, shuffled as in draw_layout."""
+    rng = np.random.default_rng(seed)
+    if prefix is None:
+        prefix = rng.integers(wl.prefix_lo, wl.prefix_hi + 1, size=wl.rows)
+    prefix = np.asarray(prefix, dtype=np.int64)
+    chunks = np.full(len(prefix), wl.chunk, dtype=np.int64) if chunks is None \
+        else np.asarray(chunks, dtype=np.int64)
+    lay = layout_from_contexts(Workload(wl.name, len(prefix), wl.q_heads, wl.kv_heads,
+                                        wl.head_dim, 1, int((prefix + chunks).max())),
+                               prefix + chunks, seed + 1)
+    rows_np = np.concatenate([np.full(c, r, dtype=np.int32) for r, c in enumerate(chunks)])
+    positions_np = np.concatenate([np.arange(p, p + c, dtype=np.int32)
+                                   for p, c in zip(prefix, chunks)])
+    device = torch.device(device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+
+    def normal(*shape, dtype=torch.bfloat16):
+        return torch.randn(*shape, generator=gen, device=device, dtype=dtype)
+
+    tokens = len(rows_np)
+    pool_len = lay.num_pages * wl.kv_heads * wl.page_size * wl.head_dim
+    q = normal(tokens, wl.q_heads, wl.head_dim)
+    k_new = normal(tokens, wl.kv_heads, wl.head_dim)
+    v_new = normal(tokens, wl.kv_heads, wl.head_dim)
+    k_pool = normal(pool_len)
+    v_pool = normal(pool_len)
+    sinks = normal(wl.q_heads, dtype=torch.float32) if wl.sinks else None
+    return PrefillBatch(wl, prefix, lay.table, rows_np, positions_np, lay.num_pages, q, k_new,
+                        v_new, k_pool, v_pool, sinks, torch.from_numpy(lay.table).to(device),
+                        torch.from_numpy(rows_np).to(device),
+                        torch.from_numpy(positions_np).to(device))

@@ -76,3 +76,32 @@ def oracle_step(batch: Batch, host: HostCopy, *, window: int, sinks, scale: floa
                                host.table, host.positions, kv_heads=wl.kv_heads,
                                page_size=wl.page_size, num_pages=host.num_pages, layout=layout,
                                sinks=sinks_np, window=window, scale=scale, nthreads=nthreads)
+
+
+def snapshot_pages(k_pool: torch.Tensor, v_pool: torch.Tensor, table: np.ndarray, table_rows,
+                   pages_per_row, *, kv_heads: int, head_dim: int, page_size: int = 64,
+                   layout: int = oracle.PAGE_MAJOR):
+    """Copies the first pages_per_row[i] pages of table rows table_rows[i] out
+    of the pools into a compact pool (pages renumbered 0..k-1 in first-use
+    order) and returns (k, v, compact table [len(table_rows), width],
+    num_pages).  Relabelling pages leaves every oracle result unchanged."""
+    uniq, remap = [], {}
+    ctable = np.zeros((len(table_rows), table.shape[1]), dtype=np.int32)
+    for i, (r, k) in enumerate(zip(table_rows, pages_per_row)):
+        for j in range(int(k)):
+            pg = int(table[r, j])
+            if pg not in remap:
+                remap[pg] = len(uniq)
+                uniq.append(pg)
+            ctable[i, j] = remap[pg]
+    idx = torch.tensor(uniq if uniq else [0], dtype=torch.long, device=k_pool.device)
+    tile = page_size * head_dim
+
+    def gather(pool):
+        if layout == oracle.PAGE_MAJOR:
+            view = pool.view(-1, kv_heads * tile)
+            return bf16_bits(view.index_select(0, idx)).reshape(-1).copy()
+        view = pool.view(kv_heads, -1, tile)
+        return bf16_bits(view.index_select(1, idx)).reshape(-1).copy()
+
+    return gather(k_pool), gather(v_pool), ctable, max(len(uniq), 1)

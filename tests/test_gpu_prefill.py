@@ -1,0 +1,192 @@
+"""GPU parity for the prefill row: page_slots and kv_write_slots bit-exact
+against the oracle, paged prefill attention (packed prompt chunks over their
+rows' pages, with sinks and windows) and step_paged (prompts and decode steps
+in one call) within the tolerance, on small cases and sampled tokens of the
+full prefill workloads."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_gqa_decode_gb300 as pgd
+from pgd_inputs import (PREFILL_WORKLOADS, WORKLOADS, PrefillWorkload, bf16_bits, draw_layout,
+                        make_batch, make_prefill_batch)
+from tests.oracle_side import snapshot_pages
+from tests.parity import compare
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    yield
+    torch.cuda.synchronize()
+
+
+def pages_needed(n_last: np.ndarray) -> np.ndarray:
+    return n_last // 64 + 1
+
+
+def prefill_check(b, *, window=None, sinks="batch", layout=pgd.PAGE_MAJOR, sample=None, pps=0,
+                  kernel=pgd.KERNEL_AUTO, what=""):
+    """Oracle inputs are copied out before the CUDA path writes anything; the
+    oracle then does its own slot computation, writes and prefill."""
+    wl = b.wl
+    window = wl.window if window is None else window
+    sinks = b.sinks if isinstance(sinks, str) else sinks
+    rows_used = sorted(set(b.rows_np.tolist()))
+    last = np.array([b.positions_np[b.rows_np == r].max() for r in rows_used])
+    k_host, v_host, ctable, num = snapshot_pages(
+        b.k_pool, b.v_pool, b.table_np, rows_used, pages_needed(last), kv_heads=wl.kv_heads,
+        head_dim=wl.head_dim, layout=layout)
+    slots = pgd.page_slots(b.table, b.positions, b.rows, num_pages=b.num_pages)
+    pgd.kv_write_slots(b.k_new, b.v_new, slots, b.k_pool, b.v_pool, layout=layout)
+    out = pgd.paged_prefill_attention(b.q, b.k_pool, b.v_pool, b.table, b.rows, b.positions,
+                                      sinks, window, wl.scale, num_kv_heads=wl.kv_heads,
+                                      layout=layout, pages_per_split=pps, kernel=kernel)
+    status = pgd.get_device_error()
+    assert status == pgd.OK, pgd.status_string(status)
+    # slots: bit-exact against the oracle's page_slots on the original table
+    per_token_table = b.table_np[b.rows_np]
+    want_slots = oracle.page_slots(per_token_table, b.positions_np, 64, b.num_pages)
+    assert np.array_equal(slots.cpu().numpy().astype(np.int64), want_slots)
+    # the oracle's own write and prefill on the compact pool
+    crow = {r: i for i, r in enumerate(rows_used)}
+    crows = np.array([crow[int(r)] for r in b.rows_np], dtype=np.int32)
+    oslots = oracle.page_slots(ctable[crows], b.positions_np, 64, num)
+    geo = dict(kv_heads=wl.kv_heads, head_dim=wl.head_dim, page_size=64, num_pages=num,
+               layout=layout)
+    oracle.write_tokens(k_host, bf16_bits(b.k_new), oslots, **geo)
+    oracle.write_tokens(v_host, bf16_bits(b.v_new), oslots, **geo)
+    idx = np.arange(len(b.rows_np)) if sample is None else np.asarray(sample)
+    sinks_np = None if sinks is None else sinks.cpu().numpy()
+    want, _, _ = oracle.prefill_paged(bf16_bits(b.q)[idx], k_host, v_host, ctable, crows[idx],
+                                      b.positions_np[idx], kv_heads=wl.kv_heads, num_pages=num,
+                                      layout=layout, sinks=sinks_np, window=window,
+                                      scale=wl.scale)
+    got = out.index_select(0, torch.as_tensor(idx, device=out.device))
+    return compare(got, want, what or wl.name)
+
+
+# ---------------------------------------------------------------------------
+
+
+def test_page_slots_decode_mode_bit_exact():
+    wl = WORKLOADS["gptoss_full"]
+    lay = draw_layout(wl, 1002)
+    table = torch.from_numpy(lay.table).to(DEV)
+    pos = torch.from_numpy(lay.positions).to(DEV)
+    got = pgd.page_slots(table, pos, num_pages=lay.num_pages).cpu().numpy()
+    want = oracle.page_slots(lay.table, lay.positions, 64, lay.num_pages)
+    assert np.array_equal(got.astype(np.int64), want)
+    assert pgd.get_device_error() == pgd.OK
+
+
+def test_page_slots_bad_entries_give_minus_one_and_an_error():
+    table = torch.tensor([[3, 7], [5, 99]], dtype=torch.int32, device=DEV)
+    pos = torch.tensor([70, 64, -1, 200], dtype=torch.int32, device=DEV)
+    rows = torch.tensor([0, 1, 0, 0], dtype=torch.int32, device=DEV)
+    got = pgd.page_slots(table, pos, rows, num_pages=8).cpu().tolist()
+    assert got == [7 * 64 + 6, -1, -1, -1]
+    assert pgd.get_device_error() == pgd.EDEVICE_BOUNDS
+
+
+@pytest.mark.parametrize("layout", [pgd.PAGE_MAJOR, pgd.HEAD_MAJOR])
+def test_write_slots_bit_exact(layout):
+    wl = PREFILL_WORKLOADS["mistral_prefill"].replace(rows=3, chunk=70)
+    b = make_prefill_batch(wl, 5, DEV, prefix=[0, 63, 130])
+    k_host, v_host = bf16_bits(b.k_pool).copy(), bf16_bits(b.v_pool).copy()
+    slots = pgd.page_slots(b.table, b.positions, b.rows, num_pages=b.num_pages)
+    slots[5] = -1                                   # a padding token writes nothing
+    pgd.kv_write_slots(b.k_new, b.v_new, slots, b.k_pool, b.v_pool, layout=layout)
+    assert pgd.get_device_error() == pgd.OK
+    s64 = slots.cpu().numpy().astype(np.int64)
+    geo = dict(kv_heads=wl.kv_heads, head_dim=wl.head_dim, page_size=64,
+               num_pages=b.num_pages, layout=layout)
+    oracle.write_tokens(k_host, bf16_bits(b.k_new), s64, **geo)
+    oracle.write_tokens(v_host, bf16_bits(b.v_new), s64, **geo)
+    assert np.array_equal(bf16_bits(b.k_pool), k_host)
+    assert np.array_equal(bf16_bits(b.v_pool), v_host)
+
+
+SMALL = [
+    # name, q, kv, d, window, sinks
+    ("mistral", 32, 8, 128, 0, False),
+    ("gptoss_sliding", 64, 8, 64, 128, True),
+    ("gptoss_full", 64, 8, 64, 0, True),
+    ("qwen", 14, 2, 64, 0, False),
+    ("narrow_window", 16, 4, 128, 65, True),
+    ("window_one", 8, 8, 64, 1, True),
+]
+
+
+@pytest.mark.parametrize("name,hq,hkv,d,window,sinks", SMALL)
+@pytest.mark.parametrize("pps", [0, 1])
+def test_prefill_small(name, hq, hkv, d, window, sinks, pps):
+    wl = PrefillWorkload(name, rows=4, q_heads=hq, kv_heads=hkv, head_dim=d, prefix_lo=0,
+                         prefix_hi=300, chunk=0, window=window, sinks=sinks)
+    b = make_prefill_batch(wl, 11 + hq + d, DEV, prefix=[0, 63, 64, 200],
+                           chunks=[1, 64, 100, 130])
+    prefill_check(b, pps=pps, what=f"prefill {name} pps={pps}")
+
+
+@pytest.mark.parametrize("layout", [pgd.PAGE_MAJOR, pgd.HEAD_MAJOR])
+def test_prefill_head_major_and_cuda_core(layout):
+    wl = PrefillWorkload("hm", rows=3, q_heads=16, kv_heads=4, head_dim=64, prefix_lo=0,
+                         prefix_hi=300, chunk=0, window=0, sinks=True)
+    b = make_prefill_batch(wl, 12, DEV, prefix=[10, 0, 190], chunks=[80, 5, 70])
+    prefill_check(b, layout=layout, kernel=pgd.KERNEL_CUDA_CORE if layout else pgd.KERNEL_AUTO)
+
+
+def test_prefill_interleaved_token_order():
+    """Packed tokens need not be grouped by row or sorted by position."""
+    wl = PrefillWorkload("mixed", rows=3, q_heads=8, kv_heads=2, head_dim=128, prefix_lo=0,
+                         prefix_hi=300, chunk=0, window=100, sinks=True)
+    b = make_prefill_batch(wl, 13, DEV, prefix=[0, 120, 250], chunks=[40, 40, 40])
+    perm = np.random.default_rng(0).permutation(len(b.rows_np))
+    t = torch.as_tensor(perm, device=DEV)
+    b.rows_np, b.positions_np = b.rows_np[perm], b.positions_np[perm]
+    b.rows, b.positions = b.rows[t].contiguous(), b.positions[t].contiguous()
+    b.q, b.k_new, b.v_new = b.q[t].contiguous(), b.k_new[t].contiguous(), b.v_new[t].contiguous()
+    prefill_check(b)
+
+
+def test_step_paged_prompts_and_steps_in_one_call():
+    """step_paged: two rows prefill a chunk, three other rows take a decode
+    step; one write of every token and one attention call over all of them
+    matches the oracle's prefill over the same concatenation (which for the
+    step tokens is exactly decode_paged)."""
+    wl = PrefillWorkload("step", rows=5, q_heads=32, kv_heads=8, head_dim=128, prefix_lo=0,
+                         prefix_hi=2000, chunk=0, window=0, sinks=False)
+    b = make_prefill_batch(wl, 14, DEV, prefix=[0, 900, 1500, 64, 1999],
+                           chunks=[150, 70, 1, 1, 1])
+    prefill_check(b, what="step_paged")
+
+
+@pytest.mark.parametrize("name,sample", [("mistral_prefill", 192), ("gptoss_prefill_sliding", 256)])
+def test_prefill_full_size_sampled(name, sample):
+    wl = PREFILL_WORKLOADS[name]
+    b = make_prefill_batch(wl, 2000 + list(PREFILL_WORKLOADS).index(name), DEV)
+    rng = np.random.default_rng(3)
+    tokens = len(b.rows_np)
+    idx = np.unique(np.concatenate([rng.choice(tokens, size=sample - 2, replace=False),
+                                    [0, tokens - 1]]))
+    prefill_check(b, sample=idx)
+
+
+def test_prefill_row_outside_table_is_zero_and_reported():
+    wl = PrefillWorkload("bad", rows=2, q_heads=8, kv_heads=2, head_dim=64, prefix_lo=0,
+                         prefix_hi=100, chunk=0)
+    b = make_prefill_batch(wl, 15, DEV, prefix=[0, 50], chunks=[10, 10])
+    rows = b.rows.clone()
+    rows[3] = 7
+    out = pgd.paged_prefill_attention(b.q, b.k_pool, b.v_pool, b.table, rows, b.positions,
+                                      num_kv_heads=2)
+    assert pgd.get_device_error() == pgd.EDEVICE_BOUNDS
+    assert torch.all(out[3] == 0) and torch.any(out[4] != 0)
