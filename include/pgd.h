@@ -89,9 +89,12 @@ typedef struct {
 /* Decode kernel variants.  Both compute the same function; they differ in
  * where the per-page Q.K^T and P.V products run. */
 enum {
-  PGD_KERNEL_AUTO = 0,        /* the tensor-core kernel */
-  PGD_KERNEL_TENSOR_CORE = 1, /* mma.sync bf16 products, fp32 accumulate */
-  PGD_KERNEL_CUDA_CORE = 2    /* fp32 FMA products on the CUDA cores */
+  PGD_KERNEL_AUTO = 0,          /* decode: tensor-core; prefill: see below */
+  PGD_KERNEL_TENSOR_CORE = 1,   /* mma.sync bf16 products, fp32 accumulate, per token */
+  PGD_KERNEL_CUDA_CORE = 2,     /* fp32 FMA products on the CUDA cores, per token */
+  PGD_KERNEL_PREFILL_TILED = 3  /* prefill only: blocks of tokens share each page
+                                   load (tensor cores, no key splits); AUTO picks
+                                   it when the blocks fill the GPU */
 };
 
 /* Optional tuning of the decode launch; pass NULL for the defaults.  The same

@@ -49,7 +49,7 @@ class Dims(ctypes.Structure):
         "max_pages_per_row", "layout")]
 
 
-KERNEL_AUTO, KERNEL_TENSOR_CORE, KERNEL_CUDA_CORE = range(3)
+KERNEL_AUTO, KERNEL_TENSOR_CORE, KERNEL_CUDA_CORE, KERNEL_PREFILL_TILED = range(4)
 
 
 class DecodeOptions(ctypes.Structure):

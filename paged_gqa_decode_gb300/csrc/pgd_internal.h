@@ -63,4 +63,10 @@ cudaError_t launch_decode_d128(const DecodeParams& p, const CUtensorMap& k_map,
                                const CUtensorMap& v_map, int padded, int kernel, int grid_splits,
                                cudaStream_t stream);
 
+// Tiled prefill (tokens of a block share each page load); no key splits.
+cudaError_t launch_prefill_tiled(const DecodeParams& p, const CUtensorMap& k_map,
+                                 const CUtensorMap& v_map, int head_dim, int padded,
+                                 cudaStream_t stream);
+int prefill_block_tokens(int padded);
+
 }  // namespace pgd

@@ -127,13 +127,24 @@ SMALL = [
 
 
 @pytest.mark.parametrize("name,hq,hkv,d,window,sinks", SMALL)
-@pytest.mark.parametrize("pps", [0, 1])
-def test_prefill_small(name, hq, hkv, d, window, sinks, pps):
+@pytest.mark.parametrize("kernel,pps", [(pgd.KERNEL_TENSOR_CORE, 0), (pgd.KERNEL_TENSOR_CORE, 1),
+                                        (pgd.KERNEL_PREFILL_TILED, 0)])
+def test_prefill_small(name, hq, hkv, d, window, sinks, kernel, pps):
     wl = PrefillWorkload(name, rows=4, q_heads=hq, kv_heads=hkv, head_dim=d, prefix_lo=0,
                          prefix_hi=300, chunk=0, window=window, sinks=sinks)
     b = make_prefill_batch(wl, 11 + hq + d, DEV, prefix=[0, 63, 64, 200],
                            chunks=[1, 64, 100, 130])
-    prefill_check(b, pps=pps, what=f"prefill {name} pps={pps}")
+    prefill_check(b, pps=pps, kernel=kernel, what=f"prefill {name} k={kernel} pps={pps}")
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(8, 8, 64), (4, 2, 128), (12, 4, 64), (10, 2, 64)])
+def test_prefill_tiled_groups_and_long_prefix(hq, hkv, d):
+    """Group sizes 1, 2, 3 (padded to 4) and 5 (padded to 8) in the tiled
+    kernel, chunks that start mid-page after long prefixes."""
+    wl = PrefillWorkload("tiled", rows=3, q_heads=hq, kv_heads=hkv, head_dim=d, prefix_lo=0,
+                         prefix_hi=3000, chunk=0, window=0, sinks=True)
+    b = make_prefill_batch(wl, 16 + hq, DEV, prefix=[2000, 37, 1500], chunks=[70, 150, 9])
+    prefill_check(b, kernel=pgd.KERNEL_PREFILL_TILED, what=f"tiled {hq}/{hkv} d{d}")
 
 
 @pytest.mark.parametrize("layout", [pgd.PAGE_MAJOR, pgd.HEAD_MAJOR])
@@ -144,7 +155,8 @@ def test_prefill_head_major_and_cuda_core(layout):
     prefill_check(b, layout=layout, kernel=pgd.KERNEL_CUDA_CORE if layout else pgd.KERNEL_AUTO)
 
 
-def test_prefill_interleaved_token_order():
+@pytest.mark.parametrize("kernel", [pgd.KERNEL_AUTO, pgd.KERNEL_PREFILL_TILED])
+def test_prefill_interleaved_token_order(kernel):
     """Packed tokens need not be grouped by row or sorted by position."""
     wl = PrefillWorkload("mixed", rows=3, q_heads=8, kv_heads=2, head_dim=128, prefix_lo=0,
                          prefix_hi=300, chunk=0, window=100, sinks=True)
@@ -154,10 +166,11 @@ def test_prefill_interleaved_token_order():
     b.rows_np, b.positions_np = b.rows_np[perm], b.positions_np[perm]
     b.rows, b.positions = b.rows[t].contiguous(), b.positions[t].contiguous()
     b.q, b.k_new, b.v_new = b.q[t].contiguous(), b.k_new[t].contiguous(), b.v_new[t].contiguous()
-    prefill_check(b)
+    prefill_check(b, kernel=kernel)
 
 
-def test_step_paged_prompts_and_steps_in_one_call():
+@pytest.mark.parametrize("kernel", [pgd.KERNEL_AUTO, pgd.KERNEL_PREFILL_TILED])
+def test_step_paged_prompts_and_steps_in_one_call(kernel):
     """step_paged: two rows prefill a chunk, three other rows take a decode
     step; one write of every token and one attention call over all of them
     matches the oracle's prefill over the same concatenation (which for the
@@ -166,7 +179,7 @@ def test_step_paged_prompts_and_steps_in_one_call():
                          prefix_hi=2000, chunk=0, window=0, sinks=False)
     b = make_prefill_batch(wl, 14, DEV, prefix=[0, 900, 1500, 64, 1999],
                            chunks=[150, 70, 1, 1, 1])
-    prefill_check(b, what="step_paged")
+    prefill_check(b, kernel=kernel, what="step_paged")
 
 
 @pytest.mark.parametrize("name,sample", [("mistral_prefill", 192), ("gptoss_prefill_sliding", 256)])
@@ -180,13 +193,20 @@ def test_prefill_full_size_sampled(name, sample):
     prefill_check(b, sample=idx)
 
 
-def test_prefill_row_outside_table_is_zero_and_reported():
+@pytest.mark.parametrize("kernel", [pgd.KERNEL_TENSOR_CORE, pgd.KERNEL_PREFILL_TILED])
+def test_prefill_bad_rows_and_pages_are_zero_and_reported(kernel):
     wl = PrefillWorkload("bad", rows=2, q_heads=8, kv_heads=2, head_dim=64, prefix_lo=0,
                          prefix_hi=100, chunk=0)
     b = make_prefill_batch(wl, 15, DEV, prefix=[0, 50], chunks=[10, 10])
     rows = b.rows.clone()
     rows[3] = 7
     out = pgd.paged_prefill_attention(b.q, b.k_pool, b.v_pool, b.table, rows, b.positions,
-                                      num_kv_heads=2)
+                                      num_kv_heads=2, kernel=kernel)
     assert pgd.get_device_error() == pgd.EDEVICE_BOUNDS
     assert torch.all(out[3] == 0) and torch.any(out[4] != 0)
+    table = b.table.clone()
+    table[1, 0] = 10 ** 6          # row 1's first page is outside the pool
+    out = pgd.paged_prefill_attention(b.q, b.k_pool, b.v_pool, table, b.rows, b.positions,
+                                      num_kv_heads=2, kernel=kernel)
+    assert pgd.get_device_error() == pgd.EDEVICE_BOUNDS
+    assert torch.all(out[10:] == 0) and torch.any(out[:10] != 0)
