@@ -560,14 +560,73 @@ def run_prefill(args, wl):
     print(json.dumps(line), flush=True)
 
 
+def run_rows(args, wl):
+    """decode_rows step over dense per-row caches: write_rows + decode."""
+    import paged_gqa_decode_gb300 as pgd
+    from pgd_inputs import ROWS_WORKLOADS, make_rows_batch
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    b = make_rows_batch(wl, 3000 + list(ROWS_WORKLOADS).index(wl.name), device)
+    by = algorithmic_bytes(wl, b.positions_np)
+    out = torch.empty_like(b.q)
+    kernel = {"auto": 0, "tensor": 1, "cuda": 2}[args.kernel]
+
+    def step():
+        pgd.kv_append_rows(b.k_new, b.v_new, b.positions, b.cache_k, b.cache_v)
+        pgd.decode_rows_attention(b.q, b.cache_k, b.cache_v, b.positions, b.sinks, wl.window,
+                                  wl.scale, out=out, pages_per_split=args.pages_per_split,
+                                  kernel=kernel)
+
+    for _ in range(args.warmup):
+        step()
+    assert pgd.get_device_error() == pgd.OK
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        step()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=side):
+            step()
+    torch.cuda.synchronize()
+    flush = torch.empty(2 ** 30, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        g.replay()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    assert pgd.get_device_error() == pgd.OK
+    ms = sum(a.elapsed_time(z) for a, z in ev) / args.steps
+    peak, kind = measured_peak()
+    gbs = by["step"] / (ms * 1e-3) / 1e9
+    line = {
+        "metric": "decode_rows attention (dense per-row caches): achieved HBM GB/s; row-tokens/s",
+        "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "dtype": "f32", "storage_dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{describe(wl)}, dense caches MaxSeq {b.max_seq}",
+                   "l2": "1 GiB L2 flush between steps",
+                   "timing": "CUDA graph replay per step (write_rows + decode)"},
+        "row_tokens_per_s": wl.rows / (ms * 1e-3),
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "peak_kind": kind,
+                     "unit": "GB/s", "frac": gbs / peak},
+        "bytes_per_step": by, "gpu_launches": 3 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["pgd", "reference"], default="pgd")
-    ap.add_argument("--path", choices=["decode", "prefill"], default="decode",
-                    help="decode step (default) or packed prefill chunks")
+    ap.add_argument("--path", choices=["decode", "prefill", "rows"], default="decode",
+                    help="decode step over pages (default), packed prefill chunks, or "
+                         "decode_rows over dense per-row caches")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     help=f"decode: {', '.join(WORKLOADS)}; prefill: mistral_prefill, "
                          "gptoss_prefill_sliding")
@@ -588,6 +647,14 @@ def main():
         if args.rows > 0:
             wl = wl.replace(rows=args.rows)
         run_prefill(args, wl)
+        return
+    if args.path == "rows":
+        from pgd_inputs import ROWS_WORKLOADS
+        name = args.workload if args.workload in ROWS_WORKLOADS else "gptoss_rows_serve"
+        wl = ROWS_WORKLOADS[name]
+        if args.rows > 0:
+            wl = wl.replace(rows=args.rows)
+        run_rows(args, wl)
         return
     if args.workload not in WORKLOADS:
         ap.error(f"unknown decode workload {args.workload}")

@@ -71,8 +71,17 @@ enum {
  * form one contiguous tile, so a page tile is read with a single copy. */
 enum {
   PGD_PAGE_MAJOR = 0, /* [num_pages][num_kv_heads][64][head_dim] */
-  PGD_HEAD_MAJOR = 1  /* [num_kv_heads][num_pages * 64][head_dim]: the pages'
+  PGD_HEAD_MAJOR = 1, /* [num_kv_heads][num_pages * 64][head_dim]: the pages'
                          own cache_k[0] layout, [KvHeads, MaxSeq, D] */
+  PGD_ROW_MAJOR = 2   /* [num_pages / P][num_kv_heads][P * 64][head_dim] with
+                         P = max_pages_per_row: the dense per-row caches of
+                         decode_rows, [Batch, KvHeads, MaxSeq, D] with
+                         MaxSeq = 64 P (GPT-OSS 20B and Mistral 7B Instruct
+                         v0.3 model files, src/attention.linnet, cache_k and
+                         decode_rows); page b * P + j is positions
+                         64 j .. 64 j + 63 of row b.  With this layout the
+                         table may be NULL: row b's pages are then
+                         b * P + j (decode_rows), and rows <= num_pages / P. */
 };
 
 typedef struct {
@@ -83,7 +92,7 @@ typedef struct {
   int32_t page_size;         /* positions per page: must be 64 */
   int32_t num_pages;         /* pool capacity in pages, >= 1 */
   int32_t max_pages_per_row; /* table row stride (entries per row), >= 1 */
-  int32_t layout;            /* PGD_PAGE_MAJOR or PGD_HEAD_MAJOR */
+  int32_t layout;            /* PGD_PAGE_MAJOR, PGD_HEAD_MAJOR or PGD_ROW_MAJOR */
 } pgd_dims;
 
 /* Decode kernel variants.  Both compute the same function; they differ in
@@ -109,7 +118,9 @@ typedef struct {
 /*
  * kv_append_paged -- page_slots + write_tokens.
  *   k_new, v_new  bf16 [R][Hkv][D]: the new token's key and value per row.
- *   table         int32 [R][max_pages_per_row]: row b's pages in order.
+ *   table         int32 [R][max_pages_per_row]: row b's pages in order
+ *                 (NULL with PGD_ROW_MAJOR: row b's pages are b * P + j, i.e.
+ *                 write_rows into dense per-row caches).
  *   positions     int32 [R]: the new token's 0-based position (< 0: inactive).
  *   k_pool,v_pool bf16 pools in dims->layout, num_pages pages each.
  * Row b's token is written at position positions[b] % 64 of page
@@ -165,7 +176,8 @@ PGD_API size_t pgd_paged_decode_workspace_bytes(const pgd_dims* dims, const pgd_
  *   q          bf16 [R][Hq][D]: queries (rope already applied).
  *   k_pool, v_pool  the pools, holding each active row's positions
  *              0..positions[b] (append first: the new token attends to itself).
- *   table, positions  as for pgd_kv_append_paged.
+ *   table, positions  as for pgd_kv_append_paged (the table may be NULL with
+ *              PGD_ROW_MAJOR: decode_rows over dense per-row caches).
  *   sinks      fp32 [Hq] sink logits (score space: not multiplied by scale),
  *              or NULL for none.
  *   window     > 0: row b attends to positions (n - window, n];

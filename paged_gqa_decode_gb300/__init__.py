@@ -13,6 +13,8 @@ Entry points (same names as the C ABI, without the ``pgd_`` prefix):
   its pages, with optional per-head sink logits and sliding window.
 - ``page_slots``, ``kv_write_slots``, ``paged_prefill_attention``: packed
   prompt tokens (prefill) and prompts plus decode steps in one pass.
+- ``kv_append_rows``, ``decode_rows_attention``: the same step over dense
+  per-row caches [Batch, KvHeads, MaxSeq, D] (decode_rows).
 - ``paged_decode_workspace_bytes``, ``get_device_error``.
 """
 from __future__ import annotations
@@ -27,6 +29,7 @@ import torch
 PAGE_SIZE = 64
 PAGE_MAJOR = 0
 HEAD_MAJOR = 1
+ROW_MAJOR = 2
 
 OK, EINVAL, EUNSUPPORTED, ECUDA, EDEVICE_BOUNDS, EDEVICE_TIMEOUT, EWORKSPACE = range(7)
 
@@ -316,6 +319,78 @@ def paged_prefill_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch
             ctypes.byref(opts), _stream_handle(stream))
     if rc != OK:
         raise PgdError(rc, "paged_prefill_attention")
+    return out
+
+
+def _dense_dims(cache: torch.Tensor, rows: int, num_q_heads: int) -> Dims:
+    if cache.dim() != 4 or cache.shape[2] % PAGE_SIZE:
+        raise ValueError("dense caches are [Batch, KvHeads, MaxSeq, D] with MaxSeq % 64 == 0")
+    batch, hkv, max_seq, d = cache.shape
+    if rows > batch:
+        raise ValueError("more rows than cache rows")
+    per_row = max_seq // PAGE_SIZE
+    return make_dims(rows=rows, num_q_heads=num_q_heads, num_kv_heads=hkv, head_dim=d,
+                     num_pages=batch * per_row, max_pages_per_row=per_row, layout=ROW_MAJOR)
+
+
+def kv_append_rows(k_new: torch.Tensor, v_new: torch.Tensor, positions: torch.Tensor,
+                   cache_k: torch.Tensor, cache_v: torch.Tensor, *,
+                   stream: torch.cuda.Stream | None = None) -> None:
+    """write_rows: row b's new key and value (bf16 [R, Hkv, D]) go to position
+    positions[b] of row b of the dense caches (bf16 [Batch, Hkv, MaxSeq, D])."""
+    dev = _check_cuda(k_new, v_new, positions, cache_k, cache_v)
+    for t, n in ((k_new, "k_new"), (v_new, "v_new"), (cache_k, "cache_k"), (cache_v, "cache_v")):
+        _dtype(t, torch.bfloat16, n)
+    _dtype(positions, torch.int32, "positions")
+    if v_new.shape != k_new.shape or cache_k.shape != cache_v.shape \
+            or positions.shape != (k_new.shape[0],):
+        raise ValueError("inconsistent shapes")
+    dims = _dense_dims(cache_k, k_new.shape[0], k_new.shape[1])
+    with torch.cuda.device(dev):
+        rc = load_library().pgd_kv_append_paged(
+            ctypes.byref(dims), _ptr(k_new), _ptr(v_new), None, _ptr(positions), _ptr(cache_k),
+            _ptr(cache_v), _stream_handle(stream))
+    if rc != OK:
+        raise PgdError(rc, "kv_append_rows")
+
+
+def decode_rows_attention(q: torch.Tensor, cache_k: torch.Tensor, cache_v: torch.Tensor,
+                          positions: torch.Tensor, sinks: torch.Tensor | None = None,
+                          window: int = 0, scale: float | None = None, *,
+                          out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                          pages_per_split: int = 0, kernel: int = KERNEL_AUTO,
+                          stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """decode_rows: row b's queries (q bf16 [R, Hq, D]) attend over row b of the
+    dense caches (bf16 [Batch, Hkv, MaxSeq, D]) up to positions[b]."""
+    dev = _check_cuda(q, cache_k, cache_v, positions, sinks, out, workspace)
+    _dtype(q, torch.bfloat16, "q")
+    _dtype(cache_k, torch.bfloat16, "cache_k")
+    _dtype(cache_v, torch.bfloat16, "cache_v")
+    _dtype(positions, torch.int32, "positions")
+    if sinks is not None:
+        _dtype(sinks, torch.float32, "sinks")
+    rows, hq, d = q.shape
+    if cache_k.shape != cache_v.shape or positions.shape != (rows,) or cache_k.shape[3] != d \
+            or (sinks is not None and sinks.shape != (hq,)):
+        raise ValueError("inconsistent shapes")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dims = _dense_dims(cache_k, rows, hq)
+    opts = DecodeOptions(pages_per_split, kernel)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        if out is None:
+            out = torch.empty_like(q)
+        need = lib.pgd_paged_decode_workspace_bytes(ctypes.byref(dims), ctypes.byref(opts))
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        rc = lib.pgd_paged_decode_attention(
+            ctypes.byref(dims), _ptr(q), _ptr(cache_k), _ptr(cache_v), None, _ptr(positions),
+            _ptr(sinks), int(window), float(scale), _ptr(out), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), ctypes.byref(opts),
+            _stream_handle(stream))
+    if rc != OK:
+        raise PgdError(rc, "decode_rows_attention")
     return out
 
 

@@ -16,7 +16,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
   if (p.slots) {  // explicit pool position (prefill's write at the caller's slots)
     const int slot = p.slots[b];
     if (slot < 0) return;  // padding token
-    if (slot / kPage >= p.num_pages) {
+    if (slot / kPage >= p.num_pages) {  // (maxp is only used by PGD_ROW_MAJOR)
       if (threadIdx.x == 0) record_error(p.err, PGD_EDEVICE_BOUNDS);
       return;
     }
@@ -30,7 +30,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
       if (threadIdx.x == 0) record_error(p.err, PGD_EDEVICE_BOUNDS);
       return;
     }
-    page = p.table[(size_t)b * p.maxp + page_index];
+    page = page_of(p.table, b, page_index, p.maxp);
     if (page < 0 || page >= p.num_pages) {
       if (threadIdx.x == 0) record_error(p.err, PGD_EDEVICE_BOUNDS);
       return;
@@ -44,9 +44,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
     const int h = (c % per_tensor) / chunks;
     const int ch = c % chunks;
     const uint16_t* src = (which ? p.v_new : p.k_new) + ((size_t)b * p.hkv + h) * p.head_dim + ch * 8;
-    const size_t tile = p.layout == PGD_PAGE_MAJOR ? (size_t)page * p.hkv + h
-                                                   : (size_t)h * p.num_pages + page;
-    uint16_t* dst = (which ? p.v_pool : p.k_pool) + (tile * kPage + in_page) * p.head_dim + ch * 8;
+    const int64_t row0 = tile_first_row(p.layout, page, h, p.hkv, p.num_pages, p.maxp);
+    uint16_t* dst = (which ? p.v_pool : p.k_pool) + ((size_t)row0 + in_page) * p.head_dim + ch * 8;
     *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
   }
 }

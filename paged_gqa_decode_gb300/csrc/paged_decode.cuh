@@ -494,7 +494,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, STAGES, Consumer>::kThreads)
   const int page0 = span.first_page + split * p.pages_per_split;
   const int npages = min(p.pages_per_split, span.pages - split * p.pages_per_split);
   const int h0 = kvh * p.group;
-  const int32_t* trow = p.table + (size_t)table_row * p.maxp + page0;
+  const int32_t* trow = p.table ? p.table + (size_t)table_row * p.maxp + page0 : nullptr;
+  const int dense0 = table_row * p.maxp + page0;  // page of index page0 without a table
 
   extern __shared__ unsigned char smem_raw[];
   unsigned char* stages = reinterpret_cast<unsigned char*>(
@@ -508,7 +509,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, STAGES, Consumer>::kThreads)
   // Every table entry this split reads must name a pool page.
   bool bad = false;
   for (int i = tid; i < npages; i += C::kThreads) {
-    const int pg = trow[i];
+    const int pg = trow ? trow[i] : dense0 + i;
     bad |= (pg < 0) | (pg >= p.num_pages);
   }
   bad = __syncthreads_or(bad);
@@ -555,9 +556,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, STAGES, Consumer>::kThreads)
         // abandon the split themselves; only they write abort_flag.
         if (i >= C::kStages && !mbar_wait_bounded(&empty[s], ((i / C::kStages) - 1) & 1, p.err))
           break;
-        const int page = trow[i];
-        const int y = p.layout == PGD_PAGE_MAJOR ? (page * p.hkv + kvh) * kPage
-                                                 : (kvh * p.num_pages + page) * kPage;
+        const int page = trow ? trow[i] : dense0 + i;
+        const int y = (int)tile_first_row(p.layout, page, kvh, p.hkv, p.num_pages, p.maxp);
         unsigned char* st = stages + s * C::kStageBytes;
         mbar_arrive_expect_tx(&full[s], C::kStageBytes);
 #pragma unroll

@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, GP, STAGES>::kThreads)
         const int lo = p.window > 0 ? max(tok_pos[rs] - p.window + 1, 0) : 0;
         const int first = lo / kPage, last = tok_pos[re - 1] / kPage;
         for (int pg = first + tid; pg <= last; pg += C::kThreads) {
-          const int page = p.table[(size_t)row * p.maxp + pg];
+          const int page = page_of(p.table, row, pg, p.maxp);
           if (page < 0 || page >= p.num_pages) run_bad[r] = 1;
         }
       }
@@ -154,7 +154,6 @@ __global__ void __launch_bounds__(PrefillCfg<D, GP, STAGES>::kThreads)
         if (row >= 0 && !run_bad[r]) {
           const int lo = p.window > 0 ? max(tok_pos[rs] - p.window + 1, 0) : 0;
           const int first = lo / kPage, last = tok_pos[re - 1] / kPage;
-          const int32_t* trow = p.table + (size_t)row * p.maxp;
           for (int pg = first; pg <= last; ++pg, ++i) {
             const int s = i % C::kStages;
             // every consumer warp takes every page, in order, so each parity
@@ -164,9 +163,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, GP, STAGES>::kThreads)
               abort_flag = 1;
               break;
             }
-            const int page = trow[pg];
-            const int y = p.layout == PGD_PAGE_MAJOR ? (page * p.hkv + kvh) * kPage
-                                                     : (kvh * p.num_pages + page) * kPage;
+            const int page = page_of(p.table, row, pg, p.maxp);
+            const int y = (int)tile_first_row(p.layout, page, kvh, p.hkv, p.num_pages, p.maxp);
             unsigned char* st = stages + s * C::kStageBytes;
             mbar_arrive_expect_tx(&full[s], C::kStageBytes);
 #pragma unroll

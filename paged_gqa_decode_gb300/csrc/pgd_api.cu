@@ -56,7 +56,9 @@ int check_dims(const pgd_dims* d) {
       d->num_pages <= 0 || d->max_pages_per_row <= 0)
     return PGD_EINVAL;
   if (d->num_q_heads % d->num_kv_heads != 0) return PGD_EINVAL;
-  if (d->layout != PGD_PAGE_MAJOR && d->layout != PGD_HEAD_MAJOR) return PGD_EINVAL;
+  if (d->layout != PGD_PAGE_MAJOR && d->layout != PGD_HEAD_MAJOR && d->layout != PGD_ROW_MAJOR)
+    return PGD_EINVAL;
+  if (d->layout == PGD_ROW_MAJOR && d->num_pages % d->max_pages_per_row != 0) return PGD_EINVAL;
   if (d->page_size != kPageSize) return PGD_EUNSUPPORTED;
   if (d->head_dim != 64 && d->head_dim != 128) return PGD_EUNSUPPORTED;
   if (padded_group(d->num_q_heads / d->num_kv_heads) == 0) return PGD_EUNSUPPORTED;
@@ -181,7 +183,11 @@ static int append_impl(const pgd_dims* dims, const void* k_new, const void* v_ne
   if (rc != PGD_OK) return rc;
   if (dims->rows == 0) return PGD_OK;
   if (!k_new || !v_new || !k_pool || !v_pool) return PGD_EINVAL;
-  if (slots == nullptr && (!table || !positions)) return PGD_EINVAL;
+  if (slots == nullptr && (!positions || (!table && dims->layout != PGD_ROW_MAJOR)))
+    return PGD_EINVAL;
+  if (slots == nullptr && !table &&
+      (int64_t)dims->rows * dims->max_pages_per_row > dims->num_pages)
+    return PGD_EINVAL;  // dense rows: every row needs its own P pages
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool))
     return PGD_EINVAL;
   DeviceInfo* dev = nullptr;
@@ -260,8 +266,12 @@ static int decode_impl(const pgd_dims* dims, int32_t table_rows, const int32_t* 
   int rc = check_dims(dims);
   if (rc != PGD_OK) return rc;
   if (dims->rows == 0) return PGD_OK;
-  if (!q || !k_pool || !v_pool || !table || !positions || !out) return PGD_EINVAL;
+  if (!q || !k_pool || !v_pool || !positions || !out) return PGD_EINVAL;
+  if (!table && dims->layout != PGD_ROW_MAJOR) return PGD_EINVAL;
   if (row_of != nullptr && table_rows <= 0) return PGD_EINVAL;
+  if (!table && (int64_t)(row_of ? table_rows : dims->rows) * dims->max_pages_per_row >
+                    dims->num_pages)
+    return PGD_EINVAL;  // dense rows: every row needs its own P pages
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
     return PGD_EINVAL;
   if (!std::isfinite(scale)) return PGD_EINVAL;

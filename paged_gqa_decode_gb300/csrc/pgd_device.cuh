@@ -138,6 +138,21 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// First row of the (page, kv head) tile in the pool seen as a 2-D tensor of
+// head_dim-wide rows (`maxp` is the pages per row of PGD_ROW_MAJOR).
+__device__ __forceinline__ int64_t tile_first_row(int layout, int64_t page, int kvh, int hkv,
+                                                  int num_pages, int maxp) {
+  if (layout == PGD_PAGE_MAJOR) return (page * hkv + kvh) * kPage;
+  if (layout == PGD_HEAD_MAJOR) return ((int64_t)kvh * num_pages + page) * kPage;
+  return (((page / maxp) * hkv + kvh) * maxp + page % maxp) * kPage;  // PGD_ROW_MAJOR
+}
+
+// Pool page holding page index j of table row r; with no table (dense rows)
+// row r's pages are r * maxp + j.
+__device__ __forceinline__ int page_of(const int32_t* table, int r, int j, int maxp) {
+  return table ? table[(size_t)r * maxp + j] : r * maxp + j;
+}
+
 // Row attention geometry shared by the decode and combine kernels.
 struct RowSpan {
   int n;           // position of the new token (< 0: inactive)

@@ -254,3 +254,60 @@ def make_prefill_batch(wl: PrefillWorkload, seed: int, device: str | torch.devic
                         v_new, k_pool, v_pool, sinks, torch.from_numpy(lay.table).to(device),
                         torch.from_numpy(rows_np).to(device),
                         torch.from_numpy(positions_np).to(device))
+
+
+# ---------------------------------------------------------------------------
+# decode_rows: dense per-row caches [Batch, KvHeads, MaxSeq, D].
+
+ROWS_WORKLOADS = {
+    # the pages' own serving setup: 64 fixed cache rows of 640 positions,
+    # prompts of 128-512 tokens plus up to 128 new ones (gpt-oss heads, sinks)
+    "gptoss_rows_serve": Workload("gptoss_rows_serve", rows=64, q_heads=64, kv_heads=8,
+                                  head_dim=64, ctx_lo=129, ctx_hi=640, sinks=True),
+    "mistral_rows": Workload("mistral_rows", rows=64, q_heads=32, kv_heads=8, head_dim=128,
+                             ctx_lo=1024, ctx_hi=8192),
+}
+
+
+@dataclasses.dataclass
+class RowsBatch:
+    wl: Workload
+    contexts: np.ndarray
+    positions_np: np.ndarray
+    max_seq: int
+    q: torch.Tensor          # bf16 [R, Hq, D]
+    k_new: torch.Tensor      # bf16 [R, Hkv, D]
+    v_new: torch.Tensor
+    cache_k: torch.Tensor    # bf16 [R, Hkv, MaxSeq, D]
+    cache_v: torch.Tensor
+    sinks: torch.Tensor | None
+    positions: torch.Tensor
+
+
+def make_rows_batch(wl: Workload, seed: int, device: str | torch.device = "cpu",
+                    contexts=None, max_seq: int | None = None) -> RowsBatch:
+    """Contexts ~ U[ctx_lo, ctx_hi] (or given); MaxSeq = ctx_hi rounded up to a
+    whole number of 64-position pages; caches, q, k, v ~ N(0, 1) bf16."""
+    rng = np.random.default_rng(seed)
+    if contexts is None:
+        contexts = rng.integers(wl.ctx_lo, wl.ctx_hi + 1, size=wl.rows)
+    contexts = np.asarray(contexts, dtype=np.int64)
+    if max_seq is None:
+        max_seq = int(math.ceil(max(wl.ctx_hi, int(contexts.max())) / wl.page_size) * wl.page_size)
+    rows = len(contexts)
+    device = torch.device(device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+
+    def normal(*shape, dtype=torch.bfloat16):
+        return torch.randn(*shape, generator=gen, device=device, dtype=dtype)
+
+    q = normal(rows, wl.q_heads, wl.head_dim)
+    k_new = normal(rows, wl.kv_heads, wl.head_dim)
+    v_new = normal(rows, wl.kv_heads, wl.head_dim)
+    cache_k = normal(rows, wl.kv_heads, max_seq, wl.head_dim)
+    cache_v = normal(rows, wl.kv_heads, max_seq, wl.head_dim)
+    sinks = normal(wl.q_heads, dtype=torch.float32) if wl.sinks else None
+    positions_np = np.where(contexts > 0, contexts - 1, -1).astype(np.int32)
+    return RowsBatch(wl, contexts, positions_np, max_seq, q, k_new, v_new, cache_k, cache_v,
+                     sinks, torch.from_numpy(positions_np).to(device))
