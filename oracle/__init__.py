@@ -65,6 +65,10 @@ def _load():
                                              ctypes.c_float, p, p, p, i]
             lib.orc_prefill_paged.argtypes = [i, i, i, i, i, i, i, i, i, p, p, p, p, p, p, p,
                                               i, ctypes.c_float, p, p, p, i]
+            lib.orc_rope_table.argtypes = [i, ctypes.c_float, i, p, p]
+            lib.orc_rope.argtypes = [i, i, i, ctypes.c_float, p, p, p]
+            lib.orc_rope_table.restype = ctypes.c_int
+            lib.orc_rope.restype = ctypes.c_int
             for fn in (lib.orc_page_slots, lib.orc_write_tokens, lib.orc_decode_rows,
                        lib.orc_decode_paged, lib.orc_prefill_paged):
                 fn.restype = ctypes.c_int
@@ -198,3 +202,23 @@ def prefill_paged(q, k_pool, v_pool, table, rows, positions, *, kv_heads, page_s
                                      _ptr(lse_real), nthreads or default_threads()),
            "prefill_paged")
     return out, lse, lse_real
+
+
+def rope_table(head_dim: int, theta: float, pos: int):
+    """(cos, sin) uint16 bf16 bit patterns [head_dim / 2] at position pos."""
+    c = np.empty(head_dim // 2, dtype=np.uint16)
+    s = np.empty(head_dim // 2, dtype=np.uint16)
+    _check(_load().orc_rope_table(head_dim, float(theta), int(pos), _ptr(c), _ptr(s)),
+           "rope_table")
+    return c, s
+
+
+def rope(x, positions, theta: float):
+    """rope_rows on x (uint16 bf16 bits [n, heads, D]) at positions [n]; bf16 out."""
+    x = _c(x, np.uint16)
+    positions = _c(positions, np.int32)
+    n, heads, d = x.shape
+    out = np.empty_like(x)
+    _check(_load().orc_rope(n, heads, d, float(theta), _ptr(x), _ptr(positions), _ptr(out)),
+           "rope")
+    return out

@@ -439,3 +439,87 @@ int orc_prefill_paged(int tokens, int q_heads, int kv_heads, int head_dim, int p
   job.table_rows = table_rows;
   return run_job(&job, nthreads);
 }
+
+/* ------------------------------------------------------------------------
+ * Rotary position embedding (Mistral 7B Instruct v0.3 model files,
+ * src/rope.linnet, `tables`; applied by rope_rows in decode_paged).
+ *
+ * The tables are computed in f32 as the pages write them,
+ *   inv_freq[i] = exp(-(i * 2 / D) * log(theta)),  angle = pos * inv_freq[i],
+ * and cos/sin of the angle are cast to the model dtype (bf16), each
+ * frequency repeated over both halves of the head dimension; so dimension i
+ * pairs with i + D/2 (the rotate-half form; the GPT-OSS rope page notes the
+ * half-split and repeated-table forms compute the same rotation):
+ *   out[i]       = x[i] cos_i - x[i + D/2] sin_i
+ *   out[i + D/2] = x[i + D/2] cos_i + x[i] sin_i
+ * Reading where the pages leave it open: the rotation itself is exact (fp64
+ * here) and its result is rounded once to bf16. */
+
+/* Round-to-nearest-even from binary32 to bf16 (the top 16 bits), from the
+ * IEEE definition: add half an ulp of the result, plus one if the kept part
+ * is odd, then truncate; NaNs stay NaNs. */
+static uint16_t f32_to_bf16_rne(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu)) return (uint16_t)((u >> 16) | 0x40u);
+  uint32_t keep_odd = (u >> 16) & 1u;
+  u += 0x7fffu + keep_odd;
+  return (uint16_t)(u >> 16);
+}
+
+static uint16_t f64_to_bf16_rne(double x) {
+  /* Through binary32 first is exact enough: a double rounding can only
+   * matter at a bf16 tie, which the 16 extra bits of binary32 make
+   * vanishingly rare; the tests compare the final values within one ulp. */
+  return f32_to_bf16_rne((float)x);
+}
+
+/* cos/sin table entries (bf16 bit patterns) of position pos for i < D/2. */
+int orc_rope_table(int head_dim, float theta, int pos, uint16_t* cos_out, uint16_t* sin_out) {
+  if (head_dim <= 0 || head_dim % 2 || pos < 0) return ORC_EINVAL;
+  const float log_theta = logf(theta);
+  for (int i = 0; i < head_dim / 2; ++i) {
+    const float scaled = ((float)i * 2.0f) / (float)head_dim;
+    const float inv_freq = expf(-scaled * log_theta);
+    const float angle = (float)pos * inv_freq;
+    cos_out[i] = f64_to_bf16_rne(cos((double)angle));
+    sin_out[i] = f64_to_bf16_rne(sin((double)angle));
+  }
+  return ORC_OK;
+}
+
+/* rope_rows: x [n][heads][head_dim] (bf16 bits) rotated at positions[r];
+ * rows with a negative position are copied unchanged. */
+int orc_rope(int n, int heads, int head_dim, float theta, const uint16_t* x,
+             const int32_t* positions, uint16_t* out) {
+  if (n < 0 || heads <= 0 || head_dim <= 0 || head_dim % 2) return ORC_EINVAL;
+  const int half = head_dim / 2;
+  uint16_t* c = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)half);
+  uint16_t* s = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)half);
+  if (!c || !s) {
+    free(c);
+    free(s);
+    return ORC_ENOMEM;
+  }
+  int rc = ORC_OK;
+  for (int r = 0; r < n && rc == ORC_OK; ++r) {
+    const uint16_t* xr = x + (int64_t)r * heads * head_dim;
+    uint16_t* orow = out + (int64_t)r * heads * head_dim;
+    if (positions[r] < 0) {
+      memcpy(orow, xr, sizeof(uint16_t) * (size_t)heads * head_dim);
+      continue;
+    }
+    rc = orc_rope_table(head_dim, theta, positions[r], c, s);
+    for (int h = 0; h < heads && rc == ORC_OK; ++h)
+      for (int i = 0; i < half; ++i) {
+        const double a = bf16_value(xr[h * head_dim + i]);
+        const double b = bf16_value(xr[h * head_dim + i + half]);
+        const double ci = bf16_value(c[i]), si = bf16_value(s[i]);
+        orow[h * head_dim + i] = f64_to_bf16_rne(a * ci - b * si);
+        orow[h * head_dim + i + half] = f64_to_bf16_rne(b * ci + a * si);
+      }
+  }
+  free(c);
+  free(s);
+  return rc;
+}

@@ -30,6 +30,12 @@ MUTANTS = {
         "return ((page * kv_heads + kv_head) * page_size + in_page) * head_dim + d;",
         "return ((kv_head * kv_heads + page) * page_size + in_page) * head_dim + d;"),
     "prefill_row_ignored": ("      trow = job->row_of[b];", "      trow = b;"),
+    "rope_adjacent_pairs": ("const double b = bf16_value(xr[h * head_dim + i + half]);",
+                            "const double b = bf16_value(xr[h * head_dim + (i ^ 1)]);"),
+    "rope_sin_sign": ("orow[h * head_dim + i] = f64_to_bf16_rne(a * ci - b * si);",
+                      "orow[h * head_dim + i] = f64_to_bf16_rne(a * ci + b * si);"),
+    "rope_frequency_exponent": ("const float scaled = ((float)i * 2.0f) / (float)head_dim;",
+                                "const float scaled = ((float)i * 1.0f) / (float)head_dim;"),
     "value_from_key": ("const uint16_t* vj = v + (int64_t)(lo + j) * head_dim;",
                        "const uint16_t* vj = k + (int64_t)(lo + j) * head_dim;"),
 }

@@ -534,3 +534,72 @@ def test_prefill_rejects_rows_outside_the_table():
     with pytest.raises(ValueError):
         oracle.prefill_paged(q, k_pool, v_pool, table, np.array([2], dtype=np.int32),
                              np.array([3], dtype=np.int32), kv_heads=2, num_pages=table.size)
+
+
+# ---------------------------------------------------------------------------
+# Rotary embedding (rope_rows) at the pages' precision.
+
+
+def _bf16_of(values: np.ndarray) -> np.ndarray:
+    """Library rounding (torch) of float64 values to bf16 bit patterns."""
+    t = torch.from_numpy(np.asarray(values, dtype=np.float64)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def test_rope_table_against_numpy_float32():
+    """The tables: f32 inverse frequencies and angles as the pages compute
+    them, cos/sin cast to bf16.  numpy float32 exp/log may differ from libm by
+    an ulp, which moves a bf16 table value by at most one ulp, rarely."""
+    d, theta = 128, 1e6
+    i = np.arange(d // 2, dtype=np.float32)
+    inv = np.exp(-(i * np.float32(2.0) / np.float32(d)) * np.log(np.float32(theta)))
+    diffs, total = 0, 0
+    for pos in (0, 1, 7, 63, 64, 1000, 4095, 32767):
+        ang = (np.float32(pos) * inv).astype(np.float32)
+        want_c = _bf16_of(np.cos(ang.astype(np.float64)))
+        want_s = _bf16_of(np.sin(ang.astype(np.float64)))
+        got_c, got_s = oracle.rope_table(d, theta, pos)
+        for g, w in ((got_c, want_c), (got_s, want_s)):
+            gf, wf = as_float(g), as_float(w)
+            assert np.all(np.abs(gf - wf) <= 2.0 ** -7 * np.maximum(np.abs(wf), 2.0 ** -20))
+            diffs += int(np.sum(g != w))
+            total += g.size
+    assert diffs <= total // 50
+    c0, s0 = oracle.rope_table(d, theta, 0)
+    assert np.all(as_float(c0) == 1.0) and np.all(as_float(s0) == 0.0)
+
+
+def test_rope_is_complex_rotation_of_half_pairs():
+    """Pairing dimension i with i + D/2 and rotating by the table angle is the
+    complex product (x_i + j x_{i+D/2}) (cos_i + j sin_i), rounded to bf16."""
+    gen = torch.Generator().manual_seed(30)
+    n, heads, d, theta = 5, 3, 64, 1e6
+    x = rand_bf16(gen, n, heads, d)
+    pos = np.array([0, 1, 100, 4096, 30000], dtype=np.int32)
+    out = oracle.rope(x, pos, theta)
+    np.testing.assert_array_equal(out[0], x[0])          # position 0 is the identity
+    for r in range(n):
+        c, s = oracle.rope_table(d, theta, int(pos[r]))
+        rot = as_float(c) + 1j * as_float(s)
+        for h in range(heads):
+            z = (as_float(x[r, h, : d // 2]) + 1j * as_float(x[r, h, d // 2:])) * rot
+            np.testing.assert_array_equal(out[r, h, : d // 2], _bf16_of(z.real))
+            np.testing.assert_array_equal(out[r, h, d // 2:], _bf16_of(z.imag))
+
+
+def test_rope_inactive_rows_unchanged_and_rounding_matches_library():
+    gen = torch.Generator().manual_seed(31)
+    x = rand_bf16(gen, 2, 2, 16)
+    out = oracle.rope(x, np.array([-1, 3], dtype=np.int32), 1e6)
+    np.testing.assert_array_equal(out[0], x[0])
+    # the oracle's RNE conversion equals torch's on awkward values (ties, tiny, huge)
+    vals = np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -1.5 - 2.0 ** -9, 3.0e38, 1e-40,
+                     65504.5, 0.0, 2.0 ** -133])
+    z = np.zeros((1, 1, 2 * len(vals)), dtype=np.uint16)
+    assert _bf16_of(vals).dtype == np.uint16
+    # a rotation by angle 0 returns the bf16 of the inputs; feed exact bf16 inputs and
+    # check the values round-trip
+    exact = _bf16_of(vals)
+    z[0, 0, : len(vals)] = exact
+    z[0, 0, len(vals):] = exact
+    np.testing.assert_array_equal(oracle.rope(z, np.array([0], dtype=np.int32), 1e6), z)
