@@ -305,12 +305,19 @@ def run_pgd(args, wl: Workload):
     if by["step"] < 4 * L2_BYTES:
         flush = torch.empty(2 ** 30, dtype=torch.uint8, device=device)
 
+    q_rot = batch.q.clone() if args.rope else None
+
     def append():
-        pgd.kv_append_paged(batch.k_new, batch.v_new, batch.table, batch.positions,
-                            batch.k_pool, batch.v_pool)
+        if args.rope:   # rope_rows on q and k fused into the append (base 1e6)
+            q_rot.copy_(batch.q)
+            pgd.rope_append_paged(q_rot, batch.k_new, batch.v_new, batch.table,
+                                  batch.positions, batch.k_pool, batch.v_pool, theta=1e6)
+        else:
+            pgd.kv_append_paged(batch.k_new, batch.v_new, batch.table, batch.positions,
+                                batch.k_pool, batch.v_pool)
 
     def decode():
-        pgd.paged_decode_attention(batch.q, batch.k_pool, batch.v_pool, batch.table,
+        pgd.paged_decode_attention(q_rot if args.rope else batch.q, batch.k_pool, batch.v_pool, batch.table,
                                    batch.positions, batch.sinks, wl.window, wl.scale,
                                    num_kv_heads=wl.kv_heads, out=out, workspace=ws,
                                    pages_per_split=args.pages_per_split,
@@ -437,7 +444,7 @@ def run_pgd(args, wl: Workload):
                    "timing": "direct calls, back to back" if flush is None
                    else "CUDA graph replay per step, events around each call",
                    "pages_per_split": args.pages_per_split or "auto",
-                   "kernel": args.kernel,
+                   "kernel": args.kernel, "rope": bool(args.rope),
                    "parallelism": f"replicas over rows x{world}"},
         "row_tokens_per_s": total_rows / (step_ms * 1e-3),
         "pct_of_nominal_8tbs": 100.0 * value / world / NOMINAL_HBM_GBS,
@@ -633,6 +640,8 @@ def main():
     ap.add_argument("--pages-per-split", type=int, default=0)
     ap.add_argument("--kernel", choices=["auto", "tensor", "cuda"], default="auto",
                     help="decode kernel variant (tensor-core or CUDA-core products)")
+    ap.add_argument("--rope", action="store_true",
+                    help="decode path: fuse rope_rows (base 1e6) into the append")
     ap.add_argument("--rows", type=int, default=0,
                     help="override the workload's row count (small profiling cases)")
     ap.add_argument("--reference-rows", type=int, default=2)

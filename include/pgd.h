@@ -165,6 +165,28 @@ PGD_API int pgd_kv_write_slots(const pgd_dims* dims, const void* k_new, const vo
                                pgd_stream_t stream);
 
 /*
+ * rope_append_paged -- rope_rows + append in one launch (Mistral 7B Instruct
+ * v0.3 model files, src/attention.linnet, decode_paged: q and k rotated at
+ * positions[b], then write_tokens; src/rope.linnet, tables with base theta).
+ *   theta         rotary base (1e6 for Mistral v0.3 and Qwen2.5).
+ *   q             bf16 [R][Hq][D], rotated in place (NULL: k only).
+ *   k_new, v_new  bf16 [R][Hkv][D], un-rotated; k is rotated on its way into
+ *                 the pool, v copied.
+ *   table, positions, pools  as for pgd_kv_append_paged; or
+ *   slots         int32 [R]: explicit pool positions (prefill), overriding
+ *                 the table (which may then be NULL); NULL otherwise.
+ * Tables as the pages compute them: inv_freq[i] = exp(-(2i / D) log theta)
+ * and angle = position * inv_freq[i] in f32, cos/sin rounded to bf16; dims i
+ * and i + D/2 are rotated together and each result rounded to bf16.
+ * Rows with positions[b] < 0 are left alone.  Device errors as for
+ * pgd_kv_append_paged (the row is then left alone, q included).
+ */
+PGD_API int pgd_rope_append_paged(const pgd_dims* dims, float theta, void* q,
+                                  const void* k_new, const void* v_new, const int32_t* table,
+                                  const int32_t* positions, const int32_t* slots, void* k_pool,
+                                  void* v_pool, pgd_stream_t stream);
+
+/*
  * Bytes of device workspace pgd_paged_decode_attention needs for these dims
  * and options on the current device: split partials (m, l and an unnormalised
  * fp32 accumulator per row, query head and split).  0 if dims are invalid.

@@ -11,6 +11,7 @@ Entry points (same names as the C ABI, without the ``pgd_`` prefix):
 - ``kv_append_paged``: write each row's new key and value at its page slot.
 - ``paged_decode_attention``: grouped-query decode attention of each row over
   its pages, with optional per-head sink logits and sliding window.
+- ``rope_append_paged``: rope_rows on q and k fused into the append.
 - ``page_slots``, ``kv_write_slots``, ``paged_prefill_attention``: packed
   prompt tokens (prefill) and prompts plus decode steps in one pass.
 - ``kv_append_rows``, ``decode_rows_attention``: the same step over dense
@@ -75,6 +76,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             opts_p = ctypes.POINTER(DecodeOptions)
             lib.pgd_kv_append_paged.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, vp]
             lib.pgd_kv_append_paged.restype = ctypes.c_int
+            lib.pgd_rope_append_paged.argtypes = [dims_p, ctypes.c_float, vp, vp, vp, vp, vp,
+                                                  vp, vp, vp, vp]
+            lib.pgd_rope_append_paged.restype = ctypes.c_int
             lib.pgd_page_slots.argtypes = [dims_p, i32, vp, vp, vp, vp, vp]
             lib.pgd_page_slots.restype = ctypes.c_int
             lib.pgd_kv_write_slots.argtypes = [dims_p, vp, vp, vp, vp, vp, vp]
@@ -224,6 +228,36 @@ def paged_decode_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.
     if rc != OK:
         raise PgdError(rc, "paged_decode_attention")
     return out
+
+
+def rope_append_paged(q: torch.Tensor | None, k_new: torch.Tensor, v_new: torch.Tensor,
+                      table: torch.Tensor | None, positions: torch.Tensor, k_pool: torch.Tensor,
+                      v_pool: torch.Tensor, *, theta: float, slots: torch.Tensor | None = None,
+                      layout: int = PAGE_MAJOR, max_pages_per_row: int | None = None,
+                      stream: torch.cuda.Stream | None = None) -> None:
+    """rope_rows + append: rotates q (bf16 [R, Hq, D], in place) and k_new at
+    positions[b] (base theta), writes rotated k and v into the pools at each
+    row's slot (from the table, or the explicit slots)."""
+    dev = _check_cuda(q, k_new, v_new, table, positions, slots, k_pool, v_pool)
+    for t, n in ((k_new, "k_new"), (v_new, "v_new"), (k_pool, "k_pool"), (v_pool, "v_pool")):
+        _dtype(t, torch.bfloat16, n)
+    if q is not None:
+        _dtype(q, torch.bfloat16, "q")
+    _dtype(positions, torch.int32, "positions")
+    rows, hkv, d = k_new.shape
+    if v_new.shape != k_new.shape or positions.shape != (rows,) or k_pool.shape != v_pool.shape \
+            or (q is not None and (q.shape[0] != rows or q.shape[2] != d)):
+        raise ValueError("inconsistent shapes")
+    width = table.shape[1] if table is not None else (max_pages_per_row or 1)
+    dims = make_dims(rows=rows, num_q_heads=q.shape[1] if q is not None else hkv,
+                     num_kv_heads=hkv, head_dim=d, num_pages=_pool_pages(k_pool, hkv, d),
+                     max_pages_per_row=width, layout=layout)
+    with torch.cuda.device(dev):
+        rc = load_library().pgd_rope_append_paged(
+            ctypes.byref(dims), float(theta), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(table),
+            _ptr(positions), _ptr(slots), _ptr(k_pool), _ptr(v_pool), _stream_handle(stream))
+    if rc != OK:
+        raise PgdError(rc, "rope_append_paged")
 
 
 def page_slots(table: torch.Tensor, positions: torch.Tensor, rows: torch.Tensor | None = None, *,

@@ -217,6 +217,51 @@ int pgd_kv_append_paged(const pgd_dims* dims, const void* k_new, const void* v_n
   return append_impl(dims, k_new, v_new, table, positions, nullptr, k_pool, v_pool, stream);
 }
 
+int pgd_rope_append_paged(const pgd_dims* dims, float theta, void* q, const void* k_new,
+                          const void* v_new, const int32_t* table, const int32_t* positions,
+                          const int32_t* slots, void* k_pool, void* v_pool, pgd_stream_t stream) {
+  int rc = check_dims(dims);
+  if (rc != PGD_OK) return rc;
+  if (dims->rows == 0) return PGD_OK;
+  if (!(theta > 0.f) || !std::isfinite(theta)) return PGD_EINVAL;
+  if (!k_new || !v_new || !positions || !k_pool || !v_pool) return PGD_EINVAL;
+  if (!slots && !table && dims->layout != PGD_ROW_MAJOR) return PGD_EINVAL;
+  if (!slots && !table && (int64_t)dims->rows * dims->max_pages_per_row > dims->num_pages)
+    return PGD_EINVAL;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool) ||
+      (q && !aligned16(q)))
+    return PGD_EINVAL;
+  DeviceInfo* dev = nullptr;
+  if ((rc = current_device(&dev)) != PGD_OK) return rc;
+  RopeAppendParams p;
+  p.q = static_cast<uint16_t*>(q);
+  p.k_new = static_cast<const uint16_t*>(k_new);
+  p.v_new = static_cast<const uint16_t*>(v_new);
+  p.table = table;
+  p.positions = positions;
+  p.slots = slots;
+  p.k_pool = static_cast<uint16_t*>(k_pool);
+  p.v_pool = static_cast<uint16_t*>(v_pool);
+  p.err = dev->err;
+  p.rows = dims->rows;
+  p.hq = dims->num_q_heads;
+  p.hkv = dims->num_kv_heads;
+  p.head_dim = dims->head_dim;
+  p.maxp = dims->max_pages_per_row;
+  p.num_pages = dims->num_pages;
+  p.layout = dims->layout;
+  if (dims->head_dim / 2 > 64) return PGD_EUNSUPPORTED;
+  // inv_freq[i] = exp(-(i * 2 / D) * log(theta)), in f32 as the tables are written
+  const float log_theta = logf(theta);
+  for (int i = 0; i < dims->head_dim / 2; ++i) {
+    const float scaled = ((float)i * 2.0f) / (float)dims->head_dim;
+    p.inv_freq[i] = expf(-scaled * log_theta);
+  }
+  return launch_rope_append(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PGD_OK
+             : PGD_ECUDA;
+}
+
 int pgd_page_slots(const pgd_dims* dims, int32_t table_rows, const int32_t* table,
                    const int32_t* rows, const int32_t* positions, int32_t* slots,
                    pgd_stream_t stream) {

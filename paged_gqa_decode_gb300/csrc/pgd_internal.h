@@ -44,6 +44,21 @@ int padded_group(int group);  // 0 if unsupported
 
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
 
+struct RopeAppendParams {
+  uint16_t* q;  // [R][Hq][D] rotated in place, or nullptr
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  const int32_t* table;
+  const int32_t* positions;
+  const int32_t* slots;  // explicit pool positions, or nullptr (table + positions)
+  uint16_t* k_pool;
+  uint16_t* v_pool;
+  unsigned int* err;
+  int rows, hq, hkv, head_dim, maxp, num_pages, layout;
+  float inv_freq[64];  // theta^(-2i/D) for i < D/2, computed in f32 on the host
+};
+cudaError_t launch_rope_append(const RopeAppendParams& p, cudaStream_t stream);
+
 struct SlotParams {
   const int32_t* table;
   const int32_t* row_of;  // nullptr: token p uses table row p
