@@ -11,6 +11,8 @@
 namespace pgd {
 
 __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
+  pdl_wait();
+  pdl_allow_dependents();
   const int b = blockIdx.x;
   int page, in_page;
   if (p.slots) {  // explicit pool position (prefill's write at the caller's slots)
@@ -61,6 +63,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
 // rounded to bf16.  One CTA per row: q is rotated in place, k is rotated on
 // its way into the pool, v is copied.
 __global__ void __launch_bounds__(256) rope_append_kernel(const RopeAppendParams p) {
+  pdl_wait();
+  pdl_allow_dependents();
   const int b = blockIdx.x;
   const int n = p.positions[b];
   if (n < 0) return;  // inactive row: nothing rotated or written
@@ -124,12 +128,13 @@ __global__ void __launch_bounds__(256) rope_append_kernel(const RopeAppendParams
 
 cudaError_t launch_rope_append(const RopeAppendParams& p, cudaStream_t stream) {
   if (p.rows == 0) return cudaSuccess;
-  rope_append_kernel<<<p.rows, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(rope_append_kernel, dim3(p.rows), dim3(256), 0, stream, p);
 }
 
 // page_slots for P tokens: one thread per token.
 __global__ void __launch_bounds__(256) page_slots_kernel(const SlotParams p) {
+  pdl_wait();
+  pdl_allow_dependents();
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= p.tokens) return;
   const int n = p.positions[t];
@@ -150,16 +155,14 @@ __global__ void __launch_bounds__(256) page_slots_kernel(const SlotParams p) {
 
 cudaError_t launch_page_slots(const SlotParams& p, cudaStream_t stream) {
   if (p.tokens == 0) return cudaSuccess;
-  page_slots_kernel<<<(p.tokens + 255) / 256, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(page_slots_kernel, dim3((p.tokens + 255) / 256), dim3(256), 0, stream, p);
 }
 
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream) {
   if (p.rows == 0) return cudaSuccess;
   const int work = 2 * p.hkv * (p.head_dim / 8);
   int threads = work < 256 ? ((work + 31) / 32) * 32 : 256;
-  kv_append_kernel<<<p.rows, threads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kv_append_kernel, dim3(p.rows), dim3(threads), 0, stream, p);
 }
 
 }  // namespace pgd

@@ -467,16 +467,25 @@ struct DecodeCfg {
   static constexpr int kHeads = Consumer::kHeads;
   static constexpr int kSmemBytes =
       1024 + kStages * kStageBytes + Consumer::kSharedFloats * 4 + 2 * kStages * 8;
+  // CTAs per SM the shared memory allows (228 KB per SM), at most 3 (three
+  // 160-thread CTAs leave 136 registers per thread); the CUDA-core consumer
+  // keeps its registers (no bound).
+  static constexpr int kSmemBlocks = (228 * 1024) / (kSmemBytes + 1024);
+  static constexpr int kMinBlocks =
+      Consumer::kSharedFloats > 0 ? 1 : (kSmemBlocks >= 3 ? 3 : kSmemBlocks);
   static_assert(kWarps * kHeads * (D + 2) * 4 <= kStages * kStageBytes, "merge buffer");
   static_assert(D == 64 || D == 128, "head_dim");
 };
 
 template <int D, int STAGES, class Consumer>
-__global__ void __launch_bounds__(DecodeCfg<D, STAGES, Consumer>::kThreads)
+__global__ void __launch_bounds__(DecodeCfg<D, STAGES, Consumer>::kThreads,
+                                  DecodeCfg<D, STAGES, Consumer>::kMinBlocks)
     paged_decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                               const __grid_constant__ CUtensorMap v_map, const DecodeParams p) {
   using C = DecodeCfg<D, STAGES, Consumer>;
   constexpr int GP = C::kHeads;
+  pdl_wait();
+  pdl_allow_dependents();
   const int split = blockIdx.x;
   const int kvh = blockIdx.y;
   const int b = blockIdx.z;
@@ -649,9 +658,13 @@ __global__ void __launch_bounds__(DecodeCfg<D, STAGES, Consumer>::kThreads)
 // (recording PGD_EDEVICE_BOUNDS) and rows with a split skipped for a bad
 // table entry (marked l < 0).
 // One warp per (row, query head); lane l owns dims [D/32 * l, D/32 * (l + 1)).
+// The splits' (m, l) are read 32 at a time, one per lane, so the loads are
+// independent; the weights are then broadcast by shuffle.
 template <int D>
 __global__ void __launch_bounds__(128) paged_decode_combine_kernel(const DecodeParams p) {
   constexpr int kDims = D / 32;
+  pdl_wait();
+  pdl_allow_dependents();
   const int b = blockIdx.y;
   const int h = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -677,34 +690,45 @@ __global__ void __launch_bounds__(128) paged_decode_combine_kernel(const DecodeP
   const float sk = p.sinks ? p.sinks[h] * kLog2e : -INFINITY;
   float mx = sk;
   bool skipped = false;
-  for (int i = 0; i < nsplit; ++i) {
-    mx = fmaxf(mx, ml[2 * i]);
-    skipped |= ml[2 * i + 1] < 0.f;
+  for (int base = 0; base < nsplit; base += 32) {
+    const int i = base + lane;
+    const float mi = i < nsplit ? ml[2 * i] : -INFINITY;
+    const float li = i < nsplit ? ml[2 * i + 1] : 0.f;
+    mx = fmaxf(mx, warp_max(mi));
+    skipped |= __any_sync(0xffffffffu, li < 0.f);
   }
-  float res[kDims];
-#pragma unroll
-  for (int j = 0; j < kDims; ++j) res[j] = 0.f;
   if (skipped || mx == -INFINITY) {
 #pragma unroll
     for (int j = 0; j < kDims; ++j) o[j] = 0;
     return;
   }
-  float den = exp2_approx(sk - mx);
-  for (int i = 0; i < nsplit; ++i) {
-    const float f = exp2_approx(ml[2 * i] - mx);
-    den = fmaf(ml[2 * i + 1], f, den);
-    if constexpr (kDims == 2) {
-      const float2 a = *reinterpret_cast<const float2*>(ac + (size_t)i * D);
-      res[0] = fmaf(a.x, f, res[0]);
-      res[1] = fmaf(a.y, f, res[1]);
-    } else {
-      const float4 a = *reinterpret_cast<const float4*>(ac + (size_t)i * D);
-      res[0] = fmaf(a.x, f, res[0]);
-      res[1] = fmaf(a.y, f, res[1]);
-      res[2] = fmaf(a.z, f, res[2]);
-      res[3] = fmaf(a.w, f, res[3]);
+  float res[kDims];
+#pragma unroll
+  for (int j = 0; j < kDims; ++j) res[j] = 0.f;
+  float den = 0.f;
+  for (int base = 0; base < nsplit; base += 32) {
+    const int i = base + lane;
+    const float fi = i < nsplit ? exp2_approx(ml[2 * i] - mx) : 0.f;
+    den += warp_sum(i < nsplit ? ml[2 * i + 1] * fi : 0.f);
+    const int cnt = min(32, nsplit - base);
+#pragma unroll 4
+    for (int k = 0; k < cnt; ++k) {
+      const float f = __shfl_sync(0xffffffffu, fi, k);
+      const float* a = ac + (size_t)(base + k) * D;
+      if constexpr (kDims == 2) {
+        const float2 v = *reinterpret_cast<const float2*>(a);
+        res[0] = fmaf(v.x, f, res[0]);
+        res[1] = fmaf(v.y, f, res[1]);
+      } else {
+        const float4 v = *reinterpret_cast<const float4*>(a);
+        res[0] = fmaf(v.x, f, res[0]);
+        res[1] = fmaf(v.y, f, res[1]);
+        res[2] = fmaf(v.z, f, res[2]);
+        res[3] = fmaf(v.w, f, res[3]);
+      }
     }
   }
+  den += exp2_approx(sk - mx);
   const float inv = 1.f / den;
 #pragma unroll
   for (int j = 0; j < kDims; ++j) o[j] = __bfloat16_as_ushort(__float2bfloat16_rn(res[j] * inv));
@@ -724,17 +748,19 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& k_map,
     e = cudaFuncSetAttribute(paged_decode_split_kernel<D, STAGES, Consumer>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(paged_decode_split_kernel<D, STAGES, Consumer>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev].store(true, std::memory_order_release);
   }
   if (p.rows == 0) return cudaSuccess;
   dim3 grid(grid_splits, p.hkv, p.rows);
-  paged_decode_split_kernel<D, STAGES, Consumer>
-      <<<grid, C::kThreads, C::kSmemBytes, stream>>>(k_map, v_map, p);
-  e = cudaGetLastError();
+  e = launch_pdl(paged_decode_split_kernel<D, STAGES, Consumer>, grid, dim3(C::kThreads),
+                 C::kSmemBytes, stream, k_map, v_map, p);
   if (e != cudaSuccess) return e;
   dim3 cgrid((p.hq + 3) / 4, p.rows);
-  paged_decode_combine_kernel<D><<<cgrid, 128, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(paged_decode_combine_kernel<D>, cgrid, dim3(128), 0, stream, p);
 }
 
 // Kernel choice for one head_dim: the tensor-core consumer unless the caller
@@ -742,10 +768,19 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& k_map,
 template <int D>
 cudaError_t launch_decode_for_dim(const DecodeParams& p, const CUtensorMap& k_map,
                                   const CUtensorMap& v_map, int padded, int kernel,
-                                  int grid_splits, cudaStream_t stream) {
+                                  int grid_splits, int pages_per_cta, cudaStream_t stream) {
   constexpr int kStages = D == 128 ? 3 : 6;
-  if (kernel != PGD_KERNEL_CUDA_CORE)
+  if (kernel != PGD_KERNEL_CUDA_CORE) {
+    // A ring no deeper than the pages a split can stream: shallower rings let
+    // more CTAs share an SM when splits are short (windows, small contexts).
+    if (pages_per_cta <= 1)
+      return launch_decode<D, 1, MmaConsumer<D>>(p, k_map, v_map, grid_splits, stream);
+    if (pages_per_cta <= 2)
+      return launch_decode<D, 2, MmaConsumer<D>>(p, k_map, v_map, grid_splits, stream);
+    if (D == 64 && pages_per_cta <= 3)
+      return launch_decode<D, 3, MmaConsumer<D>>(p, k_map, v_map, grid_splits, stream);
     return launch_decode<D, kStages, MmaConsumer<D>>(p, k_map, v_map, grid_splits, stream);
+  }
   switch (padded) {
     case 1: return launch_decode<D, kStages, ScalarConsumer<D, 1>>(p, k_map, v_map, grid_splits, stream);
     case 2: return launch_decode<D, kStages, ScalarConsumer<D, 2>>(p, k_map, v_map, grid_splits, stream);

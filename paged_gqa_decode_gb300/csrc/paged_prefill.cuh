@@ -56,6 +56,8 @@ __global__ void __launch_bounds__(PrefillCfg<D, GP, STAGES>::kThreads)
   using C = PrefillCfg<D, GP, STAGES>;
   constexpr int kSteps = D / 16;   // k-steps of Q.K^T
   constexpr int kDimTiles = D / 8;  // n-tiles of P.V
+  pdl_wait();
+  pdl_allow_dependents();
   const int kvh = blockIdx.y;
   const int t_begin = blockIdx.x * C::kTokens;
   const int t_end = min(t_begin + C::kTokens, p.rows);
@@ -351,7 +353,7 @@ __global__ void __launch_bounds__(PrefillCfg<D, GP, STAGES>::kThreads)
           const uint32_t l3_ = pack_bf16x2(sc[2 * kk + 1][2] - bf16_lo(h3_),
                                            sc[2 * kk + 1][3] - bf16_hi(h3_));
 #pragma unroll
-          for (int jp = 0; jp < kDimTiles / 2; ++jp) {  // dim tiles 2jp, 2jp+1
+          for (int jp = 0; jp < kDimTiles / 2; ++jp) {
             uint32_t b0, b1, b2, b3;
             ldsm_x4_trans(vt + (jp >> 2) * kBoxBytes + kk * 2048 + off_v[jp & 3], b0, b1, b2, b3);
             mma_bf16(o[2 * jp], h0_, h1_, h2_, h3_, b0, b1);
@@ -409,12 +411,16 @@ cudaError_t launch_prefill(const DecodeParams& p, const CUtensorMap& k_map,
     e = cudaFuncSetAttribute(paged_prefill_kernel<D, GP, STAGES>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(paged_prefill_kernel<D, GP, STAGES>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev].store(true, std::memory_order_release);
   }
   if (p.rows == 0) return cudaSuccess;
   dim3 grid((p.rows + C::kTokens - 1) / C::kTokens, p.hkv);
-  paged_prefill_kernel<D, GP, STAGES><<<grid, C::kThreads, C::kSmemBytes, stream>>>(k_map, v_map, p);
-  return cudaGetLastError();
+  return launch_pdl(paged_prefill_kernel<D, GP, STAGES>, grid, dim3(C::kThreads), C::kSmemBytes,
+                    stream, k_map, v_map, p);
 }
 
 template <int D>

@@ -363,6 +363,7 @@ static int decode_impl(const pgd_dims* dims, int32_t table_rows, const int32_t* 
     if (wp < grid_pages) grid_pages = (int)wp;
   }
   const int grid_splits = (grid_pages + pl.pages_per_split - 1) / pl.pages_per_split;
+  const int pages_per_cta = grid_pages < pl.pages_per_split ? grid_pages : pl.pages_per_split;
 
   const int padded = padded_group(p.group);
   int kernel = opts ? opts->kernel : PGD_KERNEL_AUTO;
@@ -379,8 +380,9 @@ static int decode_impl(const pgd_dims* dims, int32_t table_rows, const int32_t* 
                ? PGD_OK
                : PGD_ECUDA;
   cudaError_t e =
-      dims->head_dim == 64 ? launch_decode_d64(p, k_map, v_map, padded, kernel, grid_splits, st)
-                           : launch_decode_d128(p, k_map, v_map, padded, kernel, grid_splits, st);
+      dims->head_dim == 64
+          ? launch_decode_d64(p, k_map, v_map, padded, kernel, grid_splits, pages_per_cta, st)
+          : launch_decode_d128(p, k_map, v_map, padded, kernel, grid_splits, pages_per_cta, st);
   return e == cudaSuccess ? PGD_OK : PGD_ECUDA;
 }
 

@@ -6,9 +6,28 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "pgd.h"
 
 namespace pgd {
+
+// Launches `kernel` with programmatic stream serialization (see pdl_wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 struct AppendParams {
   const uint16_t* k_new;  // [R][Hkv][D] bf16
@@ -71,12 +90,13 @@ cudaError_t launch_page_slots(const SlotParams& p, cudaStream_t stream);
 
 // Split kernel + combine kernel for one head_dim; `padded` is the padded
 // group size, `kernel` a PGD_KERNEL_* choice.
+// `pages_per_cta` bounds the pages one split streams (it picks the ring depth).
 cudaError_t launch_decode_d64(const DecodeParams& p, const CUtensorMap& k_map,
                               const CUtensorMap& v_map, int padded, int kernel, int grid_splits,
-                              cudaStream_t stream);
+                              int pages_per_cta, cudaStream_t stream);
 cudaError_t launch_decode_d128(const DecodeParams& p, const CUtensorMap& k_map,
                                const CUtensorMap& v_map, int padded, int kernel, int grid_splits,
-                               cudaStream_t stream);
+                               int pages_per_cta, cudaStream_t stream);
 
 // Tiled prefill (tokens of a block share each page load); no key splits.
 cudaError_t launch_prefill_tiled(const DecodeParams& p, const CUtensorMap& k_map,
