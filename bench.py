@@ -204,9 +204,13 @@ def kernel_traffic(source_digest: str, workload: str):
 
 
 def source_digest() -> str:
+    """Digest of the sources the decode step is built from (the prefill
+    kernel's own files excluded)."""
     csrc = os.path.join(ROOT, "paged_gqa_decode_gb300", "csrc")
     h = hashlib.sha256()
     for name in sorted(os.listdir(csrc)):
+        if name.startswith("paged_prefill"):
+            continue
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -333,22 +337,28 @@ def run_pgd(args, wl: Workload):
     # Small workloads run between L2 flushes; their calls are captured once
     # as CUDA graphs so host-side call overhead cannot land inside the timed
     # device spans.  Large ones are called directly (the host runs far ahead).
-    step_append, step_decode = append, decode
+    step_append, step_decode, step_whole = append, decode, None
     if flush is not None:
+        # the whole step (append + decode, launched back to back so each kernel
+        # overlaps its predecessor's tail) and each call alone, as graphs
         side = torch.cuda.Stream()
         side.wait_stream(stream)
         graphs = []
+
+        def whole():
+            append()
+            decode()
+
         with torch.cuda.stream(side):
-            for fn in (append, decode):
+            for fn in (append, decode, whole):
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g, stream=side):
                     fn()
                 graphs.append(g)
         torch.cuda.synchronize()
-        step_append, step_decode = graphs[0].replay, graphs[1].replay
+        step_append, step_decode, step_whole = (g.replay for g in graphs)
         for _ in range(3):
-            step_append()
-            step_decode()
+            step_whole()
         torch.cuda.synchronize()
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
@@ -359,13 +369,17 @@ def run_pgd(args, wl: Workload):
     torch.cuda.synchronize()
     clocks.mark_start()
     for i in range(args.steps):
-        if flush is not None:
+        if flush is not None:      # whole steps between flushes
             flush.fill_(i & 0xFF)
-        ev[i][0].record(stream)
-        step_append()
-        ev[i][1].record(stream)
-        step_decode()
-        ev[i][2].record(stream)
+            ev[i][0].record(stream)
+            step_whole()
+            ev[i][2].record(stream)
+        else:                      # back to back, a span per call
+            ev[i][0].record(stream)
+            step_append()
+            ev[i][1].record(stream)
+            step_decode()
+            ev[i][2].record(stream)
     torch.cuda.synchronize()
     clocks.mark_end()
     barrier(world)
@@ -373,9 +387,24 @@ def run_pgd(args, wl: Workload):
     status = pgd.get_device_error()
     if status != pgd.OK:
         raise RuntimeError(f"device error in the timed region: {pgd.status_string(status)}")
-    append_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
-    decode_ms = sum(e[1].elapsed_time(e[2]) for e in ev)
-    step_ms = append_ms + decode_ms if flush is not None else ev[0][0].elapsed_time(ev[-1][2])
+    if flush is None:
+        append_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
+        decode_ms = sum(e[1].elapsed_time(e[2]) for e in ev)
+        step_ms = ev[0][0].elapsed_time(ev[-1][2])
+    else:
+        step_ms = sum(e[0].elapsed_time(e[2]) for e in ev)
+        # each call alone, for the per-kernel spans (outside the step timing)
+        spans = {"append": 0.0, "decode": 0.0}
+        for i in range(args.steps):
+            for name, fn in (("append", step_append), ("decode", step_decode)):
+                flush.fill_(i & 0xFF)
+                a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                z.record(stream)
+                torch.cuda.synchronize()
+                spans[name] += a.elapsed_time(z)
+        append_ms, decode_ms = spans["append"], spans["decode"]
     step_ms = max_over_ranks(step_ms, world, device)
     decode_ms = max_over_ranks(decode_ms, world, device)
     total_bytes = sum_over_ranks(by["step"] * args.steps, world, device)
@@ -442,7 +471,7 @@ def run_pgd(args, wl: Workload):
                    "pool_gb_per_gpu": 2 * lay.num_pages * wl.kv_heads * 64 * wl.head_dim * 2 / 1e9,
                    "l2": "inputs larger than L2" if flush is None else "1 GiB L2 flush between steps",
                    "timing": "direct calls, back to back" if flush is None
-                   else "CUDA graph replay per step, events around each call",
+                   else "CUDA graph replay of each whole step; each call alone for its span",
                    "pages_per_split": args.pages_per_split or "auto",
                    "kernel": args.kernel, "rope": bool(args.rope),
                    "parallelism": f"replicas over rows x{world}"},
