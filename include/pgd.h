@@ -288,6 +288,18 @@ PGD_API int pgd_paged_decode_attention_static(const pgd_dims* dims, const void* 
  * synchronisation itself failed. */
 PGD_API int pgd_get_device_error(pgd_stream_t stream);
 
+/*
+ * Self-test of failure detection, not part of the attention path: launches a
+ * one-thread kernel whose two pipeline waits (an mbarrier phase and a shared
+ * word, as the decode and prefill kernels use them) are never satisfied.
+ * Each gives up after its limit (2 s), so the call takes about 4 s; the
+ * kernel records PGD_EDEVICE_TIMEOUT and returns without faulting.
+ *   outcome  device int: bit 0 / bit 1 set if the first / second wait was
+ *            (wrongly) satisfied; 0 after a correct run.
+ * Read the status with pgd_get_device_error; the context stays usable.
+ */
+PGD_API int pgd_selftest_bounded_wait(int32_t* outcome, pgd_stream_t stream);
+
 /* A static, human-readable name for a status code. */
 PGD_API const char* pgd_status_string(int status);
 

@@ -79,6 +79,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             lib.pgd_rope_append_paged.argtypes = [dims_p, ctypes.c_float, vp, vp, vp, vp, vp,
                                                   vp, vp, vp, vp]
             lib.pgd_rope_append_paged.restype = ctypes.c_int
+            lib.pgd_selftest_bounded_wait.argtypes = [vp, vp]
+            lib.pgd_selftest_bounded_wait.restype = ctypes.c_int
             lib.pgd_page_slots.argtypes = [dims_p, i32, vp, vp, vp, vp, vp]
             lib.pgd_page_slots.restype = ctypes.c_int
             lib.pgd_kv_write_slots.argtypes = [dims_p, vp, vp, vp, vp, vp, vp]
@@ -426,6 +428,17 @@ def decode_rows_attention(q: torch.Tensor, cache_k: torch.Tensor, cache_v: torch
     if rc != OK:
         raise PgdError(rc, "decode_rows_attention")
     return out
+
+
+def selftest_bounded_wait(stream: torch.cuda.Stream | None = None) -> tuple[int, int]:
+    """Runs the bounded-wait self-test (about 4 s): returns (device status,
+    outcome bits); a correct run gives (EDEVICE_TIMEOUT, 0)."""
+    outcome = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    rc = load_library().pgd_selftest_bounded_wait(_ptr(outcome), _stream_handle(stream))
+    if rc != OK:
+        raise PgdError(rc, "selftest_bounded_wait")
+    status = get_device_error(stream)
+    return status, int(outcome.item())
 
 
 def get_device_error(stream: torch.cuda.Stream | None = None) -> int:

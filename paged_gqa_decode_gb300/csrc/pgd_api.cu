@@ -421,6 +421,17 @@ int pgd_get_device_error(pgd_stream_t stream) {
   return (int)word;
 }
 
+int pgd_selftest_bounded_wait(int32_t* outcome, pgd_stream_t stream) {
+  if (!outcome) return PGD_EINVAL;
+  DeviceInfo* dev = nullptr;
+  const int rc = current_device(&dev);
+  if (rc != PGD_OK) return rc;
+  return launch_bounded_wait_selftest(dev->err, outcome, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? PGD_OK
+             : PGD_ECUDA;
+}
+
 const char* pgd_status_string(int status) {
   switch (status) {
     case PGD_OK: return "ok";

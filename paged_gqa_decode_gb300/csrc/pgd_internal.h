@@ -87,6 +87,7 @@ struct SlotParams {
   int tokens, table_rows, maxp, num_pages;
 };
 cudaError_t launch_page_slots(const SlotParams& p, cudaStream_t stream);
+cudaError_t launch_bounded_wait_selftest(unsigned int* err, int* outcome, cudaStream_t stream);
 
 // Split kernel + combine kernel for one head_dim; `padded` is the padded
 // group size, `kernel` a PGD_KERNEL_* choice.

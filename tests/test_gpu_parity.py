@@ -315,3 +315,14 @@ def test_cuda_graph_replay_matches_eager():
         graph.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, want)
+
+
+def test_bounded_waits_time_out_into_an_error_and_the_context_survives():
+    """A pipeline wait that nothing satisfies gives up after its limit and
+    reports PGD_EDEVICE_TIMEOUT; no fault, and a normal step works after."""
+    status, outcome = pgd.selftest_bounded_wait()
+    assert status == pgd.EDEVICE_TIMEOUT
+    assert outcome == 0
+    wl = WORKLOADS["qwen_small"]
+    batch = make_batch(wl, seed=1000, device=DEV)
+    run_and_check(batch)
