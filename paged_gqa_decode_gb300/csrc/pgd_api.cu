@@ -21,6 +21,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kPageSize = 64;
+constexpr int kMinPagesPerSplit = 16;
 constexpr int kMaxPagesPerSplit = 64;
 
 struct DeviceInfo {
@@ -75,7 +76,10 @@ struct Plan {
 };
 
 // Pages per split: enough CTAs for several waves of 2 CTAs per SM when rows
-// are about half full, capped so one split is at most 64 pages.
+// are about half full, but at least 16 pages (a sweep over 1..64 on GB300
+// found every workload fastest at 16 or more: a split's fixed costs --
+// setup, merge, partials and the combine -- outweigh the parallelism that
+// shorter splits add) and at most 64.
 Plan make_plan(const pgd_dims* d, const pgd_decode_options* opts, int sm_count) {
   Plan pl;
   int pps = opts ? opts->pages_per_split : 0;
@@ -84,7 +88,8 @@ Plan make_plan(const pgd_dims* d, const pgd_decode_options* opts, int sm_count) 
     const int64_t expected = (int64_t)d->rows * d->num_kv_heads *
                              (d->max_pages_per_row > 1 ? d->max_pages_per_row / 2 : 1);
     int64_t v = (expected + target - 1) / target;
-    pps = (int)(v < 1 ? 1 : (v > kMaxPagesPerSplit ? kMaxPagesPerSplit : v));
+    pps = (int)(v < kMinPagesPerSplit ? kMinPagesPerSplit
+                                      : (v > kMaxPagesPerSplit ? kMaxPagesPerSplit : v));
   }
   if (pps > d->max_pages_per_row) pps = d->max_pages_per_row;
   pl.pages_per_split = pps;
