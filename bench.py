@@ -325,7 +325,7 @@ def run_pgd(args, wl: Workload):
                                    batch.positions, batch.sinks, wl.window, wl.scale,
                                    num_kv_heads=wl.kv_heads, out=out, workspace=ws,
                                    pages_per_split=args.pages_per_split,
-                                   kernel={"auto": 0, "tensor": 1, "cuda": 2}[args.kernel])
+                                   kernel=KERNEL_IDS[args.kernel])
 
     for _ in range(args.warmup):
         append()
@@ -518,6 +518,10 @@ def prefill_work(wl, b) -> dict:
             "flops": flops, "tokens": tokens}
 
 
+# --kernel names -> PGD_KERNEL_* values
+KERNEL_IDS = {"auto": 0, "tensor": 1, "cuda": 2, "tiled": 3, "umma": 4}
+
+
 def measured_tensor_peak() -> tuple[float, str]:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -537,7 +541,7 @@ def run_prefill(args, wl):
     b = make_prefill_batch(wl, 2000 + list(PREFILL_WORKLOADS).index(wl.name), device)
     work = prefill_work(wl, b)
     opts = dict(num_kv_heads=wl.kv_heads, pages_per_split=args.pages_per_split,
-                kernel={"auto": 0, "tensor": 1, "cuda": 2}[args.kernel])
+                kernel=KERNEL_IDS[args.kernel])
     out = torch.empty_like(b.q)
     dims = pgd.make_dims(rows=work["tokens"], num_q_heads=wl.q_heads, num_kv_heads=wl.kv_heads,
                          head_dim=wl.head_dim, num_pages=b.num_pages,
@@ -605,7 +609,7 @@ def run_rows(args, wl):
     b = make_rows_batch(wl, 3000 + list(ROWS_WORKLOADS).index(wl.name), device)
     by = algorithmic_bytes(wl, b.positions_np)
     out = torch.empty_like(b.q)
-    kernel = {"auto": 0, "tensor": 1, "cuda": 2}[args.kernel]
+    kernel = KERNEL_IDS[args.kernel]
 
     def step():
         pgd.kv_append_rows(b.k_new, b.v_new, b.positions, b.cache_k, b.cache_v)
@@ -667,8 +671,9 @@ def main():
                     help=f"decode: {', '.join(WORKLOADS)}; prefill: mistral_prefill, "
                          "gptoss_prefill_sliding")
     ap.add_argument("--pages-per-split", type=int, default=0)
-    ap.add_argument("--kernel", choices=["auto", "tensor", "cuda"], default="auto",
-                    help="decode kernel variant (tensor-core or CUDA-core products)")
+    ap.add_argument("--kernel", choices=list(KERNEL_IDS), default="auto",
+                    help="kernel variant: decode tensor-core or CUDA-core products; prefill "
+                         "also the token-block kernels (mma.sync 'tiled', tcgen05 'umma')")
     ap.add_argument("--rope", action="store_true",
                     help="decode path: fuse rope_rows (base 1e6) into the append")
     ap.add_argument("--rows", type=int, default=0,

@@ -101,9 +101,12 @@ enum {
   PGD_KERNEL_AUTO = 0,          /* decode: tensor-core; prefill: see below */
   PGD_KERNEL_TENSOR_CORE = 1,   /* mma.sync bf16 products, fp32 accumulate, per token */
   PGD_KERNEL_CUDA_CORE = 2,     /* fp32 FMA products on the CUDA cores, per token */
-  PGD_KERNEL_PREFILL_TILED = 3  /* prefill only: blocks of tokens share each page
-                                   load (tensor cores, no key splits); AUTO picks
-                                   it when the blocks fill the GPU */
+  PGD_KERNEL_PREFILL_TILED = 3, /* prefill only: blocks of tokens share each page
+                                   load (mma.sync tensor cores, no key splits);
+                                   AUTO picks it when the blocks fill the GPU */
+  PGD_KERNEL_PREFILL_UMMA = 4   /* prefill only: 128 query rows per block on the
+                                   tcgen05 tensor cores (TMEM accumulators), no
+                                   key splits */
 };
 
 /* Optional tuning of the decode launch; pass NULL for the defaults.  The same

@@ -53,7 +53,8 @@ class Dims(ctypes.Structure):
         "max_pages_per_row", "layout")]
 
 
-KERNEL_AUTO, KERNEL_TENSOR_CORE, KERNEL_CUDA_CORE, KERNEL_PREFILL_TILED = range(4)
+KERNEL_AUTO, KERNEL_TENSOR_CORE, KERNEL_CUDA_CORE, KERNEL_PREFILL_TILED, KERNEL_PREFILL_UMMA = \
+    range(5)
 
 
 class DecodeOptions(ctypes.Structure):

@@ -1,0 +1,12 @@
+// Prefill kernels on the tcgen05 tensor cores for head_dim 64 and 128.
+#include "paged_prefill_umma.cuh"
+
+namespace pgd {
+
+cudaError_t launch_prefill_umma(const DecodeParams& p, const CUtensorMap& k_map,
+                                const CUtensorMap& v_map, int head_dim, cudaStream_t stream) {
+  return head_dim == 64 ? launch_prefill_umma<64, 6>(p, k_map, v_map, stream)
+                        : launch_prefill_umma<128, 3>(p, k_map, v_map, stream);
+}
+
+}  // namespace pgd

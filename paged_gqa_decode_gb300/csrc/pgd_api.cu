@@ -372,14 +372,19 @@ static int decode_impl(const pgd_dims* dims, int32_t table_rows, const int32_t* 
 
   const int padded = padded_group(p.group);
   int kernel = opts ? opts->kernel : PGD_KERNEL_AUTO;
-  if (kernel < PGD_KERNEL_AUTO || kernel > PGD_KERNEL_PREFILL_TILED) return PGD_EINVAL;
-  if (kernel == PGD_KERNEL_PREFILL_TILED && row_of == nullptr) return PGD_EINVAL;
+  if (kernel < PGD_KERNEL_AUTO || kernel > PGD_KERNEL_PREFILL_UMMA) return PGD_EINVAL;
+  if ((kernel == PGD_KERNEL_PREFILL_TILED || kernel == PGD_KERNEL_PREFILL_UMMA) &&
+      row_of == nullptr)
+    return PGD_EINVAL;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (row_of != nullptr && kernel == PGD_KERNEL_AUTO) {
     const int64_t blocks = ((int64_t)dims->rows + prefill_block_tokens(padded) - 1) /
                            prefill_block_tokens(padded);
     if (blocks * dims->num_kv_heads >= 2ll * dev->sm_count) kernel = PGD_KERNEL_PREFILL_TILED;
   }
+  if (kernel == PGD_KERNEL_PREFILL_UMMA)
+    return launch_prefill_umma(p, k_map, v_map, dims->head_dim, st) == cudaSuccess ? PGD_OK
+                                                                                   : PGD_ECUDA;
   if (kernel == PGD_KERNEL_PREFILL_TILED)
     return launch_prefill_tiled(p, k_map, v_map, dims->head_dim, padded, st) == cudaSuccess
                ? PGD_OK

@@ -105,4 +105,8 @@ cudaError_t launch_prefill_tiled(const DecodeParams& p, const CUtensorMap& k_map
                                  cudaStream_t stream);
 int prefill_block_tokens(int padded);
 
+// Prefill on the tcgen05 tensor cores: 128 / group tokens per block.
+cudaError_t launch_prefill_umma(const DecodeParams& p, const CUtensorMap& k_map,
+                                const CUtensorMap& v_map, int head_dim, cudaStream_t stream);
+
 }  // namespace pgd

@@ -128,7 +128,8 @@ SMALL = [
 
 @pytest.mark.parametrize("name,hq,hkv,d,window,sinks", SMALL)
 @pytest.mark.parametrize("kernel,pps", [(pgd.KERNEL_TENSOR_CORE, 0), (pgd.KERNEL_TENSOR_CORE, 1),
-                                        (pgd.KERNEL_PREFILL_TILED, 0)])
+                                        (pgd.KERNEL_PREFILL_TILED, 0),
+                                        (pgd.KERNEL_PREFILL_UMMA, 0)])
 def test_prefill_small(name, hq, hkv, d, window, sinks, kernel, pps):
     wl = PrefillWorkload(name, rows=4, q_heads=hq, kv_heads=hkv, head_dim=d, prefix_lo=0,
                          prefix_hi=300, chunk=0, window=window, sinks=sinks)
@@ -137,14 +138,20 @@ def test_prefill_small(name, hq, hkv, d, window, sinks, kernel, pps):
     prefill_check(b, pps=pps, kernel=kernel, what=f"prefill {name} k={kernel} pps={pps}")
 
 
-@pytest.mark.parametrize("hq,hkv,d", [(8, 8, 64), (4, 2, 128), (12, 4, 64), (10, 2, 64)])
-def test_prefill_tiled_groups_and_long_prefix(hq, hkv, d):
-    """Group sizes 1, 2, 3 (padded to 4) and 5 (padded to 8) in the tiled
-    kernel, chunks that start mid-page after long prefixes."""
+TILED_KERNELS = [pgd.KERNEL_PREFILL_TILED, pgd.KERNEL_PREFILL_UMMA]
+
+
+@pytest.mark.parametrize("kernel", TILED_KERNELS)
+@pytest.mark.parametrize("hq,hkv,d", [(8, 8, 64), (4, 2, 128), (12, 4, 64), (10, 2, 64),
+                                      (64, 8, 64)])
+def test_prefill_tiled_groups_and_long_prefix(hq, hkv, d, kernel):
+    """Group sizes 1, 2, 3, 5 and 8 in the token-block kernels (blocks of
+    128 / G tokens on the tcgen05 kernel, so 25 tokens and 125 query rows for
+    G = 5), chunks that start mid-page after long prefixes."""
     wl = PrefillWorkload("tiled", rows=3, q_heads=hq, kv_heads=hkv, head_dim=d, prefix_lo=0,
                          prefix_hi=3000, chunk=0, window=0, sinks=True)
     b = make_prefill_batch(wl, 16 + hq, DEV, prefix=[2000, 37, 1500], chunks=[70, 150, 9])
-    prefill_check(b, kernel=pgd.KERNEL_PREFILL_TILED, what=f"tiled {hq}/{hkv} d{d}")
+    prefill_check(b, kernel=kernel, what=f"kernel {kernel} {hq}/{hkv} d{d}")
 
 
 @pytest.mark.parametrize("layout", [pgd.PAGE_MAJOR, pgd.HEAD_MAJOR])
@@ -155,7 +162,7 @@ def test_prefill_head_major_and_cuda_core(layout):
     prefill_check(b, layout=layout, kernel=pgd.KERNEL_CUDA_CORE if layout else pgd.KERNEL_AUTO)
 
 
-@pytest.mark.parametrize("kernel", [pgd.KERNEL_AUTO, pgd.KERNEL_PREFILL_TILED])
+@pytest.mark.parametrize("kernel", [pgd.KERNEL_AUTO] + TILED_KERNELS)
 def test_prefill_interleaved_token_order(kernel):
     """Packed tokens need not be grouped by row or sorted by position."""
     wl = PrefillWorkload("mixed", rows=3, q_heads=8, kv_heads=2, head_dim=128, prefix_lo=0,
@@ -169,7 +176,7 @@ def test_prefill_interleaved_token_order(kernel):
     prefill_check(b, kernel=kernel)
 
 
-@pytest.mark.parametrize("kernel", [pgd.KERNEL_AUTO, pgd.KERNEL_PREFILL_TILED])
+@pytest.mark.parametrize("kernel", [pgd.KERNEL_AUTO] + TILED_KERNELS)
 def test_step_paged_prompts_and_steps_in_one_call(kernel):
     """step_paged: two rows prefill a chunk, three other rows take a decode
     step; one write of every token and one attention call over all of them
@@ -182,18 +189,19 @@ def test_step_paged_prompts_and_steps_in_one_call(kernel):
     prefill_check(b, kernel=kernel, what="step_paged")
 
 
+@pytest.mark.parametrize("kernel", [pgd.KERNEL_AUTO] + TILED_KERNELS)
 @pytest.mark.parametrize("name,sample", [("mistral_prefill", 192), ("gptoss_prefill_sliding", 256)])
-def test_prefill_full_size_sampled(name, sample):
+def test_prefill_full_size_sampled(name, sample, kernel):
     wl = PREFILL_WORKLOADS[name]
     b = make_prefill_batch(wl, 2000 + list(PREFILL_WORKLOADS).index(name), DEV)
     rng = np.random.default_rng(3)
     tokens = len(b.rows_np)
     idx = np.unique(np.concatenate([rng.choice(tokens, size=sample - 2, replace=False),
                                     [0, tokens - 1]]))
-    prefill_check(b, sample=idx)
+    prefill_check(b, sample=idx, kernel=kernel)
 
 
-@pytest.mark.parametrize("kernel", [pgd.KERNEL_TENSOR_CORE, pgd.KERNEL_PREFILL_TILED])
+@pytest.mark.parametrize("kernel", [pgd.KERNEL_TENSOR_CORE] + TILED_KERNELS)
 def test_prefill_bad_rows_and_pages_are_zero_and_reported(kernel):
     wl = PrefillWorkload("bad", rows=2, q_heads=8, kv_heads=2, head_dim=64, prefix_lo=0,
                          prefix_hi=100, chunk=0)
@@ -210,3 +218,40 @@ def test_prefill_bad_rows_and_pages_are_zero_and_reported(kernel):
                                       num_kv_heads=2, kernel=kernel)
     assert pgd.get_device_error() == pgd.EDEVICE_BOUNDS
     assert torch.all(out[10:] == 0) and torch.any(out[:10] != 0)
+
+
+@pytest.mark.parametrize("kernel", [pgd.KERNEL_TENSOR_CORE] + TILED_KERNELS)
+def test_prefill_poisoned_slots_outside_attention_are_never_read(kernel):
+    """Every pool position that no token attends to holds NaN before the
+    chunk is written (including the rest of each row's last page and, with the
+    window, the positions below it on its first page): any read of one that
+    reached a result would show."""
+    wl = PrefillWorkload("poison", rows=3, q_heads=16, kv_heads=4, head_dim=128, prefix_lo=0,
+                         prefix_hi=600, chunk=0, window=90, sinks=True)
+    b = make_prefill_batch(wl, 17, DEV, prefix=[10, 300, 523], chunks=[70, 33, 40])
+    keep = np.zeros(b.num_pages * 64, dtype=bool)
+    for r, n in zip(b.rows_np, b.positions_np):
+        for s in range(max(0, int(n) - wl.window + 1), int(n) + 1):
+            keep[b.table_np[r, s // 64] * 64 + s % 64] = True
+    nan_slots = torch.from_numpy(~keep).to(DEV)
+    for pool in (b.k_pool, b.v_pool):
+        view = pool.view(b.num_pages, wl.kv_heads, 64, wl.head_dim)
+        view.masked_fill_(nan_slots.view(b.num_pages, 1, 64, 1).expand_as(view), float("nan"))
+    prefill_check(b, kernel=kernel, what=f"poison k={kernel}")
+
+
+@pytest.mark.parametrize("kernel", TILED_KERNELS)
+def test_prefill_large_logits(kernel):
+    """Queries scaled by 6 give scores with a spread of tens of units in log2,
+    so the running maximum is raised many times along a row (on the tcgen05
+    kernel each raise by more than 2^8 rescales that row of O in TMEM).  The
+    softmax is then nearly one-hot, so an output is close to a single V entry;
+    V is halved (exactly) to keep outputs below 2.56, above which rounding to
+    bf16 alone can exceed the 1e-2 absolute bound."""
+    wl = PrefillWorkload("large", rows=2, q_heads=32, kv_heads=8, head_dim=128, prefix_lo=0,
+                         prefix_hi=2000, chunk=0, window=0, sinks=True)
+    b = make_prefill_batch(wl, 18, DEV, prefix=[1900, 700], chunks=[96, 64])
+    b.q = (b.q.float() * 6.0).to(torch.bfloat16)
+    b.v_pool.mul_(0.5)
+    b.v_new = b.v_new * 0.5
+    prefill_check(b, kernel=kernel, what=f"large logits k={kernel}")
