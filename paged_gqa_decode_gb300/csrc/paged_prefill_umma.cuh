@@ -9,24 +9,30 @@
 // positions[p]], the head's sink logit in the denominator only.
 //
 // Decomposition: one CTA per (block of 128 / G consecutive packed tokens, kv
-// head).  Its 128 query rows are (token, head of the group) pairs, row
-// m = token * G + head, one per TMEM lane.  Tokens split into runs (same table
-// row, consecutive positions); each run is one pass over the pages of the
-// union of its tokens' key ranges.  Six warps:
-//   warp 4      TMA producer: K and V tiles (64 x D bf16, 128-byte swizzle)
-//               of each page into a ring of shared stages.
-//   warp 5      MMA issuer (one thread) and TMEM owner:
-//                 S_i = Q K_i^T      M 128, N 64, K D   -> TMEM S buffer i % 2
-//                 O  += P_i V_i      M 128, N D,  K 64  -> TMEM O
-//               issued in the order S_0, S_1, PV_0, S_2, PV_1, ... so that
-//               the next page's scores are ready when the softmax finishes.
-//   warps 0-3   softmax, one thread per query row: S row from TMEM, causal
-//               and window mask, online softmax in log2 units with a lazy
-//               reference max (raised only when a score exceeds it by more
-//               than 2^8, which then rescales that row of O in TMEM), P
-//               written to shared memory as a bf16 head and residual (two
-//               MMAs, so P V keeps fp32 accuracy); at the end of a run the O
-//               row is normalised with the sink and stored.
+// head), two CTAs per SM.  Its 128 query rows are (token, head of the group)
+// pairs, row m = token * G + head, one per TMEM lane.  Tokens split into runs
+// (same table row, consecutive positions); each run is one pass over the pages
+// of the union of its tokens' key ranges.  Six warps:
+//   warp 4      TMA producer: K and V tiles (64 x D bf16, 128-byte swizzle) of
+//               each page into two rings of shared slots, and pages pulled into
+//               L2 several pages ahead of their loads.
+//   warp 5      MMA issuer (one thread) and TMEM owner, per page i:
+//                 S_i  = Q K_i^T    M 128, N 64, K D   (Q from TMEM, K shared)
+//                 O   += P_i V_i    M 128, N D,  K 64  (P from TMEM, V shared)
+//               in the order S_0, PV_0, S_1, PV_1, ...
+//   warps 0-3   softmax, one thread per query row (= TMEM lane): the S row
+//               from TMEM, causal and window mask, online softmax in log2 units
+//               with a lazy reference max (raised only when a score exceeds it
+//               by more than 2^8, which then rescales that row of O in TMEM),
+//               P written over S as a bf16 head and residual (two MMAs, so P V
+//               keeps fp32 accuracy); at the end of a run the O row is
+//               normalised with the sink and stored.
+// Per CTA the page chain is serial (softmax, then P V, then the next S); the
+// second CTA on the SM runs its softmax while this one's products run, and
+// hides its setup and first loads.
+// TMEM (256 columns): S / P [0, 64) (P per chunk of 32 keys: the bf16 head in
+// the chunk's first 16 columns, the residual in the next 16, as packed pairs),
+// Q [64, 64 + D / 2) as packed pairs, O [128, 128 + D).
 // V rows outside the run's key range on its boundary pages are zeroed in
 // shared memory before the product.  Every wait is bounded; a timeout records
 // PGD_EDEVICE_TIMEOUT, stops all roles, drains in-flight copies and MMAs and
@@ -38,7 +44,7 @@
 
 namespace pgd {
 
-template <int D, int STAGES>
+template <int D, int RING>
 struct UmmaPrefillCfg {
   static constexpr int kRows = 128;  // query rows per CTA (TMEM lanes)
   static constexpr int kSoftmaxThreads = 128;
@@ -46,25 +52,25 @@ struct UmmaPrefillCfg {
   static constexpr int kMmaWarp = 5;
   static constexpr int kThreads = 192;
   static constexpr int kBoxes = D / 64;
-  static constexpr int kTileBytes = kPage * D * 2;
-  static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kQBoxBytes = kRows * 128;  // 128 rows x 64 bf16
-  static constexpr int kQBytes = kBoxes * kQBoxBytes;
-  static constexpr int kPBytes = kRows * kPage * 2;  // one 128 x 64 bf16 tile
-  static constexpr int kQOff = STAGES * kStageBytes;
-  static constexpr int kPOff = kQOff + kQBytes;  // [buffer 0 hi, lo][buffer 1 hi, lo]
-  static constexpr int kBarOff = kPOff + 4 * kPBytes;
-  static constexpr int kNumBars = 2 * STAGES + 9;
+  static constexpr int kTileBytes = kPage * D * 2;  // one K or V slot (one page)
+  static constexpr int kVOff = RING * kTileBytes;   // K slots at 0, V slots here
+  static constexpr int kBarOff = 2 * RING * kTileBytes;
+  static constexpr int kNumBars = 4 * RING + 4;
   static constexpr int kSmemBytes = 1024 + kBarOff + kNumBars * 8;
-  static constexpr uint32_t kTmemCols = 256;  // S buffers at 0 and 64, O at 128
-  static constexpr uint32_t kOCol = 128;
-  static constexpr uint32_t kIdescS = umma_idesc_bf16(128, 64, 0, 0);
+  static constexpr uint32_t kTmemCols = 256;
+  static constexpr uint32_t kQCol = 64, kOCol = 128;
+  static constexpr uint32_t kIdescS = umma_idesc_bf16(128, kPage, 0, 0);
   static constexpr uint32_t kIdescPV = umma_idesc_bf16(128, D, 0, 1);
   static_assert(D == 64 || D == 128, "head_dim");
+  // two CTAs per SM (each with its static arrays and the 1 KB the SM reserves)
+  static_assert(2 * (kSmemBytes + 4 * 1024) <= 228 * 1024, "shared memory");
 };
 
 // Reference-max slack in log2 units: P values stay below 2^8.
 constexpr float kLazyRescaleLog2 = 8.0f;
+
+// How far ahead of its load the producer pulls a page into L2.
+constexpr int kL2PrefetchPages = 8;
 
 // mbarrier wait that also gives up when another role of the CTA has set
 // *abort (after its own wait timed out).
@@ -85,11 +91,11 @@ __device__ __forceinline__ bool mbar_wait_abortable(uint64_t* bar, uint32_t pari
   }
 }
 
-template <int D, int STAGES>
-__global__ void __launch_bounds__(192, 1)
+template <int D, int RING>
+__global__ void __launch_bounds__(192, 2)
     paged_prefill_umma_kernel(const __grid_constant__ CUtensorMap k_map,
                               const __grid_constant__ CUtensorMap v_map, const DecodeParams p) {
-  using C = UmmaPrefillCfg<D, STAGES>;
+  using C = UmmaPrefillCfg<D, RING>;
   pdl_wait();
   pdl_allow_dependents();
   const int kvh = blockIdx.y;
@@ -105,16 +111,16 @@ __global__ void __launch_bounds__(192, 1)
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  unsigned char* stages = base;
-  unsigned char* q_s = base + C::kQOff;
-  unsigned char* p_s = base + C::kPOff;
-  uint64_t* full = reinterpret_cast<uint64_t*>(base + C::kBarOff);
-  uint64_t* empty = full + STAGES;
-  uint64_t* s_full = empty + STAGES;  // S_i in TMEM (MMA commit)
-  uint64_t* s_free = s_full + 2;      // S_i read by all softmax threads
-  uint64_t* p_full = s_free + 2;      // P_i in shared memory (softmax threads)
-  uint64_t* p_free = p_full + 2;      // PV_i done (MMA commit)
-  uint64_t* fin = p_free + 2;         // every MMA of the CTA done
+  unsigned char* k_slots = base;
+  unsigned char* v_slots = base + C::kVOff;
+  uint64_t* k_full = reinterpret_cast<uint64_t*>(base + C::kBarOff);  // TMA landed
+  uint64_t* k_empty = k_full + RING;  // S of the page done (MMA commit)
+  uint64_t* v_full = k_empty + RING;
+  uint64_t* v_empty = v_full + RING;  // P V of the page done (MMA commit)
+  uint64_t* s_full = v_empty + RING;  // S in TMEM (MMA commit; covers the previous P V)
+  uint64_t* p_full = s_full + 1;      // P in TMEM, boundary V rows zeroed (softmax)
+  uint64_t* o_done = p_full + 1;      // P V done (MMA commit)
+  uint64_t* fin = o_done + 1;         // every MMA of the CTA done
   __shared__ int run_end[C::kRows + 1];
   __shared__ int tok_row[C::kRows], tok_pos[C::kRows], tok_run[C::kRows];
   __shared__ int run_bad[C::kRows];
@@ -147,16 +153,15 @@ __global__ void __launch_bounds__(192, 1)
     }
     runs = r;
     for (int k = 0; k < r; ++k) run_bad[k] = 0;
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < RING; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&s_free[b], C::kSoftmaxThreads);
-      mbar_init(&p_full[b], C::kSoftmaxThreads);
-      mbar_init(&p_free[b], 1);
-    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, C::kSoftmaxThreads);
+    mbar_init(o_done, 1);
     mbar_init(fin, 1);
     mbar_init_fence();
     abort_flag = 0;
@@ -184,30 +189,41 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
     tmem_alloc(&tmem_slot, C::kTmemCols);
   }
-  // Q rows into shared memory (128-byte swizzle, K-major); rows of no token
-  // are zero.
-  if (tid < C::kSoftmaxThreads) {
-    const int m = tid, tl = m / G, g = m % G;
-    const bool ok = tl < tokens && t_begin + tl < t_end && tok_row[tl] >= 0;
-    uint4 v[D / 8];
-    if (ok) {
-      const uint4* src =
-          reinterpret_cast<const uint4*>(p.q + ((size_t)(t_begin + tl) * p.hq + h0 + g) * D);
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c) v[c] = src[c];
-    } else {
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c) v[c] = make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int c = 0; c < D / 8; ++c)
-      *reinterpret_cast<uint4*>(q_s + (c >> 3) * C::kQBoxBytes + sw128_offset(m, c & 7)) = v[c];
-    fence_proxy_async_shared();
-  }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = tmem_slot;
+  // Q rows into TMEM as packed bf16 pairs (the A operand of S); rows of no
+  // token are zero.
+  if (tid < C::kSoftmaxThreads) {
+    const int m = tid, tl = m / G, g = m % G;
+    const bool ok = tl < tokens && t_begin + tl < t_end && tok_row[tl] >= 0;
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
+#pragma unroll
+    for (int c16 = 0; c16 < D / 32; ++c16) {
+      uint32_t w[16];
+      if (ok) {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            p.q + ((size_t)(t_begin + tl) * p.hq + h0 + g) * D + 32 * c16);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const uint4 x = src[v];
+          w[4 * v] = x.x;
+          w[4 * v + 1] = x.y;
+          w[4 * v + 2] = x.z;
+          w[4 * v + 3] = x.w;
+        }
+      } else {
+#pragma unroll
+        for (int v = 0; v < 16; ++v) w[v] = 0u;
+      }
+      tmem_st16(lane_base + C::kQCol + 16 * c16, w);
+    }
+    tmem_wait_st();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
   if (tid == 0)
     for (int r = 0; r < runs; ++r)
       if (run_bad[r]) record_error(p.err, PGD_EDEVICE_BOUNDS);
@@ -221,100 +237,146 @@ __global__ void __launch_bounds__(192, 1)
     }
   }
 
+  // Page sequence of the CTA's passes: run by run (inactive and bad runs
+  // skipped), pages first..last of each.  Every role walks it in this order.
+  struct Cursor {
+    int r, pg, last, row;
+  };
+  auto next_run = [&](Cursor& c) {
+    for (++c.r; c.r < runs; ++c.r) {
+      const int rs = c.r == 0 ? 0 : run_end[c.r - 1];
+      c.row = tok_row[rs];
+      if (c.row < 0 || run_bad[c.r]) continue;
+      const int lo = p.window > 0 ? max(tok_pos[rs] - p.window + 1, 0) : 0;
+      c.pg = lo / kPage;
+      c.last = tok_pos[run_end[c.r] - 1] / kPage;
+      return;
+    }
+  };
+  auto advance = [&](Cursor& c) {
+    if (++c.pg > c.last) next_run(c);
+  };
+
   if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tensormap(&k_map);
       prefetch_tensormap(&v_map);
-      int i = 0, rs = 0;
-      for (int r = 0; r < runs && !abort_flag; ++r) {
-        const int re = run_end[r];
-        const int row = tok_row[rs];
-        if (row >= 0 && !run_bad[r]) {
-          const int lo = p.window > 0 ? max(tok_pos[rs] - p.window + 1, 0) : 0;
-          const int first = lo / kPage, last = tok_pos[re - 1] / kPage;
-          for (int pg = first; pg <= last; ++pg, ++i) {
-            const int s = i % STAGES;
-            if (i >= STAGES &&
-                !mbar_wait_abortable(&empty[s], ((i / STAGES) - 1) & 1, p.err, &abort_flag))
-              break;
-            const int page = page_of(p.table, row, pg, p.maxp);
-            const int y = (int)tile_first_row(p.layout, page, kvh, p.hkv, p.num_pages, p.maxp);
-            unsigned char* st = stages + s * C::kStageBytes;
-            mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+      auto tile_y = [&](const Cursor& c) {
+        const int page = page_of(p.table, c.row, c.pg, p.maxp);
+        return (int)tile_first_row(p.layout, page, kvh, p.hkv, p.num_pages, p.maxp);
+      };
+      Cursor kc{-1, 0, -1, -1}, vc{-1, 0, -1, -1}, pc{-1, 0, -1, -1};
+      next_run(kc);
+      next_run(vc);
+      next_run(pc);
+      int ik = 0, iv = 0, ip = 0;  // K loads, V loads, L2 prefetches issued
+      // V of page j is issued before K of page j + 1: its slot frees (P V of
+      // page j - RING) before K's does (S of page j + 1 - RING, issued after
+      // that P V), so each wait below is for the next completion in the MMA's
+      // order.
+      while ((kc.r < runs || vc.r < runs) && !abort_flag) {
+        if (kc.r < runs && ik <= iv) {
+          // The token blocks of a request reach each page together; pulling
+          // pages into L2 ahead of their loads keeps DRAM latency off the rings.
+          for (; pc.r < runs && ip < ik + kL2PrefetchPages; advance(pc), ++ip) {
+            const int y = tile_y(pc);
 #pragma unroll
             for (int bx = 0; bx < C::kBoxes; ++bx) {
-              tma_load_2d(st + bx * kBoxBytes, &k_map, bx * 64, y, &full[s]);
-              tma_load_2d(st + C::kTileBytes + bx * kBoxBytes, &v_map, bx * 64, y, &full[s]);
+              tma_prefetch_l2_2d(&k_map, bx * 64, y);
+              tma_prefetch_l2_2d(&v_map, bx * 64, y);
             }
           }
+          const int s = ik % RING;
+          if (ik >= RING &&
+              !mbar_wait_abortable(&k_empty[s], ((ik / RING) - 1) & 1, p.err, &abort_flag))
+            break;
+          const int y = tile_y(kc);
+          mbar_arrive_expect_tx(&k_full[s], C::kTileBytes);
+#pragma unroll
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            tma_load_2d(k_slots + s * C::kTileBytes + bx * kBoxBytes, &k_map, bx * 64, y,
+                        &k_full[s]);
+          advance(kc);
+          ++ik;
+        } else {
+          const int s = iv % RING;
+          if (iv >= RING &&
+              !mbar_wait_abortable(&v_empty[s], ((iv / RING) - 1) & 1, p.err, &abort_flag))
+            break;
+          const int y = tile_y(vc);
+          mbar_arrive_expect_tx(&v_full[s], C::kTileBytes);
+#pragma unroll
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            tma_load_2d(v_slots + s * C::kTileBytes + bx * kBoxBytes, &v_map, bx * 64, y,
+                        &v_full[s]);
+          advance(vc);
+          ++iv;
         }
-        rs = re;
       }
       // drain: the copies still in flight land before the CTA exits
-      for (int j = max(0, i - STAGES); j < i; ++j)
-        mbar_wait_bounded(&full[j % STAGES], (j / STAGES) & 1, p.err);
+      for (int j = max(0, ik - RING); j < ik; ++j)
+        mbar_wait_bounded(&k_full[j % RING], (j / RING) & 1, p.err);
+      for (int j = max(0, iv - RING); j < iv; ++j)
+        mbar_wait_bounded(&v_full[j % RING], (j / RING) & 1, p.err);
     }
   } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t q_addr = smem_addr(q_s), p_addr = smem_addr(p_s);
-      const uint32_t st_addr = smem_addr(stages);
-      auto issue_pv = [&](int j) -> bool {
-        if (!mbar_wait_abortable(&p_full[j & 1], (j >> 1) & 1, p.err, &abort_flag)) return false;
+      const uint32_t k_addr = smem_addr(k_slots), v_addr = smem_addr(v_slots);
+      auto wait = [&](uint64_t* bar, uint32_t parity) {
+        return mbar_wait_abortable(bar, parity, p.err, &abort_flag);
+      };
+      // S_i overwrites the P that P V_{i-1} reads: the tensor core executes
+      // one thread's MMAs in issue order, reading an MMA's operands before
+      // later MMAs write, so S_i is queued right behind it; its commit tells
+      // the softmax that P V_{i-1} is done as well.
+      auto issue_s = [&](int i) -> bool {
+        if (!wait(&k_full[i % RING], (i / RING) & 1)) return false;
         tc_fence_after_sync();
-        const uint32_t vt = st_addr + (j % STAGES) * C::kStageBytes + C::kTileBytes;
-        const uint32_t ph = p_addr + (j & 1) * 2 * C::kPBytes, pl = ph + C::kPBytes;
+        const uint32_t kt = k_addr + (i % RING) * C::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_bf16(tmem + C::kOCol, umma_desc_sw128(ph + kk * 32, 16, 1024),
-                    umma_desc_sw128(vt + kk * 2048, kBoxBytes, 1024), C::kIdescPV,
-                    j > 0 || kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_bf16(tmem + C::kOCol, umma_desc_sw128(pl + kk * 32, 16, 1024),
-                    umma_desc_sw128(vt + kk * 2048, kBoxBytes, 1024), C::kIdescPV, true);
-        umma_commit(&p_free[j & 1]);
-        umma_commit(&empty[j % STAGES]);
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_bf16_tmem_a(tmem, tmem + C::kQCol + kk * 8,
+                           umma_desc_sw128(kt + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
+                           C::kIdescS, kk > 0);
+        umma_commit(s_full);
+        umma_commit(&k_empty[i % RING]);
         return true;
       };
-      int i = 0, rs = 0;
-      bool ok = true;
-      for (int r = 0; r < runs && ok; ++r) {
-        const int re = run_end[r];
-        const int row = tok_row[rs];
-        if (row >= 0 && !run_bad[r]) {
-          const int lo = p.window > 0 ? max(tok_pos[rs] - p.window + 1, 0) : 0;
-          const int first = lo / kPage, last = tok_pos[re - 1] / kPage;
-          for (int pg = first; pg <= last; ++pg, ++i) {
-            const int s = i % STAGES;
-            if (!mbar_wait_abortable(&full[s], (i / STAGES) & 1, p.err, &abort_flag) ||
-                (i >= 2 &&
-                 !mbar_wait_abortable(&s_free[i & 1], ((i >> 1) - 1) & 1, p.err, &abort_flag))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after_sync();
-            const uint32_t kt = st_addr + s * C::kStageBytes;
+      // keys 16 kk .. 16 kk + 15: chunk kk / 2 of the P columns, half kk % 2 of
+      // its 16 head (then residual) columns
+      auto issue_pv = [&](int i) -> bool {
+        if (!wait(p_full, i & 1) || !wait(&v_full[i % RING], (i / RING) & 1)) return false;
+        tc_fence_after_sync();
+        const uint32_t vt = v_addr + (i % RING) * C::kTileBytes;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              umma_bf16(tmem + (i & 1) * 64,
-                        umma_desc_sw128(q_addr + (kk >> 2) * C::kQBoxBytes + (kk & 3) * 32, 16,
-                                        1024),
-                        umma_desc_sw128(kt + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
-                        C::kIdescS, kk > 0);
-            umma_commit(&s_full[i & 1]);
-            if (i >= 1 && !issue_pv(i - 1)) {
-              ok = false;
-              break;
-            }
-          }
-        }
-        rs = re;
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16_tmem_a(tmem + C::kOCol, tmem + 32 * (kk >> 1) + 8 * (kk & 1),
+                           umma_desc_sw128(vt + kk * 2048, kBoxBytes, 1024), C::kIdescPV,
+                           !(i == 0 && kk == 0));
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16_tmem_a(tmem + C::kOCol, tmem + 32 * (kk >> 1) + 16 + 8 * (kk & 1),
+                           umma_desc_sw128(vt + kk * 2048, kBoxBytes, 1024), C::kIdescPV, true);
+        umma_commit(o_done);
+        umma_commit(&v_empty[i % RING]);
+        return true;
+      };
+      Cursor c{-1, 0, -1, -1};
+      next_run(c);
+      int i = 0;
+      bool ok = c.r < runs && issue_s(0);
+      const bool issued = ok;
+      while (ok) {
+        if (!issue_pv(i)) break;
+        advance(c);
+        if (c.r >= runs) break;
+        ++i;
+        ok = issue_s(i);
       }
-      if (ok && i >= 1) issue_pv(i - 1);
       // drain: every MMA issued so far completes before TMEM is freed
-      if (i >= 1) {
+      if (issued) {
         umma_commit(fin);
         mbar_wait_bounded(fin, 0, p.err);
       }
@@ -323,10 +385,11 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------------------ softmax
     const int m = tid, tl = m / G, g = m % G;
     const bool row_ok = tl < tokens && t_begin + tl < t_end;
-    const uint32_t t_lane = tmem + ((uint32_t)(32 * warp) << 16);
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
     const float c = p.q_scale_log2;
-    unsigned char* ph_base = p_s;
+    const float cc = c > 0.f ? c : 1.f;
     int i = 0, rs = 0;
+    auto all_ok = [&](bool ok) { return __all_sync(0xffffffffu, ok); };
     for (int r = 0; r < runs; ++r) {
       const int re = run_end[r];
       const int row = tok_row[rs];
@@ -343,38 +406,39 @@ __global__ void __launch_bounds__(192, 1)
       float m_ref = -INFINITY, l = 0.f;
       bool ok = true;
       for (int pg = first; pg <= last; ++pg, ++i) {
-        const int b = i & 1;
-        ok = mbar_wait_abortable(&s_full[b], (i >> 1) & 1, p.err, &abort_flag);
-        if (!__all_sync(0xffffffffu, ok)) {
+        if (!all_ok(mbar_wait_abortable(s_full, i & 1, p.err, &abort_flag))) {
           ok = false;
           break;
         }
+        // the S commit also covers P V of the previous page: O is stable
         tc_fence_after_sync();
-        float sv[64];
+        float sv[kPage];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          tmem_ld16(t_lane + b * 64 + 16 * q4, *reinterpret_cast<float(*)[16]>(&sv[16 * q4]));
+        for (int q = 0; q < kPage / 16; ++q)
+          tmem_ld16(lane_base + 16 * q, *reinterpret_cast<float(*)[16]>(&sv[16 * q]));
         tmem_wait_ld();
-        tc_fence_before_sync();
-        mbar_arrive(&s_free[b]);
-
-        const int pos0 = pg * kPage;
-        float mx = -INFINITY;
-        if (live && pos0 >= lo && pos0 + kPage - 1 <= pos) {
+        // scores stay raw: the scale is folded into the exponent's FMA (for a
+        // positive scale; otherwise it is applied here)
+        if (!(c > 0.f)) {
 #pragma unroll
-          for (int k = 0; k < 64; ++k) {
-            sv[k] *= c;
-            mx = fmaxf(mx, sv[k]);
-          }
-        } else {
-#pragma unroll
-          for (int k = 0; k < 64; ++k) {
-            const int kp = pos0 + k;
-            const bool in = live && kp >= lo && kp <= pos;
-            sv[k] = in ? sv[k] * c : -INFINITY;
-            mx = fmaxf(mx, sv[k]);
-          }
+          for (int k = 0; k < kPage; ++k) sv[k] *= c;
         }
+        const int pos0 = pg * kPage;
+        if (!(live && pos0 >= lo && pos0 + kPage - 1 <= pos)) {
+#pragma unroll
+          for (int k = 0; k < kPage; ++k)
+            if (!(live && pos0 + k >= lo && pos0 + k <= pos)) sv[k] = -INFINITY;
+        }
+        float part[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) part[j] = sv[j];
+#pragma unroll
+        for (int k = 8; k < kPage; k += 16)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) part[j] = fmax3(part[j], sv[k + 2 * j], sv[k + 2 * j + 1]);
+        const float mx = fmax3(fmax3(part[0], part[1], part[2]), fmax3(part[3], part[4], part[5]),
+                               fmaxf(part[6], part[7])) *
+                         cc;
         float alpha = 1.f;
         bool rescale_o = false;
         if (mx > m_ref + kLazyRescaleLog2) {
@@ -385,100 +449,84 @@ __global__ void __launch_bounds__(192, 1)
           l *= alpha;
           m_ref = mx;
         }
-        const float ml = m_ref == -INFINITY ? 0.f : m_ref;
-        float sum = 0.f;
+        const float nml = m_ref == -INFINITY ? 0.f : -m_ref;
+        // P = 2^(s - m_ref) as a bf16 head and residual over the S columns
+        // (per chunk of 32 keys: head at +0, residual at +16, column j of a
+        // half holding keys 2j, 2j + 1); pairs through the packed fp32 pipe
+        const float2 cc2 = make_float2(cc, cc), nml2 = make_float2(nml, nml);
+        const float2 minus1 = make_float2(-1.f, -1.f);
+        float2 sum2[4];
 #pragma unroll
-        for (int k = 0; k < 64; ++k) {
-          sv[k] = exp2_approx(sv[k] - ml);
-          sum += sv[k];
-        }
-        l += sum;
-
-        // P buffer b is free once PV_{i-2} is done
-        if (i >= 2) {
-          ok = mbar_wait_abortable(&p_free[b], ((i >> 1) - 1) & 1, p.err, &abort_flag);
-          if (!__all_sync(0xffffffffu, ok)) {
-            ok = false;
-            break;
+        for (int j = 0; j < 4; ++j) sum2[j] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < kPage / 32; ++q) {
+          uint32_t hw[16], lw[16];
+#pragma unroll
+          for (int w = 0; w < 16; ++w) {
+            const float2 y =
+                __ffma2_rn(make_float2(sv[32 * q + 2 * w], sv[32 * q + 2 * w + 1]), cc2, nml2);
+            const float2 x = make_float2(exp2_approx(y.x), exp2_approx(y.y));
+            sum2[w & 3] = __fadd2_rn(sum2[w & 3], x);
+            hw[w] = pack_bf16x2(x.x, x.y);
+            const float2 rr = __ffma2_rn(make_float2(bf16_lo(hw[w]), bf16_hi(hw[w])), minus1, x);
+            lw[w] = pack_bf16x2(rr.x, rr.y);
           }
+          tmem_st16(lane_base + 32 * q, hw);
+          tmem_st16(lane_base + 32 * q + 16, lw);
         }
+        const float2 s4 = __fadd2_rn(__fadd2_rn(sum2[0], sum2[1]), __fadd2_rn(sum2[2], sum2[3]));
+        l += s4.x + s4.y;
         if (__any_sync(0xffffffffu, rescale_o)) {
-          // PV_{i-1} done before this warp's O rows are rescaled
-          ok = mbar_wait_abortable(&p_free[b ^ 1], ((i - 1) >> 1) & 1, p.err, &abort_flag);
-          if (!__all_sync(0xffffffffu, ok)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
 #pragma unroll
           for (int q16 = 0; q16 < D / 16; ++q16) {
             float ov[16];
-            tmem_ld16(t_lane + C::kOCol + 16 * q16, ov);
+            tmem_ld16(lane_base + C::kOCol + 16 * q16, ov);
             tmem_wait_ld();
 #pragma unroll
             for (int k = 0; k < 16; ++k) ov[k] *= alpha;
-            tmem_st16(t_lane + C::kOCol + 16 * q16, ov);
+            tmem_st16(lane_base + C::kOCol + 16 * q16, ov);
           }
-          tmem_wait_st();
         }
         // V rows outside the run's key range on a boundary page -> zero
         const int rlo = max(lo_run - pos0, 0), rhi = min(pos_last - pos0, kPage - 1);
         if (rlo > 0 || rhi < kPage - 1) {
-          const int s = i % STAGES;
-          ok = mbar_wait_abortable(&full[s], (i / STAGES) & 1, p.err, &abort_flag);
-          if (!__all_sync(0xffffffffu, ok)) {
+          const int s = i % RING;
+          if (!all_ok(mbar_wait_abortable(&v_full[s], (i / RING) & 1, p.err, &abort_flag))) {
             ok = false;
             break;
           }
-          unsigned char* vt = stages + s * C::kStageBytes + C::kTileBytes;
-          for (int e = tid; e < kPage * (D / 8); e += C::kSoftmaxThreads) {
-            const int rr = e / (D / 8), ch = e % (D / 8);
-            if (rr < rlo || rr > rhi)
-              *reinterpret_cast<uint4*>(vt + (ch >> 3) * kBoxBytes + rr * 128 + (ch & 7) * 16) =
+          unsigned char* vt = v_slots + s * C::kTileBytes;
+          for (int e = m; e < kPage * (D / 8); e += C::kSoftmaxThreads) {
+            const int k = e / (D / 8), ch = e % (D / 8);
+            if (k < rlo || k > rhi)
+              *reinterpret_cast<uint4*>(vt + (ch >> 3) * kBoxBytes + k * 128 + (ch & 7) * 16) =
                   make_uint4(0u, 0u, 0u, 0u);
           }
+          fence_proxy_async_shared();  // the zeros are read by the tensor core
         }
-        // P row m as bf16 head + residual, 128-byte swizzled K-major
-        unsigned char* ph = ph_base + b * 2 * C::kPBytes;
-        unsigned char* pl = ph + C::kPBytes;
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          uint32_t hw[4], lw[4];
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const float x0 = sv[8 * ch + 2 * w], x1 = sv[8 * ch + 2 * w + 1];
-            hw[w] = pack_bf16x2(x0, x1);
-            lw[w] = pack_bf16x2(x0 - bf16_lo(hw[w]), x1 - bf16_hi(hw[w]));
-          }
-          const uint32_t off = sw128_offset(m, ch);
-          *reinterpret_cast<uint4*>(ph + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4*>(pl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-        }
-        fence_proxy_async_shared();
+        tmem_wait_st();
         tc_fence_before_sync();
-        mbar_arrive(&p_full[b]);
+        mbar_arrive(p_full);
       }
       if (!ok) break;
 
-      // end of run: O rows of this run are final once PV of its last page is done
-      const int jl = i - 1;
-      ok = mbar_wait_abortable(&p_free[jl & 1], (jl >> 1) & 1, p.err, &abort_flag);
-      if (!__all_sync(0xffffffffu, ok)) break;
+      // end of run: O rows of this run are final once P V of its last page is done
+      if (!all_ok(mbar_wait_abortable(o_done, (i - 1) & 1, p.err, &abort_flag))) break;
       tc_fence_after_sync();
-      const int h = h0 + g;
+      const int hh = h0 + g;
       float inv = 0.f;
       if (live) {
-        const float sk = p.sinks ? p.sinks[h] * kLog2e : -INFINITY;
+        const float sk = p.sinks ? p.sinks[hh] * kLog2e : -INFINITY;
         const float mf = fmaxf(m_ref, sk);
         const float scl = exp2_approx(m_ref - mf);
         const float total = fmaf(l, scl, exp2_approx(sk - mf));
         inv = total > 0.f ? scl / total : 0.f;
       }
-      uint16_t* orow = p.out + ((size_t)(t_begin + tl) * p.hq + h) * D;
+      uint16_t* orow = p.out + ((size_t)(t_begin + tl) * p.hq + hh) * D;
 #pragma unroll
       for (int q16 = 0; q16 < D / 16; ++q16) {
         float ov[16];
-        tmem_ld16(t_lane + C::kOCol + 16 * q16, ov);
+        tmem_ld16(lane_base + C::kOCol + 16 * q16, ov);
         tmem_wait_ld();
         if (live) {
           uint32_t w[8];
@@ -504,25 +552,28 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
-template <int D, int STAGES>
+template <int D, int RING>
 cudaError_t launch_prefill_umma(const DecodeParams& p, const CUtensorMap& k_map,
                                 const CUtensorMap& v_map, cudaStream_t stream) {
-  using C = UmmaPrefillCfg<D, STAGES>;
-  static_assert(C::kSmemBytes + 4 * 1024 <= 227 * 1024, "shared memory");
+  using C = UmmaPrefillCfg<D, RING>;
   static std::atomic<bool> configured[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(paged_prefill_umma_kernel<D, STAGES>,
+    e = cudaFuncSetAttribute(paged_prefill_umma_kernel<D, RING>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(paged_prefill_umma_kernel<D, RING>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev].store(true, std::memory_order_release);
   }
   if (p.rows == 0) return cudaSuccess;
   const int tokens = C::kRows / p.group;
   dim3 grid((p.rows + tokens - 1) / tokens, p.hkv);
-  return launch_pdl(paged_prefill_umma_kernel<D, STAGES>, grid, dim3(C::kThreads), C::kSmemBytes,
+  return launch_pdl(paged_prefill_umma_kernel<D, RING>, grid, dim3(C::kThreads), C::kSmemBytes,
                     stream, k_map, v_map, p);
 }
 

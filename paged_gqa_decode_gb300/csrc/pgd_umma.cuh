@@ -1,6 +1,6 @@
 // tcgen05 (5th-generation tensor core) building blocks for sm_103a: TMEM
-// allocation, UMMA shared-memory and instruction descriptors, MMA issue and
-// commit, and TMEM loads / stores.
+// allocation, UMMA shared-memory and instruction descriptors, MMA issue (A
+// from shared memory or from TMEM) and commit, and TMEM loads / stores.
 //
 // Operand layouts used here (128-byte swizzle, the layout 2-D TMA writes
 // with CU_TENSOR_MAP_SWIZZLE_128B): a box is rows of 64 bf16 (128 bytes),
@@ -48,6 +48,19 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]: A (M rows = TMEM lanes) holds K in packed
+// bf16 pairs, column j = elements 2j (low half) and 2j + 1; a k-step of 16
+// advances A by 8 columns.
+__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
+                                                 uint64_t b_desc, uint32_t idesc,
+                                                 bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
 // Arrives on `bar` once every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
@@ -91,6 +104,16 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
       : "memory");
 #pragma unroll
   for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
 }
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
