@@ -101,7 +101,7 @@ size_t workspace_bytes(const pgd_dims* d, const Plan& pl) {
   return (size_t)d->rows * d->num_q_heads * pl.max_splits * (d->head_dim + 2) * sizeof(float);
 }
 
-int encode_pool_map_uncached(CUtensorMap* map, const void* pool, const pgd_dims* d);
+int encode_pool_map_uncached(CUtensorMap* map, const void* pool, const pgd_dims* d, bool whole);
 
 // Encoded pool descriptors are reused while the same pool is passed again: a
 // small per-process cache keyed by (device, address, pages, kv heads, dim).
@@ -109,6 +109,7 @@ struct MapEntry {
   int dev;
   const void* pool;
   int32_t num_pages, kv_heads, head_dim;
+  bool whole;
   CUtensorMap map;
 };
 constexpr int kMapCache = 16;
@@ -116,7 +117,9 @@ MapEntry g_maps[kMapCache];
 int g_map_count = 0, g_map_next = 0;
 std::mutex g_map_mutex;
 
-int encode_pool_map(CUtensorMap* map, const void* pool, const pgd_dims* d) {
+// `whole`: one box per page tile (head_dim 128 as a 3-D map); else 64-wide boxes.
+int encode_pool_map(CUtensorMap* map, const void* pool, const pgd_dims* d, bool whole = false) {
+  whole = whole && d->head_dim == 128;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PGD_ECUDA;
   {
@@ -124,23 +127,23 @@ int encode_pool_map(CUtensorMap* map, const void* pool, const pgd_dims* d) {
     for (int i = 0; i < g_map_count; ++i) {
       const MapEntry& m = g_maps[i];
       if (m.dev == dev && m.pool == pool && m.num_pages == d->num_pages &&
-          m.kv_heads == d->num_kv_heads && m.head_dim == d->head_dim) {
+          m.kv_heads == d->num_kv_heads && m.head_dim == d->head_dim && m.whole == whole) {
         *map = m.map;
         return PGD_OK;
       }
     }
   }
-  const int rc = encode_pool_map_uncached(map, pool, d);
+  const int rc = encode_pool_map_uncached(map, pool, d, whole);
   if (rc != PGD_OK) return rc;
   std::lock_guard<std::mutex> lock(g_map_mutex);
   MapEntry& slot = g_maps[g_map_next];
-  slot = MapEntry{dev, pool, d->num_pages, d->num_kv_heads, d->head_dim, *map};
+  slot = MapEntry{dev, pool, d->num_pages, d->num_kv_heads, d->head_dim, whole, *map};
   g_map_next = (g_map_next + 1) % kMapCache;
   if (g_map_count < kMapCache) ++g_map_count;
   return PGD_OK;
 }
 
-int encode_pool_map_uncached(CUtensorMap* map, const void* pool, const pgd_dims* d) {
+int encode_pool_map_uncached(CUtensorMap* map, const void* pool, const pgd_dims* d, bool whole) {
   std::call_once(g_encode_once, [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -154,6 +157,20 @@ int encode_pool_map_uncached(CUtensorMap* map, const void* pool, const pgd_dims*
   // (page, kv head, position) in either layout.  A box is 64 rows x 64
   // values (128 bytes): one page tile, or half of one when head_dim is 128.
   const cuuint64_t rows = (cuuint64_t)d->num_pages * d->num_kv_heads * kPageSize;
+  if (whole) {
+    // head_dim 128 as (64 values, rows, 2 halves): strides 256 bytes (a row)
+    // and 128 bytes (a half), box 64 x 64 x 2 -- one copy lands a page tile as
+    // the two consecutive 128-byte-swizzled 64-wide boxes the 2-D map gives.
+    const cuuint64_t dims3[3] = {64, rows, 2};
+    const cuuint64_t strides3[2] = {256, 128};
+    const cuuint32_t box3[3] = {64, (cuuint32_t)kPageSize, 2};
+    const cuuint32_t elem3[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool),
+                          dims3, strides3, box3, elem3, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PGD_OK : PGD_ECUDA;
+  }
   const cuuint64_t dims[2] = {(cuuint64_t)d->head_dim, rows};
   const cuuint64_t strides[1] = {(cuuint64_t)d->head_dim * 2};
   const cuuint32_t box[2] = {64, (cuuint32_t)kPageSize};
@@ -332,9 +349,22 @@ static int decode_impl(const pgd_dims* dims, int32_t table_rows, const int32_t* 
   if (workspace_size < need) return PGD_EWORKSPACE;
   if (!workspace || !aligned16(workspace)) return PGD_EINVAL;
 
+  int kernel = opts ? opts->kernel : PGD_KERNEL_AUTO;
+  if (kernel < PGD_KERNEL_AUTO || kernel > PGD_KERNEL_PREFILL_UMMA) return PGD_EINVAL;
+  if ((kernel == PGD_KERNEL_PREFILL_TILED || kernel == PGD_KERNEL_PREFILL_UMMA) &&
+      row_of == nullptr)
+    return PGD_EINVAL;
+  const int padded = padded_group(dims->num_q_heads / dims->num_kv_heads);
+  if (row_of != nullptr && kernel == PGD_KERNEL_AUTO) {
+    const int64_t blocks = ((int64_t)dims->rows + prefill_block_tokens(padded) - 1) /
+                           prefill_block_tokens(padded);
+    if (blocks * dims->num_kv_heads >= 2ll * dev->sm_count) kernel = PGD_KERNEL_PREFILL_TILED;
+  }
+  // the tcgen05 prefill copies a head_dim-128 page tile with one 3-D box
+  const bool whole = kernel == PGD_KERNEL_PREFILL_UMMA;
   CUtensorMap k_map, v_map;
-  if ((rc = encode_pool_map(&k_map, k_pool, dims)) != PGD_OK) return rc;
-  if ((rc = encode_pool_map(&v_map, v_pool, dims)) != PGD_OK) return rc;
+  if ((rc = encode_pool_map(&k_map, k_pool, dims, whole)) != PGD_OK) return rc;
+  if ((rc = encode_pool_map(&v_map, v_pool, dims, whole)) != PGD_OK) return rc;
 
   DecodeParams p;
   p.q = static_cast<const uint16_t*>(q);
@@ -370,21 +400,12 @@ static int decode_impl(const pgd_dims* dims, int32_t table_rows, const int32_t* 
   const int grid_splits = (grid_pages + pl.pages_per_split - 1) / pl.pages_per_split;
   const int pages_per_cta = grid_pages < pl.pages_per_split ? grid_pages : pl.pages_per_split;
 
-  const int padded = padded_group(p.group);
-  int kernel = opts ? opts->kernel : PGD_KERNEL_AUTO;
-  if (kernel < PGD_KERNEL_AUTO || kernel > PGD_KERNEL_PREFILL_UMMA) return PGD_EINVAL;
-  if ((kernel == PGD_KERNEL_PREFILL_TILED || kernel == PGD_KERNEL_PREFILL_UMMA) &&
-      row_of == nullptr)
-    return PGD_EINVAL;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (row_of != nullptr && kernel == PGD_KERNEL_AUTO) {
-    const int64_t blocks = ((int64_t)dims->rows + prefill_block_tokens(padded) - 1) /
-                           prefill_block_tokens(padded);
-    if (blocks * dims->num_kv_heads >= 2ll * dev->sm_count) kernel = PGD_KERNEL_PREFILL_TILED;
-  }
   if (kernel == PGD_KERNEL_PREFILL_UMMA)
-    return launch_prefill_umma(p, k_map, v_map, dims->head_dim, st) == cudaSuccess ? PGD_OK
-                                                                                   : PGD_ECUDA;
+    return launch_prefill_umma(p, k_map, v_map, dims->head_dim, dev->sm_count, st) ==
+                   cudaSuccess
+               ? PGD_OK
+               : PGD_ECUDA;
   if (kernel == PGD_KERNEL_PREFILL_TILED)
     return launch_prefill_tiled(p, k_map, v_map, dims->head_dim, padded, st) == cudaSuccess
                ? PGD_OK

@@ -105,8 +105,10 @@ cudaError_t launch_prefill_tiled(const DecodeParams& p, const CUtensorMap& k_map
                                  cudaStream_t stream);
 int prefill_block_tokens(int padded);
 
-// Prefill on the tcgen05 tensor cores: 128 / group tokens per block.
+// Prefill on the tcgen05 tensor cores: persistent, one CTA per SM, blocks of
+// 128 / group tokens; the first word of p.ws_acc is its work counter.
 cudaError_t launch_prefill_umma(const DecodeParams& p, const CUtensorMap& k_map,
-                                const CUtensorMap& v_map, int head_dim, cudaStream_t stream);
+                                const CUtensorMap& v_map, int head_dim, int sm_count,
+                                cudaStream_t stream);
 
 }  // namespace pgd
