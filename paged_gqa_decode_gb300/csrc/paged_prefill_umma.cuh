@@ -15,12 +15,12 @@
 // the tokens split into runs (same table row, consecutive positions); each run
 // is one pass over the pages of the union of its tokens' key ranges.  The
 // pages of all of a CTA's items form one sequence, and every role walks it:
-//   warp 4      producer: per item, reads its tokens, builds the runs, checks
-//               the table and zeroes uncovered outputs (whole warp); then
-//               streams each page's K and V tiles
-//               (64 x D bf16, 128-byte swizzle) into two rings of shared
-//               slots with TMA, K four pages ahead of V, pulling pages into L2
-//               ahead of their loads (lane 0).
+//   warp 4      K producer: per item, reads its tokens, builds the runs,
+//               checks the table and zeroes uncovered outputs (whole warp);
+//               then streams each page's K tile (64 x D bf16, 128-byte
+//               swizzle) into a ring of shared slots with TMA, pulling pages
+//               into L2 ahead of their loads.
+//   warp 7      V producer: the same pages' V tiles into a second ring.
 //   warp 5      S issuer (one thread) and TMEM owner, per page i:
 //                 S_i  = Q K_i^T    M 128, N 64, K D   (Q from TMEM, K shared)
 //               into TMEM buffer i % 4 once P V_{i-4} (which reads that
@@ -59,7 +59,8 @@ struct UmmaPrefillCfg {
   static constexpr int kProducerWarp = 4;
   static constexpr int kMmaWarp = 5;  // S issuer, TMEM owner
   static constexpr int kPvWarp = 6;
-  static constexpr int kThreads = 224;
+  static constexpr int kVWarp = 7;
+  static constexpr int kThreads = 256;
   static constexpr int kBoxes = D / 64;
   static constexpr int kSBufs = 4;  // S / P buffers: S runs this many pages ahead
   static constexpr int kTileBytes = kPage * D * 2;  // one K or V slot (one page)
@@ -72,6 +73,7 @@ struct UmmaPrefillCfg {
   static constexpr uint32_t kIdescS = umma_idesc_bf16(128, kPage, 0, 0);
   static constexpr uint32_t kIdescPV = umma_idesc_bf16(128, D, 0, 1);
   static_assert(D == 64 || D == 128, "head_dim");
+  static_assert(RK == RV, "the K and V rings are streamed by one helper");
   static_assert(kSmemBytes + 8 * 1024 <= 227 * 1024, "shared memory");
 };
 
@@ -79,7 +81,7 @@ struct UmmaPrefillCfg {
 constexpr float kLazyRescaleLog2 = 8.0f;
 
 // How far ahead of its load the producer pulls a page into L2.
-constexpr int kL2PrefetchPages = 8;
+constexpr int kL2PrefetchPages = 16;
 
 // mbarrier wait that also gives up when another role of the CTA has set
 // *abort (after its own wait timed out).
@@ -135,7 +137,7 @@ __device__ __forceinline__ bool item_advance(const PrefillItem& it, int window, 
 }
 
 template <int D, int RK, int RV>
-__global__ void __launch_bounds__(224, 1)
+__global__ void __launch_bounds__(256, 1)
     paged_prefill_umma_kernel(const __grid_constant__ CUtensorMap k_map,
                               const __grid_constant__ CUtensorMap v_map, const DecodeParams p,
                               int* item_counter) {
@@ -163,11 +165,11 @@ __global__ void __launch_bounds__(224, 1)
   uint64_t* p_full = s_full + C::kSBufs;   // [page % 4] P in TMEM, boundary V rows zeroed
   uint64_t* o_done = p_full + C::kSBufs;   // [page % 4] P V done (MMA commit)
   uint64_t* item_ready = o_done + C::kSBufs;  // [item % 2] descriptor written (producer)
-  uint64_t* item_free = item_ready + 2;       // [item % 2] descriptor consumed (softmax, issuers)
+  uint64_t* item_free = item_ready + 2;       // [item % 2] consumed (softmax, issuers, V producer)
   uint64_t* q_ready = item_free + 2;          // [item % 2] Q in TMEM (softmax)
   uint64_t* fin = q_ready + 2;                // [issuer] every MMA it issued done
   __shared__ PrefillItem items[2];
-  __shared__ int y_ring[64];  // tile rows of upcoming pages, by page number % 64
+  __shared__ int y_ring[2][64];  // [K, V producer] tile rows of upcoming pages, by page % 64
   __shared__ volatile int abort_flag;
   __shared__ uint32_t tmem_slot;
 
@@ -187,7 +189,7 @@ __global__ void __launch_bounds__(224, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&item_ready[b], 1);
-      mbar_init(&item_free[b], C::kSoftmaxThreads + 2);
+      mbar_init(&item_free[b], C::kSoftmaxThreads + 3);
       mbar_init(&q_ready[b], C::kSoftmaxThreads);
     }
     mbar_init(&fin[0], 1);
@@ -213,13 +215,68 @@ __global__ void __launch_bounds__(224, 1)
       tma_load_2d(dst, map, 0, y, bar);
   };
 
+  auto all_ok = [&](bool v) { return __all_sync(0xffffffffu, v); };
+  // Streams the pages of item `it` into one ring with the whole warp, page
+  // number i onwards: tile rows are looked up 32 at a time (one table load per
+  // lane) into `ring` (by page number % 64); lane 0 waits for each slot and
+  // issues its copy, and with `prefetch` pulls K and V pages into L2 ahead (the
+  // token blocks of a request reach each page together).
+  auto stream_item = [&](const PrefillItem& it, int kvh, const CUtensorMap* map,
+                         unsigned char* slots, uint64_t* full, uint64_t* empty, int* ring, int& i,
+                         bool prefetch) -> bool {
+    int n_pages = 0;
+    {
+      ItemCursor cc{-1, 0, -1, -1, 0, 0};
+      for (bool more = item_next_run(it, p.window, cc); more;
+           more = item_next_run(it, p.window, cc))
+        n_pages += cc.last - cc.pg + 1;
+    }
+    const int i_end = i + n_pages;
+    ItemCursor fc{-1, 0, -1, -1, 0, 0};
+    bool f_more = item_next_run(it, p.window, fc);
+    int i_fetch = i, ip = i;
+    for (; i < i_end; ++i) {
+      while (f_more && i_fetch < i + 16) {
+        const int n = min(32, fc.last - fc.pg + 1);
+        if (lane < n) {
+          const int page = page_of(p.table, fc.row, fc.pg + lane, p.maxp);
+          ring[(i_fetch + lane) & 63] =
+              (int)tile_first_row(p.layout, page, kvh, p.hkv, p.num_pages, p.maxp);
+        }
+        __syncwarp();
+        i_fetch += n;
+        fc.pg += n - 1;
+        f_more = item_advance(it, p.window, fc);
+      }
+      if (prefetch && lane == 0) {
+        for (; ip < min(i + kL2PrefetchPages, i_fetch); ++ip) {
+          const int y = ring[ip & 63];
+          if constexpr (D == 128) {
+            tma_prefetch_l2_3d(&k_map, 0, y, 0);
+            tma_prefetch_l2_3d(&v_map, 0, y, 0);
+          } else {
+            tma_prefetch_l2_2d(&k_map, 0, y);
+            tma_prefetch_l2_2d(&v_map, 0, y);
+          }
+        }
+      }
+      const int s = i % RK;
+      if (i >= RK && !all_ok(wait(&empty[s], ((i / RK) - 1) & 1))) return false;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&full[s], C::kTileBytes);
+        load_tile(slots + s * C::kTileBytes, map, ring[i & 63], &full[s]);
+      }
+    }
+    return true;
+  };
+
   if (warp == C::kProducerWarp) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ K producer
     if (lane == 0) {
       prefetch_tensormap(&k_map);
       prefetch_tensormap(&v_map);
     }
-    int ik = 0, iv = 0, ip = 0;  // K loads, V loads, L2 prefetches issued (all items)
+    int ik = 0;  // K loads issued (all items)
     bool ok = true;
     for (int seq = 0; ok; ++seq) {
       const int d = seq & 1;
@@ -313,88 +370,26 @@ __global__ void __launch_bounds__(224, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&item_ready[d]);
-      // Pages of the item, streamed by the whole warp (lane 0 issues the
-      // copies).  V of page j is issued before K of page j + 4, in the order
-      // their slots free (P V_{j-RV} completes before S_{j+4-RK}, which waits
-      // for P V_{j-RK}).  The pages' tile rows are looked up 32 at a time, one
-      // table load per lane, into a ring indexed by the CTA's page number.
-      {
-        int n_pages = 0;
-        {
-          ItemCursor cc{-1, 0, -1, -1, 0, 0};
-          for (bool more = item_next_run(it, p.window, cc); more;
-               more = item_next_run(it, p.window, cc))
-            n_pages += cc.last - cc.pg + 1;
-        }
-        const int i_end = ik + n_pages;  // every earlier page's K and V are issued
-        ItemCursor fc{-1, 0, -1, -1, 0, 0};
-        bool f_more = item_next_run(it, p.window, fc);
-        int i_fetch = ik;
-        auto all_ok = [&](bool v) { return __all_sync(0xffffffffu, v); };
-        while ((ik < i_end || iv < i_end) && ok) {
-          if (ik < i_end && ik < iv + C::kSBufs) {
-            while (f_more && i_fetch < ik + 16) {
-              const int n = min(32, fc.last - fc.pg + 1);
-              if (lane < n) {
-                const int page = page_of(p.table, fc.row, fc.pg + lane, p.maxp);
-                y_ring[(i_fetch + lane) & 63] =
-                    (int)tile_first_row(p.layout, page, kvh, p.hkv, p.num_pages, p.maxp);
-              }
-              __syncwarp();
-              i_fetch += n;
-              fc.pg += n - 1;
-              f_more = item_advance(it, p.window, fc);
-            }
-            if (lane == 0) {
-              // the token blocks of a request reach each page together; pulling
-              // pages into L2 ahead of their loads keeps DRAM latency off the rings
-              for (; ip < min(ik + kL2PrefetchPages, i_fetch); ++ip) {
-                const int y = y_ring[ip & 63];
-#pragma unroll
-                if constexpr (D == 128) {
-                  tma_prefetch_l2_3d(&k_map, 0, y, 0);
-                  tma_prefetch_l2_3d(&v_map, 0, y, 0);
-                } else {
-                  tma_prefetch_l2_2d(&k_map, 0, y);
-                  tma_prefetch_l2_2d(&v_map, 0, y);
-                }
-              }
-            }
-            const int s = ik % RK;
-            if (ik >= RK && !all_ok(wait(&k_empty[s], ((ik / RK) - 1) & 1))) {
-              ok = false;
-              break;
-            }
-            if (lane == 0) {
-              const int y = y_ring[ik & 63];
-              mbar_arrive_expect_tx(&k_full[s], C::kTileBytes);
-              load_tile(k_slots + s * C::kTileBytes, &k_map, y, &k_full[s]);
-            }
-            ++ik;
-          } else {
-            const int s = iv % RV;
-            if (iv >= RV && !all_ok(wait(&v_empty[s], ((iv / RV) - 1) & 1))) {
-              ok = false;
-              break;
-            }
-            if (lane == 0) {
-              const int y = y_ring[iv & 63];
-              mbar_arrive_expect_tx(&v_full[s], C::kTileBytes);
-              load_tile(v_slots + s * C::kTileBytes, &v_map, y, &v_full[s]);
-            }
-            ++iv;
-          }
-        }
-        ip = ik;  // prefetches do not cross items
-      }
+      ok = stream_item(it, kvh, &k_map, k_slots, k_full, k_empty, y_ring[0], ik, true);
     }
     // drain: the copies still in flight land before the CTA exits
-    if (lane == 0) {
+    if (lane == 0)
       for (int j = max(0, ik - RK); j < ik; ++j)
         mbar_wait_bounded(&k_full[j % RK], (j / RK) & 1, p.err);
+  } else if (warp == C::kVWarp) {
+    // ------------------------------------------------------------ V producer
+    int iv = 0;  // V loads issued (all items)
+    for (int seq = 0;; ++seq) {
+      const int d = seq & 1;
+      if (!all_ok(wait(&item_ready[d], (seq >> 1) & 1))) break;
+      const PrefillItem& it = items[d];
+      if (!it.valid) break;
+      if (!stream_item(it, it.kvh, &v_map, v_slots, v_full, v_empty, y_ring[1], iv, false)) break;
+      if (lane == 0) mbar_arrive(&item_free[d]);
+    }
+    if (lane == 0)
       for (int j = max(0, iv - RV); j < iv; ++j)
         mbar_wait_bounded(&v_full[j % RV], (j / RV) & 1, p.err);
-    }
   } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------ S issuer
     if (lane == 0) {
@@ -489,7 +484,6 @@ __global__ void __launch_bounds__(224, 1)
     const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
     const float c = p.q_scale_log2;
     const float cc = c > 0.f ? c : 1.f;
-    auto all_ok = [&](bool v) { return __all_sync(0xffffffffu, v); };
     int i = 0;  // page index over all items
     bool ok = true;
     for (int seq = 0; ok; ++seq) {
