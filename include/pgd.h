@@ -95,18 +95,21 @@ typedef struct {
   int32_t layout;            /* PGD_PAGE_MAJOR, PGD_HEAD_MAJOR or PGD_ROW_MAJOR */
 } pgd_dims;
 
-/* Decode kernel variants.  Both compute the same function; they differ in
- * where the per-page Q.K^T and P.V products run. */
+/* Kernel variants.  All compute the same function; they differ in where the
+ * per-page Q.K^T and P.V products run and in how tokens share page loads. */
 enum {
-  PGD_KERNEL_AUTO = 0,          /* decode: tensor-core; prefill: see below */
-  PGD_KERNEL_TENSOR_CORE = 1,   /* mma.sync bf16 products, fp32 accumulate, per token */
+  PGD_KERNEL_AUTO = 0,          /* decode: TENSOR_CORE; prefill: PREFILL_UMMA when
+                                   the tokens average at least 8 per table row
+                                   (prompt chunks), else TENSOR_CORE */
+  PGD_KERNEL_TENSOR_CORE = 1,   /* mma.sync bf16 products, fp32 accumulate, per token,
+                                   key range split over CTAs + combine */
   PGD_KERNEL_CUDA_CORE = 2,     /* fp32 FMA products on the CUDA cores, per token */
   PGD_KERNEL_PREFILL_TILED = 3, /* prefill only: blocks of tokens share each page
-                                   load (mma.sync tensor cores, no key splits);
-                                   AUTO picks it when the blocks fill the GPU */
-  PGD_KERNEL_PREFILL_UMMA = 4   /* prefill only: 128 query rows per block on the
-                                   tcgen05 tensor cores (TMEM accumulators), no
-                                   key splits */
+                                   load (mma.sync tensor cores, no key splits) */
+  PGD_KERNEL_PREFILL_UMMA = 4   /* prefill only: persistent, 128 query rows per
+                                   block on the tcgen05 tensor cores (TMEM
+                                   accumulators), no key splits; uses the first
+                                   4 bytes of the workspace as a work counter */
 };
 
 /* Optional tuning of the decode launch; pass NULL for the defaults.  The same
@@ -240,6 +243,9 @@ PGD_API int pgd_paged_decode_attention(const pgd_dims* dims, const void* q, cons
  * step_paged (prompts and one decode step per row in one pass) is one call
  * over the concatenation: the step of row b is a token with rows = b at its
  * step position.
+ * Kernels (opts->kernel): AUTO chooses PREFILL_UMMA (tokens in blocks of
+ * 128 / (Hq / Hkv) share every page load; persistent, one CTA per SM) when
+ * P >= 8 * table_rows, else the per-token TENSOR_CORE split kernel.
  * Device errors: rows[p] outside [0, table_rows), plus those of
  * pgd_paged_decode_attention; the token's output is zero.
  */

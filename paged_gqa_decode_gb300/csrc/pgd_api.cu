@@ -355,11 +355,11 @@ static int decode_impl(const pgd_dims* dims, int32_t table_rows, const int32_t* 
       row_of == nullptr)
     return PGD_EINVAL;
   const int padded = padded_group(dims->num_q_heads / dims->num_kv_heads);
-  if (row_of != nullptr && kernel == PGD_KERNEL_AUTO) {
-    const int64_t blocks = ((int64_t)dims->rows + prefill_block_tokens(padded) - 1) /
-                           prefill_block_tokens(padded);
-    if (blocks * dims->num_kv_heads >= 2ll * dev->sm_count) kernel = PGD_KERNEL_PREFILL_TILED;
-  }
+  // Prefill: the tcgen05 kernel shares each page load among the tokens of a
+  // block, which pays when they come in runs (prompt chunks); tokens that are
+  // mostly one per table row (decode steps) go to the per-token split kernel.
+  if (row_of != nullptr && kernel == PGD_KERNEL_AUTO && dims->rows >= 8ll * table_rows)
+    kernel = PGD_KERNEL_PREFILL_UMMA;
   // the tcgen05 prefill copies a head_dim-128 page tile with one 3-D box
   const bool whole = kernel == PGD_KERNEL_PREFILL_UMMA;
   CUtensorMap k_map, v_map;
