@@ -29,14 +29,18 @@
 //                 O   += P_i V_i    M 128, N D,  K 64  (P from TMEM, V shared)
 //               Two issuing threads keep the tensor core fed while either
 //               waits.
-//   warps 0-3   softmax, one thread per query row: its Q row of each item
-//               into TMEM; per page the S row from TMEM, causal and
-//               window mask, online softmax in log2 units with a lazy
-//               reference max (raised only when a score exceeds it by more
-//               than 2^8, which then rescales that row of O in TMEM), P
-//               written over S as a bf16 head and residual (two MMAs, so P V
-//               keeps fp32 accuracy); at the end of a run the O row is
-//               normalised with the sink and stored.
+//   warps 0-7   softmax: warpgroup h (warps 4h .. 4h + 3), one thread per
+//               query row, takes the pages i with i % 2 == h.  Each loads half
+//               of its row's Q into TMEM per item; per page the S row from
+//               TMEM, causal and window mask, online softmax in log2 units
+//               with a lazy reference max common to both warpgroups (raised
+//               only when a score exceeds it by more than 2^8, which then
+//               rescales that row of O in TMEM): page i's reference is page
+//               i - 1's, published through shared memory, raised if needed.
+//               P is written over S as a bf16 head and residual (two MMAs, so
+//               P V keeps fp32 accuracy).  Each warpgroup keeps its own row
+//               sum; at the end of a run they meet, add the sums and each
+//               normalises and stores half of the O row, with the sink.
 // TMEM (512 columns): S / P buffers b = 0..3 at [64 b, 64 b + 64) (P per chunk
 // of 32 keys: the bf16 head in the chunk's first 16 columns, the residual in
 // the next 16, as packed pairs), O at [256, 256 + D), Q buffers q = 0, 1 at
@@ -55,18 +59,18 @@ namespace pgd {
 template <int D, int RK, int RV>
 struct UmmaPrefillCfg {
   static constexpr int kRows = 128;  // query rows per item (TMEM lanes)
-  static constexpr int kSoftmaxThreads = 128;
-  static constexpr int kProducerWarp = 4;
-  static constexpr int kMmaWarp = 5;  // S issuer, TMEM owner
-  static constexpr int kPvWarp = 6;
-  static constexpr int kVWarp = 7;
-  static constexpr int kThreads = 256;
+  static constexpr int kSoftmaxThreads = 256;  // two warpgroups
+  static constexpr int kProducerWarp = 8;
+  static constexpr int kMmaWarp = 9;  // S issuer, TMEM owner
+  static constexpr int kPvWarp = 10;
+  static constexpr int kVWarp = 11;
+  static constexpr int kThreads = 384;
   static constexpr int kBoxes = D / 64;
   static constexpr int kSBufs = 4;  // S / P buffers: S runs this many pages ahead
   static constexpr int kTileBytes = kPage * D * 2;  // one K or V slot (one page)
   static constexpr int kVOff = RK * kTileBytes;
   static constexpr int kBarOff = (RK + RV) * kTileBytes;
-  static constexpr int kNumBars = 2 * RK + 2 * RV + 3 * kSBufs + 8;
+  static constexpr int kNumBars = 2 * RK + 2 * RV + 3 * kSBufs + 11;
   static constexpr int kSmemBytes = 1024 + kBarOff + kNumBars * 8;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kOCol = 256, kQCol = 384;
@@ -137,7 +141,7 @@ __device__ __forceinline__ bool item_advance(const PrefillItem& it, int window, 
 }
 
 template <int D, int RK, int RV>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     paged_prefill_umma_kernel(const __grid_constant__ CUtensorMap k_map,
                               const __grid_constant__ CUtensorMap v_map, const DecodeParams p,
                               int* item_counter) {
@@ -168,8 +172,13 @@ __global__ void __launch_bounds__(256, 1)
   uint64_t* item_free = item_ready + 2;       // [item % 2] consumed (softmax, issuers, V producer)
   uint64_t* q_ready = item_free + 2;          // [item % 2] Q in TMEM (softmax)
   uint64_t* fin = q_ready + 2;                // [issuer] every MMA it issued done
+  uint64_t* mref_bar = fin + 2;               // [page % 2] the page's reference max published
+  uint64_t* l_bar = mref_bar + 2;             // both warpgroups' row sums of a run published
   __shared__ PrefillItem items[2];
   __shared__ int y_ring[2][64];  // [K, V producer] tile rows of upcoming pages, by page % 64
+  // per row: the reference max after page i in mref_x[i % 2]; the warpgroups'
+  // row sums at the end of run r in l_x[r % 2]
+  __shared__ float mref_x[2][C::kRows], l_x[2][2][C::kRows];
   __shared__ volatile int abort_flag;
   __shared__ uint32_t tmem_slot;
 
@@ -184,16 +193,18 @@ __global__ void __launch_bounds__(256, 1)
     }
     for (int b = 0; b < C::kSBufs; ++b) {
       mbar_init(&s_full[b], 1);
-      mbar_init(&p_full[b], C::kSoftmaxThreads);
+      mbar_init(&p_full[b], C::kRows);  // the page's warpgroup
       mbar_init(&o_done[b], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&item_ready[b], 1);
       mbar_init(&item_free[b], C::kSoftmaxThreads + 3);
+      mbar_init(&mref_bar[b], C::kSoftmaxThreads / 2);
       mbar_init(&q_ready[b], C::kSoftmaxThreads);
     }
     mbar_init(&fin[0], 1);
     mbar_init(&fin[1], 1);
+    mbar_init(l_bar, C::kSoftmaxThreads);
     mbar_init_fence();
     abort_flag = 0;
   }
@@ -480,11 +491,12 @@ __global__ void __launch_bounds__(256, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int m = tid;
-    const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
+    const int m = tid & 127, h = tid >> 7;  // row; warpgroup (pages i % 2 == h)
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     const float c = p.q_scale_log2;
     const float cc = c > 0.f ? c : 1.f;
-    int i = 0;  // page index over all items
+    int i = 0;     // page index over all items
+    int nrun = 0;  // runs finished
     bool ok = true;
     for (int seq = 0; ok; ++seq) {
       const int d = seq & 1;
@@ -494,21 +506,21 @@ __global__ void __launch_bounds__(256, 1)
       const int t_begin = it.t_begin, t_end = it.t_end, h0 = it.kvh * G;
       const int tl = m / G, g = m % G;
       const bool row_ok = tl < tokens && t_begin + tl < t_end;
-      // Q row into TMEM buffer seq % 2 (rows of no token: zero)
+      // half h of the Q row into TMEM buffer seq % 2 (rows of no token: zero)
       {
         const bool q_ok = row_ok && it.tok_row[tl] >= 0;
-        uint4 v[D / 8];
+        uint4 v[D / 16];
         if (q_ok) {
-          const uint4* src =
-              reinterpret_cast<const uint4*>(p.q + ((size_t)(t_begin + tl) * p.hq + h0 + g) * D);
+          const uint4* src = reinterpret_cast<const uint4*>(
+              p.q + ((size_t)(t_begin + tl) * p.hq + h0 + g) * D + h * (D / 2));
 #pragma unroll
-          for (int ch = 0; ch < D / 8; ++ch) v[ch] = src[ch];
+          for (int ch = 0; ch < D / 16; ++ch) v[ch] = src[ch];
         } else {
 #pragma unroll
-          for (int ch = 0; ch < D / 8; ++ch) v[ch] = make_uint4(0u, 0u, 0u, 0u);
+          for (int ch = 0; ch < D / 16; ++ch) v[ch] = make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
-        for (int c16 = 0; c16 < D / 32; ++c16) {
+        for (int c16 = 0; c16 < D / 64; ++c16) {
           uint32_t w[16];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -517,7 +529,7 @@ __global__ void __launch_bounds__(256, 1)
             w[4 * k + 2] = v[4 * c16 + k].z;
             w[4 * k + 3] = v[4 * c16 + k].w;
           }
-          tmem_st16(lane_base + C::kQCol + d * (D / 2) + 16 * c16, w);
+          tmem_st16(lane_base + C::kQCol + d * (D / 2) + h * (D / 4) + 16 * c16, w);
         }
         tmem_wait_st();
         tc_fence_before_sync();
@@ -538,8 +550,10 @@ __global__ void __launch_bounds__(256, 1)
         const int lo_run = p.window > 0 ? max(it.tok_pos[rs] - p.window + 1, 0) : 0;
         const int pos_last = it.tok_pos[re - 1];
         const int first = lo_run / kPage, last = pos_last / kPage;
-        float m_ref = -INFINITY, l = 0.f;
+        float m_own = -INFINITY;  // reference max as of this warpgroup's last page
+        float l = 0.f;            // this warpgroup's row sum, relative to m_own
         for (int pg = first; pg <= last; ++pg, ++i) {
+          if ((i & 1) != h) continue;  // the other warpgroup's page
           const int b = i % C::kSBufs;
           if (!all_ok(wait(&s_full[b], (i / C::kSBufs) & 1))) {
             ok = false;
@@ -575,18 +589,32 @@ __global__ void __launch_bounds__(256, 1)
           const float mx = fmax3(fmax3(part[0], part[1], part[2]),
                                  fmax3(part[3], part[4], part[5]), fmaxf(part[6], part[7])) *
                            cc;
-          float alpha = 1.f;
-          bool rescale_o = false;
-          if (mx > m_ref + kLazyRescaleLog2) {
-            if (m_ref != -INFINITY) {
-              alpha = exp2_approx(m_ref - mx);
-              rescale_o = true;
+          // the run's reference after the previous page (the other warpgroup's)
+          float m_prev = -INFINITY;
+          if (pg > first) {
+            if (!all_ok(wait(&mref_bar[(i - 1) & 1], ((i - 1) >> 1) & 1))) {
+              ok = false;
+              break;
             }
-            l *= alpha;
-            m_ref = mx;
+            m_prev = mref_x[(i - 1) & 1][m];
           }
-          const float nml = m_ref == -INFINITY ? 0.f : -m_ref;
-          // P = 2^(s - m_ref) as a bf16 head and residual over the S columns
+          float m_new = m_prev, alpha = 1.f;
+          bool rose = false;
+          if (mx > m_prev + kLazyRescaleLog2) {
+            m_new = mx;
+            if (m_prev != -INFINITY) {
+              alpha = exp2_approx(m_prev - mx);
+              rose = true;
+            }
+          }
+          mref_x[i & 1][m] = m_new;
+          mbar_arrive(&mref_bar[i & 1]);
+          if (m_own != m_new) {
+            l = m_own == -INFINITY ? 0.f : l * exp2_approx(m_own - m_new);
+            m_own = m_new;
+          }
+          const float nml = m_new == -INFINITY ? 0.f : -m_new;
+          // P = 2^(s - m_new) as a bf16 head and residual over the S columns
           // (per chunk of 32 keys: head at +0, residual at +16, column j of a
           // half holding keys 2j, 2j + 1); pairs through the packed fp32 pipe
           const float2 cc2 = make_float2(cc, cc), nml2 = make_float2(nml, nml);
@@ -614,7 +642,7 @@ __global__ void __launch_bounds__(256, 1)
           const float2 s4 =
               __fadd2_rn(__fadd2_rn(sum2[0], sum2[1]), __fadd2_rn(sum2[2], sum2[3]));
           l += s4.x + s4.y;
-          if (__any_sync(0xffffffffu, rescale_o)) {
+          if (__any_sync(0xffffffffu, rose)) {
             // O holds P V up to the previous page, which must be done
             const int bp = (i - 1) % C::kSBufs;
             if (!all_ok(wait(&o_done[bp], ((i - 1) / C::kSBufs) & 1))) {
@@ -641,7 +669,7 @@ __global__ void __launch_bounds__(256, 1)
               break;
             }
             unsigned char* vt = v_slots + s * C::kTileBytes;
-            for (int e = m; e < kPage * (D / 8); e += C::kSoftmaxThreads) {
+            for (int e = m; e < kPage * (D / 8); e += C::kRows) {
               const int k = e / (D / 8), ch = e % (D / 8);
               if (k < rlo || k > rhi)
                 *reinterpret_cast<uint4*>(vt + (ch >> 3) * kBoxBytes + k * 128 + (ch & 7) * 16) =
@@ -655,9 +683,27 @@ __global__ void __launch_bounds__(256, 1)
         }
         if (!ok) break;
 
-        // end of run: O rows of this run are final once P V of its last page is done
-        const int bl = (i - 1) % C::kSBufs;
-        if (!all_ok(wait(&o_done[bl], ((i - 1) / C::kSBufs) & 1))) {
+        // end of run: the final reference, both row sums, then the O row once
+        // P V of the last page is done; each warpgroup stores half of it
+        const int il = i - 1;
+        float m_fin = m_own;
+        if ((il & 1) != h) {
+          if (!all_ok(wait(&mref_bar[il & 1], (il >> 1) & 1))) {
+            ok = false;
+            break;
+          }
+          m_fin = mref_x[il & 1][m];
+        }
+        if (m_own != m_fin) l = m_own == -INFINITY ? 0.f : l * exp2_approx(m_own - m_fin);
+        l_x[nrun & 1][h][m] = l;
+        mbar_arrive(l_bar);
+        if (!all_ok(wait(l_bar, nrun & 1))) {
+          ok = false;
+          break;
+        }
+        const float l_row = l_x[nrun & 1][0][m] + l_x[nrun & 1][1][m];
+        ++nrun;
+        if (!all_ok(wait(&o_done[il % C::kSBufs], (il / C::kSBufs) & 1))) {
           ok = false;
           break;
         }
@@ -666,16 +712,16 @@ __global__ void __launch_bounds__(256, 1)
         float inv = 0.f;
         if (live) {
           const float sk = p.sinks ? p.sinks[hh] * kLog2e : -INFINITY;
-          const float mf = fmaxf(m_ref, sk);
-          const float scl = exp2_approx(m_ref - mf);
-          const float total = fmaf(l, scl, exp2_approx(sk - mf));
+          const float mf = fmaxf(m_fin, sk);
+          const float scl = exp2_approx(m_fin - mf);
+          const float total = fmaf(l_row, scl, exp2_approx(sk - mf));
           inv = total > 0.f ? scl / total : 0.f;
         }
-        uint16_t* orow = p.out + ((size_t)(t_begin + tl) * p.hq + hh) * D;
+        uint16_t* orow = p.out + ((size_t)(t_begin + tl) * p.hq + hh) * D + h * (D / 2);
 #pragma unroll
-        for (int q16 = 0; q16 < D / 16; ++q16) {
+        for (int q16 = 0; q16 < D / 32; ++q16) {
           float ov[16];
-          tmem_ld16(lane_base + C::kOCol + 16 * q16, ov);
+          tmem_ld16(lane_base + C::kOCol + h * (D / 2) + 16 * q16, ov);
           tmem_wait_ld();
           if (live) {
             uint32_t w[8];
