@@ -36,7 +36,8 @@
 //     r + 32 for the scores; lane l owns D/32 output dims for P.V).
 // At the end the warps' states are merged through shared memory.  A row with
 // one split writes its output directly (sink included); otherwise the split
-// writes (m, l, acc) to the workspace and the combine kernel merges.
+// writes (m, l, acc) to the workspace and the combine kernel merges.  When no
+// row has more than one split the combine kernel is not launched at all.
 //
 // Pages wholly outside the window are never visited (the split range starts
 // at the window's first page).  Positions outside the window or past n inside
@@ -496,13 +497,30 @@ __global__ void __launch_bounds__(DecodeCfg<D, STAGES, Consumer>::kThreads,
   const int n = p.positions[b];
   const RowSpan span = row_span(n, p.window);
   const int nsplit = (span.pages + p.pages_per_split - 1) / p.pages_per_split;
-  if (split >= nsplit) return;     // inactive row, or past this row's splits
-  if (n / kPage >= p.maxp) return;  // reported (and zeroed) by the combine kernel
+  const int h0 = kvh * p.group;
+  // With one split per row (a grid one split wide) no combine kernel runs:
+  // this CTA zeroes its heads' outputs of an inactive or out-of-range row
+  // itself (and the kv head 0 CTA reports the latter).
+  const bool alone = gridDim.x == 1;
+  auto zero_heads = [&]() {
+    for (int e = tid; e < p.group * D; e += C::kThreads)
+      p.out[((size_t)b * p.hq + h0 + e / D) * D + e % D] = 0;
+  };
+  if (split >= nsplit) {  // inactive row, or past this row's splits
+    if (alone && n < 0) zero_heads();
+    return;
+  }
   const int table_row = p.row_of ? p.row_of[b] : b;
-  if (p.row_of && (table_row < 0 || table_row >= p.table_rows)) return;  // likewise
+  if (n / kPage >= p.maxp || (p.row_of && (table_row < 0 || table_row >= p.table_rows))) {
+    // otherwise reported and zeroed by the combine kernel
+    if (alone) {
+      zero_heads();
+      if (kvh == 0 && tid == 0) record_error(p.err, PGD_EDEVICE_BOUNDS);
+    }
+    return;
+  }
   const int page0 = span.first_page + split * p.pages_per_split;
   const int npages = min(p.pages_per_split, span.pages - split * p.pages_per_split);
-  const int h0 = kvh * p.group;
   const int32_t* trow = p.table ? p.table + (size_t)table_row * p.maxp + page0 : nullptr;
   const int dense0 = table_row * p.maxp + page0;  // page of index page0 without a table
 
@@ -758,7 +776,7 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& k_map,
   dim3 grid(grid_splits, p.hkv, p.rows);
   e = launch_pdl(paged_decode_split_kernel<D, STAGES, Consumer>, grid, dim3(C::kThreads),
                  C::kSmemBytes, stream, k_map, v_map, p);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || grid_splits == 1) return e;  // one split: written directly
   dim3 cgrid((p.hq + 3) / 4, p.rows);
   return launch_pdl(paged_decode_combine_kernel<D>, cgrid, dim3(128), 0, stream, p);
 }
