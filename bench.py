@@ -6,8 +6,8 @@ one shuffled pool of ~18 GB per K and V), the largest of the five workloads.
 One step = one append of each row's new K/V at its page slot, then grouped
 decode attention of every row over its pages.  Inputs are resident in HBM and
 much larger than L2 (129 MB), so no flush is needed between steps; smaller
-workloads (--workload) are timed step by step with a 1 GiB L2 flush between
-steps, outside the timed spans.
+workloads (--workload) are timed step by step with an L2 flush between steps,
+outside the timed spans (see L2Flush).
 
 Prints one JSON line.  `value` is achieved HBM GB/s of the whole step over
 all ranks (algorithmic bytes: every attended K/V row read once, q read, out
@@ -45,6 +45,24 @@ DEFAULT_WORKLOAD = "mistral_serve"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2 ** 20
+
+
+class L2Flush:
+    """Between timed steps: write a 1 GiB buffer (evicting everything the step
+    left in L2), then read a 512 MiB one, so that L2 holds clean lines of an
+    unrelated buffer.  After the write alone L2 would be full of dirty lines,
+    and the next step would pay for writing them back to HBM as it reads
+    (11 us of a 62 us decode call on the gpt-oss full-context workload)."""
+
+    label = "1 GiB write + 512 MiB read flush of L2 between steps"
+
+    def __init__(self, device):
+        self.dirty = torch.empty(2 ** 30, dtype=torch.uint8, device=device)
+        self.clean = torch.ones(2 ** 27, dtype=torch.float32, device=device)
+
+    def __call__(self, i: int):
+        self.dirty.fill_(i & 0xFF)
+        self.clean.sum()
 
 
 # --------------------------------------------------------------------------- bytes
@@ -307,7 +325,7 @@ def run_pgd(args, wl: Workload):
     by = algorithmic_bytes(wl, lay.positions)
     flush = None
     if by["step"] < 4 * L2_BYTES:
-        flush = torch.empty(2 ** 30, dtype=torch.uint8, device=device)
+        flush = L2Flush(device)
 
     q_rot = batch.q.clone() if args.rope else None
 
@@ -370,7 +388,7 @@ def run_pgd(args, wl: Workload):
     clocks.mark_start()
     for i in range(args.steps):
         if flush is not None:      # whole steps between flushes
-            flush.fill_(i & 0xFF)
+            flush(i)
             ev[i][0].record(stream)
             step_whole()
             ev[i][2].record(stream)
@@ -397,7 +415,7 @@ def run_pgd(args, wl: Workload):
         spans = {"append": 0.0, "decode": 0.0}
         for i in range(args.steps):
             for name, fn in (("append", step_append), ("decode", step_decode)):
-                flush.fill_(i & 0xFF)
+                flush(i)
                 a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
                 fn()
@@ -444,7 +462,7 @@ def run_pgd(args, wl: Workload):
         e2e_ms = e0.elapsed_time(e1)
     else:
         for i in range(args.steps):
-            flush.fill_(i & 0xFF)
+            flush(i)
             e0.record(stream)
             e2e_step()
             e1.record(stream)
@@ -469,7 +487,7 @@ def run_pgd(args, wl: Workload):
         "config": {"workload": describe(wl), "rows_per_gpu": wl.rows,
                    "pool_pages_per_gpu": lay.num_pages,
                    "pool_gb_per_gpu": 2 * lay.num_pages * wl.kv_heads * 64 * wl.head_dim * 2 / 1e9,
-                   "l2": "inputs larger than L2" if flush is None else "1 GiB L2 flush between steps",
+                   "l2": "inputs larger than L2" if flush is None else L2Flush.label,
                    "timing": "direct calls, back to back" if flush is None
                    else "CUDA graph replay of each whole step; each call alone for its span",
                    "pages_per_split": args.pages_per_split or "auto",
@@ -488,7 +506,8 @@ def run_pgd(args, wl: Workload):
                      "traffic": traffic, "algorithmic_bytes_per_launch": by["decode"]},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (1 + pgd.attention_kernel_count(
+            dims, 0, wl.window, args.pages_per_split, KERNEL_IDS[args.kernel])) * args.steps,
         "clocks": clk,
         "kernel_source_digest": digest,
     }
@@ -559,12 +578,12 @@ def run_prefill(args, wl):
     for _ in range(args.warmup):
         step()
     assert pgd.get_device_error() == pgd.OK
-    flush = torch.empty(2 ** 30, dtype=torch.uint8, device=device)
+    flush = L2Flush(device)
     e = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     stream = torch.cuda.current_stream()
     torch.cuda.synchronize()
     for i in range(args.steps):
-        flush.fill_(i & 0xFF)
+        flush(i)
         e[i][0].record(stream)
         step()
         e[i][1].record(stream)
@@ -585,7 +604,7 @@ def run_prefill(args, wl):
         "config": {"workload": f"{wl.name}: {wl.rows} rows, {wl.q_heads}q/{wl.kv_heads}kv, "
                                f"d{wl.head_dim}, prefix U[{wl.prefix_lo},{wl.prefix_hi}], "
                                f"chunk {wl.chunk}, window {wl.window}, sinks {wl.sinks}",
-                   "tokens": work["tokens"], "l2": "1 GiB L2 flush between steps",
+                   "tokens": work["tokens"], "l2": L2Flush.label,
                    "kernel": args.kernel},
         "gbs": gbs, "tflops": tflops,
         "roofline": {"bound": bound,
@@ -595,7 +614,10 @@ def run_prefill(args, wl):
                      "unit": "TFLOP/s" if bound == "tensor" else "GB/s",
                      "frac": tflops / tf if bound == "tensor" else gbs / hbm},
         "work": work,
-        "gpu_launches": 4 * args.steps,
+        # page_slots + kv_write_slots + the attention call's kernels
+        "gpu_launches": (2 + pgd.attention_kernel_count(
+            dims, b.table.shape[0], wl.window, args.pages_per_split,
+            KERNEL_IDS[args.kernel])) * args.steps,
     }
     print(json.dumps(line), flush=True)
 
@@ -629,11 +651,11 @@ def run_rows(args, wl):
         with torch.cuda.graph(g, stream=side):
             step()
     torch.cuda.synchronize()
-    flush = torch.empty(2 ** 30, dtype=torch.uint8, device=device)
+    flush = L2Flush(device)
     stream = torch.cuda.current_stream()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     for i in range(args.steps):
-        flush.fill_(i & 0xFF)
+        flush(i)
         ev[i][0].record(stream)
         g.replay()
         ev[i][1].record(stream)
@@ -648,12 +670,15 @@ def run_rows(args, wl):
         "ms_per_step": ms, "higher_is_better": True, "dtype": "f32", "storage_dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": f"{describe(wl)}, dense caches MaxSeq {b.max_seq}",
-                   "l2": "1 GiB L2 flush between steps",
+                   "l2": L2Flush.label,
                    "timing": "CUDA graph replay per step (write_rows + decode)"},
         "row_tokens_per_s": wl.rows / (ms * 1e-3),
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "peak_kind": kind,
                      "unit": "GB/s", "frac": gbs / peak},
-        "bytes_per_step": by, "gpu_launches": 3 * args.steps,
+        "bytes_per_step": by,
+        "gpu_launches": (1 + pgd.attention_kernel_count(
+            pgd._dense_dims(b.cache_k, wl.rows, wl.q_heads), 0, wl.window,
+            args.pages_per_split, kernel)) * args.steps,
     }
     print(json.dumps(line), flush=True)
 

@@ -200,6 +200,24 @@ PGD_API int pgd_rope_append_paged(const pgd_dims* dims, float theta, void* q,
 PGD_API size_t pgd_paged_decode_workspace_bytes(const pgd_dims* dims, const pgd_decode_options* opts);
 
 /*
+ * attention_kernel_count -- how many kernels one attention call with these
+ * arguments launches on the current device (for callers that count launches
+ * or size CUDA graphs; the pages have no counterpart).
+ *   table_rows  0 for pgd_paged_decode_attention; the table_rows argument of
+ *               pgd_paged_prefill_attention (> 0) for a prefill call.
+ *   window, opts  as passed to that call.
+ *   count       out: 0 when dims->rows == 0; 1 for the prefill kernels
+ *               (PREFILL_UMMA also issues one 4-byte cudaMemsetAsync) and
+ *               for split kernels whose rows all fit one split (it writes
+ *               every output); 2 when a row can span several splits (split
+ *               kernel + combine kernel).
+ * Returns PGD_EINVAL for a NULL count, negative table_rows or a kernel the
+ * call would reject, and the pgd_dims checks' codes.
+ */
+PGD_API int pgd_attention_kernel_count(const pgd_dims* dims, int32_t table_rows, int32_t window,
+                                       const pgd_decode_options* opts, int32_t* count);
+
+/*
  * paged_decode_attention -- paged_attention with an optional sink and window.
  *   q          bf16 [R][Hq][D]: queries (rope already applied).
  *   k_pool, v_pool  the pools, holding each active row's positions

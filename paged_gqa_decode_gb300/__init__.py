@@ -92,6 +92,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             lib.pgd_paged_prefill_attention.restype = ctypes.c_int
             lib.pgd_paged_decode_workspace_bytes.argtypes = [dims_p, opts_p]
             lib.pgd_paged_decode_workspace_bytes.restype = ctypes.c_size_t
+            lib.pgd_attention_kernel_count.argtypes = [dims_p, i32, i32, opts_p, vp]
+            lib.pgd_attention_kernel_count.restype = ctypes.c_int
             lib.pgd_paged_decode_attention.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, i32,
                                                       ctypes.c_float, vp, vp, ctypes.c_size_t,
                                                       opts_p, vp]
@@ -181,6 +183,21 @@ def kv_append_paged(k_new: torch.Tensor, v_new: torch.Tensor, table: torch.Tenso
 def paged_decode_workspace_bytes(dims: Dims, pages_per_split: int = 0) -> int:
     opts = DecodeOptions(pages_per_split, KERNEL_AUTO)
     return load_library().pgd_paged_decode_workspace_bytes(ctypes.byref(dims), ctypes.byref(opts))
+
+
+def attention_kernel_count(dims: Dims, table_rows: int = 0, window: int = 0,
+                           pages_per_split: int = 0, kernel: int = KERNEL_AUTO) -> int:
+    """Kernels one paged_decode_attention (table_rows 0) or
+    paged_prefill_attention (table_rows > 0) call with these arguments
+    launches on the current device."""
+    opts = DecodeOptions(pages_per_split, kernel)
+    count = ctypes.c_int32(0)
+    rc = load_library().pgd_attention_kernel_count(ctypes.byref(dims), int(table_rows),
+                                                   int(window), ctypes.byref(opts),
+                                                   ctypes.byref(count))
+    if rc != OK:
+        raise PgdError(rc, "attention_kernel_count")
+    return count.value
 
 
 def paged_decode_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,

@@ -50,6 +50,7 @@
 #include <math.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include "pgd_device.cuh"
 #include "pgd_internal.h"
@@ -669,28 +670,101 @@ __global__ void __launch_bounds__(DecodeCfg<D, STAGES, Consumer>::kThreads,
   }
 }
 
-// Merges the split partials of rows with two or more splits and folds in the
+// Merges nsplit >= 2 partials of one (row, query head) and folds in the
 // sink: M = max(max_i m_i, sink), L = sum_i l_i 2^(m_i - M) + 2^(sink - M),
-// out = sum_i acc_i 2^(m_i - M) / L.  Also zeroes inactive rows, rows whose
+// out = sum_i acc_i 2^(m_i - M) / L, written as bf16 to o.  Partial i is
+// (m, l) at ml + i * ml_stride and acc at ac + i * ac_stride (ac already
+// offset to this lane's dims).  A partial marked l < 0 (skipped for a bad
+// table entry or an abandoned wait) zeroes the output.
+// One warp; lane l owns dims [D/32 * l, D/32 * (l + 1)).  The partials'
+// (m, l) are read 32 at a time, one per lane, together with the first
+// kEarly accumulators, so the merge costs about one round trip to L2; the
+// weights are then broadcast by shuffle.
+template <int D>
+__device__ __forceinline__ void merge_partials(const float* ml, int ml_stride, const float* ac,
+                                               int ac_stride, int nsplit, float sk, uint16_t* o,
+                                               int lane) {
+  constexpr int kDims = D / 32;
+  constexpr int kEarly = 8;
+  using Vec = typename std::conditional<kDims == 2, float2, float4>::type;
+  Vec early[kEarly];
+#pragma unroll
+  for (int k = 0; k < kEarly; ++k)
+    if (k < nsplit) early[k] = *reinterpret_cast<const Vec*>(ac + (size_t)k * ac_stride);
+  float mx = sk;
+  bool skipped = false;
+  for (int base = 0; base < nsplit; base += 32) {
+    const int i = base + lane;
+    const float2 mli = i < nsplit ? *reinterpret_cast<const float2*>(ml + (size_t)i * ml_stride)
+                                  : make_float2(-INFINITY, 0.f);
+    mx = fmaxf(mx, warp_max(mli.x));
+    skipped |= __any_sync(0xffffffffu, mli.y < 0.f);
+  }
+  if (skipped || mx == -INFINITY) {
+#pragma unroll
+    for (int j = 0; j < kDims; ++j) o[j] = 0;
+    return;
+  }
+  float res[kDims];
+#pragma unroll
+  for (int j = 0; j < kDims; ++j) res[j] = 0.f;
+  float den = 0.f;
+  auto add = [&](const Vec& v, float f) {
+    res[0] = fmaf(v.x, f, res[0]);
+    res[1] = fmaf(v.y, f, res[1]);
+    if constexpr (kDims == 4) {
+      res[2] = fmaf(v.z, f, res[2]);
+      res[3] = fmaf(v.w, f, res[3]);
+    }
+  };
+  for (int base = 0; base < nsplit; base += 32) {
+    const int i = base + lane;
+    const float2 mli = i < nsplit ? *reinterpret_cast<const float2*>(ml + (size_t)i * ml_stride)
+                                  : make_float2(-INFINITY, 0.f);
+    const float fi = i < nsplit ? exp2_approx(mli.x - mx) : 0.f;
+    den += warp_sum(i < nsplit ? mli.y * fi : 0.f);
+    const int cnt = min(32, nsplit - base);
+    int k = 0;
+    if (base == 0) {
+#pragma unroll
+      for (; k < kEarly; ++k)
+        if (k < cnt) add(early[k], __shfl_sync(0xffffffffu, fi, k));
+      k = min(kEarly, cnt);
+    }
+#pragma unroll 4
+    for (; k < cnt; ++k)
+      add(*reinterpret_cast<const Vec*>(ac + (size_t)(base + k) * ac_stride),
+          __shfl_sync(0xffffffffu, fi, k));
+  }
+  den += exp2_approx(sk - mx);
+  const float inv = 1.f / den;
+#pragma unroll
+  for (int j = 0; j < kDims; ++j) o[j] = __bfloat16_as_ushort(__float2bfloat16_rn(res[j] * inv));
+}
+
+// Combine for the split kernel: merges the partials of rows with two or
+// more splits (merge_partials).  Also zeroes inactive rows and rows whose
 // position lies beyond their table or whose table row is out of range
-// (recording PGD_EDEVICE_BOUNDS) and rows with a split skipped for a bad
-// table entry (marked l < 0).
-// One warp per (row, query head); lane l owns dims [D/32 * l, D/32 * (l + 1)).
-// The splits' (m, l) are read 32 at a time, one per lane, so the loads are
-// independent; the weights are then broadcast by shuffle.
+// (recording PGD_EDEVICE_BOUNDS).  One warp per (row, query head).
 template <int D>
 __global__ void __launch_bounds__(128) paged_decode_combine_kernel(const DecodeParams p) {
   constexpr int kDims = D / 32;
-  pdl_wait();
-  pdl_allow_dependents();
   const int b = blockIdx.y;
   const int h = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (h >= p.hq) return;
-  const size_t bh = (size_t)b * p.hq + h;
-  uint16_t* o = p.out + bh * D + lane * kDims;
+  // positions, the token rows and the sinks are inputs of the split kernel
+  // as well, which reads them only after its own dependency wait; this grid
+  // starts after every split CTA has passed that wait, so they are final
+  // here and are read before this grid's wait, off its critical path.
+  const bool live = h < p.hq;
+  const size_t bh = (size_t)b * p.hq + (live ? h : 0);
   const int n = p.positions[b];
   const int table_row = p.row_of ? p.row_of[b] : b;
+  const float sk = (p.sinks && live) ? p.sinks[h] * kLog2e : -INFINITY;
+  pdl_wait();
+  pdl_allow_dependents();
+  if (!live) return;
+  uint16_t* o = p.out + bh * D + lane * kDims;
   const bool beyond = n >= 0 && (n / kPage >= p.maxp ||
                                  (p.row_of && (table_row < 0 || table_row >= p.table_rows)));
   if (n < 0 || beyond) {
@@ -702,54 +776,8 @@ __global__ void __launch_bounds__(128) paged_decode_combine_kernel(const DecodeP
   const RowSpan span = row_span(n, p.window);
   const int nsplit = (span.pages + p.pages_per_split - 1) / p.pages_per_split;
   if (nsplit <= 1) return;  // written by the split kernel
-
-  const float* ml = p.ws_ml + bh * p.max_splits * 2;
-  const float* ac = p.ws_acc + bh * p.max_splits * D + lane * kDims;
-  const float sk = p.sinks ? p.sinks[h] * kLog2e : -INFINITY;
-  float mx = sk;
-  bool skipped = false;
-  for (int base = 0; base < nsplit; base += 32) {
-    const int i = base + lane;
-    const float mi = i < nsplit ? ml[2 * i] : -INFINITY;
-    const float li = i < nsplit ? ml[2 * i + 1] : 0.f;
-    mx = fmaxf(mx, warp_max(mi));
-    skipped |= __any_sync(0xffffffffu, li < 0.f);
-  }
-  if (skipped || mx == -INFINITY) {
-#pragma unroll
-    for (int j = 0; j < kDims; ++j) o[j] = 0;
-    return;
-  }
-  float res[kDims];
-#pragma unroll
-  for (int j = 0; j < kDims; ++j) res[j] = 0.f;
-  float den = 0.f;
-  for (int base = 0; base < nsplit; base += 32) {
-    const int i = base + lane;
-    const float fi = i < nsplit ? exp2_approx(ml[2 * i] - mx) : 0.f;
-    den += warp_sum(i < nsplit ? ml[2 * i + 1] * fi : 0.f);
-    const int cnt = min(32, nsplit - base);
-#pragma unroll 4
-    for (int k = 0; k < cnt; ++k) {
-      const float f = __shfl_sync(0xffffffffu, fi, k);
-      const float* a = ac + (size_t)(base + k) * D;
-      if constexpr (kDims == 2) {
-        const float2 v = *reinterpret_cast<const float2*>(a);
-        res[0] = fmaf(v.x, f, res[0]);
-        res[1] = fmaf(v.y, f, res[1]);
-      } else {
-        const float4 v = *reinterpret_cast<const float4*>(a);
-        res[0] = fmaf(v.x, f, res[0]);
-        res[1] = fmaf(v.y, f, res[1]);
-        res[2] = fmaf(v.z, f, res[2]);
-        res[3] = fmaf(v.w, f, res[3]);
-      }
-    }
-  }
-  den += exp2_approx(sk - mx);
-  const float inv = 1.f / den;
-#pragma unroll
-  for (int j = 0; j < kDims; ++j) o[j] = __bfloat16_as_ushort(__float2bfloat16_rn(res[j] * inv));
+  merge_partials<D>(p.ws_ml + bh * p.max_splits * 2, 2,
+                    p.ws_acc + bh * p.max_splits * D + lane * kDims, D, nsplit, sk, o, lane);
 }
 
 template <int D, int STAGES, class Consumer>

@@ -21,7 +21,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kPageSize = 64;
-constexpr int kMinPagesPerSplit = 16;
+constexpr int kMinPagesPerSplit = 24;
 constexpr int kMaxPagesPerSplit = 64;
 
 struct DeviceInfo {
@@ -76,8 +76,8 @@ struct Plan {
 };
 
 // Pages per split: enough CTAs for several waves of 2 CTAs per SM when rows
-// are about half full, but at least 16 pages (a sweep over 1..64 on GB300
-// found every workload fastest at 16 or more: a split's fixed costs --
+// are about half full, but at least 24 pages (sweeps over 1..64 on GB300
+// found every workload fastest at 24 or more: a split's fixed costs --
 // setup, merge, partials and the combine -- outweigh the parallelism that
 // shorter splits add) and at most 64.
 Plan make_plan(const pgd_dims* d, const pgd_decode_options* opts, int sm_count) {
@@ -99,6 +99,34 @@ Plan make_plan(const pgd_dims* d, const pgd_decode_options* opts, int sm_count) 
 
 size_t workspace_bytes(const pgd_dims* d, const Plan& pl) {
   return (size_t)d->rows * d->num_q_heads * pl.max_splits * (d->head_dim + 2) * sizeof(float);
+}
+
+// The kernel a call runs: opts->kernel, or for AUTO the per-token split
+// kernel, except that prefill with tokens in runs goes to the tcgen05 kernel.
+int resolve_kernel(const pgd_dims* dims, int32_t table_rows, bool prefill,
+                   const pgd_decode_options* opts, int* kernel) {
+  int k = opts ? opts->kernel : PGD_KERNEL_AUTO;
+  if (k < PGD_KERNEL_AUTO || k > PGD_KERNEL_PREFILL_UMMA) return PGD_EINVAL;
+  if ((k == PGD_KERNEL_PREFILL_TILED || k == PGD_KERNEL_PREFILL_UMMA) && !prefill)
+    return PGD_EINVAL;
+  // Prefill: the tcgen05 kernel shares each page load among the tokens of a
+  // block, which pays when they come in runs (prompt chunks); tokens that are
+  // mostly one per table row (decode steps) go to the per-token split kernel.
+  if (prefill && k == PGD_KERNEL_AUTO && dims->rows >= 8ll * table_rows)
+    k = PGD_KERNEL_PREFILL_UMMA;
+  *kernel = k;
+  return PGD_OK;
+}
+
+// Pages the split grid must cover per row: the table width, or with a
+// window at most ceil((window - 1) / 64) + 1 pages.
+int span_pages(const pgd_dims* dims, int32_t window) {
+  int grid_pages = dims->max_pages_per_row;
+  if (window > 0) {
+    const int64_t wp = ((int64_t)window + kPageSize - 2) / kPageSize + 1;
+    if (wp < grid_pages) grid_pages = (int)wp;
+  }
+  return grid_pages;
 }
 
 int encode_pool_map_uncached(CUtensorMap* map, const void* pool, const pgd_dims* d, bool whole);
@@ -324,6 +352,29 @@ size_t pgd_paged_decode_workspace_bytes(const pgd_dims* dims, const pgd_decode_o
   return workspace_bytes(dims, make_plan(dims, opts, dev->sm_count));
 }
 
+int pgd_attention_kernel_count(const pgd_dims* dims, int32_t table_rows, int32_t window,
+                               const pgd_decode_options* opts, int32_t* count) {
+  if (!count) return PGD_EINVAL;
+  int rc = check_dims(dims);
+  if (rc != PGD_OK) return rc;
+  if (table_rows < 0) return PGD_EINVAL;
+  // The kernel choice does not depend on the device; the split size does.
+  int kernel = 0;
+  if ((rc = resolve_kernel(dims, table_rows, table_rows > 0, opts, &kernel)) != PGD_OK) return rc;
+  DeviceInfo* dev = nullptr;
+  if ((rc = current_device(&dev)) != PGD_OK) return rc;
+  const Plan pl = make_plan(dims, opts, dev->sm_count);
+  if (dims->rows == 0) {
+    *count = 0;
+  } else if (kernel == PGD_KERNEL_PREFILL_UMMA || kernel == PGD_KERNEL_PREFILL_TILED) {
+    *count = 1;
+  } else {
+    const int pages = span_pages(dims, window > 0 ? window : 0);
+    *count = (pages + pl.pages_per_split - 1) / pl.pages_per_split > 1 ? 2 : 1;
+  }
+  return PGD_OK;
+}
+
 static int decode_impl(const pgd_dims* dims, int32_t table_rows, const int32_t* row_of,
                        const void* q, const void* k_pool, const void* v_pool,
                        const int32_t* table, const int32_t* positions, const float* sinks,
@@ -349,17 +400,10 @@ static int decode_impl(const pgd_dims* dims, int32_t table_rows, const int32_t* 
   if (workspace_size < need) return PGD_EWORKSPACE;
   if (!workspace || !aligned16(workspace)) return PGD_EINVAL;
 
-  int kernel = opts ? opts->kernel : PGD_KERNEL_AUTO;
-  if (kernel < PGD_KERNEL_AUTO || kernel > PGD_KERNEL_PREFILL_UMMA) return PGD_EINVAL;
-  if ((kernel == PGD_KERNEL_PREFILL_TILED || kernel == PGD_KERNEL_PREFILL_UMMA) &&
-      row_of == nullptr)
-    return PGD_EINVAL;
+  int kernel = 0;
+  if ((rc = resolve_kernel(dims, table_rows, row_of != nullptr, opts, &kernel)) != PGD_OK)
+    return rc;
   const int padded = padded_group(dims->num_q_heads / dims->num_kv_heads);
-  // Prefill: the tcgen05 kernel shares each page load among the tokens of a
-  // block, which pays when they come in runs (prompt chunks); tokens that are
-  // mostly one per table row (decode steps) go to the per-token split kernel.
-  if (row_of != nullptr && kernel == PGD_KERNEL_AUTO && dims->rows >= 8ll * table_rows)
-    kernel = PGD_KERNEL_PREFILL_UMMA;
   // the tcgen05 prefill copies a head_dim-128 page tile with one 3-D box
   const bool whole = kernel == PGD_KERNEL_PREFILL_UMMA;
   CUtensorMap k_map, v_map;
@@ -391,12 +435,7 @@ static int decode_impl(const pgd_dims* dims, int32_t table_rows, const int32_t* 
   p.max_splits = pl.max_splits;
   p.q_scale_log2 = (float)((double)scale * 1.4426950408889634);
 
-  // With a window, a row spans at most ceil((window - 1) / 64) + 1 pages.
-  int grid_pages = dims->max_pages_per_row;
-  if (p.window > 0) {
-    const int64_t wp = ((int64_t)p.window + kPageSize - 2) / kPageSize + 1;
-    if (wp < grid_pages) grid_pages = (int)wp;
-  }
+  const int grid_pages = span_pages(dims, p.window);
   const int grid_splits = (grid_pages + pl.pages_per_split - 1) / pl.pages_per_split;
   const int pages_per_cta = grid_pages < pl.pages_per_split ? grid_pages : pl.pages_per_split;
 

@@ -30,7 +30,8 @@ def test_header_declares_the_entry_points():
         "pgd_kv_append_paged", "pgd_paged_decode_workspace_bytes", "pgd_paged_decode_attention",
         "pgd_get_device_error", "pgd_status_string", "pgd_version",
         "pgd_paged_decode_attention_static", "pgd_page_slots", "pgd_kv_write_slots",
-        "pgd_paged_prefill_attention", "pgd_rope_append_paged", "pgd_selftest_bounded_wait"}
+        "pgd_paged_prefill_attention", "pgd_rope_append_paged", "pgd_selftest_bounded_wait",
+        "pgd_attention_kernel_count"}
 
 
 def test_library_exports_every_declared_symbol_and_nothing_else(lib):
@@ -79,6 +80,8 @@ def test_host_rejects_bad_dims_without_a_device(lib, kw, status):
                                        0.125, None, None, 0, None, None)
     assert rc == status
     assert so.pgd_paged_decode_workspace_bytes(ctypes.byref(d), None) == 0
+    count = ctypes.c_int32(-1)
+    assert so.pgd_attention_kernel_count(ctypes.byref(d), 0, 0, None, ctypes.byref(count)) == status
 
 
 def test_bad_page_size_is_unsupported(lib):
@@ -95,6 +98,13 @@ def test_zero_rows_is_ok_and_null_pointers_are_rejected(lib):
     d = _dims()
     assert so.pgd_kv_append_paged(ctypes.byref(d), None, None, None, None, None, None, None) == 1
     assert so.pgd_kv_append_paged(None, None, None, None, None, None, None, None) == 1
+    assert so.pgd_attention_kernel_count(ctypes.byref(d), 0, 0, None, None) == 1
+    count = ctypes.c_int32(-1)
+    assert so.pgd_attention_kernel_count(ctypes.byref(d), -1, 0, None, ctypes.byref(count)) == 1
+    import paged_gqa_decode_gb300 as pgd
+    opts = pgd.DecodeOptions(0, pgd.KERNEL_PREFILL_UMMA)   # a prefill kernel for a decode call
+    assert so.pgd_attention_kernel_count(ctypes.byref(d), 0, 0, ctypes.byref(opts),
+                                         ctypes.byref(count)) == 1
 
 
 def test_product_package_does_not_import_the_oracle():

@@ -164,15 +164,17 @@ def test_split_sizes_force_the_combine(pps, window):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-def test_head_major_layout(d):
+@pytest.mark.parametrize("pps", [0, 3])
+def test_head_major_layout(d, pps):
     wl = Workload("headmajor", rows=7, q_heads=16, kv_heads=4, head_dim=d, ctx_lo=1, ctx_hi=900,
                   sinks=True)
     lay = layout_from_contexts(wl, [900, 1, 64, 65, 500, 129, 0], seed=11)
     batch = make_batch(wl, seed=61, device=DEV, layout=lay)
-    run_and_check(batch, layout=pgd.HEAD_MAJOR, pages_per_split=3)
+    run_and_check(batch, layout=pgd.HEAD_MAJOR, pages_per_split=pps)
 
 
-def test_shared_prefix_and_reversed_pages():
+@pytest.mark.parametrize("pps", [0, 1])
+def test_shared_prefix_and_reversed_pages(pps):
     """Rows 0 and 1 share their first three pages (a shared prefix) and
     differ in the page holding the new token; row 2 lists its pages in
     reverse pool order; row 3 is inactive and lists page 0."""
@@ -185,10 +187,11 @@ def test_shared_prefix_and_reversed_pages():
     contexts = [250, 230, 256, 0]
     lay = layout_from_contexts(wl, contexts, seed=0, num_pages=12, table=table)
     batch = make_batch(wl, seed=71, device=DEV, layout=lay)
-    run_and_check(batch, pages_per_split=1)
+    run_and_check(batch, pages_per_split=pps)
 
 
-def test_poisoned_slots_outside_attention_are_never_read():
+@pytest.mark.parametrize("pps", [0, 2])
+def test_poisoned_slots_outside_attention_are_never_read(pps):
     """Every pool position no row attends to holds NaN: any read of it that
     reached the result would show."""
     wl = Workload("poison", rows=6, q_heads=8, kv_heads=2, head_dim=128, ctx_lo=1, ctx_hi=600,
@@ -205,7 +208,7 @@ def test_poisoned_slots_outside_attention_are_never_read():
         view = pool.view(lay.num_pages, wl.kv_heads, 64, wl.head_dim)
         mask = nan_slots.view(lay.num_pages, 1, 64, 1).expand_as(view)
         view.masked_fill_(mask, float("nan"))
-    run_and_check(batch, window=window, pages_per_split=2)
+    run_and_check(batch, window=window, pages_per_split=pps)
 
 
 def test_inactive_rows_are_zero_and_untouched():
@@ -226,6 +229,28 @@ def test_zero_rows_is_a_no_op():
     assert out.shape == (0, 8, 64)
 
 
+def test_kernel_count_follows_the_split_plan():
+    """One kernel when every row fits one split (the split kernel writes the
+    outputs), two when a row can span several (split + combine)."""
+    def dims(wl, maxp, rows=None):
+        return pgd.make_dims(rows=wl.rows if rows is None else rows, num_q_heads=wl.q_heads,
+                             num_kv_heads=wl.kv_heads, head_dim=wl.head_dim, num_pages=100000,
+                             max_pages_per_row=maxp)
+    w = WORKLOADS
+    assert pgd.attention_kernel_count(dims(w["qwen_serve"], 10)) == 1
+    assert pgd.attention_kernel_count(dims(w["gptoss_full"], 64)) == 2
+    assert pgd.attention_kernel_count(dims(w["mistral_serve"], 512)) == 2
+    assert pgd.attention_kernel_count(dims(w["gptoss_sliding"], 512), window=128) == 1
+    assert pgd.attention_kernel_count(dims(w["gptoss_sliding"], 512), window=128,
+                                      pages_per_split=1) == 2
+    assert pgd.attention_kernel_count(dims(w["qwen_serve"], 10),
+                                      kernel=pgd.KERNEL_CUDA_CORE) == 1
+    assert pgd.attention_kernel_count(dims(w["gptoss_full"], 64, rows=0)) == 0
+    # prefill: tokens in runs take the tcgen05 kernel; one token per row the split kernel
+    assert pgd.attention_kernel_count(dims(w["mistral_serve"], 512, rows=4096), table_rows=8) == 1
+    assert pgd.attention_kernel_count(dims(w["mistral_serve"], 512, rows=8), table_rows=8) == 2
+
+
 # ---------------------------------------------------------------------------
 # Errors: caught on the host, or recorded on the device without a fault.
 
@@ -242,10 +267,11 @@ def test_device_bounds_errors_do_not_fault():
     assert torch.all(out[1] == 0)
     bad_pos = batch.positions.clone()
     bad_pos[2] = 64 * batch.table.shape[1] + 5      # beyond the row's table
-    out = pgd.paged_decode_attention(batch.q, batch.k_pool, batch.v_pool, batch.table, bad_pos,
-                                     num_kv_heads=2, pages_per_split=1)
-    assert pgd.get_device_error() == pgd.EDEVICE_BOUNDS
-    assert torch.all(out[2] == 0)
+    for pps in (1, 0):        # split kernel, balanced kernel
+        out = pgd.paged_decode_attention(batch.q, batch.k_pool, batch.v_pool, batch.table,
+                                         bad_pos, num_kv_heads=2, pages_per_split=pps)
+        assert pgd.get_device_error() == pgd.EDEVICE_BOUNDS
+        assert torch.all(out[2] == 0) and torch.any(out[0] != 0)
     before = batch.k_pool.clone()
     pgd.kv_append_paged(batch.k_new, batch.v_new, bad_table, bad_pos, batch.k_pool, batch.v_pool)
     assert pgd.get_device_error() == pgd.EDEVICE_BOUNDS

@@ -255,3 +255,29 @@ def test_prefill_large_logits(kernel):
     b.v_pool.mul_(0.5)
     b.v_new = b.v_new * 0.5
     prefill_check(b, kernel=kernel, what=f"large logits k={kernel}")
+
+
+@pytest.mark.parametrize("kernel", [pgd.KERNEL_TENSOR_CORE] + TILED_KERNELS)
+@pytest.mark.parametrize("hq,hkv,d", [(16, 4, 128), (8, 8, 128), (64, 8, 64)])
+def test_prefill_padding_tokens_fill_whole_blocks(hq, hkv, d, kernel):
+    """Padding tokens (position < 0) give zero outputs and write nothing.
+    Here they fill whole blocks of 128 / G consecutive tokens (and the tail),
+    so the token-block kernels meet work items with no pages at all, which
+    must still hand their slot back to the loaders."""
+    wl = PrefillWorkload("pad", rows=3, q_heads=hq, kv_heads=hkv, head_dim=d, prefix_lo=0,
+                         prefix_hi=900, chunk=0, window=0, sinks=True)
+    b = make_prefill_batch(wl, 19 + hq, DEV, prefix=[300, 0, 777], chunks=[200, 190, 300])
+    block = 128 // (hq // hkv)
+    pad = np.zeros(len(b.rows_np), dtype=bool)
+    pad[block:3 * block] = True                  # two whole blocks in the middle
+    pad[-(block + 5):] = True                    # the last block and a ragged piece
+    for r in range(3):                           # every row keeps an active token
+        assert not pad[b.rows_np == r].all()
+    b.positions_np = np.where(pad, -1, b.positions_np).astype(np.int32)
+    b.positions = torch.from_numpy(b.positions_np).to(DEV)
+    prefill_check(b, kernel=kernel, what=f"padding k={kernel} {hq}/{hkv}")
+    out = pgd.paged_prefill_attention(b.q, b.k_pool, b.v_pool, b.table, b.rows, b.positions,
+                                      b.sinks, 0, wl.scale, num_kv_heads=hkv, kernel=kernel)
+    assert pgd.get_device_error() == pgd.OK
+    padded = torch.from_numpy(pad).to(DEV)
+    assert torch.all(out[padded] == 0) and torch.all(out[~padded].abs().sum((1, 2)) > 0)
