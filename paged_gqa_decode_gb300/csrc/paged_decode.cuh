@@ -458,9 +458,9 @@ struct ScalarConsumer {
 
 // ------------------------------------------------------------------ split kernel
 
-template <int D, int STAGES, class Consumer>
+template <int D, int STAGES, class Consumer, int WARPS = 4>
 struct DecodeCfg {
-  static constexpr int kWarps = 4;  // consumer warps
+  static constexpr int kWarps = WARPS;  // consumer warps
   static constexpr int kThreads = (kWarps + 1) * 32;
   static constexpr int kBoxes = D / 64;
   static constexpr int kTileBytes = kPage * D * 2;
@@ -469,22 +469,23 @@ struct DecodeCfg {
   static constexpr int kHeads = Consumer::kHeads;
   static constexpr int kSmemBytes =
       1024 + kStages * kStageBytes + Consumer::kSharedFloats * 4 + 2 * kStages * 8;
-  // CTAs per SM the shared memory allows (228 KB per SM), at most 3 (three
-  // 160-thread CTAs leave 136 registers per thread); the CUDA-core consumer
-  // keeps its registers (no bound).
+  // CTAs per SM the shared memory allows (228 KB per SM) and that leave at
+  // least 136 registers per thread (three 160-thread CTAs, seven 64-thread
+  // ones); the CUDA-core consumer keeps its registers (no bound).
   static constexpr int kSmemBlocks = (228 * 1024) / (kSmemBytes + 1024);
+  static constexpr int kRegBlocks = 65536 / (kThreads * 136);
   static constexpr int kMinBlocks =
-      Consumer::kSharedFloats > 0 ? 1 : (kSmemBlocks >= 3 ? 3 : kSmemBlocks);
+      Consumer::kSharedFloats > 0 ? 1 : (kSmemBlocks < kRegBlocks ? kSmemBlocks : kRegBlocks);
   static_assert(kWarps * kHeads * (D + 2) * 4 <= kStages * kStageBytes, "merge buffer");
   static_assert(D == 64 || D == 128, "head_dim");
 };
 
-template <int D, int STAGES, class Consumer>
-__global__ void __launch_bounds__(DecodeCfg<D, STAGES, Consumer>::kThreads,
-                                  DecodeCfg<D, STAGES, Consumer>::kMinBlocks)
+template <int D, int STAGES, class Consumer, int WARPS>
+__global__ void __launch_bounds__(DecodeCfg<D, STAGES, Consumer, WARPS>::kThreads,
+                                  DecodeCfg<D, STAGES, Consumer, WARPS>::kMinBlocks)
     paged_decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                               const __grid_constant__ CUtensorMap v_map, const DecodeParams p) {
-  using C = DecodeCfg<D, STAGES, Consumer>;
+  using C = DecodeCfg<D, STAGES, Consumer, WARPS>;
   constexpr int GP = C::kHeads;
   pdl_wait();
   pdl_allow_dependents();
@@ -780,10 +781,11 @@ __global__ void __launch_bounds__(128) paged_decode_combine_kernel(const DecodeP
                     p.ws_acc + bh * p.max_splits * D + lane * kDims, D, nsplit, sk, o, lane);
 }
 
-template <int D, int STAGES, class Consumer>
+template <int D, int STAGES, class Consumer, int WARPS = 4>
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& k_map,
                           const CUtensorMap& v_map, int grid_splits, cudaStream_t stream) {
-  using C = DecodeCfg<D, STAGES, Consumer>;
+  using C = DecodeCfg<D, STAGES, Consumer, WARPS>;
+  auto kern = paged_decode_split_kernel<D, STAGES, Consumer, WARPS>;
   static_assert(C::kSmemBytes <= 227 * 1024, "shared memory");
   // The shared-memory opt-in is per device; set it once on each.
   static std::atomic<bool> configured[64];
@@ -791,23 +793,26 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& k_map,
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(paged_decode_split_kernel<D, STAGES, Consumer>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(paged_decode_split_kernel<D, STAGES, Consumer>,
-                             cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev].store(true, std::memory_order_release);
   }
   if (p.rows == 0) return cudaSuccess;
   dim3 grid(grid_splits, p.hkv, p.rows);
-  e = launch_pdl(paged_decode_split_kernel<D, STAGES, Consumer>, grid, dim3(C::kThreads),
-                 C::kSmemBytes, stream, k_map, v_map, p);
+  e = launch_pdl(kern, grid, dim3(C::kThreads), C::kSmemBytes, stream, k_map, v_map, p);
   if (e != cudaSuccess || grid_splits == 1) return e;  // one split: written directly
   dim3 cgrid((p.hq + 3) / 4, p.rows);
   return launch_pdl(paged_decode_combine_kernel<D>, cgrid, dim3(128), 0, stream, p);
 }
+
+// Splits of at most 3 pages (windows, short tables) are latency-bound: they
+// run with kShortWarps consumer warps and a ring of kShortStages3 stages for
+// 3 pages, so more CTAs share an SM.
+constexpr int kShortWarps = 2;
+constexpr int kShortStages3 = 3;
 
 // Kernel choice for one head_dim: the tensor-core consumer unless the caller
 // asks for the CUDA-core one.
@@ -820,11 +825,11 @@ cudaError_t launch_decode_for_dim(const DecodeParams& p, const CUtensorMap& k_ma
     // A ring no deeper than the pages a split can stream: shallower rings let
     // more CTAs share an SM when splits are short (windows, small contexts).
     if (pages_per_cta <= 1)
-      return launch_decode<D, 1, MmaConsumer<D>>(p, k_map, v_map, grid_splits, stream);
+      return launch_decode<D, 1, MmaConsumer<D>, kShortWarps>(p, k_map, v_map, grid_splits, stream);
     if (pages_per_cta <= 2)
-      return launch_decode<D, 2, MmaConsumer<D>>(p, k_map, v_map, grid_splits, stream);
+      return launch_decode<D, 2, MmaConsumer<D>, kShortWarps>(p, k_map, v_map, grid_splits, stream);
     if (D == 64 && pages_per_cta <= 3)
-      return launch_decode<D, 3, MmaConsumer<D>>(p, k_map, v_map, grid_splits, stream);
+      return launch_decode<D, kShortStages3, MmaConsumer<D>, kShortWarps>(p, k_map, v_map, grid_splits, stream);
     return launch_decode<D, kStages, MmaConsumer<D>>(p, k_map, v_map, grid_splits, stream);
   }
   switch (padded) {
