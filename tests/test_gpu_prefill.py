@@ -162,6 +162,17 @@ def test_prefill_head_major_and_cuda_core(layout):
     prefill_check(b, layout=layout, kernel=pgd.KERNEL_CUDA_CORE if layout else pgd.KERNEL_AUTO)
 
 
+@pytest.mark.parametrize("kernel", TILED_KERNELS)
+@pytest.mark.parametrize("d", [64, 128])
+def test_prefill_token_block_kernels_head_major(kernel, d):
+    """The token-block kernels on the head-major pool: a (page, kv head) tile
+    is still 64 contiguous rows, at another row of the pool."""
+    wl = PrefillWorkload("hm_tiles", rows=3, q_heads=16, kv_heads=4, head_dim=d, prefix_lo=0,
+                         prefix_hi=900, chunk=0, window=0, sinks=True)
+    b = make_prefill_batch(wl, 23 + d, DEV, prefix=[700, 0, 130], chunks=[90, 140, 33])
+    prefill_check(b, layout=pgd.HEAD_MAJOR, kernel=kernel, what=f"head-major k={kernel} d{d}")
+
+
 @pytest.mark.parametrize("kernel", [pgd.KERNEL_AUTO] + TILED_KERNELS)
 def test_prefill_interleaved_token_order(kernel):
     """Packed tokens need not be grouped by row or sorted by position."""
