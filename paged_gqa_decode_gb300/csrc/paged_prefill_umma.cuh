@@ -578,14 +578,20 @@ __global__ void __launch_bounds__(384, 1)
             for (int k = 0; k < kPage; ++k)
               if (!(live && pos0 + k >= lo && pos0 + k <= pos)) sv[k] = -INFINITY;
           }
+          // eight partial maxima: the first 8 scores, then 56 more two at a
+          // time (three blocks of 16 and a last block of 8)
           float part[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) part[j] = sv[j];
 #pragma unroll
-          for (int k = 8; k < kPage; k += 16)
+          for (int k = 8; k + 16 <= kPage; k += 16)
 #pragma unroll
             for (int j = 0; j < 8; ++j)
               part[j] = fmax3(part[j], sv[k + 2 * j], sv[k + 2 * j + 1]);
+          static_assert((kPage - 8) % 16 == 8, "the last block holds 8 scores");
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            part[j] = fmax3(part[j], sv[kPage - 8 + 2 * j], sv[kPage - 7 + 2 * j]);
           const float mx = fmax3(fmax3(part[0], part[1], part[2]),
                                  fmax3(part[3], part[4], part[5]), fmaxf(part[6], part[7])) *
                            cc;

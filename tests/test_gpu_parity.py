@@ -211,6 +211,20 @@ def test_poisoned_slots_outside_attention_are_never_read(pps):
     run_and_check(batch, window=window, pages_per_split=pps)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_scores_far_below_zero(d):
+    """q = -64 and every key 2 in every dimension: all scores equal and far
+    below zero, so the output is the mean of V over the attended keys; a
+    running maximum raised above the true one would zero every weight."""
+    wl = Workload("negative", rows=4, q_heads=16, kv_heads=4, head_dim=d, ctx_lo=1, ctx_hi=900)
+    lay = layout_from_contexts(wl, [900, 65, 1, 300], seed=29)
+    batch = make_batch(wl, seed=111, device=DEV, layout=lay)
+    batch.q.fill_(-64.0)
+    batch.k_pool.fill_(2.0)
+    batch.k_new.fill_(2.0)
+    run_and_check(batch, sinks=None, what=f"negative scores d{d}")
+
+
 def test_inactive_rows_are_zero_and_untouched():
     wl = Workload("inactive", rows=4, q_heads=4, kv_heads=1, head_dim=64, ctx_lo=1, ctx_hi=128)
     lay = layout_from_contexts(wl, [0, 100, 0, 1], seed=17, num_pages=6)

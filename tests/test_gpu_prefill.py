@@ -292,3 +292,19 @@ def test_prefill_padding_tokens_fill_whole_blocks(hq, hkv, d, kernel):
     assert pgd.get_device_error() == pgd.OK
     padded = torch.from_numpy(pad).to(DEV)
     assert torch.all(out[padded] == 0) and torch.all(out[~padded].abs().sum((1, 2)) > 0)
+
+
+@pytest.mark.parametrize("kernel", [pgd.KERNEL_TENSOR_CORE] + TILED_KERNELS)
+@pytest.mark.parametrize("d,window", [(128, 0), (64, 100)])
+def test_prefill_scores_far_below_zero(kernel, d, window):
+    """q = -64 and every key 2 in every dimension: all scores equal, about
+    -1450 (d 128) in score units, so the output is the mean of V over the
+    attended keys.  A running maximum raised above the true one by anything
+    (a stray value) would underflow every weight to zero."""
+    wl = PrefillWorkload("negative", rows=2, q_heads=16, kv_heads=4, head_dim=d, prefix_lo=0,
+                         prefix_hi=500, chunk=0, window=window, sinks=False)
+    b = make_prefill_batch(wl, 27 + d, DEV, prefix=[300, 0], chunks=[70, 90])
+    b.q.fill_(-64.0)
+    b.k_pool.fill_(2.0)
+    b.k_new.fill_(2.0)
+    prefill_check(b, sinks=None, kernel=kernel, what=f"negative scores k={kernel} d{d}")
