@@ -308,3 +308,26 @@ def test_prefill_scores_far_below_zero(kernel, d, window):
     b.k_pool.fill_(2.0)
     b.k_new.fill_(2.0)
     prefill_check(b, sinks=None, kernel=kernel, what=f"negative scores k={kernel} d{d}")
+
+
+@pytest.mark.parametrize("kernel", [pgd.KERNEL_TENSOR_CORE] + TILED_KERNELS)
+@pytest.mark.parametrize("d", [64, 128])
+def test_prefill_scores_rise_every_page(kernel, d):
+    """q = 1/4 and every key of logical page j equal to step * j in every
+    dimension: a token's scores grow by about 23 log2 units from one page to
+    the next, more than the lazy-rescale slack of 8, so on the tcgen05 kernel
+    the reference maximum is raised (and O rescaled) on page after page.  The
+    keys (multiples of 6 or 8 below 256) are exact in bf16."""
+    wl = PrefillWorkload("rising", rows=2, q_heads=16, kv_heads=4, head_dim=d, prefix_lo=0,
+                         prefix_hi=1500, chunk=0, window=0, sinks=True)
+    b = make_prefill_batch(wl, 31 + d, DEV, prefix=[1400, 200], chunks=[40, 64])
+    step = 8.0 if d == 64 else 6.0   # sqrt(d) * step / 4 * log2(e) ~ 23 per page
+    b.q.fill_(0.25)
+    view = b.k_pool.view(b.num_pages, wl.kv_heads, 64, d)
+    for r in range(2):
+        n_pages = (int(b.positions_np[b.rows_np == r].max()) // 64) + 1
+        for j in range(n_pages):
+            view[int(b.table_np[r, j])] = step * j
+    pages = torch.as_tensor(b.positions_np // 64, device=DEV, dtype=torch.float32)
+    b.k_new = (pages.view(-1, 1, 1) * step).expand_as(b.k_new).to(torch.bfloat16).contiguous()
+    prefill_check(b, kernel=kernel, what=f"rising scores k={kernel} d{d}")
