@@ -225,6 +225,27 @@ def test_scores_far_below_zero(d):
     run_and_check(batch, sinks=None, what=f"negative scores d{d}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("pps", [0, 2])
+def test_scores_rise_every_page(d, pps):
+    """Keys of logical page j equal to step * j, q = 1/4: scores grow by about
+    23 log2 units per page, so the running maximum changes on every page and
+    within a split every earlier page's weight is rescaled away."""
+    wl = Workload("rising", rows=3, q_heads=16, kv_heads=4, head_dim=d, ctx_lo=1, ctx_hi=1500,
+                  sinks=True)
+    lay = layout_from_contexts(wl, [1500, 130, 64], seed=37)
+    batch = make_batch(wl, seed=121, device=DEV, layout=lay)
+    step = 8.0 if d == 64 else 6.0
+    batch.q.fill_(0.25)
+    view = batch.k_pool.view(lay.num_pages, wl.kv_heads, 64, d)
+    for r, n in enumerate(lay.positions):
+        for j in range(int(n) // 64 + 1):
+            view[int(lay.table[r, j])] = step * j
+    pages = torch.as_tensor(lay.positions // 64, device=DEV, dtype=torch.float32)
+    batch.k_new = (pages.view(-1, 1, 1) * step).expand_as(batch.k_new).to(torch.bfloat16).contiguous()
+    run_and_check(batch, pages_per_split=pps, what=f"rising scores d{d} pps{pps}")
+
+
 def test_inactive_rows_are_zero_and_untouched():
     wl = Workload("inactive", rows=4, q_heads=4, kv_heads=1, head_dim=64, ctx_lo=1, ctx_hi=128)
     lay = layout_from_contexts(wl, [0, 100, 0, 1], seed=17, num_pages=6)
