@@ -4,7 +4,9 @@ Default workload: the Mistral-7B-v0.3-shaped serving batch (256 rows, 32 query
 / 8 kv heads, head_dim 128, contexts ~ U[1024, 32768], 64-position pages in
 one shuffled pool of ~18 GB per K and V), the largest of the five workloads.
 One step = one append of each row's new K/V at its page slot, then grouped
-decode attention of every row over its pages.  Inputs are resident in HBM and
+decode attention of every row over its pages: one paged_decode_step call (the
+append inside the decode launch), or with --two-calls kv_append_paged then
+paged_decode_attention.  Inputs are resident in HBM and
 much larger than L2 (129 MB), so no flush is needed between steps; smaller
 workloads (--workload) are timed step by step with an L2 flush between steps,
 outside the timed spans (see L2Flush).
@@ -328,8 +330,13 @@ def run_pgd(args, wl: Workload):
         flush = L2Flush(device)
 
     q_rot = batch.q.clone() if args.rope else None
+    # one call per step (the append inside the decode launch) unless the two
+    # calls are asked for or the append also rotates q and k
+    fused = not (args.two_calls or args.rope)
 
     def append():
+        if fused:  # the append runs inside the decode launch (paged_decode_step)
+            return
         if args.rope:   # rope_rows on q and k fused into the append (base 1e6)
             q_rot.copy_(batch.q)
             pgd.rope_append_paged(q_rot, batch.k_new, batch.v_new, batch.table,
@@ -339,6 +346,13 @@ def run_pgd(args, wl: Workload):
                                 batch.k_pool, batch.v_pool)
 
     def decode():
+        if fused:
+            pgd.paged_decode_step(batch.q, batch.k_new, batch.v_new, batch.k_pool, batch.v_pool,
+                                  batch.table, batch.positions, batch.sinks, wl.window, wl.scale,
+                                  num_kv_heads=wl.kv_heads, out=out, workspace=ws,
+                                  pages_per_split=args.pages_per_split,
+                                  kernel=KERNEL_IDS[args.kernel])
+            return
         pgd.paged_decode_attention(q_rot if args.rope else batch.q, batch.k_pool, batch.v_pool, batch.table,
                                    batch.positions, batch.sinks, wl.window, wl.scale,
                                    num_kv_heads=wl.kv_heads, out=out, workspace=ws,
@@ -368,13 +382,16 @@ def run_pgd(args, wl: Workload):
             decode()
 
         with torch.cuda.stream(side):
-            for fn in (append, decode, whole):
+            # with the append fused the step is the decode call alone
+            for fn in ((decode, whole) if fused else (append, decode, whole)):
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g, stream=side):
                     fn()
                 graphs.append(g)
         torch.cuda.synchronize()
-        step_append, step_decode, step_whole = (g.replay for g in graphs)
+        if fused:
+            graphs.insert(0, None)
+        step_append, step_decode, step_whole = (g.replay if g else append for g in graphs)
         for _ in range(3):
             step_whole()
         torch.cuda.synchronize()
@@ -414,7 +431,8 @@ def run_pgd(args, wl: Workload):
         # each call alone, for the per-kernel spans (outside the step timing)
         spans = {"append": 0.0, "decode": 0.0}
         for i in range(args.steps):
-            for name, fn in (("append", step_append), ("decode", step_decode)):
+            for name, fn in ((("decode", step_decode),) if fused else
+                             (("append", step_append), ("decode", step_decode))):
                 flush(i)
                 a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
@@ -476,7 +494,10 @@ def run_pgd(args, wl: Workload):
         return
     peak, peak_kind = measured_peak()
     decode_s = decode_ms * 1e-3 / args.steps
-    achieved = by["decode"] / decode_s / 1e9
+    # the decode call's algorithmic bytes; with the append fused in, its
+    # read and write are part of the call
+    call_bytes = by["decode"] + (by["append"] if fused else 0)
+    achieved = call_bytes / decode_s / 1e9
     digest = source_digest()
     traffic = kernel_traffic(digest, wl.name)
     line = {
@@ -491,22 +512,24 @@ def run_pgd(args, wl: Workload):
                    "timing": "direct calls, back to back" if flush is None
                    else "CUDA graph replay of each whole step; each call alone for its span",
                    "pages_per_split": args.pages_per_split or "auto",
-                   "kernel": args.kernel, "rope": bool(args.rope),
+                   "kernel": args.kernel, "rope": bool(args.rope), "fused_append": bool(fused),
                    "parallelism": f"replicas over rows x{world}"},
         "row_tokens_per_s": total_rows / (step_ms * 1e-3),
         "pct_of_nominal_8tbs": 100.0 * value / world / NOMINAL_HBM_GBS,
         "pct_of_measured_peak": 100.0 * value / world / peak,
-        "append_ms_per_step": append_ms / args.steps,
+        "append_ms_per_step": None if fused else append_ms / args.steps,
         "decode_ms_per_step": decode_ms / args.steps,
         "bytes_per_step_per_gpu": by,
-        "roofline": {"bound": "hbm", "kernel": "paged_decode (split + combine kernels)",
+        "roofline": {"bound": "hbm",
+                     "kernel": "paged_decode_step (split kernel with the append, + combine)"
+                     if fused else "paged_decode (split + combine kernels)",
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak,
                      "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
-                     "traffic": traffic, "algorithmic_bytes_per_launch": by["decode"]},
+                     "traffic": traffic, "algorithmic_bytes_per_launch": call_bytes},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
-        "gpu_launches": (1 + pgd.attention_kernel_count(
+        "gpu_launches": ((0 if fused else 1) + pgd.attention_kernel_count(
             dims, 0, wl.window, args.pages_per_split, KERNEL_IDS[args.kernel])) * args.steps,
         "clocks": clk,
         "kernel_source_digest": digest,
@@ -699,6 +722,9 @@ def main():
     ap.add_argument("--kernel", choices=list(KERNEL_IDS), default="auto",
                     help="kernel variant: decode tensor-core or CUDA-core products; prefill "
                          "also the token-block kernels (mma.sync 'tiled', tcgen05 'umma')")
+    ap.add_argument("--two-calls", action="store_true",
+                    help="kv_append_paged and paged_decode_attention as two calls (default: "
+                         "one paged_decode_step call, the append inside the decode launch)")
     ap.add_argument("--rope", action="store_true",
                     help="decode path: fuse rope_rows (base 1e6) into the append")
     ap.add_argument("--rows", type=int, default=0,

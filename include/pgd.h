@@ -245,6 +245,27 @@ PGD_API int pgd_paged_decode_attention(const pgd_dims* dims, const void* q, cons
                                const pgd_decode_options* opts, pgd_stream_t stream);
 
 /*
+ * paged_decode_step -- pgd_kv_append_paged then pgd_paged_decode_attention
+ * in one launch (plus the combine kernel when a row spans several splits):
+ * the decode_paged step of the pages (Mistral 7B Instruct v0.3 model files,
+ * src/attention.linnet, GroupedQueryAttention.decode_paged: write_tokens,
+ * then paged_attention).  For each active row, the CTA that streams the
+ * row's last page (per kv head) first writes k_new and v_new at the slot of
+ * positions[b] and then loads that page, so the new token attends to itself.
+ *   k_new, v_new  bf16 [R][Hkv][D]; k_pool, v_pool written as by
+ *                 pgd_kv_append_paged.  Other arguments, the workspace and
+ *                 the result as for pgd_paged_decode_attention.
+ * Device errors as for pgd_paged_decode_attention; a row whose last split
+ * reads a table entry outside the pool gets no append.
+ */
+PGD_API int pgd_paged_decode_step(const pgd_dims* dims, const void* q, const void* k_new,
+                                  const void* v_new, void* k_pool, void* v_pool,
+                                  const int32_t* table, const int32_t* positions,
+                                  const float* sinks, int32_t window, float scale, void* out,
+                                  void* workspace, size_t workspace_bytes,
+                                  const pgd_decode_options* opts, pgd_stream_t stream);
+
+/*
  * paged_prefill_attention -- packed prompt tokens over their rows' pages
  * (Mistral 7B Instruct v0.3 model files, src/attention.linnet,
  * prefill_paged / step_paged and the model's prefill_paged entry; window and

@@ -98,6 +98,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                                       ctypes.c_float, vp, vp, ctypes.c_size_t,
                                                       opts_p, vp]
             lib.pgd_paged_decode_attention.restype = ctypes.c_int
+            lib.pgd_paged_decode_step.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, vp, vp, i32,
+                                                  ctypes.c_float, vp, vp, ctypes.c_size_t,
+                                                  opts_p, vp]
+            lib.pgd_paged_decode_step.restype = ctypes.c_int
             lib.pgd_get_device_error.argtypes = [vp]
             lib.pgd_get_device_error.restype = ctypes.c_int
             lib.pgd_status_string.argtypes = [ctypes.c_int]
@@ -213,7 +217,28 @@ def paged_decode_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.
     q: bf16 [R, Hq, D]; pools: bf16 with num_kv_heads kv heads in ``layout``;
     table: int32 [R, max_pages]; positions: int32 [R]; sinks: fp32 [Hq] or
     None; window <= 0 for full attention.  Returns bf16 [R, Hq, D]."""
-    dev = _check_cuda(q, k_pool, v_pool, table, positions, sinks, out, workspace)
+    return _decode(q, None, None, k_pool, v_pool, table, positions, sinks, window, scale,
+                   num_kv_heads, layout, out, workspace, pages_per_split, kernel, stream)
+
+
+def paged_decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                      k_pool: torch.Tensor, v_pool: torch.Tensor, table: torch.Tensor,
+                      positions: torch.Tensor, sinks: torch.Tensor | None = None,
+                      window: int = 0, scale: float | None = None, *, num_kv_heads: int,
+                      layout: int = PAGE_MAJOR, out: torch.Tensor | None = None,
+                      workspace: torch.Tensor | None = None, pages_per_split: int = 0,
+                      kernel: int = KERNEL_AUTO,
+                      stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """kv_append_paged then paged_decode_attention in one launch: each row's
+    new K/V (bf16 [R, Hkv, D]) goes to its slot in the pools and the row
+    attends over its pages, the new token included."""
+    return _decode(q, k_new, v_new, k_pool, v_pool, table, positions, sinks, window, scale,
+                   num_kv_heads, layout, out, workspace, pages_per_split, kernel, stream)
+
+
+def _decode(q, k_new, v_new, k_pool, v_pool, table, positions, sinks, window, scale,
+            num_kv_heads, layout, out, workspace, pages_per_split, kernel, stream):
+    dev = _check_cuda(q, k_new, v_new, k_pool, v_pool, table, positions, sinks, out, workspace)
     _dtype(q, torch.bfloat16, "q")
     _dtype(k_pool, torch.bfloat16, "k_pool")
     _dtype(v_pool, torch.bfloat16, "v_pool")
@@ -225,6 +250,11 @@ def paged_decode_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.
     if positions.shape != (rows,) or table.dim() != 2 or table.shape[0] != rows \
             or k_pool.shape != v_pool.shape or (sinks is not None and sinks.shape != (hq,)):
         raise ValueError("inconsistent shapes")
+    if k_new is not None:
+        _dtype(k_new, torch.bfloat16, "k_new")
+        _dtype(v_new, torch.bfloat16, "v_new")
+        if k_new.shape != (rows, num_kv_heads, d) or v_new.shape != k_new.shape:
+            raise ValueError("k_new and v_new must be [R, Hkv, D]")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     dims = make_dims(rows=rows, num_q_heads=hq, num_kv_heads=num_kv_heads, head_dim=d,
@@ -240,13 +270,19 @@ def paged_decode_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.
         need = lib.pgd_paged_decode_workspace_bytes(ctypes.byref(dims), ctypes.byref(opts))
         if workspace is None:
             workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
-        rc = lib.pgd_paged_decode_attention(
-            ctypes.byref(dims), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(table),
-            _ptr(positions), _ptr(sinks), int(window), float(scale), _ptr(out), _ptr(workspace),
-            workspace.numel() * workspace.element_size(), ctypes.byref(opts),
-            _stream_handle(stream))
+        tail = (_ptr(table), _ptr(positions), _ptr(sinks), int(window), float(scale), _ptr(out),
+                _ptr(workspace), workspace.numel() * workspace.element_size(),
+                ctypes.byref(opts), _stream_handle(stream))
+        if k_new is None:
+            rc = lib.pgd_paged_decode_attention(ctypes.byref(dims), _ptr(q), _ptr(k_pool),
+                                                _ptr(v_pool), *tail)
+            what = "paged_decode_attention"
+        else:
+            rc = lib.pgd_paged_decode_step(ctypes.byref(dims), _ptr(q), _ptr(k_new), _ptr(v_new),
+                                           _ptr(k_pool), _ptr(v_pool), *tail)
+            what = "paged_decode_step"
     if rc != OK:
-        raise PgdError(rc, "paged_decode_attention")
+        raise PgdError(rc, what)
     return out
 
 

@@ -575,6 +575,23 @@ __global__ void __launch_bounds__(DecodeCfg<D, STAGES, Consumer, WARPS>::kThread
 
   // ---------------------------------------------------------------- producer
   if (warp == C::kWarps) {
+    if (p.k_new != nullptr && page0 + npages - 1 == n / kPage) {
+      // Decode step: this split holds the row's last page, so it writes the
+      // new token's K and V at their slot (position n), then orders those
+      // writes before its copies of the page, which read them back.
+      const int page = trow ? trow[npages - 1] : dense0 + npages - 1;
+      const size_t dst =
+          ((size_t)tile_first_row(p.layout, page, kvh, p.hkv, p.num_pages, p.maxp) + n % kPage) * D;
+      const size_t src = ((size_t)b * p.hkv + kvh) * D;
+      for (int c = lane; c < D / 8; c += 32) {
+        *reinterpret_cast<uint4*>(p.k_pool + dst + 8 * c) =
+            *reinterpret_cast<const uint4*>(p.k_new + src + 8 * c);
+        *reinterpret_cast<uint4*>(p.v_pool + dst + 8 * c) =
+            *reinterpret_cast<const uint4*>(p.v_new + src + 8 * c);
+      }
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      __syncwarp();
+    }
     if (lane == 0) {
       prefetch_tensormap(&k_map);
       prefetch_tensormap(&v_map);

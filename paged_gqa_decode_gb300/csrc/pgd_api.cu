@@ -380,7 +380,8 @@ static int decode_impl(const pgd_dims* dims, int32_t table_rows, const int32_t* 
                        const int32_t* table, const int32_t* positions, const float* sinks,
                        int32_t window, float scale, void* out, void* workspace,
                        size_t workspace_size, const pgd_decode_options* opts,
-                       pgd_stream_t stream) {
+                       pgd_stream_t stream, const void* k_new = nullptr,
+                       const void* v_new = nullptr) {
   int rc = check_dims(dims);
   if (rc != PGD_OK) return rc;
   if (dims->rows == 0) return PGD_OK;
@@ -391,6 +392,9 @@ static int decode_impl(const pgd_dims* dims, int32_t table_rows, const int32_t* 
                     dims->num_pages)
     return PGD_EINVAL;  // dense rows: every row needs its own P pages
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
+    return PGD_EINVAL;
+  if ((k_new == nullptr) != (v_new == nullptr) || (k_new && (row_of != nullptr ||
+                                                             !aligned16(k_new) || !aligned16(v_new))))
     return PGD_EINVAL;
   if (!std::isfinite(scale)) return PGD_EINVAL;
   DeviceInfo* dev = nullptr;
@@ -434,6 +438,10 @@ static int decode_impl(const pgd_dims* dims, int32_t table_rows, const int32_t* 
   p.pages_per_split = pl.pages_per_split;
   p.max_splits = pl.max_splits;
   p.q_scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.k_new = static_cast<const uint16_t*>(k_new);
+  p.v_new = static_cast<const uint16_t*>(v_new);
+  p.k_pool = k_new ? static_cast<uint16_t*>(const_cast<void*>(k_pool)) : nullptr;
+  p.v_pool = k_new ? static_cast<uint16_t*>(const_cast<void*>(v_pool)) : nullptr;
 
   const int grid_pages = span_pages(dims, p.window);
   const int grid_splits = (grid_pages + pl.pages_per_split - 1) / pl.pages_per_split;
@@ -463,6 +471,17 @@ int pgd_paged_decode_attention(const pgd_dims* dims, const void* q, const void* 
                                const pgd_decode_options* opts, pgd_stream_t stream) {
   return decode_impl(dims, dims ? dims->rows : 0, nullptr, q, k_pool, v_pool, table, positions,
                      sinks, window, scale, out, workspace, workspace_size, opts, stream);
+}
+
+int pgd_paged_decode_step(const pgd_dims* dims, const void* q, const void* k_new,
+                          const void* v_new, void* k_pool, void* v_pool, const int32_t* table,
+                          const int32_t* positions, const float* sinks, int32_t window,
+                          float scale, void* out, void* workspace, size_t workspace_size,
+                          const pgd_decode_options* opts, pgd_stream_t stream) {
+  if (dims && dims->rows > 0 && (!k_new || !v_new)) return PGD_EINVAL;
+  return decode_impl(dims, dims ? dims->rows : 0, nullptr, q, k_pool, v_pool, table, positions,
+                     sinks, window, scale, out, workspace, workspace_size, opts, stream, k_new,
+                     v_new);
 }
 
 int pgd_paged_prefill_attention(const pgd_dims* dims, int32_t table_rows, const void* q,

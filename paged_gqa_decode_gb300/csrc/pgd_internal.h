@@ -56,6 +56,13 @@ struct DecodeParams {
   int pages_per_split;  // pages one split CTA streams
   int max_splits;       // split stride of the workspace
   float q_scale_log2;   // scale * log2(e): scores are kept in log2 units
+  // decode step (append fused in): each row's new K/V [R][Hkv][D], written
+  // into the pools at its slot by the split holding the row's last page
+  // before that page is loaded; nullptr: no append
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  uint16_t* k_pool;
+  uint16_t* v_pool;
 };
 
 // Padded query-group sizes that have a decode kernel instantiation.

@@ -31,7 +31,7 @@ def test_header_declares_the_entry_points():
         "pgd_get_device_error", "pgd_status_string", "pgd_version",
         "pgd_paged_decode_attention_static", "pgd_page_slots", "pgd_kv_write_slots",
         "pgd_paged_prefill_attention", "pgd_rope_append_paged", "pgd_selftest_bounded_wait",
-        "pgd_attention_kernel_count"}
+        "pgd_attention_kernel_count", "pgd_paged_decode_step"}
 
 
 def test_library_exports_every_declared_symbol_and_nothing_else(lib):
