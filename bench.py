@@ -657,6 +657,11 @@ def run_rows(args, wl):
     kernel = KERNEL_IDS[args.kernel]
 
     def step():
+        if not args.two_calls:   # the append inside the decode launch
+            pgd.decode_rows_step(b.q, b.k_new, b.v_new, b.cache_k, b.cache_v, b.positions,
+                                 b.sinks, wl.window, wl.scale, out=out,
+                                 pages_per_split=args.pages_per_split, kernel=kernel)
+            return
         pgd.kv_append_rows(b.k_new, b.v_new, b.positions, b.cache_k, b.cache_v)
         pgd.decode_rows_attention(b.q, b.cache_k, b.cache_v, b.positions, b.sinks, wl.window,
                                   wl.scale, out=out, pages_per_split=args.pages_per_split,
@@ -694,12 +699,12 @@ def run_rows(args, wl):
         "data": "synthetic",
         "config": {"workload": f"{describe(wl)}, dense caches MaxSeq {b.max_seq}",
                    "l2": L2Flush.label,
-                   "timing": "CUDA graph replay per step (write_rows + decode)"},
+                   "timing": "CUDA graph replay per step (write_rows + decode" + (", two calls)" if args.two_calls else " in one launch)")},
         "row_tokens_per_s": wl.rows / (ms * 1e-3),
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "peak_kind": kind,
                      "unit": "GB/s", "frac": gbs / peak},
         "bytes_per_step": by,
-        "gpu_launches": (1 + pgd.attention_kernel_count(
+        "gpu_launches": ((1 if args.two_calls else 0) + pgd.attention_kernel_count(
             pgd._dense_dims(b.cache_k, wl.rows, wl.q_heads), 0, wl.window,
             args.pages_per_split, kernel)) * args.steps,
     }

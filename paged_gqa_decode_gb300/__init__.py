@@ -452,7 +452,25 @@ def decode_rows_attention(q: torch.Tensor, cache_k: torch.Tensor, cache_v: torch
                           stream: torch.cuda.Stream | None = None) -> torch.Tensor:
     """decode_rows: row b's queries (q bf16 [R, Hq, D]) attend over row b of the
     dense caches (bf16 [Batch, Hkv, MaxSeq, D]) up to positions[b]."""
-    dev = _check_cuda(q, cache_k, cache_v, positions, sinks, out, workspace)
+    return _decode_rows(q, None, None, cache_k, cache_v, positions, sinks, window, scale, out,
+                        workspace, pages_per_split, kernel, stream)
+
+
+def decode_rows_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                     cache_k: torch.Tensor, cache_v: torch.Tensor, positions: torch.Tensor,
+                     sinks: torch.Tensor | None = None, window: int = 0,
+                     scale: float | None = None, *, out: torch.Tensor | None = None,
+                     workspace: torch.Tensor | None = None, pages_per_split: int = 0,
+                     kernel: int = KERNEL_AUTO,
+                     stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """kv_append_rows then decode_rows_attention in one launch."""
+    return _decode_rows(q, k_new, v_new, cache_k, cache_v, positions, sinks, window, scale, out,
+                        workspace, pages_per_split, kernel, stream)
+
+
+def _decode_rows(q, k_new, v_new, cache_k, cache_v, positions, sinks, window, scale, out,
+                 workspace, pages_per_split, kernel, stream):
+    dev = _check_cuda(q, k_new, v_new, cache_k, cache_v, positions, sinks, out, workspace)
     _dtype(q, torch.bfloat16, "q")
     _dtype(cache_k, torch.bfloat16, "cache_k")
     _dtype(cache_v, torch.bfloat16, "cache_v")
@@ -463,6 +481,11 @@ def decode_rows_attention(q: torch.Tensor, cache_k: torch.Tensor, cache_v: torch
     if cache_k.shape != cache_v.shape or positions.shape != (rows,) or cache_k.shape[3] != d \
             or (sinks is not None and sinks.shape != (hq,)):
         raise ValueError("inconsistent shapes")
+    if k_new is not None:
+        _dtype(k_new, torch.bfloat16, "k_new")
+        _dtype(v_new, torch.bfloat16, "v_new")
+        if k_new.shape != (rows, cache_k.shape[1], d) or v_new.shape != k_new.shape:
+            raise ValueError("k_new and v_new must be [R, Hkv, D]")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     dims = _dense_dims(cache_k, rows, hq)
@@ -474,13 +497,19 @@ def decode_rows_attention(q: torch.Tensor, cache_k: torch.Tensor, cache_v: torch
         need = lib.pgd_paged_decode_workspace_bytes(ctypes.byref(dims), ctypes.byref(opts))
         if workspace is None:
             workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
-        rc = lib.pgd_paged_decode_attention(
-            ctypes.byref(dims), _ptr(q), _ptr(cache_k), _ptr(cache_v), None, _ptr(positions),
-            _ptr(sinks), int(window), float(scale), _ptr(out), _ptr(workspace),
-            workspace.numel() * workspace.element_size(), ctypes.byref(opts),
-            _stream_handle(stream))
+        tail = (None, _ptr(positions), _ptr(sinks), int(window), float(scale), _ptr(out),
+                _ptr(workspace), workspace.numel() * workspace.element_size(),
+                ctypes.byref(opts), _stream_handle(stream))
+        if k_new is None:
+            rc = lib.pgd_paged_decode_attention(ctypes.byref(dims), _ptr(q), _ptr(cache_k),
+                                                _ptr(cache_v), *tail)
+            what = "decode_rows_attention"
+        else:
+            rc = lib.pgd_paged_decode_step(ctypes.byref(dims), _ptr(q), _ptr(k_new), _ptr(v_new),
+                                           _ptr(cache_k), _ptr(cache_v), *tail)
+            what = "decode_rows_step"
     if rc != OK:
-        raise PgdError(rc, "decode_rows_attention")
+        raise PgdError(rc, what)
     return out
 
 

@@ -575,45 +575,56 @@ __global__ void __launch_bounds__(DecodeCfg<D, STAGES, Consumer, WARPS>::kThread
 
   // ---------------------------------------------------------------- producer
   if (warp == C::kWarps) {
-    if (p.k_new != nullptr && page0 + npages - 1 == n / kPage) {
-      // Decode step: this split holds the row's last page, so it writes the
-      // new token's K and V at their slot (position n), then orders those
-      // writes before its copies of the page, which read them back.
+    // Decode step: the split holding the row's last page writes the new
+    // token's K and V at their slot (position n) -- lanes 1.. store while
+    // lane 0 already copies the earlier pages -- and the warp orders those
+    // writes before the copy of the last page, which reads them back.
+    const bool append = p.k_new != nullptr && page0 + npages - 1 == n / kPage;
+    if (append) {
       const int page = trow ? trow[npages - 1] : dense0 + npages - 1;
       const size_t dst =
           ((size_t)tile_first_row(p.layout, page, kvh, p.hkv, p.num_pages, p.maxp) + n % kPage) * D;
       const size_t src = ((size_t)b * p.hkv + kvh) * D;
-      for (int c = lane; c < D / 8; c += 32) {
+      for (int c = lane - 1; c >= 0 && c < D / 8; c += 31) {
         *reinterpret_cast<uint4*>(p.k_pool + dst + 8 * c) =
             *reinterpret_cast<const uint4*>(p.k_new + src + 8 * c);
         *reinterpret_cast<uint4*>(p.v_pool + dst + 8 * c) =
             *reinterpret_cast<const uint4*>(p.v_new + src + 8 * c);
       }
-      asm volatile("fence.proxy.async.global;" ::: "memory");
-      __syncwarp();
     }
+    int issued = 0;
+    bool ok = true;
+    // Copies page i into its stage once the stage is free (lane 0).
+    auto issue = [&](int i) {
+      const int s = i % C::kStages;
+      // On a timeout the consumers time out on the pages never issued and
+      // abandon the split themselves; only they write abort_flag.
+      if (i >= C::kStages && !mbar_wait_bounded(&empty[s], ((i / C::kStages) - 1) & 1, p.err))
+        return false;
+      const int page = trow ? trow[i] : dense0 + i;
+      const int y = (int)tile_first_row(p.layout, page, kvh, p.hkv, p.num_pages, p.maxp);
+      unsigned char* st = stages + s * C::kStageBytes;
+      mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+#pragma unroll
+      for (int bx = 0; bx < C::kBoxes; ++bx) {
+        tma_load_2d(st + bx * kBoxBytes, &k_map, bx * 64, y, &full[s]);
+        tma_load_2d(st + C::kTileBytes + bx * kBoxBytes, &v_map, bx * 64, y, &full[s]);
+      }
+      *reinterpret_cast<volatile int*>(&stage_seq[s]) = i;
+      issued = i + 1;
+      return true;
+    };
     if (lane == 0) {
       prefetch_tensormap(&k_map);
       prefetch_tensormap(&v_map);
-      int issued = 0;
-      for (int i = 0; i < npages; ++i) {
-        const int s = i % C::kStages;
-        // On a timeout the consumers time out on the pages never issued and
-        // abandon the split themselves; only they write abort_flag.
-        if (i >= C::kStages && !mbar_wait_bounded(&empty[s], ((i / C::kStages) - 1) & 1, p.err))
-          break;
-        const int page = trow ? trow[i] : dense0 + i;
-        const int y = (int)tile_first_row(p.layout, page, kvh, p.hkv, p.num_pages, p.maxp);
-        unsigned char* st = stages + s * C::kStageBytes;
-        mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-#pragma unroll
-        for (int bx = 0; bx < C::kBoxes; ++bx) {
-          tma_load_2d(st + bx * kBoxBytes, &k_map, bx * 64, y, &full[s]);
-          tma_load_2d(st + C::kTileBytes + bx * kBoxBytes, &v_map, bx * 64, y, &full[s]);
-        }
-        *reinterpret_cast<volatile int*>(&stage_seq[s]) = i;
-        issued = i + 1;
-      }
+      for (int i = 0; i < npages - (append ? 1 : 0) && ok; ++i) ok = issue(i);
+    }
+    if (append) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      __syncwarp();
+      if (lane == 0 && ok) issue(npages - 1);
+    }
+    if (lane == 0) {
       // No copy may still be landing in shared memory when the CTA exits.
       for (int i = max(0, issued - C::kStages); i < issued; ++i)
         mbar_wait_bounded(&full[i % C::kStages], (i / C::kStages) & 1, p.err);

@@ -23,7 +23,8 @@ def _built():
     torch.cuda.synchronize()
 
 
-def rows_check(b, *, window=None, sinks="batch", pps=0, kernel=pgd.KERNEL_AUTO, rows=None):
+def rows_check(b, *, window=None, sinks="batch", pps=0, kernel=pgd.KERNEL_AUTO, rows=None,
+               step=False):
     wl = b.wl
     window = wl.window if window is None else window
     sinks = b.sinks if isinstance(sinks, str) else sinks
@@ -31,9 +32,13 @@ def rows_check(b, *, window=None, sinks="batch", pps=0, kernel=pgd.KERNEL_AUTO, 
     t = torch.as_tensor(idx, device=b.cache_k.device)
     k_host = bf16_bits(b.cache_k.index_select(0, t)).copy()
     v_host = bf16_bits(b.cache_v.index_select(0, t)).copy()
-    pgd.kv_append_rows(b.k_new, b.v_new, b.positions, b.cache_k, b.cache_v)
-    out = pgd.decode_rows_attention(b.q, b.cache_k, b.cache_v, b.positions, sinks, window,
-                                    wl.scale, pages_per_split=pps, kernel=kernel)
+    if step:   # the append inside the decode launch
+        out = pgd.decode_rows_step(b.q, b.k_new, b.v_new, b.cache_k, b.cache_v, b.positions,
+                                   sinks, window, wl.scale, pages_per_split=pps, kernel=kernel)
+    else:
+        pgd.kv_append_rows(b.k_new, b.v_new, b.positions, b.cache_k, b.cache_v)
+        out = pgd.decode_rows_attention(b.q, b.cache_k, b.cache_v, b.positions, sinks, window,
+                                        wl.scale, pages_per_split=pps, kernel=kernel)
     assert pgd.get_device_error() == pgd.OK
     # the oracle's write_rows: row b's token goes to position n of row b
     kn, vn = bf16_bits(b.k_new)[idx], bf16_bits(b.v_new)[idx]
@@ -50,22 +55,25 @@ def rows_check(b, *, window=None, sinks="batch", pps=0, kernel=pgd.KERNEL_AUTO, 
     return compare(out.index_select(0, t), want, wl.name)
 
 
+@pytest.mark.parametrize("step", [False, True])
 @pytest.mark.parametrize("name", list(ROWS_WORKLOADS))
-def test_rows_workloads(name):
+def test_rows_workloads(name, step):
     wl = ROWS_WORKLOADS[name]
     b = make_rows_batch(wl, 3000 + list(ROWS_WORKLOADS).index(name), DEV)
-    rows_check(b, rows=None if name == "gptoss_rows_serve" else list(range(0, wl.rows, 8)))
+    rows_check(b, rows=None if name == "gptoss_rows_serve" else list(range(0, wl.rows, 8)),
+               step=step)
 
 
 @pytest.mark.parametrize("window", [0, 1, 64, 128])
 @pytest.mark.parametrize("hq,hkv,d", [(64, 8, 64), (32, 8, 128), (14, 2, 64)])
 @pytest.mark.parametrize("kernel,pps", [(pgd.KERNEL_AUTO, 0), (pgd.KERNEL_AUTO, 1),
                                         (pgd.KERNEL_CUDA_CORE, 2)])
-def test_rows_edges(window, hq, hkv, d, kernel, pps):
+@pytest.mark.parametrize("step", [False, True])
+def test_rows_edges(window, hq, hkv, d, kernel, pps, step):
     wl = Workload("rows_edge", rows=7, q_heads=hq, kv_heads=hkv, head_dim=d, ctx_lo=1,
                   ctx_hi=320, sinks=True)
     b = make_rows_batch(wl, 7 + window + d, DEV, contexts=[1, 63, 64, 65, 129, 320, 0])
-    rows_check(b, window=window, pps=pps, kernel=kernel)
+    rows_check(b, window=window, pps=pps, kernel=kernel, step=step)
 
 
 def test_rows_fewer_rows_than_cache_rows():
