@@ -478,8 +478,10 @@ int pgd_paged_decode_step(const pgd_dims* dims, const void* q, const void* k_new
                           const int32_t* positions, const float* sinks, int32_t window,
                           float scale, void* out, void* workspace, size_t workspace_size,
                           const pgd_decode_options* opts, pgd_stream_t stream) {
-  if (dims && dims->rows > 0 && (!k_new || !v_new)) return PGD_EINVAL;
-  return decode_impl(dims, dims ? dims->rows : 0, nullptr, q, k_pool, v_pool, table, positions,
+  const int rc = check_dims(dims);
+  if (rc != PGD_OK) return rc;
+  if (dims->rows > 0 && (!k_new || !v_new)) return PGD_EINVAL;
+  return decode_impl(dims, dims->rows, nullptr, q, k_pool, v_pool, table, positions,
                      sinks, window, scale, out, workspace, workspace_size, opts, stream, k_new,
                      v_new);
 }

@@ -80,6 +80,9 @@ def test_host_rejects_bad_dims_without_a_device(lib, kw, status):
                                        0.125, None, None, 0, None, None)
     assert rc == status
     assert so.pgd_paged_decode_workspace_bytes(ctypes.byref(d), None) == 0
+    rc = so.pgd_paged_decode_step(ctypes.byref(d), None, None, None, None, None, None, None,
+                                  None, 0, 0.125, None, None, 0, None, None)
+    assert rc == status
     count = ctypes.c_int32(-1)
     assert so.pgd_attention_kernel_count(ctypes.byref(d), 0, 0, None, ctypes.byref(count)) == status
 
@@ -99,6 +102,9 @@ def test_zero_rows_is_ok_and_null_pointers_are_rejected(lib):
     assert so.pgd_kv_append_paged(ctypes.byref(d), None, None, None, None, None, None, None) == 1
     assert so.pgd_kv_append_paged(None, None, None, None, None, None, None, None) == 1
     assert so.pgd_attention_kernel_count(ctypes.byref(d), 0, 0, None, None) == 1
+    buf = ctypes.create_string_buffer(64)   # any non-NULL host address: rejected before use
+    assert so.pgd_paged_decode_step(ctypes.byref(d), buf, None, buf, buf, buf, buf, buf, None, 0,
+                                    0.125, buf, buf, 64, None, None) == 1   # no k_new
     count = ctypes.c_int32(-1)
     assert so.pgd_attention_kernel_count(ctypes.byref(d), -1, 0, None, ctypes.byref(count)) == 1
     import paged_gqa_decode_gb300 as pgd
