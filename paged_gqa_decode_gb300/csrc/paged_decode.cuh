@@ -23,7 +23,8 @@
 // consumer waits for its own page index there before it waits on the stage's
 // barrier, so every parity wait targets the barrier's current phase.
 //
-// Consumer warps take whole pages in turn, each keeping its own fp32
+// Consumer warps (four; two for splits of at most three pages, so more CTAs
+// share an SM) take whole pages in turn, each keeping its own fp32
 // online-softmax state for the group's query heads.  Two consumers:
 //   - MmaConsumer (default, group <= 8): the page's 64 x G scores are
 //     S^T = K q^T on the tensor cores (mma.sync m16n8k16, bf16 in, fp32
@@ -38,6 +39,11 @@
 // one split writes its output directly (sink included); otherwise the split
 // writes (m, l, acc) to the workspace and the combine kernel merges.  When no
 // row has more than one split the combine kernel is not launched at all.
+//
+// Decode step (the append fused in): the split holding a row's last page
+// also writes the row's new K and V at the slot of its position -- the
+// producer warp's other lanes store while lane 0 copies the earlier pages --
+// and fences those writes before the last page's copy, which reads them.
 //
 // Pages wholly outside the window are never visited (the split range starts
 // at the window's first page).  Positions outside the window or past n inside
