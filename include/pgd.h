@@ -12,7 +12,9 @@
  *   - Mistral 7B Instruct v0.3, src/attention.linnet,
  *     GroupedQueryAttention.decode_paged, and README "Entries" (decode_paged):
  *     page_slots(table, positions), write_tokens into the pool, then
- *     paged_attention(q, cache_k, cache_v, table, positions, rsqrt(head_dim)).
+ *     paged_attention(q, cache_k, cache_v, table, positions, rsqrt(head_dim))
+ *     (pgd_kv_append_paged + pgd_paged_decode_attention, or both in one
+ *     launch: pgd_paged_decode_step).
  *   - GPT-OSS 20B, README "Attention sinks": one learned logit per query head
  *     joins the scores as an extra key and is dropped after the softmax, so it
  *     adds exp(sink - m) to the softmax denominator only.
@@ -22,8 +24,9 @@
  *     h / (num_q_heads / num_kv_heads); K/V are never copied per query head.
  *
  * Conventions for every entry point:
- *   - All pointers except `dims`, `opts` and the result of
- *     pgd_status_string are DEVICE pointers owned by the caller.  The library
+ *   - All pointers except `dims`, `opts`, the `count` of
+ *     pgd_attention_kernel_count and the result of pgd_status_string are
+ *     DEVICE pointers owned by the caller.  The library
  *     allocates no memory; scratch is the caller's `workspace`.
  *   - bf16 tensors are passed as raw 16-bit storage.  Every bf16 pointer and
  *     the workspace must be 16-byte aligned.
