@@ -31,7 +31,10 @@
 //               waits.
 //   warps 0-7   softmax: warpgroup h (warps 4h .. 4h + 3), one thread per
 //               query row, takes the pages i with i % 2 == h.  Each loads half
-//               of its row's Q into TMEM per item; per page the S row from
+//               of its row's Q into TMEM per item (at head_dim 128, for items
+//               of kStageMinPages pages or more, from rows the K producer
+//               staged in shared memory with bulk copies, and before the
+//               previous item's last outputs are written); per page the S row from
 //               TMEM, causal and window mask, online softmax in log2 units
 //               with a lazy reference max common to both warpgroups (raised
 //               only when a score exceeds it by more than 2^8, which then
@@ -69,8 +72,13 @@ struct UmmaPrefillCfg {
   static constexpr int kSBufs = 4;  // S / P buffers: S runs this many pages ahead
   static constexpr int kTileBytes = kPage * D * 2;  // one K or V slot (one page)
   static constexpr int kVOff = RK * kTileBytes;
-  static constexpr int kBarOff = (RK + RV) * kTileBytes;
-  static constexpr int kNumBars = 2 * RK + 2 * RV + 3 * kSBufs + 11;
+  // an item's q rows (128 x D bf16, row m = token * G + head), staged by the
+  // K producer for the softmax warps (head_dim 128 only, see kStageMinPages)
+  static constexpr bool kStageQ = D == 128;
+  static constexpr int kQStageOff = (RK + RV) * kTileBytes;
+  static constexpr int kQStageBytes = kStageQ ? kRows * D * 2 : 0;
+  static constexpr int kBarOff = kQStageOff + kQStageBytes;
+  static constexpr int kNumBars = 2 * RK + 2 * RV + 3 * kSBufs + 13;
   static constexpr int kSmemBytes = 1024 + kBarOff + kNumBars * 8;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kOCol = 256, kQCol = 384;
@@ -80,6 +88,25 @@ struct UmmaPrefillCfg {
   static_assert(RK == RV, "the K and V rings are streamed by one helper");
   static_assert(kSmemBytes + 8 * 1024 <= 227 * 1024, "shared memory");
 };
+
+// Copies `bytes` contiguous bytes (16-byte aligned, a multiple of 16) from
+// global to shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// At head_dim 128, items with at least this many pages get their q rows
+// staged in shared memory by the K producer, and the softmax warps take them
+// into TMEM before the previous item's last outputs are written (overlapping
+// that epilogue); shorter items, and every item at head_dim 64, load q from
+// global memory when they start (measured: the early hand-over gained 3 % on
+// 50-page items and cost 2-4 % on 3-page ones).
+constexpr int kStageMinPages = 8;
 
 // Reference-max slack in log2 units: P values stay below 2^8.
 constexpr float kLazyRescaleLog2 = 8.0f;
@@ -110,6 +137,7 @@ __device__ __forceinline__ bool mbar_wait_abortable(uint64_t* bar, uint32_t pari
 struct PrefillItem {
   int valid;  // 0: no more items
   int t_begin, t_end, kvh, runs;
+  int staged;  // q rows staged in shared memory (items of kStageMinPages pages or more)
   int run_end[129];
   int tok_row[128], tok_pos[128], run_bad[128];
 };
@@ -174,6 +202,9 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* fin = q_ready + 2;                // [issuer] every MMA it issued done
   uint64_t* mref_bar = fin + 2;               // [page % 2] the page's reference max published
   uint64_t* l_bar = mref_bar + 2;             // both warpgroups' row sums of a run published
+  uint64_t* q_full = l_bar + 1;               // the item's q rows staged (bulk copies landed)
+  uint64_t* q_free = q_full + 1;              // the softmax warps copied them into TMEM
+  unsigned char* q_stage = base + C::kQStageOff;
   __shared__ PrefillItem items[2];
   __shared__ int y_ring[2][64];  // [K, V producer] tile rows of upcoming pages, by page % 64
   // per row: the reference max after page i in mref_x[i % 2]; the warpgroups'
@@ -205,6 +236,8 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&fin[0], 1);
     mbar_init(&fin[1], 1);
     mbar_init(l_bar, C::kSoftmaxThreads);
+    mbar_init(q_full, 1);
+    mbar_init(q_free, C::kSoftmaxThreads);
     mbar_init_fence();
     abort_flag = 0;
   }
@@ -288,6 +321,7 @@ __global__ void __launch_bounds__(384, 1)
       prefetch_tensormap(&v_map);
     }
     int ik = 0;  // K loads issued (all items)
+    int n_staged = 0;  // items whose q rows were staged
     bool ok = true;
     for (int seq = 0; ok; ++seq) {
       const int d = seq & 1;
@@ -348,6 +382,7 @@ __global__ void __launch_bounds__(384, 1)
       __syncwarp();
       // a table entry outside the pool marks its run bad (zero outputs,
       // PGD_EDEVICE_BOUNDS); checked before any copy is issued
+      int item_pages = 0;
       for (int r = 0; r < it.runs; ++r) {
         const int rs = r == 0 ? 0 : it.run_end[r - 1], re = it.run_end[r];
         const int row = it.tok_row[rs];
@@ -355,6 +390,7 @@ __global__ void __launch_bounds__(384, 1)
         if (row >= 0) {
           const int lo = p.window > 0 ? max(it.tok_pos[rs] - p.window + 1, 0) : 0;
           const int first = lo / kPage, last = it.tok_pos[re - 1] / kPage;
+          item_pages += last - first + 1;
           for (int pg = first + lane; pg <= last; pg += 32) {
             const int page = page_of(p.table, row, pg, p.maxp);
             if (page < 0 || page >= p.num_pages) bad = 1;
@@ -380,6 +416,25 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       __syncwarp();
+      // a long item's q rows (G heads x D of each active token, contiguous
+      // in q) into the staging buffer once the softmax warps copied the
+      // previously staged item's rows out of it
+      const bool staged = C::kStageQ && item_pages >= kStageMinPages;
+      if (lane == 0) it.staged = staged;
+      if (staged && n_staged >= 1 && !all_ok(wait(q_free, (n_staged - 1) & 1))) break;
+      if (staged) {
+        ++n_staged;
+        int nq = 0;
+        for (int k = lane; k < tokens; k += 32) nq += (t_begin + k < t_end && it.tok_row[k] >= 0);
+        nq = __reduce_add_sync(0xffffffffu, nq);
+        if (lane == 0) mbar_arrive_expect_tx(q_full, (uint32_t)(nq * G * D * 2));
+        __syncwarp();
+        for (int k = lane; k < tokens; k += 32)
+          if (t_begin + k < t_end && it.tok_row[k] >= 0)
+            bulk_copy_g2s(q_stage + (size_t)k * G * D * 2,
+                          p.q + ((size_t)(t_begin + k) * p.hq + h0) * D, (uint32_t)(G * D * 2),
+                          q_full);
+      }
       if (lane == 0) mbar_arrive(&item_ready[d]);
       ok = stream_item(it, kvh, &k_map, k_slots, k_full, k_empty, y_ring[0], ik, true);
     }
@@ -498,21 +553,35 @@ __global__ void __launch_bounds__(384, 1)
     int i = 0;     // page index over all items
     int nrun = 0;  // runs finished
     bool ok = true;
-    for (int seq = 0; ok; ++seq) {
+    const int tl = m / G, g = m % G;
+    int n_staged = 0;  // staged items taken so far
+    // Half h of item seq's Q rows from the staging buffer into TMEM buffer
+    // seq % 2 (rows of no token: zero); false when there is no item seq.
+    // Item seq + 1's rows are taken before item seq's last outputs are
+    // written, so its first S products overlap that epilogue.
+    auto load_q = [&](int seq) -> bool {
       const int d = seq & 1;
-      if (!all_ok(wait(&item_ready[d], (seq >> 1) & 1))) break;
+      if (!all_ok(wait(&item_ready[d], (seq >> 1) & 1))) {
+        ok = false;
+        return false;
+      }
       const PrefillItem& it = items[d];
-      if (!it.valid) break;
-      const int t_begin = it.t_begin, t_end = it.t_end, h0 = it.kvh * G;
-      const int tl = m / G, g = m % G;
-      const bool row_ok = tl < tokens && t_begin + tl < t_end;
-      // half h of the Q row into TMEM buffer seq % 2 (rows of no token: zero)
+      if (!it.valid) return false;
+      const bool staged = C::kStageQ && it.staged != 0;
+      if (staged && !all_ok(wait(q_full, n_staged & 1))) {
+        ok = false;
+        return false;
+      }
+      const bool row_ok = tl < tokens && it.t_begin + tl < it.t_end;
       {
         const bool q_ok = row_ok && it.tok_row[tl] >= 0;
         uint4 v[D / 16];
         if (q_ok) {
-          const uint4* src = reinterpret_cast<const uint4*>(
-              p.q + ((size_t)(t_begin + tl) * p.hq + h0 + g) * D + h * (D / 2));
+          const uint4* src =
+              staged ? reinterpret_cast<const uint4*>(q_stage + (size_t)m * D * 2 + h * D)
+                     : reinterpret_cast<const uint4*>(
+                           p.q + ((size_t)(it.t_begin + tl) * p.hq + it.kvh * G + g) * D +
+                           h * (D / 2));
 #pragma unroll
           for (int ch = 0; ch < D / 16; ++ch) v[ch] = src[ch];
         } else {
@@ -534,6 +603,25 @@ __global__ void __launch_bounds__(384, 1)
         tmem_wait_st();
         tc_fence_before_sync();
         mbar_arrive(&q_ready[d]);
+        if (staged) {
+          mbar_arrive(q_free);
+          ++n_staged;
+        }
+      }
+      return true;
+    };
+    bool have = load_q(0);
+    for (int seq = 0; ok && have; ++seq) {
+      const int d = seq & 1;
+      const PrefillItem& it = items[d];
+      const int t_begin = it.t_begin, t_end = it.t_end, h0 = it.kvh * G;
+      const bool row_ok = tl < tokens && t_begin + tl < t_end;
+      bool next_loaded = false;
+      // the last run that has pages (its epilogue follows the next Q load)
+      int last_run = -1;
+      for (int r = 0, rs0 = 0; r < it.runs; ++r) {
+        if (it.tok_row[rs0] >= 0 && !it.run_bad[r]) last_run = r;
+        rs0 = it.run_end[r];
       }
 
       int rs = 0;
@@ -688,6 +776,13 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive(&p_full[b]);
         }
         if (!ok) break;
+        if (C::kStageQ && r == last_run && it.staged) {
+          // a long item: the producer has described (and, if long, staged)
+          // the next one long ago, so take its Q now
+          have = load_q(seq + 1);
+          next_loaded = true;
+          if (!ok) break;
+        }
 
         // end of run: the final reference, both row sums, then the O row once
         // P V of the last page is done; each warpgroup stores half of it
@@ -743,7 +838,10 @@ __global__ void __launch_bounds__(384, 1)
         rs = re;
       }
       if (!ok) break;
+      // this item's descriptor is no longer read: free its slot before
+      // waiting for the next item
       mbar_arrive(&item_free[d]);
+      if (!next_loaded) have = load_q(seq + 1);
     }
   }
 
