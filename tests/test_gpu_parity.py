@@ -153,9 +153,11 @@ def test_sink_values(kind, d):
         assert stats["max_abs"] <= 1e-6
 
 
-@pytest.mark.parametrize("pps", [1, 2, 3, 5, 64])
+@pytest.mark.parametrize("pps", [1, 2, 3, 5, 8, 12, 64])
 @pytest.mark.parametrize("window", [0, 100])
 def test_split_sizes_force_the_combine(pps, window):
+    """Rows of 1 to 24 pages cut into 1 to 24 splits (with the window, up to
+    3), merged by the combine kernel; one split writes directly."""
     wl = Workload("splits", rows=5, q_heads=16, kv_heads=4, head_dim=64, ctx_lo=1, ctx_hi=1500,
                   sinks=True)
     lay = layout_from_contexts(wl, [1500, 1, 640, 641, 1000], seed=9)
@@ -246,11 +248,18 @@ def test_scores_rise_every_page(d, pps):
     run_and_check(batch, pages_per_split=pps, what=f"rising scores d{d} pps{pps}")
 
 
-def test_inactive_rows_are_zero_and_untouched():
+@pytest.mark.parametrize("pps", [0, 1])   # one split (written directly); two (combined)
+def test_inactive_rows_are_zero_and_untouched(pps):
     wl = Workload("inactive", rows=4, q_heads=4, kv_heads=1, head_dim=64, ctx_lo=1, ctx_hi=128)
     lay = layout_from_contexts(wl, [0, 100, 0, 1], seed=17, num_pages=6)
     batch = make_batch(wl, seed=91, device=DEV, layout=lay)
-    out = gpu_step(batch, window=0, sinks=None, scale=wl.scale)
+    pgd.kv_append_paged(batch.k_new, batch.v_new, batch.table, batch.positions, batch.k_pool,
+                        batch.v_pool)
+    out = torch.full_like(batch.q, 7.0)          # every output must be written
+    out = pgd.paged_decode_attention(batch.q, batch.k_pool, batch.v_pool, batch.table,
+                                     batch.positions, None, 0, wl.scale, out=out,
+                                     num_kv_heads=wl.kv_heads, pages_per_split=pps)
+    assert pgd.get_device_error() == pgd.OK
     assert torch.all(out[0] == 0) and torch.all(out[2] == 0)
     assert torch.any(out[1] != 0)
 
@@ -273,11 +282,13 @@ def test_kernel_count_follows_the_split_plan():
                              max_pages_per_row=maxp)
     w = WORKLOADS
     assert pgd.attention_kernel_count(dims(w["qwen_serve"], 10)) == 1
-    assert pgd.attention_kernel_count(dims(w["gptoss_full"], 64)) == 2
-    assert pgd.attention_kernel_count(dims(w["mistral_serve"], 512)) == 2
+    assert pgd.attention_kernel_count(dims(w["gptoss_full"], 64)) == 2       # 3 splits
+    assert pgd.attention_kernel_count(dims(w["mistral_serve"], 512)) == 2    # 8 splits
     assert pgd.attention_kernel_count(dims(w["gptoss_sliding"], 512), window=128) == 1
     assert pgd.attention_kernel_count(dims(w["gptoss_sliding"], 512), window=128,
-                                      pages_per_split=1) == 2
+                                      pages_per_split=1) == 2                # 3 splits
+    assert pgd.attention_kernel_count(dims(w["qwen_serve"], 10), pages_per_split=10) == 1
+    assert pgd.attention_kernel_count(dims(w["qwen_serve"], 10), pages_per_split=9) == 2
     assert pgd.attention_kernel_count(dims(w["qwen_serve"], 10),
                                       kernel=pgd.KERNEL_CUDA_CORE) == 1
     assert pgd.attention_kernel_count(dims(w["gptoss_full"], 64, rows=0)) == 0
@@ -316,6 +327,33 @@ def test_device_bounds_errors_do_not_fault():
     # the context is still healthy: a valid step matches the oracle
     batch2 = make_batch(wl, seed=102, device=DEV, layout=lay)
     run_and_check(batch2)
+
+
+@pytest.mark.parametrize("pps", [1, 3, 5, 0])   # 10, 4 and 2 splits (combined); one split
+def test_bad_table_entries_in_every_split(pps):
+    """A bad table entry in the first split of one row and in a later split
+    of another zeroes exactly those rows, whichever split holds it; a
+    position beyond the table zeroes its row; the context stays usable."""
+    wl = Workload("bounds_merge", rows=3, q_heads=16, kv_heads=2, head_dim=64, ctx_lo=1,
+                  ctx_hi=600, sinks=True)
+    lay = layout_from_contexts(wl, [600, 300, 100], seed=23)
+    batch = make_batch(wl, seed=103, device=DEV, layout=lay)
+    table = batch.table.clone()
+    table[0, 7] = -1                  # row 0 (10 pages): a late split
+    table[1, 1] = 10 ** 6             # row 1 (5 pages): the first split
+    out = pgd.paged_decode_attention(batch.q, batch.k_pool, batch.v_pool, table,
+                                     batch.positions, batch.sinks, 0, wl.scale,
+                                     num_kv_heads=wl.kv_heads, pages_per_split=pps)
+    assert pgd.get_device_error() == pgd.EDEVICE_BOUNDS
+    assert torch.all(out[0] == 0) and torch.all(out[1] == 0) and torch.any(out[2] != 0)
+    bad_pos = batch.positions.clone()
+    bad_pos[0] = 64 * batch.table.shape[1] + 3
+    out = pgd.paged_decode_attention(batch.q, batch.k_pool, batch.v_pool, batch.table, bad_pos,
+                                     batch.sinks, 0, wl.scale, num_kv_heads=wl.kv_heads,
+                                     pages_per_split=pps)
+    assert pgd.get_device_error() == pgd.EDEVICE_BOUNDS
+    assert torch.all(out[0] == 0) and torch.any(out[1] != 0) and torch.any(out[2] != 0)
+    run_and_check(batch, pages_per_split=pps, what=f"after bounds errors, pps {pps}")
 
 
 def test_host_validation():

@@ -99,11 +99,12 @@ def test_step_bad_last_page_is_reported_and_not_written():
     assert changed.numel() == 4
 
 
-def test_step_in_a_cuda_graph():
+@pytest.mark.parametrize("pps", [0, 3])   # one split per row; 4 splits + the combine
+def test_step_in_a_cuda_graph(pps):
     wl = WORKLOADS["qwen_serve"]
     batch = make_batch(wl, seed=1001, device=DEV)
     k0, v0 = batch.k_pool.clone(), batch.v_pool.clone()
-    eager = both(batch, window=0, sinks=None)
+    eager = both(batch, window=0, sinks=None, pps=pps)
     out = torch.empty_like(batch.q)
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
@@ -111,14 +112,14 @@ def test_step_in_a_cuda_graph():
     with torch.cuda.stream(side):
         pgd.paged_decode_step(batch.q, batch.k_new, batch.v_new, batch.k_pool, batch.v_pool,
                               batch.table, batch.positions, None, 0, wl.scale, out=out,
-                              num_kv_heads=wl.kv_heads)
+                              num_kv_heads=wl.kv_heads, pages_per_split=pps)
         torch.cuda.synchronize()
         batch.k_pool.copy_(k0)
         batch.v_pool.copy_(v0)
         with torch.cuda.graph(g, stream=side):
             pgd.paged_decode_step(batch.q, batch.k_new, batch.v_new, batch.k_pool, batch.v_pool,
                                   batch.table, batch.positions, None, 0, wl.scale, out=out,
-                                  num_kv_heads=wl.kv_heads)
+                                  num_kv_heads=wl.kv_heads, pages_per_split=pps)
     torch.cuda.synchronize()
     batch.k_pool.copy_(k0)
     batch.v_pool.copy_(v0)
