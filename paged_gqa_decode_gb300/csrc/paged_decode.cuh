@@ -502,6 +502,13 @@ __global__ void __launch_bounds__(DecodeCfg<D, STAGES, Consumer, WARPS>::kThread
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
+  // Without a window a split's pages start at index split * pages_per_split
+  // of its table row whatever the position, so the table entries it may need
+  // are loaded together with the position rather than after it.
+  const bool spec = p.window == 0 && p.table != nullptr && p.row_of == nullptr;
+  int pg_spec = -1;
+  if (spec && tid < p.pages_per_split && split * p.pages_per_split + tid < p.maxp)
+    pg_spec = p.table[(size_t)b * p.maxp + split * p.pages_per_split + tid];
   const int n = p.positions[b];
   const RowSpan span = row_span(n, p.window);
   const int nsplit = (span.pages + p.pages_per_split - 1) / p.pages_per_split;
@@ -544,7 +551,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, STAGES, Consumer, WARPS>::kThread
   // Every table entry this split reads must name a pool page.
   bool bad = false;
   for (int i = tid; i < npages; i += C::kThreads) {
-    const int pg = trow ? trow[i] : dense0 + i;
+    const int pg = spec && i == tid ? pg_spec : (trow ? trow[i] : dense0 + i);
     bad |= (pg < 0) | (pg >= p.num_pages);
   }
   bad = __syncthreads_or(bad);
