@@ -1,5 +1,7 @@
 // Paged prefill attention on the 5th-generation tensor cores (tcgen05 UMMA
-// with TMEM accumulators), sm_103a: a persistent kernel.
+// with TMEM accumulators), sm_103a: a persistent kernel with one query tile
+// per work item.  It serves head_dim 128; at head_dim 64 the two-tile kernel
+// of paged_prefill_umma_tiles2.cuh is faster and runs instead.
 //
 // What it computes is the same as the tiled prefill kernel (Mistral 7B
 // Instruct v0.3 model files, src/attention.linnet, prefill_paged; window and

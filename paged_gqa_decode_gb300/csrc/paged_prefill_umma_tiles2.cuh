@@ -1,0 +1,790 @@
+// Paged prefill attention on the 5th-generation tensor cores (tcgen05 UMMA
+// with TMEM accumulators), sm_103a: a persistent kernel with two query tiles
+// per work item, used at head_dim 64 (gpt-oss).  Measured on the gpt-oss
+// sliding-window prefill it takes 0.066 ms against 0.080 for the one-tile
+// kernel of paged_prefill_umma.cuh; at head_dim 128 TMEM has no room for a
+// second S buffer per tile beside two O accumulators and Q, and there the
+// one-tile kernel is faster (0.331 against 0.352 ms on a Mistral-shaped
+// prefill), so that one serves head_dim 128.
+//
+// What it computes is the same as the tiled prefill kernel (Mistral 7B
+// Instruct v0.3 model files, src/attention.linnet, prefill_paged; window and
+// sinks as GPT-OSS 20B src/attention.linnet, prefill_packed): packed token p at
+// position positions[p] of table row rows[p] attends, with each query head of
+// its group, over that row's keys at positions (positions[p] - window,
+// positions[p]], the head's sink logit in the denominator only.
+//
+// Work items are (block of 2 x 128 / G consecutive packed tokens, kv head):
+// two query tiles of 128 rows, tile t holding tokens t * 128 / G ..
+// (t + 1) * 128 / G - 1 of the block, row m = token * G + head, one per TMEM
+// lane.  Both tiles share every K and V page the item loads (half the page
+// traffic of one tile per item).  One CTA per SM takes items from a counter,
+// last token blocks (the longest key ranges) first.  Within an item the
+// tokens split into runs (same table row, consecutive positions); each run
+// is one pass over the pages of the union of its tokens' key ranges.  The
+// pages of all of a CTA's items form one sequence, and every role walks it:
+//   warp 8      K producer: per item, reads its tokens, builds the runs,
+//               checks the table and zeroes uncovered outputs (whole warp);
+//               then streams each page's K tile (64 x D bf16, 128-byte
+//               swizzle) into a ring of shared slots with TMA, pulling pages
+//               into L2 ahead of their loads.
+//   warp 11     V producer: the same pages' V tiles into a second ring.
+//   warp 9      S issuer (one thread) and TMEM owner, per page i and tile t:
+//                 S_t  = Q_t K_i^T    M 128, N 64, K D   (Q from TMEM, K shared)
+//               into tile t's S buffer once P_t V_{i-1} (which reads the
+//               same columns) is done.
+//   warp 10     P V issuer (one thread), per page i and tile t:
+//                 O_t += P_t V_i      M 128, N D,  K 64  (P from TMEM, V shared)
+//   warps 0-7   softmax: warpgroup t (warps 4t .. 4t + 3) owns tile t, one
+//               thread per query row.  It loads its rows' Q into TMEM per
+//               item; per page the S row from TMEM, causal and window mask,
+//               online softmax in log2 units with a lazy running max (raised
+//               only when a score exceeds it by more than 2^8, which then
+//               rescales that row of O_t in TMEM); P is written over S as a
+//               bf16 head and residual (two MMAs, so P V keeps fp32
+//               accuracy).  At the end of a run each thread normalises its
+//               O_t row with the sink and stores it.  Warpgroup 0 also zeroes
+//               the V rows outside the run's key range on boundary pages
+//               before the products read them.
+// TMEM (512 columns): O_t at [t D, (t + 1) D), then the S / P buffers, 64
+// columns each, kSBufs per tile (two at head_dim 64, one at 128; P per chunk
+// of 32 keys: the bf16 head in the chunk's first 16 columns, the residual in
+// the next 16, as packed pairs), then Q_t, D / 2 columns of packed pairs.
+// Every wait is bounded; a timeout records PGD_EDEVICE_TIMEOUT, stops all
+// roles, drains in-flight copies and MMAs and frees TMEM before the CTA exits.
+#pragma once
+
+#include "paged_decode.cuh"
+#include "pgd_umma.cuh"
+
+namespace pgd {
+namespace tiles2 {
+
+template <int D, int RK, int RV>
+struct UmmaPrefillCfg {
+  static constexpr int kRows = 128;  // query rows per tile (TMEM lanes)
+  static constexpr int kTiles = 2;   // query tiles per item
+  static constexpr int kSoftmaxThreads = 256;  // one warpgroup per tile
+  static constexpr int kProducerWarp = 8;
+  static constexpr int kMmaWarp = 9;  // S issuer, TMEM owner
+  static constexpr int kPvWarp = 10;
+  static constexpr int kVWarp = 11;
+  static constexpr int kThreads = 384;
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kTileBytes = kPage * D * 2;  // one K or V slot (one page)
+  static constexpr int kVOff = RK * kTileBytes;
+  static constexpr int kBarOff = (RK + RV) * kTileBytes;
+  // S / P buffers per tile: two where TMEM has room (head_dim 64), so S of
+  // the next page is computed while the softmax works on this one
+  static constexpr int kSBufs = D == 64 ? 2 : 1;
+  static constexpr int kNumBars = 2 * RK + 2 * RV + 3 * kTiles * kSBufs + 8;
+  static constexpr int kSmemBytes = 1024 + kBarOff + kNumBars * 8;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kOCol = 0, kSCol = kTiles * D,
+                            kQCol = kTiles * D + kTiles * kSBufs * kPage;
+  static constexpr uint32_t kIdescS = umma_idesc_bf16(128, kPage, 0, 0);
+  static constexpr uint32_t kIdescPV = umma_idesc_bf16(128, D, 0, 1);
+  static_assert(D == 64 || D == 128, "head_dim");
+  static_assert(kQCol + kTiles * D / 2 <= kTmemCols, "TMEM columns");
+  static_assert(RK == RV, "the K and V rings are streamed by one helper");
+  static_assert(kSmemBytes + 8 * 1024 <= 227 * 1024, "shared memory");
+};
+
+// Reference-max slack in log2 units: P values stay below 2^8.
+constexpr float kLazyRescaleLog2 = 8.0f;
+
+// How far ahead of its load the producer pulls a page into L2.
+constexpr int kL2PrefetchPages = 16;
+
+// mbarrier wait that also gives up when another role of the CTA has set
+// *abort (after its own wait timed out).
+__device__ __forceinline__ bool mbar_wait_abortable(uint64_t* bar, uint32_t parity,
+                                                    unsigned int* err, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0u) {
+      if (*abort) return false;
+      if (global_ns() - t0 > kWaitLimitNs) {
+        record_error(err, PGD_EDEVICE_TIMEOUT);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// One work item as the producer laid it out for the other roles.
+struct PrefillItem {
+  int valid;  // 0: no more items
+  int t_begin, t_end, kvh, runs;
+  int run_end[257];
+  int tok_row[256], tok_pos[256], run_bad[256];
+};
+
+// Page sequence of one item: run by run (inactive and bad runs skipped),
+// pages first..last of each.
+struct ItemCursor {
+  int r, pg, last, row, rs, re;
+};
+
+__device__ __forceinline__ bool item_next_run(const PrefillItem& it, int window, ItemCursor& c) {
+  for (++c.r; c.r < it.runs; ++c.r) {
+    c.rs = c.r == 0 ? 0 : it.run_end[c.r - 1];
+    c.re = it.run_end[c.r];
+    c.row = it.tok_row[c.rs];
+    if (c.row < 0 || it.run_bad[c.r]) continue;
+    const int lo = window > 0 ? max(it.tok_pos[c.rs] - window + 1, 0) : 0;
+    c.pg = lo / kPage;
+    c.last = it.tok_pos[c.re - 1] / kPage;
+    return true;
+  }
+  return false;
+}
+
+// Next page of the item; false at its end.
+__device__ __forceinline__ bool item_advance(const PrefillItem& it, int window, ItemCursor& c) {
+  if (++c.pg <= c.last) return true;
+  return item_next_run(it, window, c);
+}
+
+template <int D, int RK, int RV>
+__global__ void __launch_bounds__(384, 1)
+    paged_prefill_umma_kernel(const __grid_constant__ CUtensorMap k_map,
+                              const __grid_constant__ CUtensorMap v_map, const DecodeParams p,
+                              int* item_counter) {
+  using C = UmmaPrefillCfg<D, RK, RV>;
+  pdl_wait();
+  pdl_allow_dependents();
+  const int G = p.group;
+  const int T = C::kRows / G;  // tokens per tile
+  const int tokens = C::kTiles * T;
+  const int n_blocks = (p.rows + tokens - 1) / tokens;
+  const int n_items = n_blocks * p.hkv;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* base = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* k_slots = base;
+  unsigned char* v_slots = base + C::kVOff;
+  uint64_t* k_full = reinterpret_cast<uint64_t*>(base + C::kBarOff);  // TMA landed
+  uint64_t* k_empty = k_full + RK;         // S of the page done (MMA commit)
+  uint64_t* v_full = k_empty + RK;
+  uint64_t* v_empty = v_full + RV;         // P V of the page done (MMA commit)
+  // per (tile t, buffer b = page % kSBufs) at t * kSBufs + b:
+  uint64_t* s_full = v_empty + RV;         // S of the page in TMEM (MMA commit)
+  uint64_t* p_full = s_full + C::kTiles * C::kSBufs;  // P in TMEM (and boundary V rows zeroed)
+  uint64_t* o_done = p_full + C::kTiles * C::kSBufs;  // P V of the page done (MMA commit)
+  uint64_t* item_ready = o_done + C::kTiles * C::kSBufs;  // [item % 2] descriptor written
+  uint64_t* item_free = item_ready + 2;       // [item % 2] consumed (softmax, issuers, V producer)
+  uint64_t* q_ready = item_free + 2;          // [item % 2] both tiles' Q in TMEM (softmax)
+  uint64_t* fin = q_ready + 2;                // [issuer] every MMA it issued done
+  __shared__ PrefillItem items[2];
+  __shared__ int y_ring[2][64];  // [K, V producer] tile rows of upcoming pages, by page % 64
+  __shared__ volatile int abort_flag;
+  __shared__ uint32_t tmem_slot;
+
+  if (tid == 0) {
+    for (int s = 0; s < RK; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < RV; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int tb = 0; tb < C::kTiles * C::kSBufs; ++tb) {
+      mbar_init(&s_full[tb], 1);
+      mbar_init(&p_full[tb], C::kRows);  // the tile's warpgroup
+      mbar_init(&o_done[tb], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&item_ready[b], 1);
+      mbar_init(&item_free[b], C::kSoftmaxThreads + 3);
+      mbar_init(&q_ready[b], C::kSoftmaxThreads);
+    }
+    mbar_init(&fin[0], 1);
+    mbar_init(&fin[1], 1);
+    mbar_init_fence();
+    abort_flag = 0;
+  }
+  if (warp == C::kMmaWarp) tmem_alloc(&tmem_slot, C::kTmemCols);
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+  auto wait = [&](uint64_t* bar, uint32_t parity) {
+    return mbar_wait_abortable(bar, parity, p.err, &abort_flag);
+  };
+
+  // One page tile (64 rows x D): head_dim 128 comes through its 3-D map as
+  // both 64-wide boxes in one copy.
+  auto load_tile = [&](unsigned char* dst, const CUtensorMap* map, int y, uint64_t* bar) {
+    if constexpr (D == 128)
+      tma_load_3d(dst, map, 0, y, 0, bar);
+    else
+      tma_load_2d(dst, map, 0, y, bar);
+  };
+
+  auto all_ok = [&](bool v) { return __all_sync(0xffffffffu, v); };
+  // Streams the pages of item `it` into one ring with the whole warp, page
+  // number i onwards: tile rows are looked up 32 at a time (one table load per
+  // lane) into `ring` (by page number % 64); lane 0 waits for each slot and
+  // issues its copy, and with `prefetch` pulls K and V pages into L2 ahead (the
+  // token blocks of a request reach each page together).
+  auto stream_item = [&](const PrefillItem& it, int kvh, const CUtensorMap* map,
+                         unsigned char* slots, uint64_t* full, uint64_t* empty, int* ring, int& i,
+                         bool prefetch) -> bool {
+    int n_pages = 0;
+    {
+      ItemCursor cc{-1, 0, -1, -1, 0, 0};
+      for (bool more = item_next_run(it, p.window, cc); more;
+           more = item_next_run(it, p.window, cc))
+        n_pages += cc.last - cc.pg + 1;
+    }
+    const int i_end = i + n_pages;
+    ItemCursor fc{-1, 0, -1, -1, 0, 0};
+    bool f_more = item_next_run(it, p.window, fc);
+    int i_fetch = i, ip = i;
+    for (; i < i_end; ++i) {
+      while (f_more && i_fetch < i + 16) {
+        const int n = min(32, fc.last - fc.pg + 1);
+        if (lane < n) {
+          const int page = page_of(p.table, fc.row, fc.pg + lane, p.maxp);
+          ring[(i_fetch + lane) & 63] =
+              (int)tile_first_row(p.layout, page, kvh, p.hkv, p.num_pages, p.maxp);
+        }
+        __syncwarp();
+        i_fetch += n;
+        fc.pg += n - 1;
+        f_more = item_advance(it, p.window, fc);
+      }
+      if (prefetch && lane == 0) {
+        for (; ip < min(i + kL2PrefetchPages, i_fetch); ++ip) {
+          const int y = ring[ip & 63];
+          if constexpr (D == 128) {
+            tma_prefetch_l2_3d(&k_map, 0, y, 0);
+            tma_prefetch_l2_3d(&v_map, 0, y, 0);
+          } else {
+            tma_prefetch_l2_2d(&k_map, 0, y);
+            tma_prefetch_l2_2d(&v_map, 0, y);
+          }
+        }
+      }
+      const int s = i % RK;
+      if (i >= RK && !all_ok(wait(&empty[s], ((i / RK) - 1) & 1))) return false;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&full[s], C::kTileBytes);
+        load_tile(slots + s * C::kTileBytes, map, ring[i & 63], &full[s]);
+      }
+    }
+    return true;
+  };
+
+  if (warp == C::kProducerWarp) {
+    // ------------------------------------------------------------ K producer
+    if (lane == 0) {
+      prefetch_tensormap(&k_map);
+      prefetch_tensormap(&v_map);
+    }
+    int ik = 0;  // K loads issued (all items)
+    bool ok = true;
+    for (int seq = 0; ok; ++seq) {
+      const int d = seq & 1;
+      PrefillItem& it = items[d];
+      int j = 0;
+      if (lane == 0) j = atomicAdd(item_counter, 1);
+      j = __shfl_sync(0xffffffffu, j, 0);
+      // the descriptor slot holds item seq - 2 until both consumers are done
+      if (seq >= 2 && !__all_sync(0xffffffffu, wait(&item_free[d], ((seq >> 1) - 1) & 1))) break;
+      if (j >= n_items) {
+        if (lane == 0) {
+          it.valid = 0;
+          mbar_arrive(&item_ready[d]);
+        }
+        break;
+      }
+      const int blk = n_blocks - 1 - j / p.hkv, kvh = j % p.hkv;
+      const int t_begin = blk * tokens, t_end = min(t_begin + tokens, p.rows);
+      const int h0 = kvh * G;
+      // tokens of the item: rows and positions; bad ones are reported and
+      // left out of every run (their outputs are zeroed below)
+      for (int k = lane; k < tokens; k += 32) {
+        const int t = t_begin + k;
+        int row = -1, pos = -1;
+        if (t < t_end) {
+          row = p.row_of ? p.row_of[t] : t;
+          pos = p.positions[t];
+          const bool bad = row < 0 || row >= p.table_rows || (pos >= 0 && pos / kPage >= p.maxp);
+          if (bad) record_error(p.err, PGD_EDEVICE_BOUNDS);
+          if (bad || pos < 0) row = -1;
+        }
+        it.tok_row[k] = row;
+        it.tok_pos[k] = pos;
+      }
+      __syncwarp();
+      // runs: token k ends one when k + 1 starts another (or is past the end)
+      {
+        int r = 0;
+        for (int k0 = 0; k0 < tokens; k0 += 32) {
+          const int k = k0 + lane;
+          bool brk = false;
+          if (k < tokens)
+            brk = k + 1 == tokens || it.tok_row[k + 1] != it.tok_row[k] ||
+                  it.tok_pos[k + 1] != it.tok_pos[k] + 1 || it.tok_row[k + 1] < 0 ||
+                  it.tok_row[k] < 0;
+          const unsigned bal = __ballot_sync(0xffffffffu, brk);
+          if (brk) it.run_end[r + __popc(bal & ((1u << lane) - 1u))] = k + 1;
+          r += __popc(bal);
+        }
+        if (lane == 0) it.runs = r;
+      }
+      if (lane == 0) {
+        it.valid = 1;
+        it.t_begin = t_begin;
+        it.t_end = t_end;
+        it.kvh = kvh;
+      }
+      __syncwarp();
+      // a table entry outside the pool marks its run bad (zero outputs,
+      // PGD_EDEVICE_BOUNDS); checked before any copy is issued
+      for (int r = 0; r < it.runs; ++r) {
+        const int rs = r == 0 ? 0 : it.run_end[r - 1], re = it.run_end[r];
+        const int row = it.tok_row[rs];
+        int bad = 0;
+        if (row >= 0) {
+          const int lo = p.window > 0 ? max(it.tok_pos[rs] - p.window + 1, 0) : 0;
+          const int first = lo / kPage, last = it.tok_pos[re - 1] / kPage;
+          for (int pg = first + lane; pg <= last; pg += 32) {
+            const int page = page_of(p.table, row, pg, p.maxp);
+            if (page < 0 || page >= p.num_pages) bad = 1;
+          }
+        }
+        bad = __any_sync(0xffffffffu, bad);
+        if (lane == 0) {
+          it.run_bad[r] = bad;
+          if (bad) record_error(p.err, PGD_EDEVICE_BOUNDS);
+        }
+      }
+      __syncwarp();
+      // outputs of tokens that no pass covers (inactive or bad run)
+      for (int r = 0; r < it.runs; ++r) {
+        const int rs = r == 0 ? 0 : it.run_end[r - 1], re = it.run_end[r];
+        if (it.tok_row[rs] >= 0 && !it.run_bad[r]) continue;
+        for (int e = lane; e < (re - rs) * G * (D / 8); e += 32) {
+          const int tl = rs + e / (G * (D / 8));
+          if (t_begin + tl >= t_end) continue;
+          const int g = (e / (D / 8)) % G, c = e % (D / 8);
+          reinterpret_cast<uint4*>(p.out + ((size_t)(t_begin + tl) * p.hq + h0 + g) * D)[c] =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&item_ready[d]);
+      ok = stream_item(it, kvh, &k_map, k_slots, k_full, k_empty, y_ring[0], ik, true);
+    }
+    // drain: the copies still in flight land before the CTA exits
+    if (lane == 0)
+      for (int j = max(0, ik - RK); j < ik; ++j)
+        mbar_wait_bounded(&k_full[j % RK], (j / RK) & 1, p.err);
+  } else if (warp == C::kVWarp) {
+    // ------------------------------------------------------------ V producer
+    int iv = 0;  // V loads issued (all items)
+    for (int seq = 0;; ++seq) {
+      const int d = seq & 1;
+      if (!all_ok(wait(&item_ready[d], (seq >> 1) & 1))) break;
+      const PrefillItem& it = items[d];
+      if (!it.valid) break;
+      if (!stream_item(it, it.kvh, &v_map, v_slots, v_full, v_empty, y_ring[1], iv, false)) break;
+      if (lane == 0) mbar_arrive(&item_free[d]);
+    }
+    if (lane == 0)
+      for (int j = max(0, iv - RV); j < iv; ++j)
+        mbar_wait_bounded(&v_full[j % RV], (j / RV) & 1, p.err);
+  } else if (warp == C::kMmaWarp) {
+    // ------------------------------------------------------------ S issuer
+    if (lane == 0) {
+      const uint32_t k_addr = smem_addr(k_slots);
+      int i = 0;  // page index over all items
+      bool issued = false, ok = true;
+      for (int seq = 0; ok; ++seq) {
+        const int d = seq & 1;
+        if (!wait(&item_ready[d], (seq >> 1) & 1)) break;
+        const PrefillItem& it = items[d];
+        if (!it.valid) break;
+        if (!wait(&q_ready[d], (seq >> 1) & 1)) break;
+        ItemCursor cur{-1, 0, -1, -1, 0, 0};
+        for (bool more = item_next_run(it, p.window, cur); more && ok;
+             more = item_advance(it, p.window, cur), ++i) {
+          if (!wait(&k_full[i % RK], (i / RK) & 1)) {
+            ok = false;
+            break;
+          }
+          const uint32_t kt = k_addr + (i % RK) * C::kTileBytes;
+          const int b = i % C::kSBufs;
+          for (int t = 0; t < C::kTiles; ++t) {
+            // the buffer holds P_t of page i - kSBufs until P V has read it
+            const int tb = t * C::kSBufs + b;
+            if (i >= C::kSBufs && !wait(&o_done[tb], ((i / C::kSBufs) - 1) & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint32_t sb = tmem + C::kSCol + tb * kPage;
+            const uint32_t qa = tmem + C::kQCol + t * (D / 2);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+              umma_bf16_tmem_a(sb, qa + kk * 8,
+                               umma_desc_sw128(kt + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
+                               C::kIdescS, kk > 0);
+            umma_commit(&s_full[tb]);
+          }
+          if (!ok) break;
+          umma_commit(&k_empty[i % RK]);
+          issued = true;
+        }
+        if (ok) mbar_arrive(&item_free[d]);
+      }
+      // drain: every MMA this thread issued completes before TMEM is freed
+      if (issued) {
+        umma_commit(fin);
+        mbar_wait_bounded(fin, 0, p.err);
+      }
+    }
+  } else if (warp == C::kPvWarp) {
+    // ------------------------------------------------------------ P V issuer
+    if (lane == 0) {
+      const uint32_t v_addr = smem_addr(v_slots);
+      int i = 0;  // page index over all items
+      bool issued = false, ok = true;
+      for (int seq = 0; ok; ++seq) {
+        const int d = seq & 1;
+        if (!wait(&item_ready[d], (seq >> 1) & 1)) break;
+        const PrefillItem& it = items[d];
+        if (!it.valid) break;
+        ItemCursor cur{-1, 0, -1, -1, 0, 0};
+        bool first = true;  // O restarts with each item
+        for (bool more = item_next_run(it, p.window, cur); more && ok;
+             more = item_advance(it, p.window, cur), ++i) {
+          if (!wait(&v_full[i % RV], (i / RV) & 1)) {
+            ok = false;
+            break;
+          }
+          const uint32_t vt = v_addr + (i % RV) * C::kTileBytes;
+          const int b = i % C::kSBufs;
+          for (int t = 0; t < C::kTiles; ++t) {
+            const int tb = t * C::kSBufs + b;
+            if (!wait(&p_full[tb], (i / C::kSBufs) & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint32_t pb = tmem + C::kSCol + tb * kPage;
+            const uint32_t od = tmem + C::kOCol + t * D;
+            // keys 16 kk .. 16 kk + 15: chunk kk / 2 of the P columns, half
+            // kk % 2 of its 16 head (then residual) columns
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16_tmem_a(od, pb + 32 * (kk >> 1) + 8 * (kk & 1),
+                               umma_desc_sw128(vt + kk * 2048, kBoxBytes, 1024), C::kIdescPV,
+                               !(first && kk == 0));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16_tmem_a(od, pb + 32 * (kk >> 1) + 16 + 8 * (kk & 1),
+                               umma_desc_sw128(vt + kk * 2048, kBoxBytes, 1024), C::kIdescPV,
+                               true);
+            umma_commit(&o_done[tb]);
+          }
+          if (!ok) break;
+          umma_commit(&v_empty[i % RV]);
+          first = false;
+          issued = true;
+        }
+        if (ok) mbar_arrive(&item_free[d]);
+      }
+      if (issued) {
+        umma_commit(fin + 1);
+        mbar_wait_bounded(fin + 1, 0, p.err);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int m = tid & 127, t = tid >> 7;  // row; tile
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const float c = p.q_scale_log2;
+    const float cc = c > 0.f ? c : 1.f;
+    int i = 0;  // page index over all items
+    bool ok = true;
+    const int tl = t * T + m / G, g = m % G;  // token of the block, head of the group
+    const bool in_tile = m / G < T;           // rows past T * G hold no token
+    // Tile t's Q rows of item seq into TMEM (rows of no token: zero); false
+    // when there is no item seq.
+    auto load_q = [&](int seq) -> bool {
+      const int d = seq & 1;
+      if (!all_ok(wait(&item_ready[d], (seq >> 1) & 1))) {
+        ok = false;
+        return false;
+      }
+      const PrefillItem& it = items[d];
+      if (!it.valid) return false;
+      const bool q_ok = in_tile && it.t_begin + tl < it.t_end && it.tok_row[tl] >= 0;
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.q + ((size_t)(it.t_begin + (q_ok ? tl : 0)) * p.hq + it.kvh * G + g) * D);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {  // half the row at a time
+        uint4 v[D / 16];
+#pragma unroll
+        for (int ch = 0; ch < D / 16; ++ch)
+          v[ch] = q_ok ? src[hh * (D / 16) + ch] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int c16 = 0; c16 < D / 64; ++c16) {
+          uint32_t w[16];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            w[4 * k] = v[4 * c16 + k].x;
+            w[4 * k + 1] = v[4 * c16 + k].y;
+            w[4 * k + 2] = v[4 * c16 + k].z;
+            w[4 * k + 3] = v[4 * c16 + k].w;
+          }
+          tmem_st16(lane_base + C::kQCol + t * (D / 2) + hh * (D / 4) + 16 * c16, w);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before_sync();
+      mbar_arrive(&q_ready[d]);
+      return true;
+    };
+    bool have = load_q(0);
+    for (int seq = 0; ok && have; ++seq) {
+      const int d = seq & 1;
+      const PrefillItem& it = items[d];
+      const int t_begin = it.t_begin, t_end = it.t_end, h0 = it.kvh * G;
+      const bool row_ok = in_tile && t_begin + tl < t_end;
+      int rs = 0;
+      for (int r = 0; r < it.runs && ok; ++r) {
+        const int re = it.run_end[r];
+        const int row = it.tok_row[rs];
+        if (row < 0 || it.run_bad[r]) {
+          rs = re;
+          continue;
+        }
+        const bool live = row_ok && tl >= rs && tl < re;
+        const int pos = live ? it.tok_pos[tl] : -1;
+        const int lo = p.window > 0 ? pos - p.window + 1 : 0;
+        const int lo_run = p.window > 0 ? max(it.tok_pos[rs] - p.window + 1, 0) : 0;
+        const int pos_last = it.tok_pos[re - 1];
+        const int first = lo_run / kPage, last = pos_last / kPage;
+        float m_run = -INFINITY;  // running (lazy) max of the row, log2 units
+        float l = 0.f;            // row sum relative to m_run
+        for (int pg = first; pg <= last; ++pg, ++i) {
+          const int tb = t * C::kSBufs + i % C::kSBufs;
+          const uint32_t scol = C::kSCol + tb * kPage;
+          if (!all_ok(wait(&s_full[tb], (i / C::kSBufs) & 1))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          float sv[kPage];
+#pragma unroll
+          for (int q = 0; q < kPage / 16; ++q)
+            tmem_ld16(lane_base + scol + 16 * q,
+                      *reinterpret_cast<float(*)[16]>(&sv[16 * q]));
+          tmem_wait_ld();
+          // scores stay raw: the scale is folded into the exponent's FMA (for
+          // a positive scale; otherwise it is applied here)
+          if (!(c > 0.f)) {
+#pragma unroll
+            for (int k = 0; k < kPage; ++k) sv[k] *= c;
+          }
+          const int pos0 = pg * kPage;
+          if (!(live && pos0 >= lo && pos0 + kPage - 1 <= pos)) {
+#pragma unroll
+            for (int k = 0; k < kPage; ++k)
+              if (!(live && pos0 + k >= lo && pos0 + k <= pos)) sv[k] = -INFINITY;
+          }
+          // eight partial maxima: the first 8 scores, then 56 more two at a
+          // time (three blocks of 16 and a last block of 8)
+          float part[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) part[j] = sv[j];
+#pragma unroll
+          for (int k = 8; k + 16 <= kPage; k += 16)
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              part[j] = fmax3(part[j], sv[k + 2 * j], sv[k + 2 * j + 1]);
+          static_assert((kPage - 8) % 16 == 8, "the last block holds 8 scores");
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            part[j] = fmax3(part[j], sv[kPage - 8 + 2 * j], sv[kPage - 7 + 2 * j]);
+          const float mx = fmax3(fmax3(part[0], part[1], part[2]),
+                                 fmax3(part[3], part[4], part[5]), fmaxf(part[6], part[7])) *
+                           cc;
+          float alpha = 1.f;
+          bool rose = false;
+          if (mx > m_run + kLazyRescaleLog2) {
+            if (m_run != -INFINITY) {
+              alpha = exp2_approx(m_run - mx);
+              rose = true;
+            }
+            l = m_run == -INFINITY ? 0.f : l * alpha;
+            m_run = mx;
+          }
+          const float nml = m_run == -INFINITY ? 0.f : -m_run;
+          // P = 2^(s - m_run) as a bf16 head and residual over the S columns
+          // (per chunk of 32 keys: head at +0, residual at +16, column j of a
+          // half holding keys 2j, 2j + 1); pairs through the packed fp32 pipe
+          const float2 cc2 = make_float2(cc, cc), nml2 = make_float2(nml, nml);
+          const float2 minus1 = make_float2(-1.f, -1.f);
+          float2 sum2[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) sum2[j] = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int q = 0; q < kPage / 32; ++q) {
+            uint32_t hw[16], lw[16];
+#pragma unroll
+            for (int w = 0; w < 16; ++w) {
+              const float2 y = __ffma2_rn(make_float2(sv[32 * q + 2 * w], sv[32 * q + 2 * w + 1]),
+                                          cc2, nml2);
+              const float2 x = make_float2(exp2_approx(y.x), exp2_approx(y.y));
+              sum2[w & 3] = __fadd2_rn(sum2[w & 3], x);
+              hw[w] = pack_bf16x2(x.x, x.y);
+              const float2 rr =
+                  __ffma2_rn(make_float2(bf16_lo(hw[w]), bf16_hi(hw[w])), minus1, x);
+              lw[w] = pack_bf16x2(rr.x, rr.y);
+            }
+            tmem_st16(lane_base + scol + 32 * q, hw);
+            tmem_st16(lane_base + scol + 32 * q + 16, lw);
+          }
+          const float2 s4 =
+              __fadd2_rn(__fadd2_rn(sum2[0], sum2[1]), __fadd2_rn(sum2[2], sum2[3]));
+          l += s4.x + s4.y;
+          if (__any_sync(0xffffffffu, rose)) {
+            // O_t holds P V up to page i - 1, which must be done (with one
+            // buffer it was, before S_t of this page was issued)
+            if (C::kSBufs > 1) {
+              const int tp = t * C::kSBufs + (i - 1) % C::kSBufs;
+              if (!all_ok(wait(&o_done[tp], ((i - 1) / C::kSBufs) & 1))) {
+                ok = false;
+                break;
+              }
+              tc_fence_after_sync();
+            }
+#pragma unroll
+            for (int q16 = 0; q16 < D / 16; ++q16) {
+              float ov[16];
+              tmem_ld16(lane_base + C::kOCol + t * D + 16 * q16, ov);
+              tmem_wait_ld();
+#pragma unroll
+              for (int k = 0; k < 16; ++k) ov[k] *= alpha;
+              tmem_st16(lane_base + C::kOCol + t * D + 16 * q16, ov);
+            }
+          }
+          // V rows outside the run's key range on a boundary page -> zero
+          // (warpgroup 0; both tiles' products read them after its P)
+          const int rlo = max(lo_run - pos0, 0), rhi = min(pos_last - pos0, kPage - 1);
+          if (t == 0 && (rlo > 0 || rhi < kPage - 1)) {
+            const int s = i % RV;
+            if (!all_ok(wait(&v_full[s], (i / RV) & 1))) {
+              ok = false;
+              break;
+            }
+            unsigned char* vt = v_slots + s * C::kTileBytes;
+            for (int e = m; e < kPage * (D / 8); e += C::kRows) {
+              const int k = e / (D / 8), ch = e % (D / 8);
+              if (k < rlo || k > rhi)
+                *reinterpret_cast<uint4*>(vt + (ch >> 3) * kBoxBytes + k * 128 + (ch & 7) * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_shared();  // the zeros are read by the tensor core
+          }
+          tmem_wait_st();
+          tc_fence_before_sync();
+          mbar_arrive(&p_full[tb]);
+        }
+        if (!ok) break;
+
+        // end of run: the O_t row once P V of the last page is done
+        const int il = i - 1;
+        if (!all_ok(wait(&o_done[t * C::kSBufs + il % C::kSBufs], (il / C::kSBufs) & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const int hh = h0 + g;
+        float inv = 0.f;
+        if (live) {
+          const float sk = p.sinks ? p.sinks[hh] * kLog2e : -INFINITY;
+          const float mf = fmaxf(m_run, sk);
+          const float scl = exp2_approx(m_run - mf);
+          const float total = fmaf(l, scl, exp2_approx(sk - mf));
+          inv = total > 0.f ? scl / total : 0.f;
+        }
+        uint16_t* orow = p.out + ((size_t)(t_begin + (live ? tl : 0)) * p.hq + hh) * D;
+#pragma unroll
+        for (int q16 = 0; q16 < D / 16; ++q16) {
+          float ov[16];
+          tmem_ld16(lane_base + C::kOCol + t * D + 16 * q16, ov);
+          tmem_wait_ld();
+          if (live) {
+            uint32_t w[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              w[k] = pack_bf16x2(ov[2 * k] * inv, ov[2 * k + 1] * inv);
+            uint4* dst = reinterpret_cast<uint4*>(orow + 16 * q16);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          }
+        }
+        tc_fence_before_sync();
+        rs = re;
+      }
+      if (!ok) break;
+      // this item's descriptor is no longer read: free its slot before
+      // waiting for the next item
+      mbar_arrive(&item_free[d]);
+      have = load_q(seq + 1);
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == C::kMmaWarp) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D, int RK, int RV>
+cudaError_t launch_prefill_umma(const DecodeParams& p, const CUtensorMap& k_map,
+                                const CUtensorMap& v_map, int sm_count, cudaStream_t stream) {
+  using C = UmmaPrefillCfg<D, RK, RV>;
+  static std::atomic<bool> configured[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(paged_prefill_umma_kernel<D, RK, RV>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured[dev].store(true, std::memory_order_release);
+  }
+  if (p.rows == 0) return cudaSuccess;
+  const int tokens = C::kTiles * (C::kRows / p.group);
+  const int items = ((p.rows + tokens - 1) / tokens) * p.hkv;
+  // the item counter lives in the first word of the caller's workspace
+  int* counter = reinterpret_cast<int*>(p.ws_acc);
+  e = cudaMemsetAsync(counter, 0, sizeof(int), stream);
+  if (e != cudaSuccess) return e;
+  const int ctas = items < sm_count ? items : sm_count;
+  return launch_pdl(paged_prefill_umma_kernel<D, RK, RV>, dim3(ctas), dim3(C::kThreads),
+                    C::kSmemBytes, stream, k_map, v_map, p, counter);
+}
+
+}  // namespace tiles2
+}  // namespace pgd
