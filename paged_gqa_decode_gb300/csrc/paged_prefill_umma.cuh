@@ -1,7 +1,6 @@
 // Paged prefill attention on the 5th-generation tensor cores (tcgen05 UMMA
-// with TMEM accumulators), sm_103a: a persistent kernel with one query tile
-// per work item.  It serves head_dim 128; at head_dim 64 the two-tile kernel
-// of paged_prefill_umma_tiles2.cuh is faster and runs instead.
+// with TMEM accumulators), sm_103a: a persistent kernel with two query tiles
+// per work item.
 //
 // What it computes is the same as the tiled prefill kernel (Mistral 7B
 // Instruct v0.3 model files, src/attention.linnet, prefill_paged; window and
@@ -10,50 +9,49 @@
 // its group, over that row's keys at positions (positions[p] - window,
 // positions[p]], the head's sink logit in the denominator only.
 //
-// Work items are (block of 128 / G consecutive packed tokens, kv head); a
-// block's 128 query rows are (token, head of the group) pairs, row
-// m = token * G + head, one per TMEM lane.  One CTA per SM takes items from a
-// counter, last token blocks (the longest key ranges) first.  Within an item
-// the tokens split into runs (same table row, consecutive positions); each run
+// Work items are (block of 2 x 128 / G consecutive packed tokens, kv head):
+// two query tiles of 128 rows, tile t holding tokens t * 128 / G ..
+// (t + 1) * 128 / G - 1 of the block, row m = token * G + head, one per TMEM
+// lane.  Both tiles share every K and V page the item loads (half the page
+// traffic of one tile per item).  One CTA per SM takes items from a counter,
+// last token blocks (the longest key ranges) first.  Within an item the
+// tokens split into runs (same table row, consecutive positions); each run
 // is one pass over the pages of the union of its tokens' key ranges.  The
 // pages of all of a CTA's items form one sequence, and every role walks it:
-//   warp 4      K producer: per item, reads its tokens, builds the runs,
+//   warp 8      K producer: per item, reads its tokens, builds the runs,
 //               checks the table and zeroes uncovered outputs (whole warp);
 //               then streams each page's K tile (64 x D bf16, 128-byte
 //               swizzle) into a ring of shared slots with TMA, pulling pages
 //               into L2 ahead of their loads.
-//   warp 7      V producer: the same pages' V tiles into a second ring.
-//   warp 5      S issuer (one thread) and TMEM owner, per page i:
-//                 S_i  = Q K_i^T    M 128, N 64, K D   (Q from TMEM, K shared)
-//               into TMEM buffer i % 4 once P V_{i-4} (which reads that
-//               buffer's P) is done, so S runs up to four pages ahead.
-//   warp 6      P V issuer (one thread), per page i:
-//                 O   += P_i V_i    M 128, N D,  K 64  (P from TMEM, V shared)
-//               Two issuing threads keep the tensor core fed while either
-//               waits.
-//   warps 0-7   softmax: warpgroup h (warps 4h .. 4h + 3), one thread per
-//               query row, takes the pages i with i % 2 == h.  Each loads half
-//               of its row's Q into TMEM per item (at head_dim 128, for items
-//               of kStageMinPages pages or more, from rows the K producer
-//               staged in shared memory with bulk copies, and before the
-//               previous item's last outputs are written); per page the S row from
-//               TMEM, causal and window mask, online softmax in log2 units
-//               with a lazy reference max common to both warpgroups (raised
+//   warp 11     V producer: the same pages' V tiles into a second ring.
+//   warp 9      S issuer (one thread) and TMEM owner, per page i and tile t:
+//                 S_t  = Q_t K_i^T    M 128, N 64, K D   (K shared; Q from TMEM
+//                                                      at head_dim 64, shared at 128)
+//               into tile t's S buffer i % 2 once P_t V_{i-2} (which reads
+//               the same columns) is done.
+//   warp 10     P V issuer (one thread), per page i and tile t:
+//                 O_t += P_t V_i      M 128, N D,  K 64  (P from TMEM, V shared)
+//   warps 0-7   softmax: warpgroup t (warps 4t .. 4t + 3) owns tile t, one
+//               thread per query row.  It loads its rows' Q per item (into
+//               TMEM, or shared memory at head_dim 128); per page the S row from TMEM, causal and window mask,
+//               online softmax in log2 units with a lazy running max (raised
 //               only when a score exceeds it by more than 2^8, which then
-//               rescales that row of O in TMEM): page i's reference is page
-//               i - 1's, published through shared memory, raised if needed.
-//               P is written over S as a bf16 head and residual (two MMAs, so
-//               P V keeps fp32 accuracy).  Each warpgroup keeps its own row
-//               sum; at the end of a run they meet, add the sums and each
-//               normalises and stores half of the O row, with the sink.
-// TMEM (512 columns): S / P buffers b = 0..3 at [64 b, 64 b + 64) (P per chunk
-// of 32 keys: the bf16 head in the chunk's first 16 columns, the residual in
-// the next 16, as packed pairs), O at [256, 256 + D), Q buffers q = 0, 1 at
-// [384 + q D / 2, 384 + (q + 1) D / 2) as packed pairs.
-// V rows outside the run's key range on its boundary pages are zeroed in
-// shared memory before the product.  Every wait is bounded; a timeout records
-// PGD_EDEVICE_TIMEOUT, stops all roles, drains in-flight copies and MMAs and
-// frees TMEM before the CTA exits.
+//               rescales that row of O_t in TMEM); P is written over S as a
+//               bf16 head and residual (two MMAs, so P V keeps fp32
+//               accuracy).  At the end of a run each thread normalises its
+//               O_t row with the sink and stores it.  Warpgroup 0 also zeroes
+//               the V rows outside the run's key range on boundary pages
+//               before the products read them.
+// TMEM (512 columns): O_t at [t D, (t + 1) D), then two S / P buffers per
+// tile, 64 columns each (S of the next page is computed while the softmax
+// works on this one; P per chunk of 32 keys: the bf16 head in the chunk's
+// first 16 columns, the residual in the next 16, as packed pairs), then at
+// head_dim 64 Q_t, D / 2 columns of packed pairs.  At head_dim 128 the O
+// accumulators and S buffers take all 512 columns, and Q_t sits in shared
+// memory instead (K-major, 128-byte swizzle), written there by the softmax
+// warps; the S products then read A from shared memory.
+// Every wait is bounded; a timeout records PGD_EDEVICE_TIMEOUT, stops all
+// roles, drains in-flight copies and MMAs and frees TMEM before the CTA exits.
 #pragma once
 
 #include "paged_decode.cuh"
@@ -63,52 +61,41 @@ namespace pgd {
 
 template <int D, int RK, int RV>
 struct UmmaPrefillCfg {
-  static constexpr int kRows = 128;  // query rows per item (TMEM lanes)
-  static constexpr int kSoftmaxThreads = 256;  // two warpgroups
+  static constexpr int kRows = 128;  // query rows per tile (TMEM lanes)
+  static constexpr int kTiles = 2;   // query tiles per item
+  static constexpr int kSoftmaxThreads = 256;  // one warpgroup per tile
   static constexpr int kProducerWarp = 8;
   static constexpr int kMmaWarp = 9;  // S issuer, TMEM owner
   static constexpr int kPvWarp = 10;
   static constexpr int kVWarp = 11;
   static constexpr int kThreads = 384;
   static constexpr int kBoxes = D / 64;
-  static constexpr int kSBufs = 4;  // S / P buffers: S runs this many pages ahead
   static constexpr int kTileBytes = kPage * D * 2;  // one K or V slot (one page)
   static constexpr int kVOff = RK * kTileBytes;
-  // an item's q rows (128 x D bf16, row m = token * G + head), staged by the
-  // K producer for the softmax warps (head_dim 128 only, see kStageMinPages)
-  static constexpr bool kStageQ = D == 128;
-  static constexpr int kQStageOff = (RK + RV) * kTileBytes;
-  static constexpr int kQStageBytes = kStageQ ? kRows * D * 2 : 0;
-  static constexpr int kBarOff = kQStageOff + kQStageBytes;
-  static constexpr int kNumBars = 2 * RK + 2 * RV + 3 * kSBufs + 13;
+  // Q: in TMEM at head_dim 64; at 128 the two O accumulators and four S
+  // buffers take all 512 columns, so Q sits in shared memory (K-major,
+  // 128-byte swizzle: the layout the MMA reads), written by the softmax warps
+  static constexpr bool kQSmem = D == 128;
+  static constexpr int kQOff = (RK + RV) * kTileBytes;
+  static constexpr int kQBoxBytes = kRows * 128;  // 128 rows x 64 values
+  static constexpr int kQTileBytes = kRows * D * 2;
+  static constexpr int kBarOff = kQOff + (kQSmem ? kTiles * kQTileBytes : 0);
+  // S / P buffers per tile: two where TMEM has room (head_dim 64), so S of
+  // the next page is computed while the softmax works on this one
+  static constexpr int kSBufs = 2;
+  static constexpr int kNumBars = 2 * RK + 2 * RV + 3 * kTiles * kSBufs + 8;
   static constexpr int kSmemBytes = 1024 + kBarOff + kNumBars * 8;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kOCol = 256, kQCol = 384;
+  static constexpr uint32_t kOCol = 0, kSCol = kTiles * D,
+                            kQCol = kTiles * D + kTiles * kSBufs * kPage;
   static constexpr uint32_t kIdescS = umma_idesc_bf16(128, kPage, 0, 0);
   static constexpr uint32_t kIdescPV = umma_idesc_bf16(128, D, 0, 1);
   static_assert(D == 64 || D == 128, "head_dim");
+  static_assert(kSCol + kTiles * kSBufs * kPage <= kTmemCols, "TMEM columns");
+  static_assert(kQSmem || kQCol + kTiles * D / 2 <= kTmemCols, "TMEM columns");
   static_assert(RK == RV, "the K and V rings are streamed by one helper");
   static_assert(kSmemBytes + 8 * 1024 <= 227 * 1024, "shared memory");
 };
-
-// Copies `bytes` contiguous bytes (16-byte aligned, a multiple of 16) from
-// global to shared memory, completing on `bar`.
-__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
-                                              uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
-
-// At head_dim 128, items with at least this many pages get their q rows
-// staged in shared memory by the K producer, and the softmax warps take them
-// into TMEM before the previous item's last outputs are written (overlapping
-// that epilogue); shorter items, and every item at head_dim 64, load q from
-// global memory when they start (measured: the early hand-over gained 3 % on
-// 50-page items and cost 2-4 % on 3-page ones).
-constexpr int kStageMinPages = 8;
 
 // Reference-max slack in log2 units: P values stay below 2^8.
 constexpr float kLazyRescaleLog2 = 8.0f;
@@ -139,9 +126,8 @@ __device__ __forceinline__ bool mbar_wait_abortable(uint64_t* bar, uint32_t pari
 struct PrefillItem {
   int valid;  // 0: no more items
   int t_begin, t_end, kvh, runs;
-  int staged;  // q rows staged in shared memory (items of kStageMinPages pages or more)
-  int run_end[129];
-  int tok_row[128], tok_pos[128], run_bad[128];
+  int run_end[257];
+  int tok_row[256], tok_pos[256], run_bad[256];
 };
 
 // Page sequence of one item: run by run (inactive and bad runs skipped),
@@ -179,7 +165,8 @@ __global__ void __launch_bounds__(384, 1)
   pdl_wait();
   pdl_allow_dependents();
   const int G = p.group;
-  const int tokens = C::kRows / G;
+  const int T = C::kRows / G;  // tokens per tile
+  const int tokens = C::kTiles * T;
   const int n_blocks = (p.rows + tokens - 1) / tokens;
   const int n_items = n_blocks * p.hkv;
   const int tid = threadIdx.x;
@@ -191,27 +178,21 @@ __global__ void __launch_bounds__(384, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* k_slots = base;
   unsigned char* v_slots = base + C::kVOff;
+  unsigned char* q_smem = base + C::kQOff;  // [tile] Q rows (head_dim 128)
   uint64_t* k_full = reinterpret_cast<uint64_t*>(base + C::kBarOff);  // TMA landed
   uint64_t* k_empty = k_full + RK;         // S of the page done (MMA commit)
   uint64_t* v_full = k_empty + RK;
   uint64_t* v_empty = v_full + RV;         // P V of the page done (MMA commit)
-  uint64_t* s_full = v_empty + RV;         // [page % 4] S in TMEM (MMA commit)
-  uint64_t* p_full = s_full + C::kSBufs;   // [page % 4] P in TMEM, boundary V rows zeroed
-  uint64_t* o_done = p_full + C::kSBufs;   // [page % 4] P V done (MMA commit)
-  uint64_t* item_ready = o_done + C::kSBufs;  // [item % 2] descriptor written (producer)
+  // per (tile t, buffer b = page % kSBufs) at t * kSBufs + b:
+  uint64_t* s_full = v_empty + RV;         // S of the page in TMEM (MMA commit)
+  uint64_t* p_full = s_full + C::kTiles * C::kSBufs;  // P in TMEM (and boundary V rows zeroed)
+  uint64_t* o_done = p_full + C::kTiles * C::kSBufs;  // P V of the page done (MMA commit)
+  uint64_t* item_ready = o_done + C::kTiles * C::kSBufs;  // [item % 2] descriptor written
   uint64_t* item_free = item_ready + 2;       // [item % 2] consumed (softmax, issuers, V producer)
-  uint64_t* q_ready = item_free + 2;          // [item % 2] Q in TMEM (softmax)
+  uint64_t* q_ready = item_free + 2;          // [item % 2] both tiles' Q in TMEM (softmax)
   uint64_t* fin = q_ready + 2;                // [issuer] every MMA it issued done
-  uint64_t* mref_bar = fin + 2;               // [page % 2] the page's reference max published
-  uint64_t* l_bar = mref_bar + 2;             // both warpgroups' row sums of a run published
-  uint64_t* q_full = l_bar + 1;               // the item's q rows staged (bulk copies landed)
-  uint64_t* q_free = q_full + 1;              // the softmax warps copied them into TMEM
-  unsigned char* q_stage = base + C::kQStageOff;
   __shared__ PrefillItem items[2];
   __shared__ int y_ring[2][64];  // [K, V producer] tile rows of upcoming pages, by page % 64
-  // per row: the reference max after page i in mref_x[i % 2]; the warpgroups'
-  // row sums at the end of run r in l_x[r % 2]
-  __shared__ float mref_x[2][C::kRows], l_x[2][2][C::kRows];
   __shared__ volatile int abort_flag;
   __shared__ uint32_t tmem_slot;
 
@@ -224,22 +205,18 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    for (int b = 0; b < C::kSBufs; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&p_full[b], C::kRows);  // the page's warpgroup
-      mbar_init(&o_done[b], 1);
+    for (int tb = 0; tb < C::kTiles * C::kSBufs; ++tb) {
+      mbar_init(&s_full[tb], 1);
+      mbar_init(&p_full[tb], C::kRows);  // the tile's warpgroup
+      mbar_init(&o_done[tb], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&item_ready[b], 1);
       mbar_init(&item_free[b], C::kSoftmaxThreads + 3);
-      mbar_init(&mref_bar[b], C::kSoftmaxThreads / 2);
       mbar_init(&q_ready[b], C::kSoftmaxThreads);
     }
     mbar_init(&fin[0], 1);
     mbar_init(&fin[1], 1);
-    mbar_init(l_bar, C::kSoftmaxThreads);
-    mbar_init(q_full, 1);
-    mbar_init(q_free, C::kSoftmaxThreads);
     mbar_init_fence();
     abort_flag = 0;
   }
@@ -323,7 +300,6 @@ __global__ void __launch_bounds__(384, 1)
       prefetch_tensormap(&v_map);
     }
     int ik = 0;  // K loads issued (all items)
-    int n_staged = 0;  // items whose q rows were staged
     bool ok = true;
     for (int seq = 0; ok; ++seq) {
       const int d = seq & 1;
@@ -384,7 +360,6 @@ __global__ void __launch_bounds__(384, 1)
       __syncwarp();
       // a table entry outside the pool marks its run bad (zero outputs,
       // PGD_EDEVICE_BOUNDS); checked before any copy is issued
-      int item_pages = 0;
       for (int r = 0; r < it.runs; ++r) {
         const int rs = r == 0 ? 0 : it.run_end[r - 1], re = it.run_end[r];
         const int row = it.tok_row[rs];
@@ -392,7 +367,6 @@ __global__ void __launch_bounds__(384, 1)
         if (row >= 0) {
           const int lo = p.window > 0 ? max(it.tok_pos[rs] - p.window + 1, 0) : 0;
           const int first = lo / kPage, last = it.tok_pos[re - 1] / kPage;
-          item_pages += last - first + 1;
           for (int pg = first + lane; pg <= last; pg += 32) {
             const int page = page_of(p.table, row, pg, p.maxp);
             if (page < 0 || page >= p.num_pages) bad = 1;
@@ -418,25 +392,6 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       __syncwarp();
-      // a long item's q rows (G heads x D of each active token, contiguous
-      // in q) into the staging buffer once the softmax warps copied the
-      // previously staged item's rows out of it
-      const bool staged = C::kStageQ && item_pages >= kStageMinPages;
-      if (lane == 0) it.staged = staged;
-      if (staged && n_staged >= 1 && !all_ok(wait(q_free, (n_staged - 1) & 1))) break;
-      if (staged) {
-        ++n_staged;
-        int nq = 0;
-        for (int k = lane; k < tokens; k += 32) nq += (t_begin + k < t_end && it.tok_row[k] >= 0);
-        nq = __reduce_add_sync(0xffffffffu, nq);
-        if (lane == 0) mbar_arrive_expect_tx(q_full, (uint32_t)(nq * G * D * 2));
-        __syncwarp();
-        for (int k = lane; k < tokens; k += 32)
-          if (t_begin + k < t_end && it.tok_row[k] >= 0)
-            bulk_copy_g2s(q_stage + (size_t)k * G * D * 2,
-                          p.q + ((size_t)(t_begin + k) * p.hq + h0) * D, (uint32_t)(G * D * 2),
-                          q_full);
-      }
       if (lane == 0) mbar_arrive(&item_ready[d]);
       ok = stream_item(it, kvh, &k_map, k_slots, k_full, k_empty, y_ring[0], ik, true);
     }
@@ -471,24 +426,41 @@ __global__ void __launch_bounds__(384, 1)
         if (!it.valid) break;
         if (!wait(&q_ready[d], (seq >> 1) & 1)) break;
         ItemCursor cur{-1, 0, -1, -1, 0, 0};
-        for (bool more = item_next_run(it, p.window, cur); more;
+        for (bool more = item_next_run(it, p.window, cur); more && ok;
              more = item_advance(it, p.window, cur), ++i) {
-          // buffer i % 4 is free once P V_{i-4} has read its P
-          if (!wait(&k_full[i % RK], (i / RK) & 1) ||
-              (i >= C::kSBufs && !wait(&o_done[i % C::kSBufs], ((i / C::kSBufs) - 1) & 1))) {
+          if (!wait(&k_full[i % RK], (i / RK) & 1)) {
             ok = false;
             break;
           }
-          tc_fence_after_sync();
           const uint32_t kt = k_addr + (i % RK) * C::kTileBytes;
-          const uint32_t sb = tmem + (i % C::kSBufs) * kPage;
-          const uint32_t qa = tmem + C::kQCol + d * (D / 2);
+          const int b = i % C::kSBufs;
+          for (int t = 0; t < C::kTiles; ++t) {
+            // the buffer holds P_t of page i - kSBufs until P V has read it
+            const int tb = t * C::kSBufs + b;
+            if (i >= C::kSBufs && !wait(&o_done[tb], ((i / C::kSBufs) - 1) & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint32_t sb = tmem + C::kSCol + tb * kPage;
+            if constexpr (C::kQSmem) {
+              const uint32_t qs = smem_addr(q_smem) + t * C::kQTileBytes;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            umma_bf16_tmem_a(sb, qa + kk * 8,
-                             umma_desc_sw128(kt + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
-                             C::kIdescS, kk > 0);
-          umma_commit(&s_full[i % C::kSBufs]);
+              for (int kk = 0; kk < D / 16; ++kk)
+                umma_bf16(sb, umma_desc_sw128(qs + (kk >> 2) * C::kQBoxBytes + (kk & 3) * 32, 16, 1024),
+                          umma_desc_sw128(kt + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
+                          C::kIdescS, kk > 0);
+            } else {
+              const uint32_t qa = tmem + C::kQCol + t * (D / 2);
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk)
+                umma_bf16_tmem_a(sb, qa + kk * 8,
+                                 umma_desc_sw128(kt + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
+                                 C::kIdescS, kk > 0);
+            }
+            umma_commit(&s_full[tb]);
+          }
+          if (!ok) break;
           umma_commit(&k_empty[i % RK]);
           issued = true;
         }
@@ -513,28 +485,38 @@ __global__ void __launch_bounds__(384, 1)
         if (!it.valid) break;
         ItemCursor cur{-1, 0, -1, -1, 0, 0};
         bool first = true;  // O restarts with each item
-        for (bool more = item_next_run(it, p.window, cur); more;
+        for (bool more = item_next_run(it, p.window, cur); more && ok;
              more = item_advance(it, p.window, cur), ++i) {
-          if (!wait(&p_full[i % C::kSBufs], (i / C::kSBufs) & 1) ||
-              !wait(&v_full[i % RV], (i / RV) & 1)) {
+          if (!wait(&v_full[i % RV], (i / RV) & 1)) {
             ok = false;
             break;
           }
-          tc_fence_after_sync();
           const uint32_t vt = v_addr + (i % RV) * C::kTileBytes;
-          const uint32_t pb = tmem + (i % C::kSBufs) * kPage;
-          // keys 16 kk .. 16 kk + 15: chunk kk / 2 of the P columns, half kk % 2
-          // of its 16 head (then residual) columns
+          const int b = i % C::kSBufs;
+          for (int t = 0; t < C::kTiles; ++t) {
+            const int tb = t * C::kSBufs + b;
+            if (!wait(&p_full[tb], (i / C::kSBufs) & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint32_t pb = tmem + C::kSCol + tb * kPage;
+            const uint32_t od = tmem + C::kOCol + t * D;
+            // keys 16 kk .. 16 kk + 15: chunk kk / 2 of the P columns, half
+            // kk % 2 of its 16 head (then residual) columns
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16_tmem_a(tmem + C::kOCol, pb + 32 * (kk >> 1) + 8 * (kk & 1),
-                             umma_desc_sw128(vt + kk * 2048, kBoxBytes, 1024), C::kIdescPV,
-                             !(first && kk == 0));
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16_tmem_a(od, pb + 32 * (kk >> 1) + 8 * (kk & 1),
+                               umma_desc_sw128(vt + kk * 2048, kBoxBytes, 1024), C::kIdescPV,
+                               !(first && kk == 0));
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16_tmem_a(tmem + C::kOCol, pb + 32 * (kk >> 1) + 16 + 8 * (kk & 1),
-                             umma_desc_sw128(vt + kk * 2048, kBoxBytes, 1024), C::kIdescPV, true);
-          umma_commit(&o_done[i % C::kSBufs]);
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16_tmem_a(od, pb + 32 * (kk >> 1) + 16 + 8 * (kk & 1),
+                               umma_desc_sw128(vt + kk * 2048, kBoxBytes, 1024), C::kIdescPV,
+                               true);
+            umma_commit(&o_done[tb]);
+          }
+          if (!ok) break;
           umma_commit(&v_empty[i % RV]);
           first = false;
           issued = true;
@@ -548,19 +530,16 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int m = tid & 127, h = tid >> 7;  // row; warpgroup (pages i % 2 == h)
+    const int m = tid & 127, t = tid >> 7;  // row; tile
     const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     const float c = p.q_scale_log2;
     const float cc = c > 0.f ? c : 1.f;
-    int i = 0;     // page index over all items
-    int nrun = 0;  // runs finished
+    int i = 0;  // page index over all items
     bool ok = true;
-    const int tl = m / G, g = m % G;
-    int n_staged = 0;  // staged items taken so far
-    // Half h of item seq's Q rows from the staging buffer into TMEM buffer
-    // seq % 2 (rows of no token: zero); false when there is no item seq.
-    // Item seq + 1's rows are taken before item seq's last outputs are
-    // written, so its first S products overlap that epilogue.
+    const int tl = t * T + m / G, g = m % G;  // token of the block, head of the group
+    const bool in_tile = m / G < T;           // rows past T * G hold no token
+    // Tile t's Q rows of item seq into TMEM (rows of no token: zero); false
+    // when there is no item seq.
     auto load_q = [&](int seq) -> bool {
       const int d = seq & 1;
       if (!all_ok(wait(&item_ready[d], (seq >> 1) & 1))) {
@@ -569,26 +548,24 @@ __global__ void __launch_bounds__(384, 1)
       }
       const PrefillItem& it = items[d];
       if (!it.valid) return false;
-      const bool staged = C::kStageQ && it.staged != 0;
-      if (staged && !all_ok(wait(q_full, n_staged & 1))) {
-        ok = false;
-        return false;
-      }
-      const bool row_ok = tl < tokens && it.t_begin + tl < it.t_end;
-      {
-        const bool q_ok = row_ok && it.tok_row[tl] >= 0;
+      const bool q_ok = in_tile && it.t_begin + tl < it.t_end && it.tok_row[tl] >= 0;
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.q + ((size_t)(it.t_begin + (q_ok ? tl : 0)) * p.hq + it.kvh * G + g) * D);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {  // half the row at a time
         uint4 v[D / 16];
-        if (q_ok) {
-          const uint4* src =
-              staged ? reinterpret_cast<const uint4*>(q_stage + (size_t)m * D * 2 + h * D)
-                     : reinterpret_cast<const uint4*>(
-                           p.q + ((size_t)(it.t_begin + tl) * p.hq + it.kvh * G + g) * D +
-                           h * (D / 2));
 #pragma unroll
-          for (int ch = 0; ch < D / 16; ++ch) v[ch] = src[ch];
-        } else {
+        for (int ch = 0; ch < D / 16; ++ch)
+          v[ch] = q_ok ? src[hh * (D / 16) + ch] : make_uint4(0u, 0u, 0u, 0u);
+        if constexpr (C::kQSmem) {
+          // half hh is box hh: row m's 16-byte chunk ch at chunk ch ^ (m % 8)
+          // of its 128-byte line in the 1024-byte group of rows m / 8
+          unsigned char* box = q_smem + t * C::kQTileBytes + hh * C::kQBoxBytes +
+                               (m >> 3) * 1024 + (m & 7) * 128;
 #pragma unroll
-          for (int ch = 0; ch < D / 16; ++ch) v[ch] = make_uint4(0u, 0u, 0u, 0u);
+          for (int ch = 0; ch < D / 16; ++ch)
+            *reinterpret_cast<uint4*>(box + ((ch ^ (m & 7)) << 4)) = v[ch];
+          continue;
         }
 #pragma unroll
         for (int c16 = 0; c16 < D / 64; ++c16) {
@@ -600,16 +577,16 @@ __global__ void __launch_bounds__(384, 1)
             w[4 * k + 2] = v[4 * c16 + k].z;
             w[4 * k + 3] = v[4 * c16 + k].w;
           }
-          tmem_st16(lane_base + C::kQCol + d * (D / 2) + h * (D / 4) + 16 * c16, w);
-        }
-        tmem_wait_st();
-        tc_fence_before_sync();
-        mbar_arrive(&q_ready[d]);
-        if (staged) {
-          mbar_arrive(q_free);
-          ++n_staged;
+          tmem_st16(lane_base + C::kQCol + t * (D / 2) + hh * (D / 4) + 16 * c16, w);
         }
       }
+      if constexpr (C::kQSmem) {
+        fence_proxy_async_shared();  // read by the tensor core
+      } else {
+        tmem_wait_st();
+        tc_fence_before_sync();
+      }
+      mbar_arrive(&q_ready[d]);
       return true;
     };
     bool have = load_q(0);
@@ -617,15 +594,7 @@ __global__ void __launch_bounds__(384, 1)
       const int d = seq & 1;
       const PrefillItem& it = items[d];
       const int t_begin = it.t_begin, t_end = it.t_end, h0 = it.kvh * G;
-      const bool row_ok = tl < tokens && t_begin + tl < t_end;
-      bool next_loaded = false;
-      // the last run that has pages (its epilogue follows the next Q load)
-      int last_run = -1;
-      for (int r = 0, rs0 = 0; r < it.runs; ++r) {
-        if (it.tok_row[rs0] >= 0 && !it.run_bad[r]) last_run = r;
-        rs0 = it.run_end[r];
-      }
-
+      const bool row_ok = in_tile && t_begin + tl < t_end;
       int rs = 0;
       for (int r = 0; r < it.runs && ok; ++r) {
         const int re = it.run_end[r];
@@ -640,12 +609,12 @@ __global__ void __launch_bounds__(384, 1)
         const int lo_run = p.window > 0 ? max(it.tok_pos[rs] - p.window + 1, 0) : 0;
         const int pos_last = it.tok_pos[re - 1];
         const int first = lo_run / kPage, last = pos_last / kPage;
-        float m_own = -INFINITY;  // reference max as of this warpgroup's last page
-        float l = 0.f;            // this warpgroup's row sum, relative to m_own
+        float m_run = -INFINITY;  // running (lazy) max of the row, log2 units
+        float l = 0.f;            // row sum relative to m_run
         for (int pg = first; pg <= last; ++pg, ++i) {
-          if ((i & 1) != h) continue;  // the other warpgroup's page
-          const int b = i % C::kSBufs;
-          if (!all_ok(wait(&s_full[b], (i / C::kSBufs) & 1))) {
+          const int tb = t * C::kSBufs + i % C::kSBufs;
+          const uint32_t scol = C::kSCol + tb * kPage;
+          if (!all_ok(wait(&s_full[tb], (i / C::kSBufs) & 1))) {
             ok = false;
             break;
           }
@@ -653,7 +622,7 @@ __global__ void __launch_bounds__(384, 1)
           float sv[kPage];
 #pragma unroll
           for (int q = 0; q < kPage / 16; ++q)
-            tmem_ld16(lane_base + b * kPage + 16 * q,
+            tmem_ld16(lane_base + scol + 16 * q,
                       *reinterpret_cast<float(*)[16]>(&sv[16 * q]));
           tmem_wait_ld();
           // scores stay raw: the scale is folded into the exponent's FMA (for
@@ -685,32 +654,18 @@ __global__ void __launch_bounds__(384, 1)
           const float mx = fmax3(fmax3(part[0], part[1], part[2]),
                                  fmax3(part[3], part[4], part[5]), fmaxf(part[6], part[7])) *
                            cc;
-          // the run's reference after the previous page (the other warpgroup's)
-          float m_prev = -INFINITY;
-          if (pg > first) {
-            if (!all_ok(wait(&mref_bar[(i - 1) & 1], ((i - 1) >> 1) & 1))) {
-              ok = false;
-              break;
-            }
-            m_prev = mref_x[(i - 1) & 1][m];
-          }
-          float m_new = m_prev, alpha = 1.f;
+          float alpha = 1.f;
           bool rose = false;
-          if (mx > m_prev + kLazyRescaleLog2) {
-            m_new = mx;
-            if (m_prev != -INFINITY) {
-              alpha = exp2_approx(m_prev - mx);
+          if (mx > m_run + kLazyRescaleLog2) {
+            if (m_run != -INFINITY) {
+              alpha = exp2_approx(m_run - mx);
               rose = true;
             }
+            l = m_run == -INFINITY ? 0.f : l * alpha;
+            m_run = mx;
           }
-          mref_x[i & 1][m] = m_new;
-          mbar_arrive(&mref_bar[i & 1]);
-          if (m_own != m_new) {
-            l = m_own == -INFINITY ? 0.f : l * exp2_approx(m_own - m_new);
-            m_own = m_new;
-          }
-          const float nml = m_new == -INFINITY ? 0.f : -m_new;
-          // P = 2^(s - m_new) as a bf16 head and residual over the S columns
+          const float nml = m_run == -INFINITY ? 0.f : -m_run;
+          // P = 2^(s - m_run) as a bf16 head and residual over the S columns
           // (per chunk of 32 keys: head at +0, residual at +16, column j of a
           // half holding keys 2j, 2j + 1); pairs through the packed fp32 pipe
           const float2 cc2 = make_float2(cc, cc), nml2 = make_float2(nml, nml);
@@ -732,33 +687,37 @@ __global__ void __launch_bounds__(384, 1)
                   __ffma2_rn(make_float2(bf16_lo(hw[w]), bf16_hi(hw[w])), minus1, x);
               lw[w] = pack_bf16x2(rr.x, rr.y);
             }
-            tmem_st16(lane_base + b * kPage + 32 * q, hw);
-            tmem_st16(lane_base + b * kPage + 32 * q + 16, lw);
+            tmem_st16(lane_base + scol + 32 * q, hw);
+            tmem_st16(lane_base + scol + 32 * q + 16, lw);
           }
           const float2 s4 =
               __fadd2_rn(__fadd2_rn(sum2[0], sum2[1]), __fadd2_rn(sum2[2], sum2[3]));
           l += s4.x + s4.y;
           if (__any_sync(0xffffffffu, rose)) {
-            // O holds P V up to the previous page, which must be done
-            const int bp = (i - 1) % C::kSBufs;
-            if (!all_ok(wait(&o_done[bp], ((i - 1) / C::kSBufs) & 1))) {
-              ok = false;
-              break;
+            // O_t holds P V up to page i - 1, which must be done (with one
+            // buffer it was, before S_t of this page was issued)
+            if (C::kSBufs > 1) {
+              const int tp = t * C::kSBufs + (i - 1) % C::kSBufs;
+              if (!all_ok(wait(&o_done[tp], ((i - 1) / C::kSBufs) & 1))) {
+                ok = false;
+                break;
+              }
+              tc_fence_after_sync();
             }
-            tc_fence_after_sync();
 #pragma unroll
             for (int q16 = 0; q16 < D / 16; ++q16) {
               float ov[16];
-              tmem_ld16(lane_base + C::kOCol + 16 * q16, ov);
+              tmem_ld16(lane_base + C::kOCol + t * D + 16 * q16, ov);
               tmem_wait_ld();
 #pragma unroll
               for (int k = 0; k < 16; ++k) ov[k] *= alpha;
-              tmem_st16(lane_base + C::kOCol + 16 * q16, ov);
+              tmem_st16(lane_base + C::kOCol + t * D + 16 * q16, ov);
             }
           }
           // V rows outside the run's key range on a boundary page -> zero
+          // (warpgroup 0; both tiles' products read them after its P)
           const int rlo = max(lo_run - pos0, 0), rhi = min(pos_last - pos0, kPage - 1);
-          if (rlo > 0 || rhi < kPage - 1) {
+          if (t == 0 && (rlo > 0 || rhi < kPage - 1)) {
             const int s = i % RV;
             if (!all_ok(wait(&v_full[s], (i / RV) & 1))) {
               ok = false;
@@ -775,38 +734,13 @@ __global__ void __launch_bounds__(384, 1)
           }
           tmem_wait_st();
           tc_fence_before_sync();
-          mbar_arrive(&p_full[b]);
+          mbar_arrive(&p_full[tb]);
         }
         if (!ok) break;
-        if (C::kStageQ && r == last_run && it.staged) {
-          // a long item: the producer has described (and, if long, staged)
-          // the next one long ago, so take its Q now
-          have = load_q(seq + 1);
-          next_loaded = true;
-          if (!ok) break;
-        }
 
-        // end of run: the final reference, both row sums, then the O row once
-        // P V of the last page is done; each warpgroup stores half of it
+        // end of run: the O_t row once P V of the last page is done
         const int il = i - 1;
-        float m_fin = m_own;
-        if ((il & 1) != h) {
-          if (!all_ok(wait(&mref_bar[il & 1], (il >> 1) & 1))) {
-            ok = false;
-            break;
-          }
-          m_fin = mref_x[il & 1][m];
-        }
-        if (m_own != m_fin) l = m_own == -INFINITY ? 0.f : l * exp2_approx(m_own - m_fin);
-        l_x[nrun & 1][h][m] = l;
-        mbar_arrive(l_bar);
-        if (!all_ok(wait(l_bar, nrun & 1))) {
-          ok = false;
-          break;
-        }
-        const float l_row = l_x[nrun & 1][0][m] + l_x[nrun & 1][1][m];
-        ++nrun;
-        if (!all_ok(wait(&o_done[il % C::kSBufs], (il / C::kSBufs) & 1))) {
+        if (!all_ok(wait(&o_done[t * C::kSBufs + il % C::kSBufs], (il / C::kSBufs) & 1))) {
           ok = false;
           break;
         }
@@ -815,16 +749,16 @@ __global__ void __launch_bounds__(384, 1)
         float inv = 0.f;
         if (live) {
           const float sk = p.sinks ? p.sinks[hh] * kLog2e : -INFINITY;
-          const float mf = fmaxf(m_fin, sk);
-          const float scl = exp2_approx(m_fin - mf);
-          const float total = fmaf(l_row, scl, exp2_approx(sk - mf));
+          const float mf = fmaxf(m_run, sk);
+          const float scl = exp2_approx(m_run - mf);
+          const float total = fmaf(l, scl, exp2_approx(sk - mf));
           inv = total > 0.f ? scl / total : 0.f;
         }
-        uint16_t* orow = p.out + ((size_t)(t_begin + tl) * p.hq + hh) * D + h * (D / 2);
+        uint16_t* orow = p.out + ((size_t)(t_begin + (live ? tl : 0)) * p.hq + hh) * D;
 #pragma unroll
-        for (int q16 = 0; q16 < D / 32; ++q16) {
+        for (int q16 = 0; q16 < D / 16; ++q16) {
           float ov[16];
-          tmem_ld16(lane_base + C::kOCol + h * (D / 2) + 16 * q16, ov);
+          tmem_ld16(lane_base + C::kOCol + t * D + 16 * q16, ov);
           tmem_wait_ld();
           if (live) {
             uint32_t w[8];
@@ -843,7 +777,7 @@ __global__ void __launch_bounds__(384, 1)
       // this item's descriptor is no longer read: free its slot before
       // waiting for the next item
       mbar_arrive(&item_free[d]);
-      if (!next_loaded) have = load_q(seq + 1);
+      have = load_q(seq + 1);
     }
   }
 
@@ -872,7 +806,7 @@ cudaError_t launch_prefill_umma(const DecodeParams& p, const CUtensorMap& k_map,
     if (dev >= 0 && dev < 64) configured[dev].store(true, std::memory_order_release);
   }
   if (p.rows == 0) return cudaSuccess;
-  const int tokens = C::kRows / p.group;
+  const int tokens = C::kTiles * (C::kRows / p.group);
   const int items = ((p.rows + tokens - 1) / tokens) * p.hkv;
   // the item counter lives in the first word of the caller's workspace
   int* counter = reinterpret_cast<int*>(p.ws_acc);

@@ -1,12 +1,12 @@
-// Prefill on the tcgen05 tensor cores at head_dim 64: two query tiles per
-// work item, two S buffers per tile.
-#include "paged_prefill_umma_tiles2.cuh"
+// Prefill on the tcgen05 tensor cores at head_dim 64 (its own translation
+// unit, so the two head dims compile in parallel).
+#include "paged_prefill_umma.cuh"
 
 namespace pgd {
 
 cudaError_t launch_prefill_umma_d64(const DecodeParams& p, const CUtensorMap& k_map,
                                     const CUtensorMap& v_map, int sm_count, cudaStream_t stream) {
-  return tiles2::launch_prefill_umma<64, 8, 8>(p, k_map, v_map, sm_count, stream);
+  return launch_prefill_umma<64, 8, 8>(p, k_map, v_map, sm_count, stream);
 }
 
 }  // namespace pgd
