@@ -209,11 +209,14 @@ PGD_API size_t pgd_paged_decode_workspace_bytes(const pgd_dims* dims, const pgd_
  *   table_rows  0 for pgd_paged_decode_attention; the table_rows argument of
  *               pgd_paged_prefill_attention (> 0) for a prefill call.
  *   window, opts  as passed to that call.
- *   count       out: 0 when dims->rows == 0; 1 for the prefill kernels
- *               (PREFILL_UMMA also issues one 4-byte cudaMemsetAsync) and
- *               for split kernels whose rows all fit one split (it writes
- *               every output); 2 when a row can span several splits (split
- *               kernel + combine kernel).
+ *   count       out: 0 when dims->rows == 0; for PREFILL_UMMA 2 without a
+ *               window when the tokens form at most 4096 blocks of
+ *               2 x (128 / group) (a pass that orders the blocks longest
+ *               first, then the prefill kernel), else 1 (the kernel, after
+ *               one 4-byte cudaMemsetAsync); 1 for PREFILL_TILED and for
+ *               split kernels whose rows all fit one split (it writes every
+ *               output); 2 when a row can span several splits (split kernel
+ *               + combine kernel).
  * Returns PGD_EINVAL for a NULL count, negative table_rows or a kernel the
  * call would reject, and the pgd_dims checks' codes.
  */

@@ -15,4 +15,12 @@ cudaError_t launch_prefill_umma(const DecodeParams& p, const CUtensorMap& k_map,
                         : launch_prefill_umma<128, 4, 4>(p, k_map, v_map, sm_count, stream);
 }
 
+int prefill_umma_launches(int rows, int group, int window) {
+  if (rows <= 0) return 0;
+  using C = UmmaPrefillCfg<128, 4, 4>;  // the block geometry is the same at head_dim 64
+  const int tokens = C::kTiles * (C::kRows / group);
+  const int n_blocks = (rows + tokens - 1) / tokens;
+  return window <= 0 && n_blocks <= kMaxSortedBlocks ? 2 : 1;
+}
+
 }  // namespace pgd

@@ -366,7 +366,9 @@ int pgd_attention_kernel_count(const pgd_dims* dims, int32_t table_rows, int32_t
   const Plan pl = make_plan(dims, opts, dev->sm_count);
   if (dims->rows == 0) {
     *count = 0;
-  } else if (kernel == PGD_KERNEL_PREFILL_UMMA || kernel == PGD_KERNEL_PREFILL_TILED) {
+  } else if (kernel == PGD_KERNEL_PREFILL_UMMA) {
+    *count = prefill_umma_launches(dims->rows, dims->num_q_heads / dims->num_kv_heads, window);
+  } else if (kernel == PGD_KERNEL_PREFILL_TILED) {
     *count = 1;
   } else {
     const int pages = span_pages(dims, window > 0 ? window : 0);

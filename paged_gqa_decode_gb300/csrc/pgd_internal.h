@@ -113,9 +113,13 @@ cudaError_t launch_prefill_tiled(const DecodeParams& p, const CUtensorMap& k_map
 int prefill_block_tokens(int padded);
 
 // Prefill on the tcgen05 tensor cores: persistent, one CTA per SM, blocks of
-// 128 / group tokens; the first word of p.ws_acc is its work counter.
+// 2 x 128 / group tokens; the first word of p.ws_acc is its work counter, the
+// block order (when one is computed) starts at the fifth.
 cudaError_t launch_prefill_umma(const DecodeParams& p, const CUtensorMap& k_map,
                                 const CUtensorMap& v_map, int head_dim, int sm_count,
                                 cudaStream_t stream);
+// Kernels that launch issues for `rows` tokens (the block-order pass and the
+// kernel, or the kernel alone).
+int prefill_umma_launches(int rows, int group, int window);
 
 }  // namespace pgd

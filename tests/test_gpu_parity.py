@@ -292,8 +292,13 @@ def test_kernel_count_follows_the_split_plan():
     assert pgd.attention_kernel_count(dims(w["qwen_serve"], 10),
                                       kernel=pgd.KERNEL_CUDA_CORE) == 1
     assert pgd.attention_kernel_count(dims(w["gptoss_full"], 64, rows=0)) == 0
-    # prefill: tokens in runs take the tcgen05 kernel; one token per row the split kernel
-    assert pgd.attention_kernel_count(dims(w["mistral_serve"], 512, rows=4096), table_rows=8) == 1
+    # prefill: tokens in runs take the tcgen05 kernel (after a pass that orders its
+    # token blocks longest first, without a window); one token per row the split kernel
+    assert pgd.attention_kernel_count(dims(w["mistral_serve"], 512, rows=4096), table_rows=8) == 2
+    assert pgd.attention_kernel_count(dims(w["mistral_serve"], 512, rows=4096), table_rows=8,
+                                      window=128) == 1
+    assert pgd.attention_kernel_count(dims(w["mistral_serve"], 512, rows=4096), table_rows=8,
+                                      kernel=pgd.KERNEL_PREFILL_TILED) == 1
     assert pgd.attention_kernel_count(dims(w["mistral_serve"], 512, rows=8), table_rows=8) == 2
 
 
