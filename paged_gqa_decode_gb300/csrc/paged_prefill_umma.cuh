@@ -99,7 +99,7 @@ struct UmmaPrefillCfg {
   static_assert(kSmemBytes + 8 * 1024 <= 227 * 1024, "shared memory");
 };
 
-// Reference-max slack in log2 units: P values stay below 2^8.
+// Slack of the lazy running max, in log2 units: P values stay below 2^8.
 constexpr float kLazyRescaleLog2 = 8.0f;
 
 // How far ahead of its load the producer pulls a page into L2.
