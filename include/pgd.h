@@ -289,7 +289,8 @@ PGD_API int pgd_paged_decode_step(const pgd_dims* dims, const void* q, const voi
  * over the concatenation: the step of row b is a token with rows = b at its
  * step position.
  * Kernels (opts->kernel): AUTO chooses PREFILL_UMMA (tokens in blocks of
- * 128 / (Hq / Hkv) share every page load; persistent, one CTA per SM) when
+ * 2 x 128 / (Hq / Hkv), two query tiles, share every page load; persistent,
+ * one CTA per SM; without a window the blocks are taken longest first) when
  * P >= 8 * table_rows, else the per-token TENSOR_CORE split kernel.
  * Device errors: rows[p] outside [0, table_rows), plus those of
  * pgd_paged_decode_attention; the token's output is zero.
