@@ -626,7 +626,13 @@ def prefill_work(wl, b) -> dict:
     kv = 0
     for r in np.unique(b.rows_np):
         sel = b.rows_np == r
-        kv += int(pos[sel].max() - lo[sel].min() + 1) * row_bytes
+        # the union of the tokens' ranges [lo, pos]: merge them in order of lo
+        covered, end = 0, -1
+        for a, z in sorted(zip(lo[sel].tolist(), pos[sel].tolist())):
+            if z > end:
+                covered += z - max(a, end + 1) + 1
+                end = z
+        kv += covered * row_bytes
     tokens = len(pos)
     q_out = 2 * tokens * wl.q_heads * wl.head_dim * 2
     writes = 2 * tokens * row_bytes
