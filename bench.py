@@ -14,8 +14,13 @@ outside the timed spans (see L2Flush).
 Prints one JSON line.  `value` is achieved HBM GB/s of the whole step over
 all ranks (algorithmic bytes: every attended K/V row read once, q read, out
 written, the append's read and write); `row_tokens_per_s` is rows decoded per
-second.  `--impl reference` times the fp64 CPU oracle on the host's cores on
-a bounded sample of the same workload instead.
+second.  On the default workload the line also carries `workloads`: the
+other four decode workloads (Qwen2.5-shaped small and serving batches,
+gpt-oss full-context and sliding-window layers), each measured the same way
+in the same process.  `cpu_baseline` times the fp64 CPU oracle on the rows of
+the batch and compares its output with the timed step's (`parity`).
+`--impl reference` times the oracle on the host's cores on a bounded sample
+of the same workload instead.
 
 Multi-GPU: one process per GPU under torchrun; rows are independent, so each
 rank decodes its own batch (weak scaling) and no collective touches the data
@@ -240,31 +245,58 @@ def source_digest() -> str:
 # --------------------------------------------------------------------------- oracle timing
 
 
-def oracle_rows_timing(batch, rows, window, nthreads=None) -> float:
-    """Seconds the oracle takes for append + decode of `rows` of the batch."""
+def oracle_rows_timing(batch, rows, window, nthreads=None, result=False):
+    """Seconds the oracle takes for append + decode of `rows` of the batch
+    (and its output for those rows when `result`)."""
     from tests.oracle_side import oracle_step, snapshot_rows
     host = snapshot_rows(batch, rows)
     t0 = time.perf_counter()
-    oracle_step(batch, host, window=window, sinks=batch.sinks, scale=batch.wl.scale,
-                nthreads=nthreads)
-    return time.perf_counter() - t0
+    want, _, _ = oracle_step(batch, host, window=window, sinks=batch.sinks,
+                             scale=batch.wl.scale, nthreads=nthreads)
+    elapsed = time.perf_counter() - t0
+    return (elapsed, want) if result else elapsed
 
 
-def cpu_baseline(batch, max_rows: int = 256) -> dict:
+# The tolerance the parity tests hold the CUDA path to (bf16 output from fp32
+# accumulation): max abs 1e-2 and max rel 2e-2, rel where |oracle| >= 1e-3.
+ABS_TOL, REL_TOL, REL_FLOOR = 1e-2, 2e-2, 1e-3
+
+
+def parity_stats(got: torch.Tensor, want: np.ndarray) -> dict:
+    g = got.float().cpu().numpy().astype(np.float64)
+    diff = np.abs(g - want)
+    big = np.abs(want) >= REL_FLOOR
+    rel = diff[big] / np.abs(want[big]) if big.any() else np.zeros(1)
+    max_abs, max_rel = float(diff.max(initial=0.0)), float(rel.max(initial=0.0))
+    finite = bool(np.all(np.isfinite(g)))
+    return {"max_abs": max_abs, "max_rel": max_rel, "finite": finite,
+            "within_tolerance": finite and max_abs <= ABS_TOL and max_rel <= REL_TOL,
+            "tolerance": {"abs": ABS_TOL, "rel": REL_TOL, "rel_where_abs_oracle_ge": REL_FLOOR}}
+
+
+def cpu_baseline(batch, out: torch.Tensor | None = None, max_rows: int = 256) -> dict:
     """The oracle (append + decode) on up to `max_rows` seeded rows of the
-    batch, on all host cores."""
+    batch, on all host cores.  With `out` (the GPU output of the timed step
+    on the same batch), the oracle's result for those rows is also compared
+    with it element by element."""
     import oracle
     wl = batch.wl
     pos = batch.layout.positions
     order = np.random.default_rng(0).permutation(wl.rows)
-    rows = order[:min(max_rows, wl.rows)]
-    elapsed = oracle_rows_timing(batch, rows, wl.window)
+    rows = np.sort(order[:min(max_rows, wl.rows)])
+    elapsed, want = oracle_rows_timing(batch, rows, wl.window, result=True)
     by = algorithmic_bytes(wl, pos[rows])
-    return {"value": by["step"] / elapsed / 1e9, "unit": "GB/s", "cores": oracle.default_threads(),
+    line = {"value": by["step"] / elapsed / 1e9, "unit": "GB/s", "cores": oracle.default_threads(),
             "kind": "oracle",
             "row_tokens_per_s": len(rows) / elapsed,
             "sample": f"{len(rows)} of {wl.rows} rows of {wl.name} (seeded choice), "
                       f"append + decode, {elapsed:.2f} s"}
+    if out is not None:
+        idx = torch.as_tensor(rows, device=out.device)
+        line["parity"] = {"rows_checked": int(len(rows)), "of_rows": int(wl.rows),
+                          "against": "output of the last timed step",
+                          **parity_stats(out.index_select(0, idx), want)}
+    return line
 
 
 # --------------------------------------------------------------------------- arms
@@ -310,11 +342,41 @@ def run_reference(args, wl: Workload):
 
 
 def run_pgd(args, wl: Workload):
-    import paged_gqa_decode_gb300 as pgd
     world, rank, local = dist_env()
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     init_dist(world, "nccl")
+    line = measure_decode(args, wl, world, rank, device, main=True)
+    # The other decode workloads, each measured the same way in this process
+    # (the headline line stays on the default, largest one).
+    if not args.only and args.rows == 0 and wl.name == DEFAULT_WORKLOAD:
+        extra = {}
+        for name, other in WORKLOADS.items():
+            if name == wl.name:
+                continue
+            r = measure_decode(args, other, world, rank, device, main=False)
+            if r is not None:
+                extra[name] = {k: r[k] for k in (
+                    "value", "unit", "ms_per_step", "row_tokens_per_s", "decode_ms_per_step",
+                    "latency_back_to_back", "e2e", "clocks", "gpu_launches")}
+                extra[name]["workload"] = r["config"]["workload"]
+                extra[name]["l2"] = r["config"]["l2"]
+                extra[name]["roofline"] = {k: r["roofline"][k] for k in (
+                    "bound", "achieved", "peak", "peak_kind", "unit", "frac")}
+                if "cpu_baseline" in r:
+                    extra[name]["cpu_baseline"] = r["cpu_baseline"]
+        if line is not None:
+            line["workloads"] = extra
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+def measure_decode(args, wl: Workload, world: int, rank: int, device, main: bool):
+    """One decode workload: timed steps, per-call spans, back-to-back latency,
+    end-to-end with host copies, clocks, and (rank 0, N = 1) the oracle on
+    its rows compared with the timed step's output.  Returns rank 0's line
+    (None on the other ranks)."""
+    import paged_gqa_decode_gb300 as pgd
     batch = make_batch(wl, seed=rank_seed(wl, rank), device=device)
     lay = batch.layout
     dims = pgd.make_dims(rows=wl.rows, num_q_heads=wl.q_heads, num_kv_heads=wl.kv_heads,
@@ -563,7 +625,7 @@ def run_pgd(args, wl: Workload):
     e2e_value = total_bytes / (e2e_ms * 1e-3) / 1e9
 
     if rank != 0:
-        return
+        return None
     peak, peak_kind = measured_peak()
     decode_s = decode_ms * 1e-3 / args.steps
     # the decode call's algorithmic bytes; with the append fused in, its
@@ -610,8 +672,10 @@ def run_pgd(args, wl: Workload):
         "kernel_source_digest": digest,
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(batch)
-    print(json.dumps(line), flush=True)
+        line["cpu_baseline"] = cpu_baseline(batch, out)
+    del batch, ws
+    torch.cuda.empty_cache()
+    return line
 
 
 def prefill_work(wl, b) -> dict:
@@ -817,6 +881,9 @@ def main():
                     help="override the workload's row count (small profiling cases)")
     ap.add_argument("--reference-rows", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", action="store_true",
+                    help="decode path: measure only --workload (by default the headline "
+                         "workload's line also carries the other four under 'workloads')")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

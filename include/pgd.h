@@ -241,8 +241,9 @@ PGD_API int pgd_attention_kernel_count(const pgd_dims* dims, int32_t table_rows,
  * m = max(max_j s_j, sink), out = sum_j e^(s_j - m) v_j /
  * (sum_j e^(s_j - m) + e^(sink - m)) with s_j = scale * q . k_j, in fp32.
  * Device errors: as for pgd_kv_append_paged (for any attended page), plus
- * PGD_EDEVICE_TIMEOUT if a pipeline wait exceeded its limit; affected rows
- * or splits contribute zero.
+ * PGD_EDEVICE_TIMEOUT if a pipeline wait exceeded its limit; the output of
+ * every (row, kv head group) whose pages were skipped, or whose split gave
+ * up waiting, is zero.
  */
 PGD_API int pgd_paged_decode_attention(const pgd_dims* dims, const void* q, const void* k_pool,
                                const void* v_pool, const int32_t* table,
@@ -293,7 +294,10 @@ PGD_API int pgd_paged_decode_step(const pgd_dims* dims, const void* q, const voi
  * one CTA per SM; without a window the blocks are taken longest first) when
  * P >= 8 * table_rows, else the per-token TENSOR_CORE split kernel.
  * Device errors: rows[p] outside [0, table_rows), plus those of
- * pgd_paged_decode_attention; the token's output is zero.
+ * pgd_paged_decode_attention; the token's output is zero.  After
+ * PGD_EDEVICE_TIMEOUT (a pipeline wait gave up) the outputs of the tokens
+ * whose work was abandoned are unspecified: the PREFILL_TILED and
+ * PREFILL_UMMA kernels stop without writing them.
  */
 PGD_API int pgd_paged_prefill_attention(const pgd_dims* dims, int32_t table_rows, const void* q,
                                         const void* k_pool, const void* v_pool,
@@ -345,12 +349,18 @@ PGD_API int pgd_get_device_error(pgd_stream_t stream);
 
 /*
  * Self-test of failure detection, not part of the attention path: launches a
- * one-thread kernel whose two pipeline waits (an mbarrier phase and a shared
+ * one-warp kernel whose two pipeline waits (an mbarrier phase and a shared
  * word, as the decode and prefill kernels use them) are never satisfied.
  * Each gives up after its limit (2 s), so the call takes about 4 s; the
- * kernel records PGD_EDEVICE_TIMEOUT and returns without faulting.
- *   outcome  device int: bit 0 / bit 1 set if the first / second wait was
- *            (wrongly) satisfied; 0 after a correct run.
+ * kernel records PGD_EDEVICE_TIMEOUT and returns without faulting.  It then
+ * runs what a decode split does after such a timeout on a fake row in shared
+ * memory: as a row's only split it must zero the row's outputs, and as one of
+ * two splits it must mark its partials so that the combine's merge gives
+ * zero even though the other split is valid.
+ *   outcome  device int32 [2]: [0] bit 0 / bit 1 set if the first / second
+ *            wait was (wrongly) satisfied; [1] bit 0 set if the only-split
+ *            case left a non-zero output, bit 1 if the merged two-split case
+ *            did.  Both 0 after a correct run.
  * Read the status with pgd_get_device_error; the context stays usable.
  */
 PGD_API int pgd_selftest_bounded_wait(int32_t* outcome, pgd_stream_t stream);

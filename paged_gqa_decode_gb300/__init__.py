@@ -513,15 +513,17 @@ def _decode_rows(q, k_new, v_new, cache_k, cache_v, positions, sinks, window, sc
     return out
 
 
-def selftest_bounded_wait(stream: torch.cuda.Stream | None = None) -> tuple[int, int]:
+def selftest_bounded_wait(stream: torch.cuda.Stream | None = None) -> tuple[int, int, int]:
     """Runs the bounded-wait self-test (about 4 s): returns (device status,
-    outcome bits); a correct run gives (EDEVICE_TIMEOUT, 0)."""
-    outcome = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    wait bits, abandoned-split bits); a correct run gives
+    (EDEVICE_TIMEOUT, 0, 0)."""
+    outcome = torch.full((2,), -1, dtype=torch.int32, device="cuda")
     rc = load_library().pgd_selftest_bounded_wait(_ptr(outcome), _stream_handle(stream))
     if rc != OK:
         raise PgdError(rc, "selftest_bounded_wait")
     status = get_device_error(stream)
-    return status, int(outcome.item())
+    waits, abandoned = outcome.tolist()
+    return status, int(waits), int(abandoned)
 
 
 def get_device_error(stream: torch.cuda.Stream | None = None) -> int:

@@ -131,27 +131,6 @@ cudaError_t launch_rope_append(const RopeAppendParams& p, cudaStream_t stream) {
   return launch_pdl(rope_append_kernel, dim3(p.rows), dim3(256), 0, stream, p);
 }
 
-// Self-test of the pipeline's bounded waits: thread 0 waits on an mbarrier
-// phase that nothing completes and then on a shared word that nothing
-// writes; each wait gives up after its limit, records PGD_EDEVICE_TIMEOUT and
-// returns, exactly as the decode and prefill kernels do.
-__global__ void bounded_wait_selftest_kernel(unsigned int* err, int* outcome) {
-  __shared__ uint64_t bar;
-  __shared__ int word;
-  if (threadIdx.x != 0) return;
-  mbar_init(&bar, 1);
-  mbar_init_fence();
-  word = 0;
-  const bool a = mbar_wait_bounded(&bar, 0, err);  // phase 0 never completes
-  const bool b = wait_seq_bounded(&word, 1, err);   // nobody writes 1
-  outcome[0] = (a ? 1 : 0) | (b ? 2 : 0);
-}
-
-cudaError_t launch_bounded_wait_selftest(unsigned int* err, int* outcome, cudaStream_t stream) {
-  bounded_wait_selftest_kernel<<<1, 32, 0, stream>>>(err, outcome);
-  return cudaGetLastError();
-}
-
 // page_slots for P tokens: one thread per token.
 __global__ void __launch_bounds__(256) page_slots_kernel(const SlotParams p) {
   pdl_wait();

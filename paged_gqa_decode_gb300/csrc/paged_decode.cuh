@@ -464,6 +464,31 @@ struct ScalarConsumer {
 
 // ------------------------------------------------------------------ split kernel
 
+// What a split CTA leaves behind when it gives up on its pages (a table
+// entry outside the pool, or a pipeline wait that timed out): with one split
+// per row it writes zeros as its query heads' outputs; otherwise it marks its
+// partials skipped (m = -inf, l = -1, accumulator zero), and the combine then
+// writes zeros for the row's heads.  Either way nothing the CTA read reaches
+// an output, and no partial a later merge reads is left from another call.
+// Threads tid = 0 .. nthreads - 1 of the caller share the writes.
+template <int D>
+__device__ __forceinline__ void abandon_split(const DecodeParams& p, int b, int h0, int split,
+                                              int nsplit, int tid, int nthreads) {
+  for (int e = tid; e < p.group * D; e += nthreads) {
+    const int g = e / D, d = e % D;
+    const size_t bh = (size_t)b * p.hq + h0 + g;
+    if (nsplit == 1) {
+      p.out[bh * D + d] = 0;
+    } else {
+      p.ws_acc[(bh * p.max_splits + split) * D + d] = 0.f;
+      if (d == 0) {
+        p.ws_ml[(bh * p.max_splits + split) * 2 + 0] = -INFINITY;
+        p.ws_ml[(bh * p.max_splits + split) * 2 + 1] = -1.f;
+      }
+    }
+  }
+}
+
 template <int D, int STAGES, class Consumer, int WARPS = 4>
 struct DecodeCfg {
   static constexpr int kWarps = WARPS;  // consumer warps
@@ -557,20 +582,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, STAGES, Consumer, WARPS>::kThread
   bad = __syncthreads_or(bad);
   if (bad) {
     if (tid == 0) record_error(p.err, PGD_EDEVICE_BOUNDS);
-    for (int e = tid; e < p.group * D; e += C::kThreads) {
-      const int g = e / D, d = e % D;
-      const size_t bh = (size_t)b * p.hq + h0 + g;
-      if (nsplit == 1) {
-        p.out[bh * D + d] = 0;
-      } else {
-        p.ws_acc[(bh * p.max_splits + split) * D + d] = 0.f;
-        if (d == 0) {
-          // l < 0 marks the split as skipped: the combine zeroes the row.
-          p.ws_ml[(bh * p.max_splits + split) * 2 + 0] = -INFINITY;
-          p.ws_ml[(bh * p.max_splits + split) * 2 + 1] = -1.f;
-        }
-      }
-    }
+    abandon_split<D>(p, b, h0, split, nsplit, tid, C::kThreads);
     return;
   }
 
@@ -674,7 +686,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, STAGES, Consumer, WARPS>::kThread
 
   constexpr int kConsumers = C::kWarps * 32;
   named_sync(1, kConsumers);  // all pages consumed; the stages are free
-  if (abort_flag) return;
+  if (abort_flag) {  // a wait timed out (recorded): the split contributes nothing
+    abandon_split<D>(p, b, h0, split, nsplit, tid, kConsumers);
+    return;
+  }
 
   // Merge the warps' states through shared memory (aliasing the stages).
   float* red = reinterpret_cast<float*>(stages);  // [kWarps][GP][D + 2]

@@ -539,7 +539,7 @@ const char* pgd_status_string(int status) {
   }
 }
 
-int pgd_version(void) { return 100; }
+int pgd_version(void) { return 200; }
 
 }  // extern "C"
 

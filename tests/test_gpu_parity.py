@@ -2,10 +2,11 @@
 seeded inputs.  Append indexing must be bit-exact; attention output must be
 within max abs 1e-2 and max rel 2e-2 (bf16 output, fp32 accumulation).
 
-Covers the five workloads (three checked on every row at full size, two at
-full size -- in the launch configuration the benchmark times -- on sampled
-rows), and the edge cases: contexts around page boundaries, window
-boundaries, group sizes 1..8 with padding, head_dim 64 and 128, sink of
+Covers the five workloads at full size: qwen_small, qwen_serve and
+gptoss_full on every row through append + decode; gptoss_sliding and
+mistral_serve on every row through the call the benchmark times (the fused
+decode step) and on sampled rows through append + decode.  And the edge
+cases: contexts around page boundaries, window boundaries, group sizes 1..8 with padding, head_dim 64 and 128, sink of
 -inf / huge / none, shared and reversed page lists, inactive rows, both pool
 layouts, split sizes that force the combine kernel, poisoned (NaN) slots
 outside every attended set, device-side bounds errors, and CUDA graphs."""
@@ -95,6 +96,27 @@ def test_workload_full_size_sampled_rows(name, sample):
     rows |= {int(np.argmax(pos)), int(np.argmin(pos))}
     run_and_check(batch, rows=sorted(rows))
     del batch
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", ["gptoss_sliding", "mistral_serve"])
+def test_workload_full_size_every_row_decode_step(name):
+    """The call the benchmark times, at full size and in its launch
+    configuration: paged_decode_step (the append inside the decode launch,
+    split size chosen by the library, the workload's window and sinks),
+    checked on every row against the oracle's write_tokens + paged_attention
+    over a host copy of the pool taken before the step."""
+    wl = WORKLOADS[name]
+    batch = make_batch(wl, seed=1000 + list(WORKLOADS).index(name), device=DEV)
+    rows = np.arange(wl.rows)
+    host = snapshot_rows(batch, rows)
+    got = pgd.paged_decode_step(batch.q, batch.k_new, batch.v_new, batch.k_pool, batch.v_pool,
+                                batch.table, batch.positions, batch.sinks, wl.window, wl.scale,
+                                num_kv_heads=wl.kv_heads)
+    assert pgd.get_device_error() == pgd.OK
+    want, _, _ = oracle_step(batch, host, window=wl.window, sinks=batch.sinks, scale=wl.scale)
+    compare(got, want, f"{name}: decode step, every row")
+    del batch, host
     torch.cuda.empty_cache()
 
 
@@ -423,10 +445,14 @@ def test_cuda_graph_replay_matches_eager():
 
 def test_bounded_waits_time_out_into_an_error_and_the_context_survives():
     """A pipeline wait that nothing satisfies gives up after its limit and
-    reports PGD_EDEVICE_TIMEOUT; no fault, and a normal step works after."""
-    status, outcome = pgd.selftest_bounded_wait()
+    reports PGD_EDEVICE_TIMEOUT; no fault, and a normal step works after.
+    The self-test also runs a decode split's give-up path after the timeout:
+    a row's only split must leave zeros, and a split abandoned beside a valid
+    one must make the combine's merge give zeros (no stale partial used)."""
+    status, waits, abandoned = pgd.selftest_bounded_wait()
     assert status == pgd.EDEVICE_TIMEOUT
-    assert outcome == 0
+    assert waits == 0
+    assert abandoned == 0
     wl = WORKLOADS["qwen_small"]
     batch = make_batch(wl, seed=1000, device=DEV)
     run_and_check(batch)
