@@ -101,9 +101,13 @@ typedef struct {
 /* Kernel variants.  All compute the same function; they differ in where the
  * per-page Q.K^T and P.V products run and in how tokens share page loads. */
 enum {
-  PGD_KERNEL_AUTO = 0,          /* decode: TENSOR_CORE; prefill: PREFILL_UMMA when
-                                   the tokens average at least 8 per table row
-                                   (prompt chunks), else TENSOR_CORE */
+  PGD_KERNEL_AUTO = 0,          /* decode: windows of 1..128 positions go to the
+                                   window kernel (one CTA per row and kv head
+                                   copies exactly the window's K/V rows; mma.sync
+                                   products; no splits), anything else to
+                                   TENSOR_CORE; prefill: PREFILL_UMMA when the
+                                   tokens average at least 8 per table row
+                                   (prompt chunks), else as decode, per token */
   PGD_KERNEL_TENSOR_CORE = 1,   /* mma.sync bf16 products, fp32 accumulate, per token,
                                    key range split over CTAs + combine */
   PGD_KERNEL_CUDA_CORE = 2,     /* fp32 FMA products on the CUDA cores, per token */
@@ -209,7 +213,8 @@ PGD_API size_t pgd_paged_decode_workspace_bytes(const pgd_dims* dims, const pgd_
  *   table_rows  0 for pgd_paged_decode_attention; the table_rows argument of
  *               pgd_paged_prefill_attention (> 0) for a prefill call.
  *   window, opts  as passed to that call.
- *   count       out: 0 when dims->rows == 0; for PREFILL_UMMA 2 without a
+ *   count       out: 0 when dims->rows == 0; 1 for AUTO with a window of
+ *               1..128 positions (the window kernel); for PREFILL_UMMA 2 without a
  *               window when the tokens form at most 4096 blocks of
  *               2 x (128 / group) (a pass that orders the blocks longest
  *               first, then the prefill kernel), else 1 (the kernel, after

@@ -164,27 +164,30 @@ struct MmaConsumer {
     }
   }
 
-  // One page: kt is the shared address of its K tile, vt_ptr its V tile,
-  // valid rows [rlo, rhi].  Returns true if it wrote zeros into the V tile.
+  // One page (NT = 4: 64 rows), or NT / 4 of one (the window kernel's
+  // 32-row slices): kt is the shared address of its K rows, vt_ptr its V
+  // rows, valid rows [rlo, rhi].  Returns true if it wrote zeros into V.
+  template <int NT = 4>
   __device__ bool page(uint32_t kt, unsigned char* vt_ptr, int rlo, int rhi, int lane) {
+    static_assert(NT == 2 || NT == 4, "row tiles");
     const uint32_t vt = smem_addr(vt_ptr);
-    float s[4][4];
+    float s[NT][4];
 #pragma unroll
-    for (int t = 0; t < 4; ++t)
+    for (int t = 0; t < NT; ++t)
 #pragma unroll
       for (int e = 0; e < 4; ++e) s[t][e] = 0.f;
 #pragma unroll
     for (int kk = 0; kk < kSteps; ++kk)
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
+      for (int t = 0; t < NT; ++t) {
         uint32_t a0, a1, a2, a3;
         ldsm_x4(kt + (kk >> 2) * kBoxBytes + t * 2048 + off_k[kk & 3], a0, a1, a2, a3);
         mma_bf16(s[t], a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
       }
 
-    const bool full = rlo == 0 && rhi == kPage - 1;
+    const bool full = rlo == 0 && rhi == 16 * NT - 1;
 #pragma unroll
-    for (int t = 0; t < 4; ++t)
+    for (int t = 0; t < NT; ++t)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int row = 16 * t + gid + ((e & 2) ? 8 : 0);
@@ -193,7 +196,7 @@ struct MmaConsumer {
       }
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
+    for (int t = 0; t < NT; ++t) {
       mx0 = fmaxf(mx0, fmaxf(s[t][0], s[t][2]));
       mx1 = fmaxf(mx1, fmaxf(s[t][1], s[t][3]));
     }
@@ -211,9 +214,9 @@ struct MmaConsumer {
     // (p = hi + lo to ~2^-17 relative) so the products keep fp32-level
     // accuracy: one bf16 rounding of p alone would err by up to 2^-9 of
     // sum_j p_j |v_j|, far more than an output near cancellation allows.
-    uint32_t pb[4][2], pl[4][2];
+    uint32_t pb[NT][2], pl[NT][2];
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
+    for (int t = 0; t < NT; ++t) {
       s[t][0] = exp2_approx(s[t][0] - ref0);
       s[t][1] = exp2_approx(s[t][1] - ref1);
       s[t][2] = exp2_approx(s[t][2] - ref0);
@@ -246,7 +249,7 @@ struct MmaConsumer {
     if (!full) {  // zero the V rows outside [rlo, rhi]
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
+      for (int half = 0; half < NT / 2; ++half) {
         const int row = lane + 32 * half;
         if (row < rlo || row > rhi) {
 #pragma unroll
@@ -262,7 +265,7 @@ struct MmaConsumer {
 #pragma unroll
     for (int mt = 0; mt < kSteps; ++mt)
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
+      for (int t = 0; t < NT; ++t) {
         uint32_t a0, a1, a2, a3;
         ldsm_x4_trans(vt + (mt >> 2) * kBoxBytes + t * 2048 + off_v[mt & 3], a0, a1, a2, a3);
         mma_bf16(o[mt], a0, a1, a2, a3, pb[t][0], pb[t][1]);
@@ -837,6 +840,232 @@ __global__ void __launch_bounds__(128) paged_decode_combine_kernel(const DecodeP
                     p.ws_acc + bh * p.max_splits * D + lane * kDims, D, nsplit, sk, o, lane);
 }
 
+// ------------------------------------------------------------------ window kernel
+
+// 16-byte copy global -> shared that bypasses the registers (and L1);
+// `bytes` 0 writes 16 zero bytes and reads nothing.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Sliding-window decode for windows of at most 64 * TILES positions
+// (GPT-OSS 20B model files, src/attention.linnet, SinkAttention.decode_rows:
+// key s is seen when n - window < s <= n).  One CTA per (kv head, row)
+// attends over exactly the window's positions, wherever they fall in the
+// row's pages, so no byte outside the window is read and no split or
+// combine is needed.  Local row r holds position lo + r; warp w owns local
+// rows 32 w .. 32 w + 31: it reads the row's position and the table entries
+// itself, copies its rows of K and V, 16 bytes per lane at a time, straight
+// into shared memory (cp.async; rows past the attended count are
+// zero-filled), waits for its own copies only and runs the tensor-core
+// consumer on them, so each warp computes as soon as its slice has landed.
+// The rows land in the layout a TMA page tile has (64-row tiles of
+// 128-byte-swizzled 64-value boxes), which the consumer reads.  The warps
+// merge through shared memory after one barrier: each thread owns a run of
+// one head's output dims, forms that head's weight per warp (its running max
+// against the overall one and the sink, over the total denominator) and
+// stores its run with 8- or 16-byte writes.
+//
+// Decode step (the append fused in): the new token's row (position n, the
+// window's last) is copied from k_new / v_new instead of the pool, and
+// stored into the pool at its slot by the warp owning that row, so the
+// kernel never reads the slot back.
+template <int D, int TILES>
+struct WindowCfg {
+  static constexpr int kWarps = 2 * TILES;  // one warp per 32 rows
+  static constexpr int kThreads = 32 * kWarps;
+  static constexpr int kChunks = D / 8;                // 16-byte chunks per row
+  static constexpr int kRowStep = 32 / kChunks;        // rows one warp pass covers
+  static constexpr int kPasses = 32 / kRowStep;
+  static constexpr int kTileBytes = kPage * D * 2;     // 64 rows of K (or V)
+  static constexpr int kBytes = TILES * kTileBytes;    // the window's K (or V)
+  static constexpr int kSmemBytes = 2 * kBytes;
+  static constexpr int kMinBlocks = (228 * 1024) / (kSmemBytes + 1024);
+  static constexpr int kHeads = MmaConsumer<D>::kHeads;
+  static constexpr int kPerThread = kHeads * D / kThreads;  // output dims per thread
+  static constexpr int kRun = kPerThread >= 8 ? 8 : 4;      // dims per store
+  static_assert(kPerThread % kRun == 0 && D % kPerThread == 0, "output runs");
+  static_assert(kWarps * kHeads * (D + 2) * 4 <= kBytes, "merge buffer");
+};
+
+template <int D, int TILES>
+__global__ void __launch_bounds__(WindowCfg<D, TILES>::kThreads, WindowCfg<D, TILES>::kMinBlocks)
+    paged_decode_window_kernel(const DecodeParams p) {
+  using C = WindowCfg<D, TILES>;
+  using Consumer = MmaConsumer<D>;
+  constexpr int GP = C::kHeads;
+  pdl_wait();
+  pdl_allow_dependents();
+  const int kvh = blockIdx.x;
+  const int b = blockIdx.y;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int h0 = kvh * p.group;
+  // the output run this thread merges and stores: head g, dims d0 ..
+  const int g = tid / (D / C::kPerThread);
+  const int d0 = (tid % (D / C::kPerThread)) * C::kPerThread;
+  const bool live = g < p.group;
+  const float sink = (p.sinks && live) ? p.sinks[h0 + g] * kLog2e : -INFINITY;
+  uint16_t* out = p.out + ((size_t)b * p.hq + h0 + (live ? g : 0)) * D + d0;
+  auto zero_run = [&]() {
+    if (live)
+#pragma unroll
+      for (int k = 0; k < C::kPerThread; k += 4)
+        *reinterpret_cast<uint2*>(out + k) = make_uint2(0u, 0u);
+  };
+  const int n = p.positions[b];
+  const int table_row = p.row_of ? p.row_of[b] : b;
+  if (n < 0) {  // inactive row
+    zero_run();
+    return;
+  }
+  if (n / kPage >= p.maxp || (p.row_of && (table_row < 0 || table_row >= p.table_rows))) {
+    zero_run();
+    if (kvh == 0 && tid == 0) record_error(p.err, PGD_EDEVICE_BOUNDS);
+    return;
+  }
+  const int lo = n - p.window + 1 > 0 ? n - p.window + 1 : 0;
+  const int cnt = n - lo + 1;  // attended positions, at most 64 * TILES
+  const int first_page = lo / kPage;
+  const int npages = n / kPage - first_page + 1;  // at most TILES + 1
+  // The window's table entries: lane k of every warp loads entry k (every
+  // warp reaches the same verdict).
+  int pg = 0;
+  if (lane < npages) pg = page_of(p.table, table_row, first_page + lane, p.maxp);
+  if (__any_sync(0xffffffffu, lane < npages && (pg < 0 || pg >= p.num_pages))) {
+    zero_run();
+    if (tid == 0) record_error(p.err, PGD_EDEVICE_BOUNDS);
+    return;
+  }
+
+  Consumer cons;
+  cons.init(p, b, h0, lane, nullptr);  // q fragments load while the rows copy
+
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* ks = smem_raw;
+  unsigned char* vs = smem_raw + C::kBytes;
+  const bool append = p.k_new != nullptr;
+  const int c = lane % C::kChunks;  // this lane's 16-byte column
+  // element offset of column c of position 64 k of the window's page k
+  size_t page_base[TILES + 1];
+#pragma unroll
+  for (int k = 0; k <= TILES; ++k)
+    page_base[k] = (size_t)tile_first_row(p.layout, __shfl_sync(0xffffffffu, pg, k), kvh, p.hkv,
+                                          p.num_pages, p.maxp) * D + 8 * c;
+  auto pool_at = [&](int s) {
+    const int k = (s >> 6) - first_page;
+    size_t at = page_base[0];
+#pragma unroll
+    for (int q = 1; q <= TILES; ++q)
+      if (k == q) at = page_base[q];
+    return at + (size_t)(s & (kPage - 1)) * D;
+  };
+  const size_t new_at = ((size_t)b * p.hkv + kvh) * D + 8 * c;
+  const int row0 = 32 * warp + lane / C::kChunks;
+  const int col = (c / 8) * kBoxBytes;
+#pragma unroll
+  for (int j = 0; j < C::kPasses; ++j) {
+    const int r = row0 + j * C::kRowStep;
+    const int s = lo + r;
+    const size_t at = pool_at(s);
+    const bool here = r < cnt;
+    const bool fresh = append && s == n;
+    const int off = (r >> 6) * C::kTileBytes + col + (r & (kPage - 1)) * 128 +
+                    (((c & 7) ^ (r & 7)) << 4);
+    cp_async16(ks + off, !here ? (const void*)p.k_read : fresh ? (const void*)(p.k_new + new_at)
+                                                              : (const void*)(p.k_read + at),
+               here ? 16u : 0u);
+    cp_async16(vs + off, !here ? (const void*)p.v_read : fresh ? (const void*)(p.v_new + new_at)
+                                                              : (const void*)(p.v_read + at),
+               here ? 16u : 0u);
+  }
+  if (append && (cnt - 1) / 32 == warp && lane < C::kChunks) {  // the new token into the pool
+    const size_t at = pool_at(n);
+    *reinterpret_cast<uint4*>(p.k_pool + at) = *reinterpret_cast<const uint4*>(p.k_new + new_at);
+    *reinterpret_cast<uint4*>(p.v_pool + at) = *reinterpret_cast<const uint4*>(p.v_new + new_at);
+  }
+  cp_async_wait_all();
+  __syncwarp();
+
+  const int rhi = min(cnt - 1 - 32 * warp, 31);
+  if (rhi >= 0) {
+    const int slice = (warp >> 1) * C::kTileBytes + (warp & 1) * 32 * 128;
+    cons.template page<2>(smem_addr(ks + slice), vs + slice, 0, rhi, lane);
+  }
+  cons.finish();
+  __syncthreads();  // every warp is done with the rows
+
+  float* red = reinterpret_cast<float*>(ks);  // [kWarps][GP][D + 2]
+  cons.store(red, warp, lane);
+  __syncthreads();
+  if (!live) return;
+  float mx = sink, f[C::kWarps];
+#pragma unroll
+  for (int w = 0; w < C::kWarps; ++w) {
+    f[w] = red[(w * GP + g) * (D + 2) + D];
+    mx = fmaxf(mx, f[w]);
+  }
+  float total = exp2_approx(sink - mx);
+#pragma unroll
+  for (int w = 0; w < C::kWarps; ++w) {
+    f[w] = exp2_approx(f[w] - mx);  // a warp without rows: m = -inf -> 0
+    total = fmaf(red[(w * GP + g) * (D + 2) + D + 1], f[w], total);
+  }
+  const float inv = 1.f / total;
+#pragma unroll
+  for (int w = 0; w < C::kWarps; ++w) f[w] *= inv;
+  constexpr int R = C::kRun;
+#pragma unroll
+  for (int k = 0; k < C::kPerThread; k += R) {
+    float a[R];
+#pragma unroll
+    for (int e = 0; e < R; ++e) a[e] = 0.f;
+#pragma unroll
+    for (int w = 0; w < C::kWarps; ++w) {
+      const float* rw = red + (w * GP + g) * (D + 2) + d0 + k;
+#pragma unroll
+      for (int e = 0; e < R; e += 2) {
+        const float2 v = *reinterpret_cast<const float2*>(rw + e);
+        a[e] = fmaf(v.x, f[w], a[e]);
+        a[e + 1] = fmaf(v.y, f[w], a[e + 1]);
+      }
+    }
+    if constexpr (R == 8)
+      *reinterpret_cast<uint4*>(out + k) =
+          make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
+                     pack_bf16x2(a[6], a[7]));
+    else
+      *reinterpret_cast<uint2*>(out + k) = make_uint2(pack_bf16x2(a[0], a[1]),
+                                                      pack_bf16x2(a[2], a[3]));
+  }
+}
+
+template <int D, int TILES>
+cudaError_t launch_window(const DecodeParams& p, cudaStream_t stream) {
+  using C = WindowCfg<D, TILES>;
+  auto kern = paged_decode_window_kernel<D, TILES>;
+  static std::atomic<bool> configured[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured[dev].store(true, std::memory_order_release);
+  }
+  if (p.rows == 0) return cudaSuccess;
+  return launch_pdl(kern, dim3(p.hkv, p.rows), dim3(C::kThreads), C::kSmemBytes, stream, p);
+}
+
 template <int D, int STAGES, class Consumer, int WARPS = 4>
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& k_map,
                           const CUtensorMap& v_map, int grid_splits, cudaStream_t stream) {
@@ -877,6 +1106,8 @@ cudaError_t launch_decode_for_dim(const DecodeParams& p, const CUtensorMap& k_ma
                                   const CUtensorMap& v_map, int padded, int kernel,
                                   int grid_splits, int pages_per_cta, cudaStream_t stream) {
   constexpr int kStages = D == 128 ? 3 : 6;
+  if (kernel == PGD_KERNEL_AUTO && p.window > 0 && p.window <= kMaxWindowKernel)
+    return p.window <= kPage ? launch_window<D, 1>(p, stream) : launch_window<D, 2>(p, stream);
   if (kernel != PGD_KERNEL_CUDA_CORE) {
     // A ring no deeper than the pages a split can stream: shallower rings let
     // more CTAs share an SM when splits are short (windows, small contexts).

@@ -370,6 +370,8 @@ int pgd_attention_kernel_count(const pgd_dims* dims, int32_t table_rows, int32_t
     *count = prefill_umma_launches(dims->rows, dims->num_q_heads / dims->num_kv_heads, window);
   } else if (kernel == PGD_KERNEL_PREFILL_TILED) {
     *count = 1;
+  } else if (kernel == PGD_KERNEL_AUTO && window > 0 && window <= kMaxWindowKernel) {
+    *count = 1;  // the window kernel
   } else {
     const int pages = span_pages(dims, window > 0 ? window : 0);
     *count = (pages + pl.pages_per_split - 1) / pl.pages_per_split > 1 ? 2 : 1;
@@ -444,6 +446,8 @@ static int decode_impl(const pgd_dims* dims, int32_t table_rows, const int32_t* 
   p.v_new = static_cast<const uint16_t*>(v_new);
   p.k_pool = k_new ? static_cast<uint16_t*>(const_cast<void*>(k_pool)) : nullptr;
   p.v_pool = k_new ? static_cast<uint16_t*>(const_cast<void*>(v_pool)) : nullptr;
+  p.k_read = static_cast<const uint16_t*>(k_pool);
+  p.v_read = static_cast<const uint16_t*>(v_pool);
 
   const int grid_pages = span_pages(dims, p.window);
   const int grid_splits = (grid_pages + pl.pages_per_split - 1) / pl.pages_per_split;

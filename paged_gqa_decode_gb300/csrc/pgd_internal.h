@@ -63,7 +63,14 @@ struct DecodeParams {
   const uint16_t* v_new;
   uint16_t* k_pool;
   uint16_t* v_pool;
+  // the pools for plain loads (the window kernel reads rows, not page tiles)
+  const uint16_t* k_read;
+  const uint16_t* v_read;
 };
+
+// With PGD_KERNEL_AUTO, decode windows of 1 .. kMaxWindowKernel positions go
+// to the window kernel (one CTA per row and kv head, no splits).
+constexpr int kMaxWindowKernel = 128;
 
 // Padded query-group sizes that have a decode kernel instantiation.
 int padded_group(int group);  // 0 if unsupported

@@ -179,12 +179,34 @@ def test_sink_values(kind, d):
 @pytest.mark.parametrize("window", [0, 100])
 def test_split_sizes_force_the_combine(pps, window):
     """Rows of 1 to 24 pages cut into 1 to 24 splits (with the window, up to
-    3), merged by the combine kernel; one split writes directly."""
+    3), merged by the combine kernel; one split writes directly.  The split
+    kernel is asked for by name: with a window of at most 128 positions AUTO
+    takes the window kernel, which has no splits."""
     wl = Workload("splits", rows=5, q_heads=16, kv_heads=4, head_dim=64, ctx_lo=1, ctx_hi=1500,
                   sinks=True)
     lay = layout_from_contexts(wl, [1500, 1, 640, 641, 1000], seed=9)
     batch = make_batch(wl, seed=51, device=DEV, layout=lay)
-    run_and_check(batch, window=window, pages_per_split=pps, what=f"pps={pps}")
+    run_and_check(batch, window=window, pages_per_split=pps, kernel=pgd.KERNEL_TENSOR_CORE,
+                  what=f"pps={pps}")
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(14, 2, 64), (64, 8, 64), (32, 8, 128), (6, 3, 128)])
+@pytest.mark.parametrize("window", [1, 64, 65, 127, 128])
+@pytest.mark.parametrize("pps", [0, 1])
+def test_split_kernel_windows(hq, hkv, d, window, pps):
+    """Windows of at most 128 positions through the split kernel (asked for by
+    name), as AUTO sends them to the window kernel.  V is scaled by 1/4
+    (exact in bf16): with a window of one position an output is a single V
+    row, and above |out| = 2.56 rounding to bf16 alone can exceed the 1e-2
+    absolute bound."""
+    wl = Workload("edge_split", rows=len(EDGE_CONTEXTS), q_heads=hq, kv_heads=hkv, head_dim=d,
+                  ctx_lo=1, ctx_hi=700, sinks=True)
+    lay = layout_from_contexts(wl, EDGE_CONTEXTS, seed=hq + d + window + 3)
+    batch = make_batch(wl, seed=33 + window, device=DEV, layout=lay)
+    batch.v_pool.mul_(0.25)
+    batch.v_new.mul_(0.25)
+    run_and_check(batch, window=window, pages_per_split=pps, kernel=pgd.KERNEL_TENSOR_CORE,
+                  what=f"split kernel hq={hq} d={d} w={window} pps={pps}")
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -214,10 +236,11 @@ def test_shared_prefix_and_reversed_pages(pps):
     run_and_check(batch, pages_per_split=pps)
 
 
-@pytest.mark.parametrize("pps", [0, 2])
-def test_poisoned_slots_outside_attention_are_never_read(pps):
+@pytest.mark.parametrize("pps,kernel", [(0, pgd.KERNEL_AUTO), (0, pgd.KERNEL_TENSOR_CORE),
+                                        (2, pgd.KERNEL_TENSOR_CORE)])
+def test_poisoned_slots_outside_attention_are_never_read(pps, kernel):
     """Every pool position no row attends to holds NaN: any read of it that
-    reached the result would show."""
+    reached the result would show (window kernel and split kernel)."""
     wl = Workload("poison", rows=6, q_heads=8, kv_heads=2, head_dim=128, ctx_lo=1, ctx_hi=600,
                   sinks=True)
     window = 70
@@ -232,7 +255,7 @@ def test_poisoned_slots_outside_attention_are_never_read(pps):
         view = pool.view(lay.num_pages, wl.kv_heads, 64, wl.head_dim)
         mask = nan_slots.view(lay.num_pages, 1, 64, 1).expand_as(view)
         view.masked_fill_(mask, float("nan"))
-    run_and_check(batch, window=window, pages_per_split=pps)
+    run_and_check(batch, window=window, pages_per_split=pps, kernel=kernel)
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -306,9 +329,16 @@ def test_kernel_count_follows_the_split_plan():
     assert pgd.attention_kernel_count(dims(w["qwen_serve"], 10)) == 1
     assert pgd.attention_kernel_count(dims(w["gptoss_full"], 64)) == 2       # 3 splits
     assert pgd.attention_kernel_count(dims(w["mistral_serve"], 512)) == 2    # 8 splits
+    # windows of at most 128 positions: the window kernel alone (AUTO)
     assert pgd.attention_kernel_count(dims(w["gptoss_sliding"], 512), window=128) == 1
     assert pgd.attention_kernel_count(dims(w["gptoss_sliding"], 512), window=128,
-                                      pages_per_split=1) == 2                # 3 splits
+                                      pages_per_split=1) == 1
+    assert pgd.attention_kernel_count(dims(w["gptoss_sliding"], 512), window=128,
+                                      pages_per_split=1,
+                                      kernel=pgd.KERNEL_TENSOR_CORE) == 2    # 3 splits
+    assert pgd.attention_kernel_count(dims(w["gptoss_sliding"], 512), window=129) == 1
+    assert pgd.attention_kernel_count(dims(w["gptoss_sliding"], 512), window=129,
+                                      pages_per_split=1) == 2
     assert pgd.attention_kernel_count(dims(w["qwen_serve"], 10), pages_per_split=10) == 1
     assert pgd.attention_kernel_count(dims(w["qwen_serve"], 10), pages_per_split=9) == 2
     assert pgd.attention_kernel_count(dims(w["qwen_serve"], 10),
@@ -381,6 +411,34 @@ def test_bad_table_entries_in_every_split(pps):
     assert pgd.get_device_error() == pgd.EDEVICE_BOUNDS
     assert torch.all(out[0] == 0) and torch.any(out[1] != 0) and torch.any(out[2] != 0)
     run_and_check(batch, pages_per_split=pps, what=f"after bounds errors, pps {pps}")
+
+
+def test_window_kernel_reads_only_the_window_table_entries():
+    """Window kernel: a bad table entry inside a row's window zeroes that row
+    and is reported; a bad entry outside every window is never read."""
+    wl = Workload("bounds_window", rows=3, q_heads=16, kv_heads=2, head_dim=64, ctx_lo=1,
+                  ctx_hi=600, sinks=True)
+    lay = layout_from_contexts(wl, [600, 300, 100], seed=23)
+    batch = make_batch(wl, seed=104, device=DEV, layout=lay)
+    host = snapshot_rows(batch, [1, 2])
+    pgd.kv_append_paged(batch.k_new, batch.v_new, batch.table, batch.positions, batch.k_pool,
+                        batch.v_pool)
+    assert pgd.get_device_error() == pgd.OK
+    table = batch.table.clone()
+    table[1, 0] = 10 ** 6      # row 1 (n = 299): page 0 lies outside its window 200..299
+    out = pgd.paged_decode_attention(batch.q, batch.k_pool, batch.v_pool, table,
+                                     batch.positions, batch.sinks, 100, wl.scale,
+                                     num_kv_heads=wl.kv_heads)
+    assert pgd.get_device_error() == pgd.OK
+    table[0, 9] = -1           # row 0 (n = 599): its window's last page
+    out_bad = pgd.paged_decode_attention(batch.q, batch.k_pool, batch.v_pool, table,
+                                         batch.positions, batch.sinks, 100, wl.scale,
+                                         num_kv_heads=wl.kv_heads)
+    assert pgd.get_device_error() == pgd.EDEVICE_BOUNDS
+    assert torch.all(out_bad[0] == 0)
+    assert torch.equal(out_bad[1:], out[1:])
+    want, _, _ = oracle_step(batch, host, window=100, sinks=batch.sinks, scale=wl.scale)
+    compare(out[1:], want, "window kernel, rows beside bad entries")
 
 
 def test_host_validation():

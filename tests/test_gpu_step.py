@@ -56,12 +56,15 @@ def test_step_workloads(name):
 @pytest.mark.parametrize("layout", [pgd.PAGE_MAJOR, pgd.HEAD_MAJOR])
 def test_step_edges(hq, hkv, d, window, pps, layout):
     """Contexts around page boundaries and an inactive row; with pps 1 or 3
-    the new token's page is the last of several splits."""
+    the split kernel is asked for by name and the new token's page is the
+    last of several splits; with pps 0 (AUTO) windows go to the window
+    kernel, which takes the new token from k_new / v_new."""
     wl = Workload("step", rows=8, q_heads=hq, kv_heads=hkv, head_dim=d, ctx_lo=1, ctx_hi=700,
                   sinks=True)
     lay = layout_from_contexts(wl, [1, 63, 64, 65, 0, 129, 256, 700], seed=hq + d + window)
     batch = make_batch(wl, seed=41 + pps, device=DEV, layout=lay)
-    both(batch, window=window, sinks=batch.sinks, layout=layout, pps=pps)
+    kernel = pgd.KERNEL_AUTO if pps == 0 else pgd.KERNEL_TENSOR_CORE
+    both(batch, window=window, sinks=batch.sinks, layout=layout, pps=pps, kernel=kernel)
 
 
 @pytest.mark.parametrize("d", [64, 128])
