@@ -54,6 +54,34 @@ FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2 ** 20
 
 
+class PackedInputs:
+    """A step's inputs in one pinned host buffer and one device buffer, each
+    tensor at a 256-byte-aligned offset, so that one copy uploads them all
+    (as a serving loop would send a step's inputs); `views` are the device
+    tensors the API is called with.  Several device buffers can share one
+    host buffer (`host`)."""
+
+    def __init__(self, tensors: dict, device, host=None):
+        offs, total = {}, 0
+        for k, t in tensors.items():
+            n = t.numel() * t.element_size()
+            offs[k] = (total, n)
+            total = (total + n + 255) // 256 * 256
+        if host is None:
+            host = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+            for k, t in tensors.items():
+                o, n = offs[k]
+                host[o:o + n].copy_(t.detach().cpu().reshape(-1).view(torch.uint8))
+        self.host = host
+        self.dev = torch.empty(total, dtype=torch.uint8, device=device)
+        self.views = {k: self.dev[o:o + n].view(t.dtype).view(t.shape)
+                      for k, t in tensors.items() for o, n in [offs[k]]}
+        self.bytes = total
+
+    def upload(self):
+        self.dev.copy_(self.host, non_blocking=True)
+
+
 class L2Flush:
     """Between timed steps: write a 1 GiB buffer (evicting everything the step
     left in L2), then read a 512 MiB one, so that L2 holds clean lines of an
@@ -523,21 +551,39 @@ def measure_decode(args, wl: Workload, world: int, rank: int, device, main: bool
     value = total_bytes / (step_ms * 1e-3) / 1e9
 
     # End to end through the public API with host buffers: per step the
-    # inputs go host -> device from pinned memory, the output comes back.
-    host_in = {k: getattr(batch, k).cpu().pin_memory() for k in ("q", "k_new", "v_new")}
-    host_in["table"] = batch.table.cpu().pin_memory()
-    host_in["positions"] = batch.positions.cpu().pin_memory()
-    if batch.sinks is not None:
-        host_in["sinks"] = batch.sinks.cpu().pin_memory()
+    # inputs go host -> device from pinned memory (packed in one buffer, one
+    # copy), the step runs on them, and the output comes back.
+    names = ["q", "k_new", "v_new", "table", "positions"] + (
+        ["sinks"] if batch.sinks is not None else [])
+    packed = PackedInputs({k: getattr(batch, k) for k in names}, device)
     host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    h2d = packed.bytes
     d2h = host_out.numel() * host_out.element_size()
 
+    def run_step(inp, o):
+        """One step on the input tensors `inp`, output into `o`."""
+        kw = dict(num_kv_heads=wl.kv_heads, out=o, workspace=ws,
+                  pages_per_split=args.pages_per_split, kernel=KERNEL_IDS[args.kernel])
+        if fused:
+            pgd.paged_decode_step(inp["q"], inp["k_new"], inp["v_new"], batch.k_pool,
+                                  batch.v_pool, inp["table"], inp["positions"], inp.get("sinks"),
+                                  wl.window, wl.scale, **kw)
+            return
+        qq = inp["q"]
+        if args.rope:
+            q_rot.copy_(inp["q"])
+            pgd.rope_append_paged(q_rot, inp["k_new"], inp["v_new"], inp["table"],
+                                  inp["positions"], batch.k_pool, batch.v_pool, theta=1e6)
+            qq = q_rot
+        else:
+            pgd.kv_append_paged(inp["k_new"], inp["v_new"], inp["table"], inp["positions"],
+                                batch.k_pool, batch.v_pool)
+        pgd.paged_decode_attention(qq, batch.k_pool, batch.v_pool, inp["table"],
+                                   inp["positions"], inp.get("sinks"), wl.window, wl.scale, **kw)
+
     def e2e_step():
-        for k, t in host_in.items():
-            getattr(batch, k).copy_(t, non_blocking=True)
-        append()
-        decode()
+        packed.upload()
+        run_step(packed.views, out)
         host_out.copy_(out, non_blocking=True)
 
     # Back-to-back steps (inputs larger than L2) are pipelined as a serving
@@ -547,7 +593,8 @@ def measure_decode(args, wl: Workload, world: int, rank: int, device, main: bool
     # region.  (Steps between L2 flushes run one at a time.)
     pipelined = flush is None and fused
     if pipelined:
-        dev_in = [{k: torch.empty_like(getattr(batch, k)) for k in host_in} for _ in range(2)]
+        bufs = [packed, PackedInputs({k: getattr(batch, k) for k in names}, device,
+                                     host=packed.host)]
         outs = [torch.empty_like(out) for _ in range(2)]
         copy = torch.cuda.Stream(device)
         ready = [torch.cuda.Event() for _ in range(2)]   # inputs of buffer j are up
@@ -556,18 +603,12 @@ def measure_decode(args, wl: Workload, world: int, rank: int, device, main: bool
         def upload(j):
             with torch.cuda.stream(copy):
                 copy.wait_event(freed[j])
-                for k, t in host_in.items():
-                    dev_in[j][k].copy_(t, non_blocking=True)
+                bufs[j].upload()
                 ready[j].record(copy)
 
         def compute(j):
-            inp = dev_in[j]
             stream.wait_event(ready[j])
-            pgd.paged_decode_step(inp["q"], inp["k_new"], inp["v_new"], batch.k_pool,
-                                  batch.v_pool, inp["table"], inp["positions"], inp.get("sinks"),
-                                  wl.window, wl.scale, num_kv_heads=wl.kv_heads, out=outs[j],
-                                  workspace=ws, pages_per_split=args.pages_per_split,
-                                  kernel=KERNEL_IDS[args.kernel])
+            run_step(bufs[j].views, outs[j])
             freed[j].record(stream)
 
         def download(j):
@@ -656,16 +697,17 @@ def measure_decode(args, wl: Workload, world: int, rank: int, device, main: bool
         "decode_ms_per_step": decode_ms / args.steps,
         "bytes_per_step_per_gpu": by,
         "roofline": {"bound": "hbm",
-                     "kernel": "paged_decode_step (split kernel with the append, + combine)"
-                     if fused else "paged_decode (split + combine kernels)",
+                     "kernel": "paged_decode_step (the decode call with the append fused in)"
+                     if fused else "paged_decode_attention (the decode call)",
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak,
                      "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
                      "traffic": traffic, "algorithmic_bytes_per_launch": call_bytes},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps,
-                "copies": "overlapped with the neighbouring steps' compute (two buffer sets)"
-                if pipelined else "in line with each step"},
+                "copies": ("inputs packed in one pinned buffer, one upload per step; "
+                           + ("overlapped with the neighbouring steps' compute (two buffer sets)"
+                              if pipelined else "in line with each step"))},
         "gpu_launches": ((0 if fused else 1) + pgd.attention_kernel_count(
             dims, 0, wl.window, args.pages_per_split, KERNEL_IDS[args.kernel])) * args.steps,
         "clocks": clk,
