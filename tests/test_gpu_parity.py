@@ -294,7 +294,8 @@ def test_scores_rise_every_page(d, pps):
 
 
 @pytest.mark.parametrize("pps", [0, 1])   # one split (written directly); two (combined)
-def test_inactive_rows_are_zero_and_untouched(pps):
+@pytest.mark.parametrize("window", [0, 64, 100])   # split kernel; window kernel (1 and 2 tiles)
+def test_inactive_rows_are_zero_and_untouched(pps, window):
     wl = Workload("inactive", rows=4, q_heads=4, kv_heads=1, head_dim=64, ctx_lo=1, ctx_hi=128)
     lay = layout_from_contexts(wl, [0, 100, 0, 1], seed=17, num_pages=6)
     batch = make_batch(wl, seed=91, device=DEV, layout=lay)
@@ -302,11 +303,11 @@ def test_inactive_rows_are_zero_and_untouched(pps):
                         batch.v_pool)
     out = torch.full_like(batch.q, 7.0)          # every output must be written
     out = pgd.paged_decode_attention(batch.q, batch.k_pool, batch.v_pool, batch.table,
-                                     batch.positions, None, 0, wl.scale, out=out,
+                                     batch.positions, None, window, wl.scale, out=out,
                                      num_kv_heads=wl.kv_heads, pages_per_split=pps)
     assert pgd.get_device_error() == pgd.OK
     assert torch.all(out[0] == 0) and torch.all(out[2] == 0)
-    assert torch.any(out[1] != 0)
+    assert torch.any(out[1] != 0) and torch.all(out[3] != 7.0)
 
 
 def test_zero_rows_is_a_no_op():
@@ -439,6 +440,14 @@ def test_window_kernel_reads_only_the_window_table_entries():
     assert torch.equal(out_bad[1:], out[1:])
     want, _, _ = oracle_step(batch, host, window=100, sinks=batch.sinks, scale=wl.scale)
     compare(out[1:], want, "window kernel, rows beside bad entries")
+    # a position beyond its table row: that row is zero and reported
+    bad_pos = batch.positions.clone()
+    bad_pos[2] = 64 * batch.table.shape[1] + 5
+    out_pos = pgd.paged_decode_attention(batch.q, batch.k_pool, batch.v_pool, batch.table,
+                                         bad_pos, batch.sinks, 100, wl.scale,
+                                         num_kv_heads=wl.kv_heads)
+    assert pgd.get_device_error() == pgd.EDEVICE_BOUNDS
+    assert torch.all(out_pos[2] == 0) and torch.equal(out_pos[:2], out[:2])
 
 
 def test_host_validation():
