@@ -6,13 +6,15 @@ namespace pgd {
 
 // paged_prefill_umma_d64.cu
 cudaError_t launch_prefill_umma_d64(const DecodeParams& p, const CUtensorMap& k_map,
-                                    const CUtensorMap& v_map, int sm_count, cudaStream_t stream);
+                                    const CUtensorMap& v_map, const CUtensorMap& q_map,
+                                    int sm_count, cudaStream_t stream);
 
 cudaError_t launch_prefill_umma(const DecodeParams& p, const CUtensorMap& k_map,
-                                const CUtensorMap& v_map, int head_dim, int sm_count,
-                                cudaStream_t stream) {
-  return head_dim == 64 ? launch_prefill_umma_d64(p, k_map, v_map, sm_count, stream)
-                        : launch_prefill_umma<128, 4, 4>(p, k_map, v_map, sm_count, stream);
+                                const CUtensorMap& v_map, const CUtensorMap& q_map, int head_dim,
+                                int sm_count, cudaStream_t stream) {
+  return head_dim == 64
+             ? launch_prefill_umma_d64(p, k_map, v_map, q_map, sm_count, stream)
+             : launch_prefill_umma<128, 4, 4>(p, k_map, v_map, q_map, sm_count, stream);
 }
 
 int prefill_umma_launches(int rows, int group, int window) {

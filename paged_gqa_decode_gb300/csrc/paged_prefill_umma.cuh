@@ -65,12 +65,13 @@ template <int D, int RK, int RV>
 struct UmmaPrefillCfg {
   static constexpr int kRows = 128;  // query rows per tile (TMEM lanes)
   static constexpr int kTiles = 2;   // query tiles per item
-  static constexpr int kSoftmaxThreads = 256;  // one warpgroup per tile
-  static constexpr int kProducerWarp = 8;
-  static constexpr int kMmaWarp = 9;  // S issuer, TMEM owner
-  static constexpr int kPvWarp = 10;
-  static constexpr int kVWarp = 11;
-  static constexpr int kThreads = 384;
+  // two warpgroups per tile, each taking half of every page's keys
+  static constexpr int kSoftmaxThreads = 512;
+  static constexpr int kProducerWarp = 16;
+  static constexpr int kMmaWarp = 17;  // S issuer, TMEM owner
+  static constexpr int kPvWarp = 18;
+  static constexpr int kVWarp = 19;
+  static constexpr int kThreads = 640;
   static constexpr int kBoxes = D / 64;
   static constexpr int kTileBytes = kPage * D * 2;  // one K or V slot (one page)
   static constexpr int kVOff = RK * kTileBytes;
@@ -85,7 +86,7 @@ struct UmmaPrefillCfg {
   // S / P buffers per tile: two where TMEM has room (head_dim 64), so S of
   // the next page is computed while the softmax works on this one
   static constexpr int kSBufs = 2;
-  static constexpr int kNumBars = 2 * RK + 2 * RV + 3 * kTiles * kSBufs + 8;
+  static constexpr int kNumBars = 2 * RK + 2 * RV + 3 * kTiles * kSBufs + 8 + 2 * kTiles + 2;
   static constexpr int kSmemBytes = 1024 + kBarOff + kNumBars * 8;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kOCol = 0, kSCol = kTiles * D,
@@ -159,9 +160,10 @@ __device__ __forceinline__ bool item_advance(const PrefillItem& it, int window, 
 }
 
 template <int D, int RK, int RV>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
     paged_prefill_umma_kernel(const __grid_constant__ CUtensorMap k_map,
-                              const __grid_constant__ CUtensorMap v_map, const DecodeParams p,
+                              const __grid_constant__ CUtensorMap v_map,
+                              const __grid_constant__ CUtensorMap q_map, const DecodeParams p,
                               int* item_counter, const int* block_order) {
   using C = UmmaPrefillCfg<D, RK, RV>;
   pdl_wait();
@@ -193,8 +195,12 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* item_free = item_ready + 2;       // [item % 2] consumed (softmax, issuers, V producer)
   uint64_t* q_ready = item_free + 2;          // [item % 2] both tiles' Q in TMEM (softmax)
   uint64_t* fin = q_ready + 2;                // [issuer] every MMA it issued done
+  uint64_t* xbar = fin + 2;                   // [tile * 2 + slot] the halves' values exchanged
+  uint64_t* q_full = xbar + 2 * C::kTiles;    // head_dim 128: the item's Q rows landed (TMA)
+  uint64_t* q_free = q_full + 1;              // head_dim 128: the item's S products done
   __shared__ PrefillItem items[2];
-  __shared__ int y_ring[2][64];  // [K, V producer] tile rows of upcoming pages, by page % 64
+  __shared__ int y_ring[2][64];
+  __shared__ float xval[C::kTiles][2][2][C::kRows];  // [tile][slot][half][row]  // [K, V producer] tile rows of upcoming pages, by page % 64
   __shared__ volatile int abort_flag;
   __shared__ uint32_t tmem_slot;
 
@@ -209,7 +215,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int tb = 0; tb < C::kTiles * C::kSBufs; ++tb) {
       mbar_init(&s_full[tb], 1);
-      mbar_init(&p_full[tb], C::kRows);  // the tile's warpgroup
+      mbar_init(&p_full[tb], 2 * C::kRows);  // the tile's two warpgroups
       mbar_init(&o_done[tb], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -219,8 +225,23 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(&fin[0], 1);
     mbar_init(&fin[1], 1);
+    for (int x = 0; x < 2 * C::kTiles; ++x) mbar_init(&xbar[x], 2 * C::kRows);
+    mbar_init(q_full, 1);
+    mbar_init(q_free, 1);
     mbar_init_fence();
     abort_flag = 0;
+  }
+  if constexpr (C::kQSmem) {
+    // rows past T * G of each Q tile hold no token: zero them once (the
+    // per-item copies fill rows 0 .. T * G - 1 only)
+    const int filled = (C::kRows / G) * G;
+    for (int e = tid; e < C::kTiles * 2 * (C::kRows - filled) * 8; e += C::kThreads) {
+      const int ch = e & 7, r = filled + (e >> 3) % (C::kRows - filled);
+      const int tb = (e >> 3) / (C::kRows - filled);  // tile * 2 + box
+      *reinterpret_cast<uint4*>(q_smem + (tb >> 1) * C::kQTileBytes + (tb & 1) * C::kQBoxBytes +
+                                r * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_shared();
   }
   if (warp == C::kMmaWarp) tmem_alloc(&tmem_slot, C::kTmemCols);
   tc_fence_before_sync();
@@ -422,12 +443,31 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t k_addr = smem_addr(k_slots);
       int i = 0;  // page index over all items
       bool issued = false, ok = true;
+      bool q_pending = false;  // a Q copy issued and not yet seen landed
+      int q_phase = 0;
       for (int seq = 0; ok; ++seq) {
         const int d = seq & 1;
         if (!wait(&item_ready[d], (seq >> 1) & 1)) break;
         const PrefillItem& it = items[d];
         if (!it.valid) break;
-        if (!wait(&q_ready[d], (seq >> 1) & 1)) break;
+        if constexpr (C::kQSmem) {
+          // the item's Q rows by TMA ([token][head] rows of 64 values: the
+          // swizzled K-major layout the products read), once the previous
+          // item's S products, which read the same shared memory, are done;
+          // the softmax warps meanwhile finish the previous item
+          if (seq > 0 && !wait(q_free, (seq - 1) & 1)) break;
+          mbar_arrive_expect_tx(q_full, C::kTiles * 2 * T * G * 128);
+          for (int t = 0; t < C::kTiles; ++t)
+            for (int bx = 0; bx < 2; ++bx)
+              tma_load_3d(q_smem + t * C::kQTileBytes + bx * C::kQBoxBytes, &q_map, 64 * bx,
+                          it.kvh * G, it.t_begin + t * T, q_full);
+          q_pending = true;
+          q_phase = seq;
+          if (!wait(q_full, seq & 1)) break;
+          q_pending = false;
+        } else {
+          if (!wait(&q_ready[d], (seq >> 1) & 1)) break;
+        }
         ItemCursor cur{-1, 0, -1, -1, 0, 0};
         for (bool more = item_next_run(it, p.window, cur); more && ok;
              more = item_advance(it, p.window, cur), ++i) {
@@ -467,13 +507,18 @@ __global__ void __launch_bounds__(384, 1)
           umma_commit(&k_empty[i % RK]);
           issued = true;
         }
+        if constexpr (C::kQSmem) {
+          if (ok) umma_commit(q_free);  // this item's S products done: Q may be replaced
+        }
         if (ok) mbar_arrive(&item_free[d]);
       }
-      // drain: every MMA this thread issued completes before TMEM is freed
+      // drain: every MMA this thread issued completes before TMEM is freed,
+      // and a Q copy still in flight lands before the CTA exits
       if (issued) {
         umma_commit(fin);
         mbar_wait_bounded(fin, 0, p.err);
       }
+      if (q_pending) mbar_wait_bounded(q_full, q_phase & 1, p.err);
     }
   } else if (warp == C::kPvWarp) {
     // ------------------------------------------------------------ P V issuer
@@ -533,7 +578,11 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int m = tid & 127, t = tid >> 7;  // row; tile
+    // row; tile; half h of every page's keys (and of the O columns) this
+    // thread takes -- the tile's other warpgroup takes the other half
+    const int m = tid & 127, t = (tid >> 7) & 1, h = tid >> 8;
+    constexpr int kHalf = kPage / 2;
+    int xn = 0;  // exchanges with the other half so far
     const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     const float c = p.q_scale_log2;
     const float cc = c > 0.f ? c : 1.f;
@@ -551,11 +600,12 @@ __global__ void __launch_bounds__(384, 1)
       }
       const PrefillItem& it = items[d];
       if (!it.valid) return false;
+      if constexpr (C::kQSmem) return true;  // the S issuer copies Q in (TMA)
       const bool q_ok = in_tile && it.t_begin + tl < it.t_end && it.tok_row[tl] >= 0;
       const uint4* src = reinterpret_cast<const uint4*>(
           p.q + ((size_t)(it.t_begin + (q_ok ? tl : 0)) * p.hq + it.kvh * G + g) * D);
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {  // half the row at a time
+      for (int hh = h; hh <= h; ++hh) {  // this half's half of the row
         uint4 v[D / 16];
 #pragma unroll
         for (int ch = 0; ch < D / 16; ++ch)
@@ -622,41 +672,56 @@ __global__ void __launch_bounds__(384, 1)
             break;
           }
           tc_fence_after_sync();
-          float sv[kPage];
+          float sv[kHalf];
 #pragma unroll
-          for (int q = 0; q < kPage / 16; ++q)
-            tmem_ld16(lane_base + scol + 16 * q,
+          for (int q = 0; q < kHalf / 16; ++q)
+            tmem_ld16(lane_base + scol + kHalf * h + 16 * q,
                       *reinterpret_cast<float(*)[16]>(&sv[16 * q]));
           tmem_wait_ld();
           // scores stay raw: the scale is folded into the exponent's FMA (for
           // a positive scale; otherwise it is applied here)
           if (!(c > 0.f)) {
 #pragma unroll
-            for (int k = 0; k < kPage; ++k) sv[k] *= c;
+            for (int k = 0; k < kHalf; ++k) sv[k] *= c;
           }
           const int pos0 = pg * kPage;
-          if (!(live && pos0 >= lo && pos0 + kPage - 1 <= pos)) {
+          const int pos0h = pos0 + kHalf * h;  // this half's first key
+          if (!(live && pos0h >= lo && pos0h + kHalf - 1 <= pos)) {
 #pragma unroll
-            for (int k = 0; k < kPage; ++k)
-              if (!(live && pos0 + k >= lo && pos0 + k <= pos)) sv[k] = -INFINITY;
+            for (int k = 0; k < kHalf; ++k)
+              if (!(live && pos0h + k >= lo && pos0h + k <= pos)) sv[k] = -INFINITY;
           }
-          // eight partial maxima: the first 8 scores, then 56 more two at a
-          // time (three blocks of 16 and a last block of 8)
+          // eight partial maxima: the first 8 scores, then 24 more two at a
+          // time (a block of 16 and a last block of 8)
           float part[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) part[j] = sv[j];
 #pragma unroll
-          for (int k = 8; k + 16 <= kPage; k += 16)
+          for (int k = 8; k + 16 <= kHalf; k += 16)
 #pragma unroll
             for (int j = 0; j < 8; ++j)
               part[j] = fmax3(part[j], sv[k + 2 * j], sv[k + 2 * j + 1]);
-          static_assert((kPage - 8) % 16 == 8, "the last block holds 8 scores");
+          static_assert((kHalf - 8) % 16 == 8, "the last block holds 8 scores");
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            part[j] = fmax3(part[j], sv[kPage - 8 + 2 * j], sv[kPage - 7 + 2 * j]);
-          const float mx = fmax3(fmax3(part[0], part[1], part[2]),
-                                 fmax3(part[3], part[4], part[5]), fmaxf(part[6], part[7])) *
-                           cc;
+            part[j] = fmax3(part[j], sv[kHalf - 8 + 2 * j], sv[kHalf - 7 + 2 * j]);
+          const float mxh = fmax3(fmax3(part[0], part[1], part[2]),
+                                  fmax3(part[3], part[4], part[5]), fmaxf(part[6], part[7])) *
+                            cc;
+          // the row's max over the whole page: the other half's through
+          // shared memory (both halves then take the same lazy decisions)
+          float mx;
+          {
+            const int sl = xn & 1;
+            xval[t][sl][h][m] = mxh;
+            mbar_arrive(&xbar[t * 2 + sl]);
+            if (!all_ok(wait(&xbar[t * 2 + sl], (xn >> 1) & 1))) {
+              ok = false;
+              break;
+            }
+            mx = fmaxf(mxh, xval[t][sl][1 - h][m]);
+            ++xn;
+          }
           float alpha = 1.f;
           bool rose = false;
           if (mx > m_run + kLazyRescaleLog2) {
@@ -677,7 +742,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int j = 0; j < 4; ++j) sum2[j] = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int q = 0; q < kPage / 32; ++q) {
+          for (int q = 0; q < kHalf / 32; ++q) {
             uint32_t hw[16], lw[16];
 #pragma unroll
             for (int w = 0; w < 16; ++w) {
@@ -690,8 +755,8 @@ __global__ void __launch_bounds__(384, 1)
                   __ffma2_rn(make_float2(bf16_lo(hw[w]), bf16_hi(hw[w])), minus1, x);
               lw[w] = pack_bf16x2(rr.x, rr.y);
             }
-            tmem_st16(lane_base + scol + 32 * q, hw);
-            tmem_st16(lane_base + scol + 32 * q + 16, lw);
+            tmem_st16(lane_base + scol + kHalf * h + 32 * q, hw);
+            tmem_st16(lane_base + scol + kHalf * h + 32 * q + 16, lw);
           }
           const float2 s4 =
               __fadd2_rn(__fadd2_rn(sum2[0], sum2[1]), __fadd2_rn(sum2[2], sum2[3]));
@@ -708,7 +773,8 @@ __global__ void __launch_bounds__(384, 1)
               tc_fence_after_sync();
             }
 #pragma unroll
-            for (int q16 = 0; q16 < D / 16; ++q16) {
+            for (int j = 0; j < D / 32; ++j) {  // this half's O columns
+              const int q16 = h * (D / 32) + j;
               float ov[16];
               tmem_ld16(lane_base + C::kOCol + t * D + 16 * q16, ov);
               tmem_wait_ld();
@@ -720,7 +786,7 @@ __global__ void __launch_bounds__(384, 1)
           // V rows outside the run's key range on a boundary page -> zero
           // (warpgroup 0; both tiles' products read them after its P)
           const int rlo = max(lo_run - pos0, 0), rhi = min(pos_last - pos0, kPage - 1);
-          if (t == 0 && (rlo > 0 || rhi < kPage - 1)) {
+          if (t == 0 && h == 0 && (rlo > 0 || rhi < kPage - 1)) {
             const int s = i % RV;
             if (!all_ok(wait(&v_full[s], (i / RV) & 1))) {
               ok = false;
@@ -748,6 +814,17 @@ __global__ void __launch_bounds__(384, 1)
           break;
         }
         tc_fence_after_sync();
+        {  // the row sum: this half's plus the other half's
+          const int sl = xn & 1;
+          xval[t][sl][h][m] = l;
+          mbar_arrive(&xbar[t * 2 + sl]);
+          if (!all_ok(wait(&xbar[t * 2 + sl], (xn >> 1) & 1))) {
+            ok = false;
+            break;
+          }
+          l += xval[t][sl][1 - h][m];
+          ++xn;
+        }
         const int hh = h0 + g;
         float inv = 0.f;
         if (live) {
@@ -759,7 +836,8 @@ __global__ void __launch_bounds__(384, 1)
         }
         uint16_t* orow = p.out + ((size_t)(t_begin + (live ? tl : 0)) * p.hq + hh) * D;
 #pragma unroll
-        for (int q16 = 0; q16 < D / 16; ++q16) {
+        for (int j = 0; j < D / 32; ++j) {  // this half's output columns
+          const int q16 = h * (D / 32) + j;
           float ov[16];
           tmem_ld16(lane_base + C::kOCol + t * D + 16 * q16, ov);
           tmem_wait_ld();
@@ -856,7 +934,8 @@ __global__ void __launch_bounds__(1024) prefill_block_order_kernel(const DecodeP
 
 template <int D, int RK, int RV>
 cudaError_t launch_prefill_umma(const DecodeParams& p, const CUtensorMap& k_map,
-                                const CUtensorMap& v_map, int sm_count, cudaStream_t stream) {
+                                const CUtensorMap& v_map, const CUtensorMap& q_map, int sm_count,
+                                cudaStream_t stream) {
   using C = UmmaPrefillCfg<D, RK, RV>;
   static std::atomic<bool> configured[64];
   int dev = 0;
@@ -885,7 +964,7 @@ cudaError_t launch_prefill_umma(const DecodeParams& p, const CUtensorMap& k_map,
   if (e != cudaSuccess) return e;
   const int ctas = items < sm_count ? items : sm_count;
   return launch_pdl(paged_prefill_umma_kernel<D, RK, RV>, dim3(ctas), dim3(C::kThreads),
-                    C::kSmemBytes, stream, k_map, v_map, p, counter,
+                    C::kSmemBytes, stream, k_map, v_map, q_map, p, counter,
                     static_cast<const int*>(order));
 }
 

@@ -171,7 +171,7 @@ int encode_pool_map(CUtensorMap* map, const void* pool, const pgd_dims* d, bool 
   return PGD_OK;
 }
 
-int encode_pool_map_uncached(CUtensorMap* map, const void* pool, const pgd_dims* d, bool whole) {
+bool load_encode() {
   std::call_once(g_encode_once, [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -180,7 +180,32 @@ int encode_pool_map_uncached(CUtensorMap* map, const void* pool, const pgd_dims*
         q == cudaDriverEntryPointSuccess)
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   });
-  if (!g_encode) return PGD_ECUDA;
+  return g_encode != nullptr;
+}
+
+// q of a packed prefill, [tokens][Hq][D] bf16, as (64 values, heads,
+// tokens) with boxes of 64 x group x (128 / group): one box is one half of a
+// query tile's rows (token-major, head-minor), 128-byte swizzled -- the
+// layout the tcgen05 prefill's S products read.  Tokens past the end read
+// as zeros.
+int encode_q_map(CUtensorMap* map, const void* q, const pgd_dims* d) {
+  if (!load_encode()) return PGD_ECUDA;
+  const int group = d->num_q_heads / d->num_kv_heads;
+  const cuuint64_t dims3[3] = {(cuuint64_t)d->head_dim, (cuuint64_t)d->num_q_heads,
+                               (cuuint64_t)d->rows};
+  const cuuint64_t strides3[2] = {(cuuint64_t)d->head_dim * 2,
+                                  (cuuint64_t)d->num_q_heads * d->head_dim * 2};
+  const cuuint32_t box3[3] = {64, (cuuint32_t)group, (cuuint32_t)(128 / group)};
+  const cuuint32_t elem3[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims3,
+                        strides3, box3, elem3, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PGD_OK : PGD_ECUDA;
+}
+
+int encode_pool_map_uncached(CUtensorMap* map, const void* pool, const pgd_dims* d, bool whole) {
+  if (!load_encode()) return PGD_ECUDA;
   // The pool as a 2-D tensor: rows of head_dim bf16 values, one row per
   // (page, kv head, position) in either layout.  A box is 64 rows x 64
   // values (128 bytes): one page tile, or half of one when head_dim is 128.
@@ -454,11 +479,14 @@ static int decode_impl(const pgd_dims* dims, int32_t table_rows, const int32_t* 
   const int pages_per_cta = grid_pages < pl.pages_per_split ? grid_pages : pl.pages_per_split;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (kernel == PGD_KERNEL_PREFILL_UMMA)
-    return launch_prefill_umma(p, k_map, v_map, dims->head_dim, dev->sm_count, st) ==
+  if (kernel == PGD_KERNEL_PREFILL_UMMA) {
+    CUtensorMap q_map = k_map;  // read only at head_dim 128
+    if (dims->head_dim == 128 && (rc = encode_q_map(&q_map, q, dims)) != PGD_OK) return rc;
+    return launch_prefill_umma(p, k_map, v_map, q_map, dims->head_dim, dev->sm_count, st) ==
                    cudaSuccess
                ? PGD_OK
                : PGD_ECUDA;
+  }
   if (kernel == PGD_KERNEL_PREFILL_TILED)
     return launch_prefill_tiled(p, k_map, v_map, dims->head_dim, padded, st) == cudaSuccess
                ? PGD_OK
