@@ -78,7 +78,8 @@ struct UmmaPrefillCfg {
   // Q: in TMEM at head_dim 64; at 128 the two O accumulators and four S
   // buffers take all 512 columns, so Q sits in shared memory (K-major,
   // 128-byte swizzle: the layout the MMA reads), written by the softmax warps
-  static constexpr bool kQSmem = D == 128;
+  static constexpr bool kQSmem = true;
+  static constexpr int kQBoxes = D / 64;  // 64-value boxes of a Q row
   static constexpr int kQOff = (RK + RV) * kTileBytes;
   static constexpr int kQBoxBytes = kRows * 128;  // 128 rows x 64 values
   static constexpr int kQTileBytes = kRows * D * 2;
@@ -235,11 +236,12 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
     // rows past T * G of each Q tile hold no token: zero them once (the
     // per-item copies fill rows 0 .. T * G - 1 only)
     const int filled = (C::kRows / G) * G;
-    for (int e = tid; e < C::kTiles * 2 * (C::kRows - filled) * 8; e += C::kThreads) {
+    for (int e = tid; e < C::kTiles * C::kQBoxes * (C::kRows - filled) * 8; e += C::kThreads) {
       const int ch = e & 7, r = filled + (e >> 3) % (C::kRows - filled);
-      const int tb = (e >> 3) / (C::kRows - filled);  // tile * 2 + box
-      *reinterpret_cast<uint4*>(q_smem + (tb >> 1) * C::kQTileBytes + (tb & 1) * C::kQBoxBytes +
-                                r * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+      const int tb = (e >> 3) / (C::kRows - filled);  // tile * kQBoxes + box
+      *reinterpret_cast<uint4*>(q_smem + (tb / C::kQBoxes) * C::kQTileBytes +
+                                (tb % C::kQBoxes) * C::kQBoxBytes + r * 128 + ch * 16) =
+          make_uint4(0u, 0u, 0u, 0u);
     }
     fence_proxy_async_shared();
   }
@@ -456,9 +458,9 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
           // item's S products, which read the same shared memory, are done;
           // the softmax warps meanwhile finish the previous item
           if (seq > 0 && !wait(q_free, (seq - 1) & 1)) break;
-          mbar_arrive_expect_tx(q_full, C::kTiles * 2 * T * G * 128);
+          mbar_arrive_expect_tx(q_full, C::kTiles * C::kQBoxes * T * G * 128);
           for (int t = 0; t < C::kTiles; ++t)
-            for (int bx = 0; bx < 2; ++bx)
+            for (int bx = 0; bx < C::kQBoxes; ++bx)
               tma_load_3d(q_smem + t * C::kQTileBytes + bx * C::kQBoxBytes, &q_map, 64 * bx,
                           it.kvh * G, it.t_begin + t * T, q_full);
           q_pending = true;

@@ -480,8 +480,8 @@ static int decode_impl(const pgd_dims* dims, int32_t table_rows, const int32_t* 
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (kernel == PGD_KERNEL_PREFILL_UMMA) {
-    CUtensorMap q_map = k_map;  // read only at head_dim 128
-    if (dims->head_dim == 128 && (rc = encode_q_map(&q_map, q, dims)) != PGD_OK) return rc;
+    CUtensorMap q_map;
+    if ((rc = encode_q_map(&q_map, q, dims)) != PGD_OK) return rc;
     return launch_prefill_umma(p, k_map, v_map, q_map, dims->head_dim, dev->sm_count, st) ==
                    cudaSuccess
                ? PGD_OK

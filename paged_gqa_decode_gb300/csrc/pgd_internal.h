@@ -122,9 +122,8 @@ int prefill_block_tokens(int padded);
 // Prefill on the tcgen05 tensor cores: persistent, one CTA per SM, blocks of
 // 2 x 128 / group tokens; the first word of p.ws_acc is its work counter, the
 // block order (when one is computed) starts at the fifth.
-// q_map: q as (64-value rows, heads, tokens) with boxes of 64 x group x
-// (128 / group), 128-byte swizzle (head_dim 128: the kernel copies each
-// item's Q with it; unused at head_dim 64).
+// q_map: q as (64 values, heads, tokens) with boxes of 64 x group x
+// (128 / group), 128-byte swizzle: the kernel copies each item's Q with it.
 cudaError_t launch_prefill_umma(const DecodeParams& p, const CUtensorMap& k_map,
                                 const CUtensorMap& v_map, const CUtensorMap& q_map, int head_dim,
                                 int sm_count, cudaStream_t stream);
