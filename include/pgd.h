@@ -113,10 +113,11 @@ enum {
   PGD_KERNEL_CUDA_CORE = 2,     /* fp32 FMA products on the CUDA cores, per token */
   PGD_KERNEL_PREFILL_TILED = 3, /* prefill only: blocks of tokens share each page
                                    load (mma.sync tensor cores, no key splits) */
-  PGD_KERNEL_PREFILL_UMMA = 4   /* prefill only: persistent, 128 query rows per
-                                   block on the tcgen05 tensor cores (TMEM
-                                   accumulators), no key splits; uses the first
-                                   4 bytes of the workspace as a work counter */
+  PGD_KERNEL_PREFILL_UMMA = 4   /* prefill only: persistent, two tiles of 128
+                                   query rows per block on the tcgen05 tensor
+                                   cores (TMEM accumulators), no key splits;
+                                   uses the start of the workspace for its work
+                                   counter and block order */
 };
 
 /* Optional tuning of the decode launch; pass NULL for the defaults.  The same
@@ -296,8 +297,10 @@ PGD_API int pgd_paged_decode_step(const pgd_dims* dims, const void* q, const voi
  * step position.
  * Kernels (opts->kernel): AUTO chooses PREFILL_UMMA (tokens in blocks of
  * 2 x 128 / (Hq / Hkv), two query tiles, share every page load; persistent,
- * one CTA per SM; without a window the blocks are taken longest first) when
- * P >= 8 * table_rows, else the per-token TENSOR_CORE split kernel.
+ * one CTA per SM; each item's Q copied in with TMA; without a window the
+ * blocks are taken longest first) when P >= 8 * table_rows, else the
+ * per-token decode kernels (the window kernel for windows of 1..128
+ * positions, the TENSOR_CORE split kernel otherwise).
  * Device errors: rows[p] outside [0, table_rows), plus those of
  * pgd_paged_decode_attention; the token's output is zero.  After
  * PGD_EDEVICE_TIMEOUT (a pipeline wait gave up) the outputs of the tokens
