@@ -353,6 +353,9 @@ def test_kernel_count_follows_the_split_plan():
     assert pgd.attention_kernel_count(dims(w["mistral_serve"], 512, rows=4096), table_rows=8,
                                       kernel=pgd.KERNEL_PREFILL_TILED) == 1
     assert pgd.attention_kernel_count(dims(w["mistral_serve"], 512, rows=8), table_rows=8) == 2
+    # one token per table row with a window: the per-token path, i.e. the window kernel
+    assert pgd.attention_kernel_count(dims(w["gptoss_sliding"], 512, rows=8), table_rows=8,
+                                      window=128) == 1
 
 
 # ---------------------------------------------------------------------------
