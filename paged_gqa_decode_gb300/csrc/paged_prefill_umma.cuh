@@ -20,38 +20,43 @@
 // tokens split into runs (same table row, consecutive positions); each run
 // is one pass over the pages of the union of its tokens' key ranges.  The
 // pages of all of a CTA's items form one sequence, and every role walks it:
-//   warp 8      K producer: per item, reads its tokens, builds the runs,
+//   warp 16     K producer: per item, reads its tokens, builds the runs,
 //               checks the table and zeroes uncovered outputs (whole warp);
 //               then streams each page's K tile (64 x D bf16, 128-byte
 //               swizzle) into a ring of shared slots with TMA, pulling pages
 //               into L2 ahead of their loads.
-//   warp 11     V producer: the same pages' V tiles into a second ring.
-//   warp 9      S issuer (one thread) and TMEM owner, per page i and tile t:
-//                 S_t  = Q_t K_i^T    M 128, N 64, K D   (K shared; Q from TMEM
-//                                                      at head_dim 64, shared at 128)
+//   warp 19     V producer: the same pages' V tiles into a second ring.
+//   warp 17     S issuer (one thread) and TMEM owner.  Per item it copies
+//               the item's Q rows into shared memory with TMA (q as 64
+//               values x heads x tokens, boxes of 64 x G x 128 / G: half a
+//               tile's rows, token-major, in the swizzled K-major layout the
+//               products read) once the previous item's S products are done;
+//               then per page i and tile t:
+//                 S_t  = Q_t K_i^T    M 128, N 64, K D   (Q and K shared)
 //               into tile t's S buffer i % 2 once P_t V_{i-2} (which reads
 //               the same columns) is done.
-//   warp 10     P V issuer (one thread), per page i and tile t:
+//   warp 18     P V issuer (one thread), per page i and tile t:
 //                 O_t += P_t V_i      M 128, N D,  K 64  (P from TMEM, V shared)
-//   warps 0-7   softmax: warpgroup t (warps 4t .. 4t + 3) owns tile t, one
-//               thread per query row.  It loads its rows' Q per item (into
-//               TMEM, or shared memory at head_dim 128); per page the S row from TMEM, causal and window mask,
-//               online softmax in log2 units with a lazy running max (raised
-//               only when a score exceeds it by more than 2^8, which then
-//               rescales that row of O_t in TMEM); P is written over S as a
-//               bf16 head and residual (two MMAs, so P V keeps fp32
-//               accuracy).  At the end of a run each thread normalises its
-//               O_t row with the sink and stores it.  Warpgroup 0 also zeroes
-//               the V rows outside the run's key range on boundary pages
-//               before the products read them.
+//   warps 0-15  softmax: tile t has two warpgroups (warps 4t .. 4t + 3 and
+//               8 + 4t .. 11 + 4t), one thread per query row in each; the
+//               first takes keys 0-31 of every page, the second keys 32-63
+//               (and half of the O columns each for the rescale and the
+//               store).  Per page its scores from TMEM, causal and window
+//               mask, its half's max, the row's max over the page through
+//               shared memory (bounded mbarrier waits), online softmax in
+//               log2 units with a lazy running max (raised only when a score
+//               exceeds it by more than 2^8, which then rescales that row of
+//               O_t in TMEM); P is written over S as a bf16 head and residual
+//               (two MMAs, so P V keeps fp32 accuracy).  At the end of a run
+//               the halves add their row sums and normalise and store their
+//               halves of the O_t row with the sink.  Warpgroup 0 also
+//               zeroes the V rows outside the run's key range on boundary
+//               pages before the products read them.
 // TMEM (512 columns): O_t at [t D, (t + 1) D), then two S / P buffers per
 // tile, 64 columns each (S of the next page is computed while the softmax
 // works on this one; P per chunk of 32 keys: the bf16 head in the chunk's
-// first 16 columns, the residual in the next 16, as packed pairs), then at
-// head_dim 64 Q_t, D / 2 columns of packed pairs.  At head_dim 128 the O
-// accumulators and S buffers take all 512 columns, and Q_t sits in shared
-// memory instead (K-major, 128-byte swizzle), written there by the softmax
-// warps; the S products then read A from shared memory.
+// first 16 columns, the residual in the next 16, as packed pairs).  At
+// head_dim 128 that is all 512 columns.
 // Every wait is bounded; a timeout records PGD_EDEVICE_TIMEOUT, stops all
 // roles, drains in-flight copies and MMAs and frees TMEM before the CTA exits.
 #pragma once
@@ -75,28 +80,25 @@ struct UmmaPrefillCfg {
   static constexpr int kBoxes = D / 64;
   static constexpr int kTileBytes = kPage * D * 2;  // one K or V slot (one page)
   static constexpr int kVOff = RK * kTileBytes;
-  // Q: in TMEM at head_dim 64; at 128 the two O accumulators and four S
-  // buffers take all 512 columns, so Q sits in shared memory (K-major,
-  // 128-byte swizzle: the layout the MMA reads), written by the softmax warps
-  static constexpr bool kQSmem = true;
+  // Q sits in shared memory (K-major, 128-byte swizzle: the layout the MMA
+  // reads), copied in per item by the S issuer with TMA; at head_dim 128 the
+  // two O accumulators and the S buffers take all 512 TMEM columns
   static constexpr int kQBoxes = D / 64;  // 64-value boxes of a Q row
   static constexpr int kQOff = (RK + RV) * kTileBytes;
   static constexpr int kQBoxBytes = kRows * 128;  // 128 rows x 64 values
   static constexpr int kQTileBytes = kRows * D * 2;
-  static constexpr int kBarOff = kQOff + (kQSmem ? kTiles * kQTileBytes : 0);
+  static constexpr int kBarOff = kQOff + kTiles * kQTileBytes;
   // S / P buffers per tile: two where TMEM has room (head_dim 64), so S of
   // the next page is computed while the softmax works on this one
   static constexpr int kSBufs = 2;
-  static constexpr int kNumBars = 2 * RK + 2 * RV + 3 * kTiles * kSBufs + 8 + 2 * kTiles + 2;
+  static constexpr int kNumBars = 2 * RK + 2 * RV + 3 * kTiles * kSBufs + 6 + 2 * kTiles + 2;
   static constexpr int kSmemBytes = 1024 + kBarOff + kNumBars * 8;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kOCol = 0, kSCol = kTiles * D,
-                            kQCol = kTiles * D + kTiles * kSBufs * kPage;
+  static constexpr uint32_t kOCol = 0, kSCol = kTiles * D;
   static constexpr uint32_t kIdescS = umma_idesc_bf16(128, kPage, 0, 0);
   static constexpr uint32_t kIdescPV = umma_idesc_bf16(128, D, 0, 1);
   static_assert(D == 64 || D == 128, "head_dim");
   static_assert(kSCol + kTiles * kSBufs * kPage <= kTmemCols, "TMEM columns");
-  static_assert(kQSmem || kQCol + kTiles * D / 2 <= kTmemCols, "TMEM columns");
   static_assert(RK == RV, "the K and V rings are streamed by one helper");
   static_assert(kSmemBytes + 8 * 1024 <= 227 * 1024, "shared memory");
 };
@@ -194,8 +196,7 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
   uint64_t* o_done = p_full + C::kTiles * C::kSBufs;  // P V of the page done (MMA commit)
   uint64_t* item_ready = o_done + C::kTiles * C::kSBufs;  // [item % 2] descriptor written
   uint64_t* item_free = item_ready + 2;       // [item % 2] consumed (softmax, issuers, V producer)
-  uint64_t* q_ready = item_free + 2;          // [item % 2] both tiles' Q in TMEM (softmax)
-  uint64_t* fin = q_ready + 2;                // [issuer] every MMA it issued done
+  uint64_t* fin = item_free + 2;              // [issuer] every MMA it issued done
   uint64_t* xbar = fin + 2;                   // [tile * 2 + slot] the halves' values exchanged
   uint64_t* q_full = xbar + 2 * C::kTiles;    // head_dim 128: the item's Q rows landed (TMA)
   uint64_t* q_free = q_full + 1;              // head_dim 128: the item's S products done
@@ -222,7 +223,6 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&item_ready[b], 1);
       mbar_init(&item_free[b], C::kSoftmaxThreads + 3);
-      mbar_init(&q_ready[b], C::kSoftmaxThreads);
     }
     mbar_init(&fin[0], 1);
     mbar_init(&fin[1], 1);
@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
     mbar_init_fence();
     abort_flag = 0;
   }
-  if constexpr (C::kQSmem) {
+  {
     // rows past T * G of each Q tile hold no token: zero them once (the
     // per-item copies fill rows 0 .. T * G - 1 only)
     const int filled = (C::kRows / G) * G;
@@ -452,7 +452,7 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
         if (!wait(&item_ready[d], (seq >> 1) & 1)) break;
         const PrefillItem& it = items[d];
         if (!it.valid) break;
-        if constexpr (C::kQSmem) {
+        {
           // the item's Q rows by TMA ([token][head] rows of 64 values: the
           // swizzled K-major layout the products read), once the previous
           // item's S products, which read the same shared memory, are done;
@@ -467,8 +467,6 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
           q_phase = seq;
           if (!wait(q_full, seq & 1)) break;
           q_pending = false;
-        } else {
-          if (!wait(&q_ready[d], (seq >> 1) & 1)) break;
         }
         ItemCursor cur{-1, 0, -1, -1, 0, 0};
         for (bool more = item_next_run(it, p.window, cur); more && ok;
@@ -488,30 +486,19 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
             }
             tc_fence_after_sync();
             const uint32_t sb = tmem + C::kSCol + tb * kPage;
-            if constexpr (C::kQSmem) {
-              const uint32_t qs = smem_addr(q_smem) + t * C::kQTileBytes;
+            const uint32_t qs = smem_addr(q_smem) + t * C::kQTileBytes;
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk)
-                umma_bf16(sb, umma_desc_sw128(qs + (kk >> 2) * C::kQBoxBytes + (kk & 3) * 32, 16, 1024),
-                          umma_desc_sw128(kt + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
-                          C::kIdescS, kk > 0);
-            } else {
-              const uint32_t qa = tmem + C::kQCol + t * (D / 2);
-#pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk)
-                umma_bf16_tmem_a(sb, qa + kk * 8,
-                                 umma_desc_sw128(kt + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
-                                 C::kIdescS, kk > 0);
-            }
+            for (int kk = 0; kk < D / 16; ++kk)
+              umma_bf16(sb, umma_desc_sw128(qs + (kk >> 2) * C::kQBoxBytes + (kk & 3) * 32, 16, 1024),
+                        umma_desc_sw128(kt + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
+                        C::kIdescS, kk > 0);
             umma_commit(&s_full[tb]);
           }
           if (!ok) break;
           umma_commit(&k_empty[i % RK]);
           issued = true;
         }
-        if constexpr (C::kQSmem) {
-          if (ok) umma_commit(q_free);  // this item's S products done: Q may be replaced
-        }
+        if (ok) umma_commit(q_free);  // this item's S products done: Q may be replaced
         if (ok) mbar_arrive(&item_free[d]);
       }
       // drain: every MMA this thread issued completes before TMEM is freed,
@@ -592,59 +579,17 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
     bool ok = true;
     const int tl = t * T + m / G, g = m % G;  // token of the block, head of the group
     const bool in_tile = m / G < T;           // rows past T * G hold no token
-    // Tile t's Q rows of item seq into TMEM (rows of no token: zero); false
-    // when there is no item seq.
-    auto load_q = [&](int seq) -> bool {
+    // Waits for the descriptor of item seq (its Q is copied in by the S
+    // issuer); false when there is no item seq.
+    auto next_item = [&](int seq) -> bool {
       const int d = seq & 1;
       if (!all_ok(wait(&item_ready[d], (seq >> 1) & 1))) {
         ok = false;
         return false;
       }
-      const PrefillItem& it = items[d];
-      if (!it.valid) return false;
-      if constexpr (C::kQSmem) return true;  // the S issuer copies Q in (TMA)
-      const bool q_ok = in_tile && it.t_begin + tl < it.t_end && it.tok_row[tl] >= 0;
-      const uint4* src = reinterpret_cast<const uint4*>(
-          p.q + ((size_t)(it.t_begin + (q_ok ? tl : 0)) * p.hq + it.kvh * G + g) * D);
-#pragma unroll
-      for (int hh = h; hh <= h; ++hh) {  // this half's half of the row
-        uint4 v[D / 16];
-#pragma unroll
-        for (int ch = 0; ch < D / 16; ++ch)
-          v[ch] = q_ok ? src[hh * (D / 16) + ch] : make_uint4(0u, 0u, 0u, 0u);
-        if constexpr (C::kQSmem) {
-          // half hh is box hh: row m's 16-byte chunk ch at chunk ch ^ (m % 8)
-          // of its 128-byte line in the 1024-byte group of rows m / 8
-          unsigned char* box = q_smem + t * C::kQTileBytes + hh * C::kQBoxBytes +
-                               (m >> 3) * 1024 + (m & 7) * 128;
-#pragma unroll
-          for (int ch = 0; ch < D / 16; ++ch)
-            *reinterpret_cast<uint4*>(box + ((ch ^ (m & 7)) << 4)) = v[ch];
-          continue;
-        }
-#pragma unroll
-        for (int c16 = 0; c16 < D / 64; ++c16) {
-          uint32_t w[16];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            w[4 * k] = v[4 * c16 + k].x;
-            w[4 * k + 1] = v[4 * c16 + k].y;
-            w[4 * k + 2] = v[4 * c16 + k].z;
-            w[4 * k + 3] = v[4 * c16 + k].w;
-          }
-          tmem_st16(lane_base + C::kQCol + t * (D / 2) + hh * (D / 4) + 16 * c16, w);
-        }
-      }
-      if constexpr (C::kQSmem) {
-        fence_proxy_async_shared();  // read by the tensor core
-      } else {
-        tmem_wait_st();
-        tc_fence_before_sync();
-      }
-      mbar_arrive(&q_ready[d]);
-      return true;
+      return items[d].valid != 0;
     };
-    bool have = load_q(0);
+    bool have = next_item(0);
     for (int seq = 0; ok && have; ++seq) {
       const int d = seq & 1;
       const PrefillItem& it = items[d];
@@ -860,7 +805,7 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
       // this item's descriptor is no longer read: free its slot before
       // waiting for the next item
       mbar_arrive(&item_free[d]);
-      have = load_q(seq + 1);
+      have = next_item(seq + 1);
     }
   }
 
