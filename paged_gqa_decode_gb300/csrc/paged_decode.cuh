@@ -866,7 +866,8 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // consumer on them, so each warp computes as soon as its slice has landed.
 // The rows land in the layout a TMA page tile has (64-row tiles of
 // 128-byte-swizzled 64-value boxes), which the consumer reads.  The warps
-// merge through shared memory after one barrier: each thread owns a run of
+// merge through shared memory (a barrier once every warp is done with the
+// rows, another once their partials are stored): each thread owns a run of
 // one head's output dims, forms that head's weight per warp (its running max
 // against the overall one and the sink, over the total denominator) and
 // stores its run with 8- or 16-byte writes.

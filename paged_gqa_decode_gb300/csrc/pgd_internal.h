@@ -103,8 +103,9 @@ struct SlotParams {
 cudaError_t launch_page_slots(const SlotParams& p, cudaStream_t stream);
 cudaError_t launch_bounded_wait_selftest(unsigned int* err, int* outcome, cudaStream_t stream);
 
-// Split kernel + combine kernel for one head_dim; `padded` is the padded
-// group size, `kernel` a PGD_KERNEL_* choice.
+// Decode kernels for one head_dim: the window kernel (AUTO, windows of at
+// most kMaxWindowKernel positions) or the split kernel + combine kernel;
+// `padded` is the padded group size, `kernel` a PGD_KERNEL_* choice.
 // `pages_per_cta` bounds the pages one split streams (it picks the ring depth).
 cudaError_t launch_decode_d64(const DecodeParams& p, const CUtensorMap& k_map,
                               const CUtensorMap& v_map, int padded, int kernel, int grid_splits,
