@@ -102,9 +102,9 @@ typedef struct {
  * per-page Q.K^T and P.V products run and in how tokens share page loads. */
 enum {
   PGD_KERNEL_AUTO = 0,          /* decode: windows of 1..128 positions go to the
-                                   window kernel (one CTA per row and kv head
-                                   copies exactly the window's K/V rows; mma.sync
-                                   products; no splits), anything else to
+                                   window kernel (the warps given each row and
+                                   kv head copy exactly the window's K/V rows;
+                                   mma.sync products; no splits), anything else to
                                    TENSOR_CORE; prefill: PREFILL_UMMA when the
                                    tokens average at least 8 per table row
                                    (prompt chunks), else as decode, per token */

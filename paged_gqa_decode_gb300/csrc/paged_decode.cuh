@@ -855,10 +855,11 @@ __device__ __forceinline__ void cp_async_wait_all() {
 
 // Sliding-window decode for windows of at most 64 * TILES positions
 // (GPT-OSS 20B model files, src/attention.linnet, SinkAttention.decode_rows:
-// key s is seen when n - window < s <= n).  One CTA per (kv head, row)
-// attends over exactly the window's positions, wherever they fall in the
-// row's pages, so no byte outside the window is read and no split or
-// combine is needed.  Local row r holds position lo + r; warp w owns local
+// key s is seen when n - window < s <= n).  A unit of 2 * TILES warps per
+// (row, kv head) attends over exactly the window's positions, wherever they
+// fall in the row's pages, so no byte outside the window is read and no split
+// or combine is needed.  A CTA holds UNITS units, each on its own shared
+// memory and named barrier.  Local row r holds position lo + r; warp w owns local
 // rows 32 w .. 32 w + 31: it reads the row's position and the table entries
 // itself, copies its rows of K and V, 16 bytes per lane at a time, straight
 // into shared memory (cp.async; rows past the attended count are
@@ -876,35 +877,61 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // window's last) is copied from k_new / v_new instead of the pool, and
 // stored into the pool at its slot by the warp owning that row, so the
 // kernel never reads the slot back.
-template <int D, int TILES>
+template <int D, int TILES, int UNITS = 1>
 struct WindowCfg {
-  static constexpr int kWarps = 2 * TILES;  // one warp per 32 rows
-  static constexpr int kThreads = 32 * kWarps;
+  static constexpr int kWarps = 2 * TILES;  // one warp per 32 rows of a unit
+  static constexpr int kUnitThreads = 32 * kWarps;
+  static constexpr int kThreads = UNITS * kUnitThreads;
   static constexpr int kChunks = D / 8;                // 16-byte chunks per row
   static constexpr int kRowStep = 32 / kChunks;        // rows one warp pass covers
   static constexpr int kPasses = 32 / kRowStep;
   static constexpr int kTileBytes = kPage * D * 2;     // 64 rows of K (or V)
   static constexpr int kBytes = TILES * kTileBytes;    // the window's K (or V)
-  static constexpr int kSmemBytes = 2 * kBytes;
-  static constexpr int kMinBlocks = (228 * 1024) / (kSmemBytes + 1024);
+  static constexpr int kUnitSmem = 2 * kBytes;
+  static constexpr int kSmemBytes = UNITS * kUnitSmem;
+  static constexpr int kMinBlocks = UNITS == 1 ? (228 * 1024) / (kUnitSmem + 1024) : 1;
   static constexpr int kHeads = MmaConsumer<D>::kHeads;
-  static constexpr int kPerThread = kHeads * D / kThreads;  // output dims per thread
-  static constexpr int kRun = kPerThread >= 8 ? 8 : 4;      // dims per store
+  static constexpr int kPerThread = kHeads * D / kUnitThreads;  // output dims per thread
+  static constexpr int kRun = kPerThread >= 8 ? 8 : 4;          // dims per store
   static_assert(kPerThread % kRun == 0 && D % kPerThread == 0, "output runs");
   static_assert(kWarps * kHeads * (D + 2) * 4 <= kBytes, "merge buffer");
+  static_assert(UNITS >= 1 && UNITS <= 15 && kThreads <= 1024 && kSmemBytes <= 227 * 1024,
+                "units per CTA");
 };
 
+// The most units one CTA can hold: shared memory, threads, and the 15 named
+// barriers a CTA has besides barrier 0.
 template <int D, int TILES>
-__global__ void __launch_bounds__(WindowCfg<D, TILES>::kThreads, WindowCfg<D, TILES>::kMinBlocks)
-    paged_decode_window_kernel(const DecodeParams p) {
+constexpr int window_max_units() {
   using C = WindowCfg<D, TILES>;
+  int u = (227 * 1024) / C::kUnitSmem;
+  if (u > 1024 / C::kUnitThreads) u = 1024 / C::kUnitThreads;
+  return u < 15 ? u : 15;
+}
+
+template <int D, int TILES, int UNITS>
+__global__ void __launch_bounds__(WindowCfg<D, TILES, UNITS>::kThreads,
+                                  WindowCfg<D, TILES, UNITS>::kMinBlocks)
+    paged_decode_window_kernel(const DecodeParams p) {
+  using C = WindowCfg<D, TILES, UNITS>;
   using Consumer = MmaConsumer<D>;
   constexpr int GP = C::kHeads;
   pdl_wait();
   pdl_allow_dependents();
-  const int kvh = blockIdx.x;
-  const int b = blockIdx.y;
-  const int tid = threadIdx.x;
+  // unit u of this CTA: (row b, kv head kvh), units numbered row-major
+  const int u = UNITS == 1 ? 0 : (int)threadIdx.x / C::kUnitThreads;
+  const int unit = blockIdx.x * UNITS + u;
+  if (unit >= p.rows * p.hkv) return;
+  const int kvh = unit % p.hkv;
+  const int b = unit / p.hkv;
+  const int tid = UNITS == 1 ? (int)threadIdx.x : (int)threadIdx.x % C::kUnitThreads;
+  // the unit's barrier: its own threads only (barrier 1 + u)
+  auto unit_sync = [&]() {
+    if constexpr (UNITS == 1)
+      __syncthreads();
+    else
+      asm volatile("bar.sync %0, %1;" ::"r"(1 + u), "r"(C::kUnitThreads) : "memory");
+  };
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int h0 = kvh * p.group;
@@ -949,8 +976,8 @@ __global__ void __launch_bounds__(WindowCfg<D, TILES>::kThreads, WindowCfg<D, TI
   cons.init(p, b, h0, lane, nullptr);  // q fragments load while the rows copy
 
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char* ks = smem_raw;
-  unsigned char* vs = smem_raw + C::kBytes;
+  unsigned char* ks = smem_raw + u * C::kUnitSmem;
+  unsigned char* vs = ks + C::kBytes;
   const bool append = p.k_new != nullptr;
   const int c = lane % C::kChunks;  // this lane's 16-byte column
   // element offset of column c of position 64 k of the window's page k
@@ -1000,11 +1027,11 @@ __global__ void __launch_bounds__(WindowCfg<D, TILES>::kThreads, WindowCfg<D, TI
     cons.template page<2>(smem_addr(ks + slice), vs + slice, 0, rhi, lane);
   }
   cons.finish();
-  __syncthreads();  // every warp is done with the rows
+  unit_sync();  // every warp of the unit is done with the rows
 
   float* red = reinterpret_cast<float*>(ks);  // [kWarps][GP][D + 2]
   cons.store(red, warp, lane);
-  __syncthreads();
+  unit_sync();
   if (!live) return;
   float mx = sink, f[C::kWarps];
 #pragma unroll
@@ -1047,10 +1074,10 @@ __global__ void __launch_bounds__(WindowCfg<D, TILES>::kThreads, WindowCfg<D, TI
   }
 }
 
-template <int D, int TILES>
-cudaError_t launch_window(const DecodeParams& p, cudaStream_t stream) {
-  using C = WindowCfg<D, TILES>;
-  auto kern = paged_decode_window_kernel<D, TILES>;
+template <int D, int TILES, int UNITS>
+cudaError_t launch_window_units(const DecodeParams& p, cudaStream_t stream) {
+  using C = WindowCfg<D, TILES, UNITS>;
+  auto kern = paged_decode_window_kernel<D, TILES, UNITS>;
   static std::atomic<bool> configured[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1064,7 +1091,35 @@ cudaError_t launch_window(const DecodeParams& p, cudaStream_t stream) {
     if (dev >= 0 && dev < 64) configured[dev].store(true, std::memory_order_release);
   }
   if (p.rows == 0) return cudaSuccess;
-  return launch_pdl(kern, dim3(p.hkv, p.rows), dim3(C::kThreads), C::kSmemBytes, stream, p);
+  const int units = p.rows * p.hkv;
+  return launch_pdl(kern, dim3((units + UNITS - 1) / UNITS), dim3(C::kThreads), C::kSmemBytes,
+                    stream, p);
+}
+
+// One unit (row, kv head) per CTA lets the block scheduler fill each SM with
+// kMinBlocks CTAs.  When that takes two rounds but the units fit one round of
+// CTAs holding as many units as shared memory allows (the hardware reserves
+// shared memory per CTA, so one large CTA per SM holds a unit more), the large
+// CTAs are launched instead: one round, no second wave of late units.
+template <int D, int TILES>
+cudaError_t launch_window(const DecodeParams& p, cudaStream_t stream) {
+  constexpr int kUnits = window_max_units<D, TILES>();
+  if constexpr (kUnits > WindowCfg<D, TILES>::kMinBlocks) {
+    static std::atomic<int> sms[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int n = dev >= 0 && dev < 64 ? sms[dev].load(std::memory_order_relaxed) : 0;
+    if (n == 0) {
+      e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+      if (dev >= 0 && dev < 64) sms[dev].store(n, std::memory_order_relaxed);
+    }
+    const long long units = (long long)p.rows * p.hkv;
+    if (units > (long long)n * WindowCfg<D, TILES>::kMinBlocks && units <= (long long)n * kUnits)
+      return launch_window_units<D, TILES, kUnits>(p, stream);
+  }
+  return launch_window_units<D, TILES, 1>(p, stream);
 }
 
 template <int D, int STAGES, class Consumer, int WARPS = 4>

@@ -69,7 +69,7 @@ struct DecodeParams {
 };
 
 // With PGD_KERNEL_AUTO, decode windows of 1 .. kMaxWindowKernel positions go
-// to the window kernel (one CTA per row and kv head, no splits).
+// to the window kernel (a unit of warps per row and kv head, no splits).
 constexpr int kMaxWindowKernel = 128;
 
 // Padded query-group sizes that have a decode kernel instantiation.

@@ -209,6 +209,65 @@ def test_split_kernel_windows(hq, hkv, d, window, pps):
                   what=f"split kernel hq={hq} d={d} w={window} pps={pps}")
 
 
+def window_rounds(d: int, window: int, sms: int) -> tuple[int, int]:
+    """(one-unit CTAs per SM, units per large CTA) of the window kernel:
+    a unit (row, kv head) keeps the window's K and V in shared memory, the
+    hardware reserves 1 KB per CTA out of 228 KB per SM, and a CTA holds at
+    most 227 KB, 1024 threads (a warp per 32 window rows) and 15 units."""
+    tiles = 1 if window <= 64 else 2
+    unit_smem = 2 * tiles * 64 * d * 2
+    per_sm = (228 * 1024) // (unit_smem + 1024)
+    units = min((227 * 1024) // unit_smem, 1024 // (64 * tiles), 15)
+    return per_sm, units
+
+
+@pytest.mark.parametrize("d,window", [(64, 128), (64, 100), (64, 65), (64, 64), (64, 7),
+                                      (128, 64), (128, 33)])
+@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("beyond", [False, True])
+def test_window_kernel_one_round_of_large_ctas(d, window, fused, beyond):
+    """A batch whose (row, kv head) units take two rounds of one-unit CTAs
+    but fit one round of CTAs holding as many units as shared memory allows:
+    the window kernel launches the large CTAs (each unit on a barrier of its
+    own, the last CTA partly empty).  With `beyond`, a batch just past one
+    round of large CTAs, which goes back to one-unit CTAs over several
+    rounds.  Every row against the oracle, with inactive rows, contexts
+    shorter than the window and the append either fused into the decode
+    launch or a call of its own.  V is scaled by 1/4 (exact in bf16): rows of
+    one or two positions output about one V row, and above |out| = 2.56
+    rounding to bf16 alone can exceed the 1e-2 absolute bound."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    per_sm, units = window_rounds(d, window, sms)
+    if units <= per_sm:
+        pytest.skip("large CTAs hold no more units per SM than one-unit CTAs")
+    hkv = 8
+    if beyond:
+        rows = (sms * units) // hkv + 3      # past one round of large CTAs
+        assert rows * hkv > sms * units
+    else:
+        rows = (sms * per_sm) // hkv + 9     # more than one round of one-unit CTAs
+        assert sms * per_sm < rows * hkv <= sms * units and (rows * hkv) % units != 0
+    wl = Workload("window_round", rows=rows, q_heads=64, kv_heads=hkv, head_dim=d, ctx_lo=1,
+                  ctx_hi=300, window=window, sinks=True)
+    base = [0, 1, 2, 7, 63, 64, 65, 100, 127, 128, 129, 191, 192, 193, 255, 300]
+    contexts = [base[(7 * b) % len(base)] for b in range(rows)]
+    lay = layout_from_contexts(wl, contexts, seed=d + window + rows)
+    batch = make_batch(wl, seed=41 + window + d, device=DEV, layout=lay)
+    batch.v_pool.mul_(0.25)
+    batch.v_new.mul_(0.25)
+    if not fused:
+        run_and_check(batch, what=f"window kernel d={d} w={window} rows={rows}")
+        return
+    idx = np.arange(rows)
+    host = snapshot_rows(batch, idx)
+    got = pgd.paged_decode_step(batch.q, batch.k_new, batch.v_new, batch.k_pool, batch.v_pool,
+                                batch.table, batch.positions, batch.sinks, window, wl.scale,
+                                num_kv_heads=hkv)
+    assert pgd.get_device_error() == pgd.OK
+    want, _, _ = oracle_step(batch, host, window=window, sinks=batch.sinks, scale=wl.scale)
+    compare(got, want, f"window kernel, decode step d={d} w={window} rows={rows}")
+
+
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("pps", [0, 3])
 def test_head_major_layout(d, pps):
