@@ -38,6 +38,21 @@ MUTANTS = {
                                 "const float scaled = ((float)i * 1.0f) / (float)head_dim;"),
     "value_from_key": ("const uint16_t* vj = v + (int64_t)(lo + j) * head_dim;",
                        "const uint16_t* vj = k + (int64_t)(lo + j) * head_dim;"),
+    "newest_key_dropped": ("int count = n - lo + 1;", "int count = n - lo;"),
+    "weights_not_normalised": ("double p = exp(score[j] - m) / z;",
+                               "double p = exp(score[j] - m);"),
+    "kv_head_values_unstrided": ("v_rows + (int64_t)g * stride * d_head, n, d_head,",
+                                 "v_rows + (int64_t)g * d_head, n, d_head,"),
+    "lse_real_against_sink_max": ("z_real += exp(score[j] - m_real);",
+                                  "z_real += exp(score[j] - m);"),
+    "dense_rows_kv_heads_unstrided": (
+        "k_rows = job->k + (int64_t)b * job->kv_heads * job->key_stride * d_head;",
+        "k_rows = job->k + (int64_t)b * job->key_stride * d_head;"),
+    "rope_angle_sin_cos_swapped": ("cos_out[i] = f64_to_bf16_rne(cos((double)angle));",
+                                   "cos_out[i] = f64_to_bf16_rne(sin((double)angle));"),
+    "head_major_head_stride": (
+        "return ((int64_t)kv_head * num_pages * page_size + slot) * head_dim + d;",
+        "return ((int64_t)kv_head * page_size + slot) * head_dim + d;"),
 }
 
 
