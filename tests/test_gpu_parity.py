@@ -512,6 +512,49 @@ def test_window_kernel_reads_only_the_window_table_entries():
     assert torch.all(out_pos[2] == 0) and torch.equal(out_pos[:2], out[:2])
 
 
+def test_window_kernel_large_ctas_bad_entries():
+    """The window kernel's large CTAs (several units each): units whose row
+    has a bad table entry inside its window or a position beyond its table
+    leave early, zero their outputs and report; the other units of the same
+    CTAs, which synchronise on barriers of their own, match the oracle."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    per_sm, units = window_rounds(64, 128, sms)
+    if units <= per_sm:
+        pytest.skip("large CTAs hold no more units per SM than one-unit CTAs")
+    hkv = 8
+    rows = (sms * per_sm) // hkv + 9
+    wl = Workload("window_bad", rows=rows, q_heads=64, kv_heads=hkv, head_dim=64, ctx_lo=1,
+                  ctx_hi=600, window=128, sinks=True)
+    contexts = [[600, 300, 129, 64, 0, 1][b % 6] for b in range(rows)]
+    lay = layout_from_contexts(wl, contexts, seed=29)
+    batch = make_batch(wl, seed=105, device=DEV, layout=lay)
+    batch.v_pool.mul_(0.25)
+    batch.v_new.mul_(0.25)
+    host = snapshot_rows(batch, np.arange(rows))
+    pgd.kv_append_paged(batch.k_new, batch.v_new, batch.table, batch.positions, batch.k_pool,
+                        batch.v_pool)
+    assert pgd.get_device_error() == pgd.OK
+    table = batch.table.clone()
+    positions = batch.positions.clone()
+    bad = [0, 7, 13, rows - 1]
+    table[0, 9] = -1                               # row 0 (n = 599): its window's last page
+    table[7, 4] = 10 ** 6                          # row 7 (n = 299): inside its window
+    positions[13] = 64 * batch.table.shape[1] + 5  # beyond its table row
+    table[rows - 1, 1] = 10 ** 6                   # last row (n = 599 or less), if in its window
+    n_last = int(positions[rows - 1])
+    if n_last < 0 or not (max(0, n_last - 127) // 64 <= 1 <= n_last // 64):
+        bad.remove(rows - 1)
+    out = pgd.paged_decode_attention(batch.q, batch.k_pool, batch.v_pool, table, positions,
+                                     batch.sinks, 128, wl.scale, num_kv_heads=hkv)
+    assert pgd.get_device_error() == pgd.EDEVICE_BOUNDS
+    for b in bad:
+        assert torch.all(out[b] == 0), f"row {b} not zeroed"
+    want, _, _ = oracle_step(batch, host, window=128, sinks=batch.sinks, scale=wl.scale)
+    good = np.array([b for b in range(rows) if b not in bad])
+    compare(out.index_select(0, torch.as_tensor(good, device=out.device)), want[good],
+            "window kernel large CTAs, rows beside bad ones")
+
+
 def test_host_validation():
     q = torch.zeros(2, 8, 64, dtype=torch.bfloat16, device=DEV)
     pool = torch.zeros(4 * 2 * 64 * 64, dtype=torch.bfloat16, device=DEV)
