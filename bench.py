@@ -779,11 +779,14 @@ def run_prefill(args, wl):
                      dtype=torch.uint8, device=device)
     slots = torch.empty(work["tokens"], dtype=torch.int32, device=device)
 
+    def attention():
+        pgd.paged_prefill_attention(b.q, b.k_pool, b.v_pool, b.table, b.rows, b.positions,
+                                    b.sinks, wl.window, wl.scale, out=out, workspace=ws, **opts)
+
     def step():
         s_ = pgd.page_slots(b.table, b.positions, b.rows, num_pages=b.num_pages)
         pgd.kv_write_slots(b.k_new, b.v_new, s_, b.k_pool, b.v_pool)
-        pgd.paged_prefill_attention(b.q, b.k_pool, b.v_pool, b.table, b.rows, b.positions,
-                                    b.sinks, wl.window, wl.scale, out=out, workspace=ws, **opts)
+        attention()
 
     for _ in range(args.warmup):
         step()
@@ -800,11 +803,24 @@ def run_prefill(args, wl):
     torch.cuda.synchronize()
     assert pgd.get_device_error() == pgd.OK
     ms = sum(a.elapsed_time(z) for a, z in e) / args.steps
+    # the attention call alone (its kernels: the block-order pass and the
+    # attention kernel), between the same flushes, for the roofline
+    spans = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush(i)
+        spans[i][0].record(stream)
+        attention()
+        spans[i][1].record(stream)
+    torch.cuda.synchronize()
+    assert pgd.get_device_error() == pgd.OK
+    attn_ms = sum(a.elapsed_time(z) for a, z in spans) / args.steps
     del slots
     hbm, hbm_kind = measured_peak()
     tf, tf_kind = measured_tensor_peak()
     gbs = work["bytes"] / (ms * 1e-3) / 1e9
     tflops = work["flops"] / (ms * 1e-3) / 1e12
+    attn_tflops = work["flops"] / (attn_ms * 1e-3) / 1e12
+    attn_gbs = (work["kv"] + work["q_out"]) / (attn_ms * 1e-3) / 1e9
     bound = "tensor" if work["flops"] / (tf * 1e12) > work["bytes"] / (hbm * 1e9) else "hbm"
     line = {
         "metric": "paged prefill attention: tokens/s (achieved GB/s, TFLOP/s)",
@@ -816,13 +832,16 @@ def run_prefill(args, wl):
                                f"chunk {wl.chunk}, window {wl.window}, sinks {wl.sinks}",
                    "tokens": work["tokens"], "l2": L2Flush.label,
                    "kernel": args.kernel},
-        "gbs": gbs, "tflops": tflops,
+        "gbs": gbs, "tflops": tflops, "attention_ms_per_step": attn_ms,
         "roofline": {"bound": bound,
-                     "achieved": tflops if bound == "tensor" else gbs,
+                     "kernel": "paged_prefill_attention (the attention call: block-order "
+                               "pass and attention kernel), timed alone between flushes",
+                     "achieved": attn_tflops if bound == "tensor" else attn_gbs,
                      "peak": tf if bound == "tensor" else hbm,
                      "peak_kind": tf_kind if bound == "tensor" else hbm_kind,
                      "unit": "TFLOP/s" if bound == "tensor" else "GB/s",
-                     "frac": tflops / tf if bound == "tensor" else gbs / hbm},
+                     "frac": attn_tflops / tf if bound == "tensor" else attn_gbs / hbm,
+                     "algorithmic_flops_per_launch": work["flops"]},
         "work": work,
         # page_slots + kv_write_slots + the attention call's kernels
         "gpu_launches": (2 + pgd.attention_kernel_count(
