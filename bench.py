@@ -761,8 +761,9 @@ def measured_tensor_peak() -> tuple[float, str]:
 
 
 def run_prefill(args, wl):
-    """Prefill step: page_slots + kv_write_slots + paged_prefill_attention over
-    the packed chunks (one GPU)."""
+    """Prefill step over the packed chunks (one GPU): one paged_prefill_step
+    call (the tokens' writes, then the attention), or with --two-calls
+    page_slots + kv_write_slots + paged_prefill_attention."""
     import paged_gqa_decode_gb300 as pgd
     from pgd_inputs import PREFILL_WORKLOADS, make_prefill_batch
     device = torch.device("cuda", 0)
@@ -784,6 +785,11 @@ def run_prefill(args, wl):
                                     b.sinks, wl.window, wl.scale, out=out, workspace=ws, **opts)
 
     def step():
+        if not args.two_calls:
+            pgd.paged_prefill_step(b.q, b.k_new, b.v_new, b.k_pool, b.v_pool, b.table, b.rows,
+                                   b.positions, b.sinks, wl.window, wl.scale, out=out,
+                                   workspace=ws, **opts)
+            return
         s_ = pgd.page_slots(b.table, b.positions, b.rows, num_pages=b.num_pages)
         pgd.kv_write_slots(b.k_new, b.v_new, s_, b.k_pool, b.v_pool)
         attention()
@@ -831,7 +837,9 @@ def run_prefill(args, wl):
                                f"d{wl.head_dim}, prefix U[{wl.prefix_lo},{wl.prefix_hi}], "
                                f"chunk {wl.chunk}, window {wl.window}, sinks {wl.sinks}",
                    "tokens": work["tokens"], "l2": L2Flush.label,
-                   "kernel": args.kernel},
+                   "kernel": args.kernel,
+                   "step": "page_slots + kv_write_slots + paged_prefill_attention"
+                   if args.two_calls else "paged_prefill_step (writes, then attention)"},
         "gbs": gbs, "tflops": tflops, "attention_ms_per_step": attn_ms,
         "roofline": {"bound": bound,
                      "kernel": "paged_prefill_attention (the attention call: block-order "
@@ -843,10 +851,13 @@ def run_prefill(args, wl):
                      "frac": attn_tflops / tf if bound == "tensor" else attn_gbs / hbm,
                      "algorithmic_flops_per_launch": work["flops"]},
         "work": work,
-        # page_slots + kv_write_slots + the attention call's kernels
-        "gpu_launches": (2 + pgd.attention_kernel_count(
-            dims, b.table.shape[0], wl.window, args.pages_per_split,
-            KERNEL_IDS[args.kernel])) * args.steps,
+        # the step's kernels: page_slots + kv_write_slots + the attention
+        # call's, or the prefill step's
+        "gpu_launches": ((2 + pgd.attention_kernel_count(
+            dims, b.table.shape[0], wl.window, args.pages_per_split, KERNEL_IDS[args.kernel]))
+            if args.two_calls else pgd.prefill_step_kernel_count(
+                dims, b.table.shape[0], wl.window, args.pages_per_split,
+                KERNEL_IDS[args.kernel])) * args.steps,
     }
     print(json.dumps(line), flush=True)
 
@@ -935,7 +946,9 @@ def main():
                          "also the token-block kernels (mma.sync 'tiled', tcgen05 'umma')")
     ap.add_argument("--two-calls", action="store_true",
                     help="kv_append_paged and paged_decode_attention as two calls (default: "
-                         "one paged_decode_step call, the append inside the decode launch)")
+                         "one paged_decode_step call, the append inside the decode launch); "
+                         "with --path prefill, page_slots + kv_write_slots + "
+                         "paged_prefill_attention instead of one paged_prefill_step call")
     ap.add_argument("--rope", action="store_true",
                     help="decode path: fuse rope_rows (base 1e6) into the append")
     ap.add_argument("--rows", type=int, default=0,

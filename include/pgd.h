@@ -315,6 +315,46 @@ PGD_API int pgd_paged_prefill_attention(const pgd_dims* dims, int32_t table_rows
                                         size_t workspace_bytes, const pgd_decode_options* opts,
                                         pgd_stream_t stream);
 
+/*
+ * paged_prefill_step -- the prefill call with the tokens' writes in it
+ * (Mistral 7B Instruct v0.3 model files, src/attention.linnet, prefill_paged:
+ * page_slots and write_tokens for every packed token, then the attention):
+ * the same as pgd_page_slots + pgd_kv_write_slots + pgd_paged_prefill_attention
+ * with the same arguments, in fewer launches.  Token p's k_new / v_new rows go
+ * to position positions[p] % 64 of page table[rows[p]][positions[p] / 64]
+ * (tokens with a negative position are not written), then every token
+ * attends as in pgd_paged_prefill_attention, its own and its row's other new
+ * keys included.
+ *   k_new, v_new  bf16 [P][Hkv][D] device pointers, 16-byte aligned.
+ *   k_pool, v_pool  written (the tokens' slots) and read.
+ *   Others as for pgd_paged_prefill_attention.
+ * Launches: one kernel writes the tokens (with PREFILL_UMMA its first CTA
+ * also prepares the attention kernel's work counter and block order in the
+ * workspace), then the attention kernels; pgd_prefill_step_kernel_count
+ * gives the number.  Two tokens with the same slot race, as with
+ * pgd_kv_write_slots.
+ * Device errors: a token whose row, page index or page is out of range is
+ * reported (PGD_EDEVICE_BOUNDS), not written, and its output is zero; others
+ * as for pgd_paged_prefill_attention.
+ */
+PGD_API int pgd_paged_prefill_step(const pgd_dims* dims, int32_t table_rows, const void* q,
+                                   const void* k_new, const void* v_new, void* k_pool,
+                                   void* v_pool, const int32_t* table, const int32_t* rows,
+                                   const int32_t* positions, const float* sinks, int32_t window,
+                                   float scale, void* out, void* workspace,
+                                   size_t workspace_bytes, const pgd_decode_options* opts,
+                                   pgd_stream_t stream);
+
+/* Kernels one pgd_paged_prefill_step call with these arguments launches on
+ * the current device: the write launch plus the attention kernels (for
+ * PREFILL_UMMA the attention kernel alone, its counter and order prepared by
+ * the write launch).  table_rows > 0; count 0 when dims->rows == 0.  Returns
+ * PGD_EINVAL for a NULL count or table_rows <= 0, else as
+ * pgd_attention_kernel_count. */
+PGD_API int pgd_prefill_step_kernel_count(const pgd_dims* dims, int32_t table_rows,
+                                          int32_t window, const pgd_decode_options* opts,
+                                          int32_t* count);
+
 /* Size of the library's own device scratch buffer used by
  * pgd_paged_decode_attention_static: 64 MiB on every device that loads the
  * library, held until the process exits. */

@@ -90,6 +90,12 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                                        i32, ctypes.c_float, vp, vp,
                                                        ctypes.c_size_t, opts_p, vp]
             lib.pgd_paged_prefill_attention.restype = ctypes.c_int
+            lib.pgd_paged_prefill_step.argtypes = [dims_p, i32, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                   vp, i32, ctypes.c_float, vp, vp,
+                                                   ctypes.c_size_t, opts_p, vp]
+            lib.pgd_paged_prefill_step.restype = ctypes.c_int
+            lib.pgd_prefill_step_kernel_count.argtypes = [dims_p, i32, i32, opts_p, vp]
+            lib.pgd_prefill_step_kernel_count.restype = ctypes.c_int
             lib.pgd_paged_decode_workspace_bytes.argtypes = [dims_p, opts_p]
             lib.pgd_paged_decode_workspace_bytes.restype = ctypes.c_size_t
             lib.pgd_attention_kernel_count.argtypes = [dims_p, i32, i32, opts_p, vp]
@@ -374,7 +380,33 @@ def paged_prefill_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch
     """Packed prompt tokens: token p (q bf16 [P, Hq, D]) attends over table row
     rows[p]'s pages up to positions[p].  Prompts and decode steps can share one
     call (a step of row b is a token with rows[p] = b).  Returns bf16 [P, Hq, D]."""
-    dev = _check_cuda(q, k_pool, v_pool, table, rows, positions, sinks, out, workspace)
+    return _prefill(q, None, None, k_pool, v_pool, table, rows, positions, sinks, window, scale,
+                    num_kv_heads, layout, out, workspace, pages_per_split, kernel, stream)
+
+
+def paged_prefill_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                       k_pool: torch.Tensor, v_pool: torch.Tensor, table: torch.Tensor,
+                       rows: torch.Tensor, positions: torch.Tensor,
+                       sinks: torch.Tensor | None = None, window: int = 0,
+                       scale: float | None = None, *, num_kv_heads: int,
+                       layout: int = PAGE_MAJOR, out: torch.Tensor | None = None,
+                       workspace: torch.Tensor | None = None, pages_per_split: int = 0,
+                       kernel: int = KERNEL_AUTO,
+                       stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """The prefill call with the tokens' writes in it: token p's k_new / v_new
+    (bf16 [P, Hkv, D]) go to its slot of table row rows[p] at positions[p],
+    then every token attends as in paged_prefill_attention -- the same as
+    page_slots + kv_write_slots + paged_prefill_attention.  Returns bf16
+    [P, Hq, D]."""
+    return _prefill(q, k_new, v_new, k_pool, v_pool, table, rows, positions, sinks, window,
+                    scale, num_kv_heads, layout, out, workspace, pages_per_split, kernel, stream)
+
+
+def _prefill(q, k_new, v_new, k_pool, v_pool, table, rows, positions, sinks, window, scale,
+             num_kv_heads, layout, out, workspace, pages_per_split, kernel, stream):
+    step = k_new is not None
+    dev = _check_cuda(q, k_new, v_new, k_pool, v_pool, table, rows, positions, sinks, out,
+                      workspace)
     _dtype(q, torch.bfloat16, "q")
     _dtype(k_pool, torch.bfloat16, "k_pool")
     _dtype(v_pool, torch.bfloat16, "v_pool")
@@ -387,6 +419,13 @@ def paged_prefill_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch
     if positions.shape != (tokens,) or rows.shape != (tokens,) or table.dim() != 2 \
             or k_pool.shape != v_pool.shape or (sinks is not None and sinks.shape != (hq,)):
         raise ValueError("inconsistent shapes")
+    if step:
+        if v_new is None:
+            raise ValueError("k_new and v_new go together")
+        _dtype(k_new, torch.bfloat16, "k_new")
+        _dtype(v_new, torch.bfloat16, "v_new")
+        if k_new.shape != (tokens, num_kv_heads, d) or v_new.shape != k_new.shape:
+            raise ValueError("k_new and v_new are bf16 [P, Hkv, D]")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     dims = make_dims(rows=tokens, num_q_heads=hq, num_kv_heads=num_kv_heads, head_dim=d,
@@ -402,14 +441,34 @@ def paged_prefill_attention(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch
         need = lib.pgd_paged_decode_workspace_bytes(ctypes.byref(dims), ctypes.byref(opts))
         if workspace is None:
             workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
-        rc = lib.pgd_paged_prefill_attention(
-            ctypes.byref(dims), table.shape[0], _ptr(q), _ptr(k_pool), _ptr(v_pool),
-            _ptr(table), _ptr(rows), _ptr(positions), _ptr(sinks), int(window), float(scale),
-            _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
-            ctypes.byref(opts), _stream_handle(stream))
+        ws = (_ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+              ctypes.byref(opts), _stream_handle(stream))
+        tail = (_ptr(table), _ptr(rows), _ptr(positions), _ptr(sinks), int(window),
+                float(scale))
+        if step:
+            rc = lib.pgd_paged_prefill_step(ctypes.byref(dims), table.shape[0], _ptr(q),
+                                            _ptr(k_new), _ptr(v_new), _ptr(k_pool),
+                                            _ptr(v_pool), *tail, *ws)
+        else:
+            rc = lib.pgd_paged_prefill_attention(ctypes.byref(dims), table.shape[0], _ptr(q),
+                                                 _ptr(k_pool), _ptr(v_pool), *tail, *ws)
     if rc != OK:
-        raise PgdError(rc, "paged_prefill_attention")
+        raise PgdError(rc, "paged_prefill_step" if step else "paged_prefill_attention")
     return out
+
+
+def prefill_step_kernel_count(dims: Dims, table_rows: int, window: int = 0,
+                              pages_per_split: int = 0, kernel: int = KERNEL_AUTO) -> int:
+    """Kernels one paged_prefill_step call with these arguments launches on
+    the current device."""
+    opts = DecodeOptions(pages_per_split, kernel)
+    count = ctypes.c_int32(0)
+    rc = load_library().pgd_prefill_step_kernel_count(ctypes.byref(dims), int(table_rows),
+                                                      int(window), ctypes.byref(opts),
+                                                      ctypes.byref(count))
+    if rc != OK:
+        raise PgdError(rc, "prefill_step_kernel_count")
+    return count.value
 
 
 def _dense_dims(cache: torch.Tensor, rows: int, num_q_heads: int) -> Dims:

@@ -833,13 +833,11 @@ constexpr int kMaxSortedBlocks = 4096;
 // another table row); equal spans keep the later block first.  A bitonic
 // sort of (span, block) keys in shared memory.  (Templated on the head_dim
 // only to give each translation unit its own instance.)
-template <int D>
-__global__ void __launch_bounds__(1024) prefill_block_order_kernel(const DecodeParams p,
-                                                                   int block_tokens, int n_blocks,
-                                                                   int* counter, int* order) {
-  pdl_wait();
-  pdl_allow_dependents();
-  __shared__ unsigned long long key[kMaxSortedBlocks];
+// The block order, by one CTA (blockDim threads, `key` in its shared memory:
+// kMaxSortedBlocks entries).
+__device__ __forceinline__ void order_blocks(const DecodeParams& p, int block_tokens,
+                                             int n_blocks, int* counter, int* order,
+                                             unsigned long long* key) {
   if (threadIdx.x == 0) *counter = 0;
   int n2 = 1;
   while (n2 < n_blocks) n2 <<= 1;
@@ -879,10 +877,78 @@ __global__ void __launch_bounds__(1024) prefill_block_order_kernel(const DecodeP
     order[b] = n_blocks - 1 - (int)(key[b] & 0xffffffffu);
 }
 
+template <int D>
+__global__ void __launch_bounds__(1024) prefill_block_order_kernel(const DecodeParams p,
+                                                                   int block_tokens, int n_blocks,
+                                                                   int* counter, int* order) {
+  pdl_wait();
+  pdl_allow_dependents();
+  __shared__ unsigned long long key[kMaxSortedBlocks];
+  order_blocks(p, block_tokens, n_blocks, counter, order, key);
+}
+
+// The prefill step's first launch (prefill_paged: page_slots + write_tokens,
+// then the attention): CTA 0 prepares the tcgen05 kernel's work counter (and,
+// when `order` is given, the longest-first block order); the other CTAs
+// write each packed token's K and V at its slot, table[rows[t]][n / 64] * 64
+// + n % 64 for its position n, one warp per token.  Inactive tokens (n < 0)
+// are skipped; a token whose row, page index or page is out of range is
+// reported (PGD_EDEVICE_BOUNDS) and not written, as page_slots and the write
+// at slots would leave it.
+template <int D>
+__global__ void __launch_bounds__(1024) prefill_write_kernel(const DecodeParams p,
+                                                             int block_tokens, int n_blocks,
+                                                             int* counter, int* order) {
+  pdl_wait();
+  pdl_allow_dependents();
+  __shared__ unsigned long long key[kMaxSortedBlocks];
+  if (blockIdx.x == 0) {
+    if (order)
+      order_blocks(p, block_tokens, n_blocks, counter, order, key);
+    else if (counter && threadIdx.x == 0)
+      *counter = 0;
+    return;
+  }
+  constexpr int kChunks = D / 8;  // 16-byte chunks of a head's row
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x - 1) * (blockDim.x >> 5);
+  for (int t = (blockIdx.x - 1) * (blockDim.x >> 5) + (threadIdx.x >> 5); t < p.rows;
+       t += warps) {
+    int page = -1, in_page = 0;
+    if (lane == 0) {
+      const int n = p.positions[t];
+      const int row = p.row_of ? p.row_of[t] : t;
+      if (n >= 0) {
+        const bool bad_row = p.row_of && (row < 0 || row >= p.table_rows);
+        const int pg = (!bad_row && n / kPage < p.maxp) ? page_of(p.table, row, n / kPage, p.maxp)
+                                                        : -1;
+        if (pg < 0 || pg >= p.num_pages)
+          record_error(p.err, PGD_EDEVICE_BOUNDS);
+        else
+          page = pg;
+        in_page = n % kPage;
+      }
+    }
+    page = __shfl_sync(0xffffffffu, page, 0);
+    in_page = __shfl_sync(0xffffffffu, in_page, 0);
+    if (page < 0) continue;
+    for (int c = lane; c < 2 * p.hkv * kChunks; c += 32) {
+      const int which = c / (p.hkv * kChunks);
+      const int h = (c / kChunks) % p.hkv, ch = c % kChunks;
+      const uint16_t* src = (which ? p.v_new : p.k_new) + ((size_t)t * p.hkv + h) * D + ch * 8;
+      const int64_t row0 = tile_first_row(p.layout, page, h, p.hkv, p.num_pages, p.maxp);
+      uint16_t* dst = (which ? p.v_pool : p.k_pool) + ((size_t)row0 + in_page) * D + ch * 8;
+      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+    }
+  }
+}
+
+// `prepared`: the step's write launch has already zeroed the work counter and
+// written the block order (prefill_write_kernel).
 template <int D, int RK, int RV>
 cudaError_t launch_prefill_umma(const DecodeParams& p, const CUtensorMap& k_map,
                                 const CUtensorMap& v_map, const CUtensorMap& q_map, int sm_count,
-                                cudaStream_t stream) {
+                                bool prepared, cudaStream_t stream) {
   using C = UmmaPrefillCfg<D, RK, RV>;
   static std::atomic<bool> configured[64];
   int dev = 0;
@@ -903,7 +969,9 @@ cudaError_t launch_prefill_umma(const DecodeParams& p, const CUtensorMap& k_map,
   int* counter = reinterpret_cast<int*>(p.ws_acc);
   const int n_blocks = (p.rows + tokens - 1) / tokens;
   int* order = p.window == 0 && n_blocks <= kMaxSortedBlocks ? counter + 4 : nullptr;
-  if (order)
+  if (prepared)
+    e = cudaSuccess;
+  else if (order)
     e = launch_pdl(prefill_block_order_kernel<D>, dim3(1), dim3(1024), 0, stream, p, tokens,
                    n_blocks, counter, order);
   else

@@ -422,8 +422,8 @@ static int decode_impl(const pgd_dims* dims, int32_t table_rows, const int32_t* 
     return PGD_EINVAL;  // dense rows: every row needs its own P pages
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
     return PGD_EINVAL;
-  if ((k_new == nullptr) != (v_new == nullptr) || (k_new && (row_of != nullptr ||
-                                                             !aligned16(k_new) || !aligned16(v_new))))
+  if ((k_new == nullptr) != (v_new == nullptr) ||
+      (k_new && (!aligned16(k_new) || !aligned16(v_new))))
     return PGD_EINVAL;
   if (!std::isfinite(scale)) return PGD_EINVAL;
   DeviceInfo* dev = nullptr;
@@ -479,14 +479,25 @@ static int decode_impl(const pgd_dims* dims, int32_t table_rows, const int32_t* 
   const int pages_per_cta = grid_pages < pl.pages_per_split ? grid_pages : pl.pages_per_split;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (kernel == PGD_KERNEL_PREFILL_UMMA) {
-    CUtensorMap q_map;
-    if ((rc = encode_q_map(&q_map, q, dims)) != PGD_OK) return rc;
-    return launch_prefill_umma(p, k_map, v_map, q_map, dims->head_dim, dev->sm_count, st) ==
-                   cudaSuccess
+  // prefill step: the tokens' K and V are written by a launch of their own
+  // first (a token's keys are read by the other tokens of its row), which
+  // also prepares the tcgen05 kernel's work counter and block order
+  const bool prefill_write = k_new != nullptr && row_of != nullptr;
+  CUtensorMap q_map;
+  if (kernel == PGD_KERNEL_PREFILL_UMMA && (rc = encode_q_map(&q_map, q, dims)) != PGD_OK)
+    return rc;
+  if (prefill_write) {
+    if (launch_prefill_write(p, dims->head_dim, kernel == PGD_KERNEL_PREFILL_UMMA, st) !=
+        cudaSuccess)
+      return PGD_ECUDA;
+    p.k_new = p.v_new = nullptr;
+    p.k_pool = p.v_pool = nullptr;
+  }
+  if (kernel == PGD_KERNEL_PREFILL_UMMA)
+    return launch_prefill_umma(p, k_map, v_map, q_map, dims->head_dim, dev->sm_count,
+                               prefill_write, st) == cudaSuccess
                ? PGD_OK
                : PGD_ECUDA;
-  }
   if (kernel == PGD_KERNEL_PREFILL_TILED)
     return launch_prefill_tiled(p, k_map, v_map, dims->head_dim, padded, st) == cudaSuccess
                ? PGD_OK
@@ -531,6 +542,38 @@ int pgd_paged_prefill_attention(const pgd_dims* dims, int32_t table_rows, const 
   if (dims->rows > 0 && !rows) return PGD_EINVAL;
   return decode_impl(dims, table_rows, rows, q, k_pool, v_pool, table, positions, sinks, window,
                      scale, out, workspace, workspace_size, opts, stream);
+}
+
+int pgd_paged_prefill_step(const pgd_dims* dims, int32_t table_rows, const void* q,
+                           const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                           const int32_t* table, const int32_t* rows, const int32_t* positions,
+                           const float* sinks, int32_t window, float scale, void* out,
+                           void* workspace, size_t workspace_size,
+                           const pgd_decode_options* opts, pgd_stream_t stream) {
+  const int rc = check_dims(dims);
+  if (rc != PGD_OK) return rc;
+  if (dims->rows > 0 && (!rows || !k_new || !v_new)) return PGD_EINVAL;
+  return decode_impl(dims, table_rows, rows, q, k_pool, v_pool, table, positions, sinks, window,
+                     scale, out, workspace, workspace_size, opts, stream, k_new, v_new);
+}
+
+int pgd_prefill_step_kernel_count(const pgd_dims* dims, int32_t table_rows, int32_t window,
+                                  const pgd_decode_options* opts, int32_t* count) {
+  if (!count) return PGD_EINVAL;
+  if (table_rows <= 0) return PGD_EINVAL;
+  int32_t attention = 0;
+  int rc = pgd_attention_kernel_count(dims, table_rows, window, opts, &attention);
+  if (rc != PGD_OK) return rc;
+  if (dims->rows == 0) {
+    *count = 0;
+    return PGD_OK;
+  }
+  int kernel = 0;
+  if ((rc = resolve_kernel(dims, table_rows, true, opts, &kernel)) != PGD_OK) return rc;
+  // the write launch, then the attention kernels (the tcgen05 kernel alone:
+  // the write launch prepared its counter and order)
+  *count = 1 + (kernel == PGD_KERNEL_PREFILL_UMMA ? 1 : attention);
+  return PGD_OK;
 }
 
 int pgd_get_device_error(pgd_stream_t stream) {

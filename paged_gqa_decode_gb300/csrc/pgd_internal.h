@@ -125,11 +125,19 @@ int prefill_block_tokens(int padded);
 // block order (when one is computed) starts at the fifth.
 // q_map: q as (64 values, heads, tokens) with boxes of 64 x group x
 // (128 / group), 128-byte swizzle: the kernel copies each item's Q with it.
+// `prepared`: launch_prefill_write (with umma) has already prepared the
+// work counter and block order in p.ws_acc, so only the kernel is launched.
 cudaError_t launch_prefill_umma(const DecodeParams& p, const CUtensorMap& k_map,
                                 const CUtensorMap& v_map, const CUtensorMap& q_map, int head_dim,
-                                int sm_count, cudaStream_t stream);
+                                int sm_count, bool prepared, cudaStream_t stream);
 // Kernels that launch issues for `rows` tokens (the block-order pass and the
 // kernel, or the kernel alone).
 int prefill_umma_launches(int rows, int group, int window);
+// The prefill step's write launch: each token's p.k_new / p.v_new at its slot
+// in p.k_pool / p.v_pool (table row p.row_of[t], position p.positions[t]);
+// with `umma`, its first CTA also prepares the tcgen05 kernel's work counter
+// and block order in p.ws_acc.  One kernel launch.
+cudaError_t launch_prefill_write(const DecodeParams& p, int head_dim, bool umma,
+                                 cudaStream_t stream);
 
 }  // namespace pgd

@@ -31,7 +31,8 @@ def test_header_declares_the_entry_points():
         "pgd_get_device_error", "pgd_status_string", "pgd_version",
         "pgd_paged_decode_attention_static", "pgd_page_slots", "pgd_kv_write_slots",
         "pgd_paged_prefill_attention", "pgd_rope_append_paged", "pgd_selftest_bounded_wait",
-        "pgd_attention_kernel_count", "pgd_paged_decode_step"}
+        "pgd_attention_kernel_count", "pgd_paged_decode_step", "pgd_paged_prefill_step",
+        "pgd_prefill_step_kernel_count"}
 
 
 def test_library_exports_every_declared_symbol_and_nothing_else(lib):
@@ -85,6 +86,11 @@ def test_host_rejects_bad_dims_without_a_device(lib, kw, status):
     assert rc == status
     count = ctypes.c_int32(-1)
     assert so.pgd_attention_kernel_count(ctypes.byref(d), 0, 0, None, ctypes.byref(count)) == status
+    rc = so.pgd_paged_prefill_step(ctypes.byref(d), 2, None, None, None, None, None, None, None,
+                                   None, None, 0, 0.125, None, None, 0, None, None)
+    assert rc == status
+    assert so.pgd_prefill_step_kernel_count(ctypes.byref(d), 2, 0, None,
+                                            ctypes.byref(count)) == status
 
 
 def test_bad_page_size_is_unsupported(lib):
@@ -111,6 +117,14 @@ def test_zero_rows_is_ok_and_null_pointers_are_rejected(lib):
     opts = pgd.DecodeOptions(0, pgd.KERNEL_PREFILL_UMMA)   # a prefill kernel for a decode call
     assert so.pgd_attention_kernel_count(ctypes.byref(d), 0, 0, ctypes.byref(opts),
                                          ctypes.byref(count)) == 1
+    # the prefill step: rows, k_new and v_new are required; table_rows > 0
+    assert so.pgd_paged_prefill_step(ctypes.byref(d), 2, buf, None, buf, buf, buf, buf, buf,
+                                     buf, None, 0, 0.125, buf, buf, 64, None, None) == 1
+    assert so.pgd_paged_prefill_step(ctypes.byref(d), 2, buf, buf, buf, buf, buf, buf, None,
+                                     buf, None, 0, 0.125, buf, buf, 64, None, None) == 1
+    assert so.pgd_prefill_step_kernel_count(ctypes.byref(d), 0, 0, None,
+                                            ctypes.byref(count)) == 1
+    assert so.pgd_prefill_step_kernel_count(ctypes.byref(d), 2, 0, None, None) == 1
 
 
 def test_product_package_does_not_import_the_oracle():

@@ -34,9 +34,12 @@ def pages_needed(n_last: np.ndarray) -> np.ndarray:
 
 
 def prefill_check(b, *, window=None, sinks="batch", layout=pgd.PAGE_MAJOR, sample=None, pps=0,
-                  kernel=pgd.KERNEL_AUTO, what=""):
+                  kernel=pgd.KERNEL_AUTO, what="", fused=False):
     """Oracle inputs are copied out before the CUDA path writes anything; the
-    oracle then does its own slot computation, writes and prefill."""
+    oracle then does its own slot computation, writes and prefill.  The CUDA
+    path is page_slots + kv_write_slots + paged_prefill_attention, or with
+    `fused` the one paged_prefill_step call (page_slots is then called only to
+    check the slots)."""
     wl = b.wl
     window = wl.window if window is None else window
     sinks = b.sinks if isinstance(sinks, str) else sinks
@@ -46,10 +49,16 @@ def prefill_check(b, *, window=None, sinks="batch", layout=pgd.PAGE_MAJOR, sampl
         b.k_pool, b.v_pool, b.table_np, rows_used, pages_needed(last), kv_heads=wl.kv_heads,
         head_dim=wl.head_dim, layout=layout)
     slots = pgd.page_slots(b.table, b.positions, b.rows, num_pages=b.num_pages)
-    pgd.kv_write_slots(b.k_new, b.v_new, slots, b.k_pool, b.v_pool, layout=layout)
-    out = pgd.paged_prefill_attention(b.q, b.k_pool, b.v_pool, b.table, b.rows, b.positions,
-                                      sinks, window, wl.scale, num_kv_heads=wl.kv_heads,
-                                      layout=layout, pages_per_split=pps, kernel=kernel)
+    if fused:
+        out = pgd.paged_prefill_step(b.q, b.k_new, b.v_new, b.k_pool, b.v_pool, b.table, b.rows,
+                                     b.positions, sinks, window, wl.scale,
+                                     num_kv_heads=wl.kv_heads, layout=layout,
+                                     pages_per_split=pps, kernel=kernel)
+    else:
+        pgd.kv_write_slots(b.k_new, b.v_new, slots, b.k_pool, b.v_pool, layout=layout)
+        out = pgd.paged_prefill_attention(b.q, b.k_pool, b.v_pool, b.table, b.rows, b.positions,
+                                          sinks, window, wl.scale, num_kv_heads=wl.kv_heads,
+                                          layout=layout, pages_per_split=pps, kernel=kernel)
     status = pgd.get_device_error()
     assert status == pgd.OK, pgd.status_string(status)
     # slots: bit-exact against the oracle's page_slots on the original table
@@ -130,12 +139,14 @@ SMALL = [
 @pytest.mark.parametrize("kernel,pps", [(pgd.KERNEL_TENSOR_CORE, 0), (pgd.KERNEL_TENSOR_CORE, 1),
                                         (pgd.KERNEL_PREFILL_TILED, 0),
                                         (pgd.KERNEL_PREFILL_UMMA, 0)])
-def test_prefill_small(name, hq, hkv, d, window, sinks, kernel, pps):
+@pytest.mark.parametrize("fused", [False, True])
+def test_prefill_small(name, hq, hkv, d, window, sinks, kernel, pps, fused):
     wl = PrefillWorkload(name, rows=4, q_heads=hq, kv_heads=hkv, head_dim=d, prefix_lo=0,
                          prefix_hi=300, chunk=0, window=window, sinks=sinks)
     b = make_prefill_batch(wl, 11 + hq + d, DEV, prefix=[0, 63, 64, 200],
                            chunks=[1, 64, 100, 130])
-    prefill_check(b, pps=pps, kernel=kernel, what=f"prefill {name} k={kernel} pps={pps}")
+    prefill_check(b, pps=pps, kernel=kernel, fused=fused,
+                  what=f"prefill {name} k={kernel} pps={pps} fused={fused}")
 
 
 TILED_KERNELS = [pgd.KERNEL_PREFILL_TILED, pgd.KERNEL_PREFILL_UMMA]
@@ -188,7 +199,8 @@ def test_prefill_interleaved_token_order(kernel):
 
 
 @pytest.mark.parametrize("kernel", [pgd.KERNEL_AUTO] + TILED_KERNELS)
-def test_step_paged_prompts_and_steps_in_one_call(kernel):
+@pytest.mark.parametrize("fused", [False, True])
+def test_step_paged_prompts_and_steps_in_one_call(kernel, fused):
     """step_paged: two rows prefill a chunk, three other rows take a decode
     step; one write of every token and one attention call over all of them
     matches the oracle's prefill over the same concatenation (which for the
@@ -197,19 +209,91 @@ def test_step_paged_prompts_and_steps_in_one_call(kernel):
                          prefix_hi=2000, chunk=0, window=0, sinks=False)
     b = make_prefill_batch(wl, 14, DEV, prefix=[0, 900, 1500, 64, 1999],
                            chunks=[150, 70, 1, 1, 1])
-    prefill_check(b, kernel=kernel, what="step_paged")
+    prefill_check(b, kernel=kernel, fused=fused, what=f"step_paged fused={fused}")
 
 
 @pytest.mark.parametrize("kernel", [pgd.KERNEL_AUTO] + TILED_KERNELS)
 @pytest.mark.parametrize("name,sample", [("mistral_prefill", 192), ("gptoss_prefill_sliding", 256)])
-def test_prefill_full_size_sampled(name, sample, kernel):
+@pytest.mark.parametrize("fused", [False, True])
+def test_prefill_full_size_sampled(name, sample, kernel, fused):
     wl = PREFILL_WORKLOADS[name]
     b = make_prefill_batch(wl, 2000 + list(PREFILL_WORKLOADS).index(name), DEV)
     rng = np.random.default_rng(3)
     tokens = len(b.rows_np)
     idx = np.unique(np.concatenate([rng.choice(tokens, size=sample - 2, replace=False),
                                     [0, tokens - 1]]))
-    prefill_check(b, sample=idx, kernel=kernel)
+    prefill_check(b, sample=idx, kernel=kernel, fused=fused)
+
+
+@pytest.mark.parametrize("kernel", [pgd.KERNEL_AUTO, pgd.KERNEL_TENSOR_CORE] + TILED_KERNELS)
+@pytest.mark.parametrize("layout,d,window", [(pgd.PAGE_MAJOR, 128, 0), (pgd.PAGE_MAJOR, 64, 100),
+                                             (pgd.HEAD_MAJOR, 64, 0), (pgd.HEAD_MAJOR, 128, 30)])
+def test_prefill_step_equals_the_three_calls(kernel, layout, d, window):
+    """paged_prefill_step leaves the pools bit-identical to page_slots +
+    kv_write_slots and gives bit-identical outputs to the attention call
+    after them (the same attention kernels, the same block order), with
+    inactive tokens among the packed ones."""
+    wl = PrefillWorkload("fused", rows=4, q_heads=32, kv_heads=8, head_dim=d, prefix_lo=0,
+                         prefix_hi=900, chunk=0, window=window, sinks=True)
+    a = make_prefill_batch(wl, 31 + d + window, DEV, prefix=[0, 700, 65, 300],
+                           chunks=[90, 140, 33, 64])
+    b = make_prefill_batch(wl, 31 + d + window, DEV, prefix=[0, 700, 65, 300],
+                           chunks=[90, 140, 33, 64])
+    for x in (a, b):
+        x.positions[7] = -1   # an inactive token: not written, zero output
+    kw = dict(num_kv_heads=wl.kv_heads, layout=layout, kernel=kernel)
+    slots = pgd.page_slots(a.table, a.positions, a.rows, num_pages=a.num_pages)
+    pgd.kv_write_slots(a.k_new, a.v_new, slots, a.k_pool, a.v_pool, layout=layout)
+    want = pgd.paged_prefill_attention(a.q, a.k_pool, a.v_pool, a.table, a.rows, a.positions,
+                                       a.sinks, window, wl.scale, **kw)
+    assert pgd.get_device_error() == pgd.OK
+    got = pgd.paged_prefill_step(b.q, b.k_new, b.v_new, b.k_pool, b.v_pool, b.table, b.rows,
+                                 b.positions, b.sinks, window, wl.scale, **kw)
+    assert pgd.get_device_error() == pgd.OK
+    assert torch.equal(b.k_pool, a.k_pool) and torch.equal(b.v_pool, a.v_pool)
+    assert torch.equal(got, want)
+    assert torch.all(got[7] == 0)
+
+
+@pytest.mark.parametrize("kernel", [pgd.KERNEL_TENSOR_CORE] + TILED_KERNELS)
+def test_prefill_step_bad_entries_are_not_written(kernel):
+    """A token whose row, page index or page is out of range is reported, not
+    written, and its output is zero; the other tokens are written and
+    attend as in the three calls."""
+    wl = PrefillWorkload("fused_bad", rows=2, q_heads=8, kv_heads=2, head_dim=64, prefix_lo=0,
+                         prefix_hi=100, chunk=0)
+    b = make_prefill_batch(wl, 15, DEV, prefix=[0, 50], chunks=[10, 10])
+    rows, positions, table = b.rows.clone(), b.positions.clone(), b.table.clone()
+    rows[3] = 7                                  # outside the table
+    positions[4] = 64 * b.table.shape[1] + 1     # beyond its table row
+    before_k, before_v = b.k_pool.clone(), b.v_pool.clone()
+    out = pgd.paged_prefill_step(b.q, b.k_new, b.v_new, b.k_pool, b.v_pool, table, rows,
+                                 positions, num_kv_heads=2, kernel=kernel)
+    assert pgd.get_device_error() == pgd.EDEVICE_BOUNDS
+    assert torch.all(out[3] == 0) and torch.all(out[4] == 0) and torch.any(out[5] != 0)
+    # the 18 good tokens' rows were written, nothing else
+    changed_k = (b.k_pool != before_k).view(-1, 64).any(dim=1).sum().item()
+    assert changed_k == 18 * wl.kv_heads
+    assert torch.equal((b.v_pool != before_v).view(-1, 64).any(dim=1),
+                       (b.k_pool != before_k).view(-1, 64).any(dim=1))
+
+
+def test_prefill_step_kernel_count():
+    w = PREFILL_WORKLOADS["mistral_prefill"]
+    dims = pgd.make_dims(rows=4096, num_q_heads=w.q_heads, num_kv_heads=w.kv_heads,
+                         head_dim=w.head_dim, num_pages=10000, max_pages_per_row=140)
+    # the write launch + the tcgen05 kernel (its counter and order prepared)
+    assert pgd.prefill_step_kernel_count(dims, 8) == 2
+    assert pgd.attention_kernel_count(dims, 8) == 2
+    assert pgd.prefill_step_kernel_count(dims, 8, kernel=pgd.KERNEL_PREFILL_TILED) == 2
+    assert pgd.prefill_step_kernel_count(dims, 8, window=128) == 2
+    one = pgd.make_dims(rows=8, num_q_heads=w.q_heads, num_kv_heads=w.kv_heads,
+                        head_dim=w.head_dim, num_pages=10000, max_pages_per_row=140)
+    # one token per row: the per-token decode kernels (the window kernel here)
+    assert pgd.prefill_step_kernel_count(one, 8, window=100) == 2
+    zero = pgd.make_dims(rows=0, num_q_heads=w.q_heads, num_kv_heads=w.kv_heads,
+                         head_dim=w.head_dim, num_pages=10000, max_pages_per_row=140)
+    assert pgd.prefill_step_kernel_count(zero, 8) == 0
 
 
 @pytest.mark.parametrize("kernel", [pgd.KERNEL_TENSOR_CORE] + TILED_KERNELS)
