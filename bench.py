@@ -748,7 +748,7 @@ def prefill_work(wl, b) -> dict:
 
 
 # --kernel names -> PGD_KERNEL_* values
-KERNEL_IDS = {"auto": 0, "tensor": 1, "cuda": 2, "tiled": 3, "umma": 4}
+KERNEL_IDS = {"auto": 0, "tensor": 1, "cuda": 2, "tiled": 3, "umma": 4, "pair": 5}
 
 
 def measured_tensor_peak() -> tuple[float, str]:
@@ -943,7 +943,8 @@ def main():
     ap.add_argument("--pages-per-split", type=int, default=0)
     ap.add_argument("--kernel", choices=list(KERNEL_IDS), default="auto",
                     help="kernel variant: decode tensor-core or CUDA-core products; prefill "
-                         "also the token-block kernels (mma.sync 'tiled', tcgen05 'umma')")
+                         "also the token-block kernels (mma.sync 'tiled', tcgen05 'umma', tcgen05 on "
+                         "pairs of SMs 'pair')")
     ap.add_argument("--two-calls", action="store_true",
                     help="kv_append_paged and paged_decode_attention as two calls (default: "
                          "one paged_decode_step call, the append inside the decode launch); "

@@ -105,19 +105,27 @@ enum {
                                    window kernel (the warps given each row and
                                    kv head copy exactly the window's K/V rows;
                                    mma.sync products; no splits), anything else to
-                                   TENSOR_CORE; prefill: PREFILL_UMMA when the
-                                   tokens average at least 8 per table row
-                                   (prompt chunks), else as decode, per token */
+                                   TENSOR_CORE; prefill: when the tokens average
+                                   at least 8 per table row (prompt chunks),
+                                   PREFILL_PAIR at head_dim 128 if its blocks x
+                                   kv heads are at most the device's SMs, else
+                                   PREFILL_UMMA; otherwise as decode, per token */
   PGD_KERNEL_TENSOR_CORE = 1,   /* mma.sync bf16 products, fp32 accumulate, per token,
                                    key range split over CTAs + combine */
   PGD_KERNEL_CUDA_CORE = 2,     /* fp32 FMA products on the CUDA cores, per token */
   PGD_KERNEL_PREFILL_TILED = 3, /* prefill only: blocks of tokens share each page
                                    load (mma.sync tensor cores, no key splits) */
-  PGD_KERNEL_PREFILL_UMMA = 4   /* prefill only: persistent, two tiles of 128
+  PGD_KERNEL_PREFILL_UMMA = 4,  /* prefill only: persistent, two tiles of 128
                                    query rows per block on the tcgen05 tensor
                                    cores (TMEM accumulators), no key splits;
                                    uses the start of the workspace for its work
                                    counter and block order */
+  PGD_KERNEL_PREFILL_PAIR = 5   /* prefill only, head_dim 128: the same blocks
+                                   on pairs of SMs (clusters of two CTAs, one
+                                   query tile each, sharing every tcgen05
+                                   product; each CTA loads every other page,
+                                   so one product spans 128 keys); the same
+                                   use of the workspace */
 };
 
 /* Optional tuning of the decode launch; pass NULL for the defaults.  The same

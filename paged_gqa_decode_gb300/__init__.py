@@ -53,8 +53,8 @@ class Dims(ctypes.Structure):
         "max_pages_per_row", "layout")]
 
 
-KERNEL_AUTO, KERNEL_TENSOR_CORE, KERNEL_CUDA_CORE, KERNEL_PREFILL_TILED, KERNEL_PREFILL_UMMA = \
-    range(5)
+(KERNEL_AUTO, KERNEL_TENSOR_CORE, KERNEL_CUDA_CORE, KERNEL_PREFILL_TILED, KERNEL_PREFILL_UMMA,
+ KERNEL_PREFILL_PAIR) = range(6)
 
 
 class DecodeOptions(ctypes.Structure):

@@ -17,7 +17,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libpgd.so")
 
 SOURCES = ["pgd_api.cu", "kv_append.cu", "paged_decode_d64.cu", "paged_decode_d128.cu",
-           "paged_prefill.cu", "paged_prefill_umma.cu", "paged_prefill_umma_d64.cu"]
+           "paged_prefill.cu", "paged_prefill_umma.cu", "paged_prefill_umma_d64.cu",
+           "paged_prefill_pair.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
          "-Xptxas", "-v", f"-I{INCLUDE}", f"-I{CSRC}"]

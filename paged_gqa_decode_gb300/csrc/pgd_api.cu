@@ -102,18 +102,29 @@ size_t workspace_bytes(const pgd_dims* d, const Plan& pl) {
 }
 
 // The kernel a call runs: opts->kernel, or for AUTO the per-token split
-// kernel, except that prefill with tokens in runs goes to the tcgen05 kernel.
+// kernel, except that prefill with tokens in runs goes to a tcgen05 kernel:
+// at head_dim 128 the paired one when its work items are no more than the
+// SMs (`sm_count`; 0 = unknown), since it puts two SMs on each item, else
+// the one-SM kernel.
 int resolve_kernel(const pgd_dims* dims, int32_t table_rows, bool prefill,
-                   const pgd_decode_options* opts, int* kernel) {
+                   const pgd_decode_options* opts, int* kernel, int sm_count = 0) {
   int k = opts ? opts->kernel : PGD_KERNEL_AUTO;
-  if (k < PGD_KERNEL_AUTO || k > PGD_KERNEL_PREFILL_UMMA) return PGD_EINVAL;
-  if ((k == PGD_KERNEL_PREFILL_TILED || k == PGD_KERNEL_PREFILL_UMMA) && !prefill)
+  if (k < PGD_KERNEL_AUTO || k > PGD_KERNEL_PREFILL_PAIR) return PGD_EINVAL;
+  if ((k == PGD_KERNEL_PREFILL_TILED || k == PGD_KERNEL_PREFILL_UMMA ||
+       k == PGD_KERNEL_PREFILL_PAIR) &&
+      !prefill)
     return PGD_EINVAL;
+  if (k == PGD_KERNEL_PREFILL_PAIR && dims->head_dim != 128) return PGD_EINVAL;
   // Prefill: the tcgen05 kernel shares each page load among the tokens of a
   // block, which pays when they come in runs (prompt chunks); tokens that are
   // mostly one per table row (decode steps) go to the per-token split kernel.
-  if (prefill && k == PGD_KERNEL_AUTO && dims->rows >= 8ll * table_rows)
+  if (prefill && k == PGD_KERNEL_AUTO && dims->rows >= 8ll * table_rows) {
     k = PGD_KERNEL_PREFILL_UMMA;
+    const int group = dims->num_q_heads / dims->num_kv_heads;
+    const int64_t block = 2 * (128 / group);  // tokens per work item
+    const int64_t items = (dims->rows + block - 1) / block * dims->num_kv_heads;
+    if (dims->head_dim == 128 && sm_count > 0 && items <= sm_count) k = PGD_KERNEL_PREFILL_PAIR;
+  }
   *kernel = k;
   return PGD_OK;
 }
@@ -129,7 +140,7 @@ int span_pages(const pgd_dims* dims, int32_t window) {
   return grid_pages;
 }
 
-int encode_pool_map_uncached(CUtensorMap* map, const void* pool, const pgd_dims* d, bool whole);
+int encode_pool_map_uncached(CUtensorMap* map, const void* pool, const pgd_dims* d, int kind);
 
 // Encoded pool descriptors are reused while the same pool is passed again: a
 // small per-process cache keyed by (device, address, pages, kv heads, dim).
@@ -137,7 +148,7 @@ struct MapEntry {
   int dev;
   const void* pool;
   int32_t num_pages, kv_heads, head_dim;
-  bool whole;
+  int kind;
   CUtensorMap map;
 };
 constexpr int kMapCache = 16;
@@ -145,9 +156,15 @@ MapEntry g_maps[kMapCache];
 int g_map_count = 0, g_map_next = 0;
 std::mutex g_map_mutex;
 
-// `whole`: one box per page tile (head_dim 128 as a 3-D map); else 64-wide boxes.
-int encode_pool_map(CUtensorMap* map, const void* pool, const pgd_dims* d, bool whole = false) {
-  whole = whole && d->head_dim == 128;
+// Box shapes of a pool's tensor map.
+enum MapKind {
+  kMapBoxes = 0,      // 64 rows x 64 values: a page tile, or a 64-wide half of one
+  kMapWholeTile = 1,  // head_dim 128: a page tile's two 64-wide boxes in one copy
+};
+
+int encode_pool_map(CUtensorMap* map, const void* pool, const pgd_dims* d,
+                    int kind = kMapBoxes) {
+  if (d->head_dim != 128) kind = kMapBoxes;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PGD_ECUDA;
   {
@@ -155,17 +172,17 @@ int encode_pool_map(CUtensorMap* map, const void* pool, const pgd_dims* d, bool 
     for (int i = 0; i < g_map_count; ++i) {
       const MapEntry& m = g_maps[i];
       if (m.dev == dev && m.pool == pool && m.num_pages == d->num_pages &&
-          m.kv_heads == d->num_kv_heads && m.head_dim == d->head_dim && m.whole == whole) {
+          m.kv_heads == d->num_kv_heads && m.head_dim == d->head_dim && m.kind == kind) {
         *map = m.map;
         return PGD_OK;
       }
     }
   }
-  const int rc = encode_pool_map_uncached(map, pool, d, whole);
+  const int rc = encode_pool_map_uncached(map, pool, d, kind);
   if (rc != PGD_OK) return rc;
   std::lock_guard<std::mutex> lock(g_map_mutex);
   MapEntry& slot = g_maps[g_map_next];
-  slot = MapEntry{dev, pool, d->num_pages, d->num_kv_heads, d->head_dim, whole, *map};
+  slot = MapEntry{dev, pool, d->num_pages, d->num_kv_heads, d->head_dim, kind, *map};
   g_map_next = (g_map_next + 1) % kMapCache;
   if (g_map_count < kMapCache) ++g_map_count;
   return PGD_OK;
@@ -204,13 +221,13 @@ int encode_q_map(CUtensorMap* map, const void* q, const pgd_dims* d) {
   return r == CUDA_SUCCESS ? PGD_OK : PGD_ECUDA;
 }
 
-int encode_pool_map_uncached(CUtensorMap* map, const void* pool, const pgd_dims* d, bool whole) {
+int encode_pool_map_uncached(CUtensorMap* map, const void* pool, const pgd_dims* d, int kind) {
   if (!load_encode()) return PGD_ECUDA;
   // The pool as a 2-D tensor: rows of head_dim bf16 values, one row per
   // (page, kv head, position) in either layout.  A box is 64 rows x 64
   // values (128 bytes): one page tile, or half of one when head_dim is 128.
   const cuuint64_t rows = (cuuint64_t)d->num_pages * d->num_kv_heads * kPageSize;
-  if (whole) {
+  if (kind != kMapBoxes) {
     // head_dim 128 as (64 values, rows, 2 halves): strides 256 bytes (a row)
     // and 128 bytes (a half), box 64 x 64 x 2 -- one copy lands a page tile as
     // the two consecutive 128-byte-swizzled 64-wide boxes the 2-D map gives.
@@ -383,15 +400,19 @@ int pgd_attention_kernel_count(const pgd_dims* dims, int32_t table_rows, int32_t
   int rc = check_dims(dims);
   if (rc != PGD_OK) return rc;
   if (table_rows < 0) return PGD_EINVAL;
-  // The kernel choice does not depend on the device; the split size does.
+  // The arguments are checked before the device is; AUTO's prefill choice
+  // then depends on the SM count, as the split size does.
   int kernel = 0;
   if ((rc = resolve_kernel(dims, table_rows, table_rows > 0, opts, &kernel)) != PGD_OK) return rc;
   DeviceInfo* dev = nullptr;
   if ((rc = current_device(&dev)) != PGD_OK) return rc;
+  if ((rc = resolve_kernel(dims, table_rows, table_rows > 0, opts, &kernel, dev->sm_count)) !=
+      PGD_OK)
+    return rc;
   const Plan pl = make_plan(dims, opts, dev->sm_count);
   if (dims->rows == 0) {
     *count = 0;
-  } else if (kernel == PGD_KERNEL_PREFILL_UMMA) {
+  } else if (kernel == PGD_KERNEL_PREFILL_UMMA || kernel == PGD_KERNEL_PREFILL_PAIR) {
     *count = prefill_umma_launches(dims->rows, dims->num_q_heads / dims->num_kv_heads, window);
   } else if (kernel == PGD_KERNEL_PREFILL_TILED) {
     *count = 1;
@@ -434,14 +455,18 @@ static int decode_impl(const pgd_dims* dims, int32_t table_rows, const int32_t* 
   if (!workspace || !aligned16(workspace)) return PGD_EINVAL;
 
   int kernel = 0;
-  if ((rc = resolve_kernel(dims, table_rows, row_of != nullptr, opts, &kernel)) != PGD_OK)
+  if ((rc = resolve_kernel(dims, table_rows, row_of != nullptr, opts, &kernel, dev->sm_count)) !=
+      PGD_OK)
     return rc;
   const int padded = padded_group(dims->num_q_heads / dims->num_kv_heads);
-  // the tcgen05 prefill copies a head_dim-128 page tile with one 3-D box
-  const bool whole = kernel == PGD_KERNEL_PREFILL_UMMA;
+  // the tcgen05 prefills copy a head_dim-128 K page tile with one 3-D box;
+  // each CTA of the paired prefill copies one 64-wide half of a V tile
+  const bool tcgen05 = kernel == PGD_KERNEL_PREFILL_UMMA || kernel == PGD_KERNEL_PREFILL_PAIR;
+  const int k_kind = tcgen05 ? kMapWholeTile : kMapBoxes;
+  const int v_kind = kernel == PGD_KERNEL_PREFILL_UMMA ? kMapWholeTile : kMapBoxes;
   CUtensorMap k_map, v_map;
-  if ((rc = encode_pool_map(&k_map, k_pool, dims, whole)) != PGD_OK) return rc;
-  if ((rc = encode_pool_map(&v_map, v_pool, dims, whole)) != PGD_OK) return rc;
+  if ((rc = encode_pool_map(&k_map, k_pool, dims, k_kind)) != PGD_OK) return rc;
+  if ((rc = encode_pool_map(&v_map, v_pool, dims, v_kind)) != PGD_OK) return rc;
 
   DecodeParams p;
   p.q = static_cast<const uint16_t*>(q);
@@ -484,15 +509,18 @@ static int decode_impl(const pgd_dims* dims, int32_t table_rows, const int32_t* 
   // also prepares the tcgen05 kernel's work counter and block order
   const bool prefill_write = k_new != nullptr && row_of != nullptr;
   CUtensorMap q_map;
-  if (kernel == PGD_KERNEL_PREFILL_UMMA && (rc = encode_q_map(&q_map, q, dims)) != PGD_OK)
-    return rc;
+  if (tcgen05 && (rc = encode_q_map(&q_map, q, dims)) != PGD_OK) return rc;
   if (prefill_write) {
-    if (launch_prefill_write(p, dims->head_dim, kernel == PGD_KERNEL_PREFILL_UMMA, st) !=
-        cudaSuccess)
+    if (launch_prefill_write(p, dims->head_dim, tcgen05, st) != cudaSuccess)
       return PGD_ECUDA;
     p.k_new = p.v_new = nullptr;
     p.k_pool = p.v_pool = nullptr;
   }
+  if (kernel == PGD_KERNEL_PREFILL_PAIR)
+    return launch_prefill_pair(p, k_map, v_map, q_map, dev->sm_count, prefill_write, st) ==
+                   cudaSuccess
+               ? PGD_OK
+               : PGD_ECUDA;
   if (kernel == PGD_KERNEL_PREFILL_UMMA)
     return launch_prefill_umma(p, k_map, v_map, q_map, dims->head_dim, dev->sm_count,
                                prefill_write, st) == cudaSuccess
@@ -572,7 +600,8 @@ int pgd_prefill_step_kernel_count(const pgd_dims* dims, int32_t table_rows, int3
   if ((rc = resolve_kernel(dims, table_rows, true, opts, &kernel)) != PGD_OK) return rc;
   // the write launch, then the attention kernels (the tcgen05 kernel alone:
   // the write launch prepared its counter and order)
-  *count = 1 + (kernel == PGD_KERNEL_PREFILL_UMMA ? 1 : attention);
+  *count = 1 + (kernel == PGD_KERNEL_PREFILL_UMMA || kernel == PGD_KERNEL_PREFILL_PAIR ? 1
+                                                                                      : attention);
   return PGD_OK;
 }
 

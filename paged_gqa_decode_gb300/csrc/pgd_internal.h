@@ -130,6 +130,13 @@ int prefill_block_tokens(int padded);
 cudaError_t launch_prefill_umma(const DecodeParams& p, const CUtensorMap& k_map,
                                 const CUtensorMap& v_map, const CUtensorMap& q_map, int head_dim,
                                 int sm_count, bool prepared, cudaStream_t stream);
+// Prefill at head_dim 128 on pairs of SMs (clusters of two CTAs sharing
+// cta_group::2 tcgen05 products); the same work items, counter, block order
+// and `prepared` convention as launch_prefill_umma.  k_map: the K pool in
+// whole page tiles (3-D boxes); v_map: the V pool in 64 x 64 boxes.
+cudaError_t launch_prefill_pair(const DecodeParams& p, const CUtensorMap& k_map,
+                                const CUtensorMap& v_map, const CUtensorMap& q_map, int sm_count,
+                                bool prepared, cudaStream_t stream);
 // Kernels that launch issues for `rows` tokens (the block-order pass and the
 // kernel, or the kernel alone).
 int prefill_umma_launches(int rows, int group, int window);

@@ -117,6 +117,16 @@ def test_zero_rows_is_ok_and_null_pointers_are_rejected(lib):
     opts = pgd.DecodeOptions(0, pgd.KERNEL_PREFILL_UMMA)   # a prefill kernel for a decode call
     assert so.pgd_attention_kernel_count(ctypes.byref(d), 0, 0, ctypes.byref(opts),
                                          ctypes.byref(count)) == 1
+    pair = pgd.DecodeOptions(0, pgd.KERNEL_PREFILL_PAIR)
+    d128 = _dims(head_dim=128)
+    assert so.pgd_attention_kernel_count(ctypes.byref(d128), 0, 0, ctypes.byref(pair),
+                                         ctypes.byref(count)) == 1   # decode call
+    d64 = _dims(head_dim=64)
+    assert so.pgd_attention_kernel_count(ctypes.byref(d64), 2, 0, ctypes.byref(pair),
+                                         ctypes.byref(count)) == 1   # head_dim 128 only
+    bad = pgd.DecodeOptions(0, pgd.KERNEL_PREFILL_PAIR + 1)
+    assert so.pgd_attention_kernel_count(ctypes.byref(d), 2, 0, ctypes.byref(bad),
+                                         ctypes.byref(count)) == 1   # no such kernel
     # the prefill step: rows, k_new and v_new are required; table_rows > 0
     assert so.pgd_paged_prefill_step(ctypes.byref(d), 2, buf, None, buf, buf, buf, buf, buf,
                                      buf, None, 0, 0.125, buf, buf, 64, None, None) == 1
