@@ -88,3 +88,25 @@ def test_random_prefill(seed):
     prefill_check(b, window=window, layout=layout, kernel=kernel,
                   what=f"seed {seed}: {hq}/{hkv} d{d} w{window} k{kernel} layout{layout} "
                        f"prefix {prefix} chunks {chunks}")
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_prefill_pair(seed):
+    """The paired-SM tcgen05 prefill (head_dim 128) on seeded random groups,
+    prefixes, chunks, windows, sinks and layouts."""
+    rng = np.random.default_rng(9700 + seed)
+    hq, hkv = heads(rng)
+    rows = int(rng.integers(1, 5))
+    prefix = [int(rng.choice([0, rng.integers(0, 64), rng.integers(0, 2000)])) for _ in range(rows)]
+    chunks = [int(rng.choice([1, rng.integers(1, 70), rng.integers(60, 300)])) for _ in range(rows)]
+    window = int(rng.choice([0, 0, 1, 128, int(rng.integers(2, 300))]))
+    wl = PrefillWorkload("random_pair", rows=rows, q_heads=hq, kv_heads=hkv, head_dim=128,
+                         prefix_lo=0, prefix_hi=2000, chunk=0, window=window,
+                         sinks=bool(rng.integers(0, 2)))
+    b = make_prefill_batch(wl, 9900 + seed, DEV, prefix=prefix, chunks=chunks)
+    b.v_pool.mul_(0.25)
+    b.v_new = b.v_new * 0.25
+    layout = int(rng.choice([pgd.PAGE_MAJOR, pgd.HEAD_MAJOR]))
+    prefill_check(b, window=window, layout=layout, kernel=pgd.KERNEL_PREFILL_PAIR,
+                  what=f"seed {seed}: {hq}/{hkv} w{window} layout{layout} prefix {prefix} "
+                       f"chunks {chunks}")
