@@ -443,7 +443,8 @@ __global__ void __cluster_dims__(2, 1, 1)
   } else if (warp == C::kSWarp) {
     // ------------------------------------------------ Q copies and S issuer
     if (lane == 0) {
-      const uint32_t k_addr = smem_addr(k_slots), q_addr = smem_addr(q_smem);
+      const uint32_t k_addr = smem_addr(k_slots);
+      const uint64_t qd = umma_desc_sw128(smem_addr(q_smem), 16, 1024);
       int i = 0;  // pair index over all items
       bool issued = false, ok = true;
       bool q_pending = false;
@@ -485,14 +486,12 @@ __global__ void __cluster_dims__(2, 1, 1)
             break;
           }
           tc_fence_after_sync();
-          const uint32_t kt = k_addr + (i % RK) * C::kKBytes;
+          const uint64_t kd = umma_desc_sw128(k_addr + (i % RK) * C::kKBytes, 16, 1024);
           const uint32_t sb = tmem + C::kSCol + b * C::kSCols;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            umma_pair_bf16(sb,
-                           umma_desc_sw128(q_addr + (kk >> 2) * C::kQBoxBytes + (kk & 3) * 32, 16,
-                                           1024),
-                           umma_desc_sw128(kt + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
+            umma_pair_bf16(sb, umma_desc_advance(qd, (kk >> 2) * C::kQBoxBytes + (kk & 3) * 32),
+                           umma_desc_advance(kd, (kk >> 2) * kBoxBytes + (kk & 3) * 32),
                            C::kIdescS, kk > 0);
           umma_pair_commit(&s_full[b], 3);
           umma_pair_commit(&k_empty[i % RK], 3);
@@ -530,25 +529,27 @@ __global__ void __cluster_dims__(2, 1, 1)
               break;
             }
             tc_fence_after_sync();
-            const uint32_t vt = v_addr + (i % RV) * C::kVBytes;
+            const uint64_t vd = umma_desc_sw128(v_addr + (i % RV) * C::kVBytes, kBoxBytes, 1024);
             const uint32_t pb = tmem + C::kSCol + b * C::kSCols;
             const uint32_t od = tmem + C::kOCol;
             // keys 16 kk .. 16 kk + 15 of the pair: chunk kk / 2 of the P
             // columns, half kk % 2 of its 16 head (then residual) columns; V
             // rows from page kk / 4's half
-            const int steps = cur.pg + 1 <= cur.last ? 8 : 4;
-            for (int kk = 0; kk < steps; ++kk)
-              umma_pair_bf16_tmem_a(
-                  od, pb + 32 * (kk >> 1) + 8 * (kk & 1),
-                  umma_desc_sw128(vt + (kk >> 2) * C::kVHalfBytes + (kk & 3) * 2048, kBoxBytes,
-                                  1024),
-                  C::kIdescPV, !(first && kk == 0));
-            for (int kk = 0; kk < steps; ++kk)
-              umma_pair_bf16_tmem_a(
-                  od, pb + 32 * (kk >> 1) + 16 + 8 * (kk & 1),
-                  umma_desc_sw128(vt + (kk >> 2) * C::kVHalfBytes + (kk & 3) * 2048, kBoxBytes,
-                                  1024),
-                  C::kIdescPV, true);
+            const bool two = cur.pg + 1 <= cur.last;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              if (kk < 4 || two)
+                umma_pair_bf16_tmem_a(
+                    od, pb + 32 * (kk >> 1) + 8 * (kk & 1),
+                    umma_desc_advance(vd, (kk >> 2) * C::kVHalfBytes + (kk & 3) * 2048),
+                    C::kIdescPV, !(first && kk == 0));
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              if (kk < 4 || two)
+                umma_pair_bf16_tmem_a(
+                    od, pb + 32 * (kk >> 1) + 16 + 8 * (kk & 1),
+                    umma_desc_advance(vd, (kk >> 2) * C::kVHalfBytes + (kk & 3) * 2048),
+                    C::kIdescPV, true);
             umma_pair_commit(&o_done[b], 3);
             umma_pair_commit(&v_empty[i % RV], 3);
             first = false;

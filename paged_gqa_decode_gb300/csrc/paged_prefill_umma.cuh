@@ -475,7 +475,7 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
             ok = false;
             break;
           }
-          const uint32_t kt = k_addr + (i % RK) * C::kTileBytes;
+          const uint64_t kd = umma_desc_sw128(k_addr + (i % RK) * C::kTileBytes, 16, 1024);
           const int b = i % C::kSBufs;
           for (int t = 0; t < C::kTiles; ++t) {
             // the buffer holds P_t of page i - kSBufs until P V has read it
@@ -486,12 +486,12 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
             }
             tc_fence_after_sync();
             const uint32_t sb = tmem + C::kSCol + tb * kPage;
-            const uint32_t qs = smem_addr(q_smem) + t * C::kQTileBytes;
+            const uint64_t qd = umma_desc_sw128(smem_addr(q_smem) + t * C::kQTileBytes, 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
-              umma_bf16(sb, umma_desc_sw128(qs + (kk >> 2) * C::kQBoxBytes + (kk & 3) * 32, 16, 1024),
-                        umma_desc_sw128(kt + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
-                        C::kIdescS, kk > 0);
+              umma_bf16(sb, umma_desc_advance(qd, (kk >> 2) * C::kQBoxBytes + (kk & 3) * 32),
+                        umma_desc_advance(kd, (kk >> 2) * kBoxBytes + (kk & 3) * 32), C::kIdescS,
+                        kk > 0);
             umma_commit(&s_full[tb]);
           }
           if (!ok) break;
@@ -528,7 +528,7 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
             ok = false;
             break;
           }
-          const uint32_t vt = v_addr + (i % RV) * C::kTileBytes;
+          const uint64_t vd = umma_desc_sw128(v_addr + (i % RV) * C::kTileBytes, kBoxBytes, 1024);
           const int b = i % C::kSBufs;
           for (int t = 0; t < C::kTiles; ++t) {
             const int tb = t * C::kSBufs + b;
@@ -544,13 +544,11 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               umma_bf16_tmem_a(od, pb + 32 * (kk >> 1) + 8 * (kk & 1),
-                               umma_desc_sw128(vt + kk * 2048, kBoxBytes, 1024), C::kIdescPV,
-                               !(first && kk == 0));
+                               umma_desc_advance(vd, kk * 2048), C::kIdescPV, !(first && kk == 0));
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               umma_bf16_tmem_a(od, pb + 32 * (kk >> 1) + 16 + 8 * (kk & 1),
-                               umma_desc_sw128(vt + kk * 2048, kBoxBytes, 1024), C::kIdescPV,
-                               true);
+                               umma_desc_advance(vd, kk * 2048), C::kIdescPV, true);
             umma_commit(&o_done[tb]);
           }
           if (!ok) break;

@@ -31,6 +31,15 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_byte_addr, uin
   return d;
 }
 
+// The descriptor of the operand `bytes` further on in shared memory: the
+// start address is the low 14 bits in 16-byte units, and shared memory
+// addresses stay below 2^18, so the sum never carries into the other
+// fields.  With a constant `bytes` this is one add per product where
+// umma_desc_sw128 is several dependent operations.
+__device__ __forceinline__ uint64_t umma_desc_advance(uint64_t desc, uint32_t bytes) {
+  return desc + (uint64_t)(bytes >> 4);
+}
+
 // kind::f16 instruction descriptor: fp32 accumulator, bf16 A and B.
 __host__ __device__ constexpr uint32_t umma_idesc_bf16(int m, int n, int a_mn_major,
                                                        int b_mn_major) {
