@@ -10,12 +10,13 @@
 // (positions[p] - window, positions[p]], the head's sink logit in the
 // denominator only.
 //
-// Why pairs: a tcgen05 product of M 128 rows and K 16 costs about the same
-// time for any N up to 128, so the one-SM kernel, whose S products cover one
-// 64-key page (N 64), spends as long on them as on the N 128 P V products.
-// A product over the CTA pair takes B split along N between the two CTAs; if
-// each CTA holds one whole page, one S product covers two pages (N 128)
-// without any rearrangement of the page tiles.
+// Why pairs: a tcgen05 product of M 128 rows and K 16 runs at two thirds of
+// the tensor pipe's rate at N 64 (the one-SM kernel's S products, one 64-key
+// page each) and at full rate from N 128 on.  A product over the CTA pair
+// takes B split along N between the two CTAs; if each CTA holds one whole
+// page, one S product covers two pages (N 128) without any rearrangement of
+// the page tiles, and each SM copies every other page.  Each work item then
+// has two SMs, which is what pays when a call has fewer items than SMs.
 //
 // Work items are the one-SM kernel's: (block of 2 x 128 / G consecutive
 // packed tokens, kv head), two query tiles of 128 rows (token, head).  A pair
