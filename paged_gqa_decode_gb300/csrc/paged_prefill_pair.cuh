@@ -85,7 +85,7 @@ struct PairPrefillCfg {
   static constexpr int kQTileBytes = kRows * D * 2;
   static constexpr int kBarOff = kQOff + kQTileBytes;
   static constexpr int kSCols = 2 * kPage;  // S / P columns of a pair
-  static constexpr int kNumBars = 2 * RK + 2 * RV + 4 * SB + 16;
+  static constexpr int kNumBars = 2 * RK + 2 * RV + 4 * SB + 14;
   static constexpr int kSmemBytes = 1024 + kBarOff + kNumBars * 8;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kOCol = 0, kSCol = D;
@@ -150,14 +150,13 @@ __global__ void __cluster_dims__(2, 1, 1)
   uint64_t* item_ready = o_done + SB;   // [item % 2] descriptor written
   uint64_t* item_free = item_ready + 2; // [item % 2] descriptor consumed by every role
   uint64_t* fin = item_free + 2;        // rank 0: [issuer] every product it issued done
-  uint64_t* xbar = fin + 2;             // [slot] the four warpgroups' values exchanged
-  uint64_t* q_full = xbar + 2;          // rank 0: both Q tiles landed; rank 1: its own
+  uint64_t* q_full = fin + 2;           // rank 0: both Q tiles landed; rank 1: its own
   uint64_t* q_free = q_full + 1;        // the item's S products done (multicast commit)
   uint64_t* j_ready = q_free + 1;       // rank 1: [item % 2] the item index written
   uint64_t* j_free = j_ready + 2;       // rank 0: [item % 2] rank 1 has read the index
   __shared__ PrefillItem items[2];
   __shared__ int y_ring[2][2][64];       // [K, V producer][page of the pair] tile rows
-  __shared__ float xval[2][4][C::kRows];  // [slot][quarter][row]
+  __shared__ float xval[2][4][C::kRows];  // [slot][quarter][row]: values exchanged at the named barrier
   __shared__ volatile int abort_flag;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int j_slot[2];
@@ -183,7 +182,6 @@ __global__ void __cluster_dims__(2, 1, 1)
       // softmax threads + S issuer, P V issuer, V producer (rank 0); + Q copier,
       // V producer (rank 1)
       mbar_init(&item_free[b], C::kSoftmaxThreads + (lead ? 3 : 2));
-      mbar_init(&xbar[b], C::kSoftmaxThreads);
       mbar_init(&j_ready[b], 1);
       mbar_init(&j_free[b], 1);
     }
@@ -609,19 +607,23 @@ __global__ void __cluster_dims__(2, 1, 1)
     const float c = p.q_scale_log2;
     const float cc = c > 0.f ? c : 1.f;
     int i = 0;
-    bool ok = true;
+    // The four warpgroups exchange values at a named barrier that also ORs
+    // a failure flag over them (as in the one-SM kernel), so they leave
+    // their loops together.
+    bool ok = true, mine = true;
     const int tl = (int)rank * T + m / G, g = m % G;  // token of the block, head of the group
     const bool in_tile = m / G < T;
     uint64_t* p_sig = lead ? p_full : p_peer;
     auto next_item = [&](int seq) -> bool {
       const int d = seq & 1;
       if (!all_ok(wait(&item_ready[d], (seq >> 1) & 1))) {
-        ok = false;
+        mine = false;
         return false;
       }
       return items[d].valid != 0;
     };
     bool have = next_item(0);
+    ok = !named_sync_or(1, C::kSoftmaxThreads, !mine);
     for (int seq = 0; ok && have; ++seq) {
       const int d = seq & 1;
       const PrefillItem& it = items[d];
@@ -647,10 +649,7 @@ __global__ void __cluster_dims__(2, 1, 1)
           const int b = i % SB;
           const uint32_t scol = C::kSCol + b * C::kSCols;
           const int pg = pg2 + h;  // this quarter's page (past `last`: none)
-          if (!all_ok(wait(&s_full[b], (i / SB) & 1))) {
-            ok = false;
-            break;
-          }
+          if (!all_ok(wait(&s_full[b], (i / SB) & 1))) mine = false;
           tc_fence_after_sync();
           float sv[kKeys];
 #pragma unroll
@@ -688,8 +687,7 @@ __global__ void __cluster_dims__(2, 1, 1)
           {
             const int sl = xn & 1;
             xval[sl][qt][m] = mxh;
-            mbar_arrive(&xbar[sl]);
-            if (!all_ok(wait(&xbar[sl], (xn >> 1) & 1))) {
+            if (named_sync_or(1, C::kSoftmaxThreads, !mine)) {
               ok = false;
               break;
             }
@@ -735,20 +733,20 @@ __global__ void __cluster_dims__(2, 1, 1)
           if (__any_sync(0xffffffffu, rose)) {
             // O holds P V up to pair i - 1, which must be done
             const int bp = (i - 1) % SB;
-            if (!all_ok(wait(&o_done[bp], ((i - 1) / SB) & 1))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after_sync();
+            if (all_ok(wait(&o_done[bp], ((i - 1) / SB) & 1))) {
+              tc_fence_after_sync();
 #pragma unroll
-            for (int j = 0; j < D / 64; ++j) {  // this quarter's O columns
-              const int q16 = qt * (D / 64) + j;
-              float ov[16];
-              tmem_ld16(lane_base + C::kOCol + 16 * q16, ov);
-              tmem_wait_ld();
+              for (int j = 0; j < D / 64; ++j) {  // this quarter's O columns
+                const int q16 = qt * (D / 64) + j;
+                float ov[16];
+                tmem_ld16(lane_base + C::kOCol + 16 * q16, ov);
+                tmem_wait_ld();
 #pragma unroll
-              for (int k = 0; k < 16; ++k) ov[k] *= alpha;
-              tmem_st16(lane_base + C::kOCol + 16 * q16, ov);
+                for (int k = 0; k < 16; ++k) ov[k] *= alpha;
+                tmem_st16(lane_base + C::kOCol + 16 * q16, ov);
+              }
+            } else {
+              mine = false;
             }
           }
           if ((qt & 1) == 0 && pg <= last) {
@@ -756,12 +754,10 @@ __global__ void __cluster_dims__(2, 1, 1)
             // from the P signal); rows outside the run's key range on a
             // boundary page -> zero
             const int s = i % RV;
-            if (!all_ok(wait(&v_full[s], (i / RV) & 1))) {
-              ok = false;
-              break;
-            }
+            const bool landed = all_ok(wait(&v_full[s], (i / RV) & 1));
+            if (!landed) mine = false;
             const int rlo = max(lo_run - pos0, 0), rhi = min(pos_last - pos0, kPage - 1);
-            if (rlo > 0 || rhi < kPage - 1) {
+            if (landed && (rlo > 0 || rhi < kPage - 1)) {
               unsigned char* vt = v_slots + s * C::kVBytes + h * C::kVHalfBytes;
               for (int e = m; e < kPage * 8; e += C::kRows) {
                 const int k = e >> 3, ch = e & 7;
@@ -780,16 +776,14 @@ __global__ void __cluster_dims__(2, 1, 1)
 
         // end of run: the O row once P V of the last pair is done
         const int il = i - 1;
-        if (!all_ok(wait(&o_done[il % SB], (il / SB) & 1))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
+        if (all_ok(wait(&o_done[il % SB], (il / SB) & 1)))
+          tc_fence_after_sync();
+        else
+          mine = false;
         {
           const int sl = xn & 1;
           xval[sl][qt][m] = l;
-          mbar_arrive(&xbar[sl]);
-          if (!all_ok(wait(&xbar[sl], (xn >> 1) & 1))) {
+          if (named_sync_or(1, C::kSoftmaxThreads, !mine)) {
             ok = false;
             break;
           }
@@ -828,6 +822,7 @@ __global__ void __cluster_dims__(2, 1, 1)
       if (!ok) break;
       mbar_arrive(&item_free[d]);
       have = next_item(seq + 1);
+      ok = !named_sync_or(1, C::kSoftmaxThreads, !mine);
     }
   }
 

@@ -43,7 +43,9 @@
 //               (and half of the O columns each for the rescale and the
 //               store).  Per page its scores from TMEM, causal and window
 //               mask, its half's max, the row's max over the page through
-//               shared memory (bounded mbarrier waits), online softmax in
+//               shared memory at the tile's named barrier (which also ORs
+//               the threads' failed-wait flags, so the two warpgroups stop
+//               together after a timeout), online softmax in
 //               log2 units with a lazy running max (raised only when a score
 //               exceeds it by more than 2^8, which then rescales that row of
 //               O_t in TMEM); P is written over S as a bf16 head and residual
@@ -91,7 +93,7 @@ struct UmmaPrefillCfg {
   // S / P buffers per tile: two where TMEM has room (head_dim 64), so S of
   // the next page is computed while the softmax works on this one
   static constexpr int kSBufs = 2;
-  static constexpr int kNumBars = 2 * RK + 2 * RV + 3 * kTiles * kSBufs + 6 + 2 * kTiles + 2;
+  static constexpr int kNumBars = 2 * RK + 2 * RV + 3 * kTiles * kSBufs + 6 + 2;
   static constexpr int kSmemBytes = 1024 + kBarOff + kNumBars * 8;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kOCol = 0, kSCol = kTiles * D;
@@ -126,6 +128,19 @@ __device__ __forceinline__ bool mbar_wait_abortable(uint64_t* bar, uint32_t pari
       }
     }
   }
+}
+
+// Named barrier `id` among `count` threads that also ORs `pred` over them:
+// every participating thread gets the same answer.
+__device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
 }
 
 // One work item as the producer laid it out for the other roles.
@@ -197,12 +212,13 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
   uint64_t* item_ready = o_done + C::kTiles * C::kSBufs;  // [item % 2] descriptor written
   uint64_t* item_free = item_ready + 2;       // [item % 2] consumed (softmax, issuers, V producer)
   uint64_t* fin = item_free + 2;              // [issuer] every MMA it issued done
-  uint64_t* xbar = fin + 2;                   // [tile * 2 + slot] the halves' values exchanged
-  uint64_t* q_full = xbar + 2 * C::kTiles;    // head_dim 128: the item's Q rows landed (TMA)
-  uint64_t* q_free = q_full + 1;              // head_dim 128: the item's S products done
+  uint64_t* q_full = fin + 2;                 // the item's Q rows landed (TMA)
+  uint64_t* q_free = q_full + 1;              // the item's S products done: Q may be replaced
   __shared__ PrefillItem items[2];
-  __shared__ int y_ring[2][64];
-  __shared__ float xval[C::kTiles][2][2][C::kRows];  // [tile][slot][half][row]  // [K, V producer] tile rows of upcoming pages, by page % 64
+  __shared__ int y_ring[2][64];  // [K, V producer] tile rows of upcoming pages, by page % 64
+  // [tile][slot][half][row]: the values the tile's two warpgroups exchange
+  // (row maximum of a page, row sum of a run) at the tile's named barrier
+  __shared__ float xval[C::kTiles][2][2][C::kRows];
   __shared__ volatile int abort_flag;
   __shared__ uint32_t tmem_slot;
 
@@ -226,7 +242,6 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
     }
     mbar_init(&fin[0], 1);
     mbar_init(&fin[1], 1);
-    for (int x = 0; x < 2 * C::kTiles; ++x) mbar_init(&xbar[x], 2 * C::kRows);
     mbar_init(q_full, 1);
     mbar_init(q_free, 1);
     mbar_init_fence();
@@ -574,7 +589,12 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
     const float c = p.q_scale_log2;
     const float cc = c > 0.f ? c : 1.f;
     int i = 0;  // page index over all items
-    bool ok = true;
+    // The tile's two warpgroups exchange values at a named barrier (id 1 +
+    // t) that also ORs a failure flag over them, so they leave their loops
+    // together: a thread whose wait gave up (`mine` false) carries on to the
+    // next exchange, and every thread of the tile stops there (`ok` false).
+    bool ok = true, mine = true;
+    const uint32_t xid = 1 + t, xcount = 2 * C::kRows;
     const int tl = t * T + m / G, g = m % G;  // token of the block, head of the group
     const bool in_tile = m / G < T;           // rows past T * G hold no token
     // Waits for the descriptor of item seq (its Q is copied in by the S
@@ -582,12 +602,13 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
     auto next_item = [&](int seq) -> bool {
       const int d = seq & 1;
       if (!all_ok(wait(&item_ready[d], (seq >> 1) & 1))) {
-        ok = false;
+        mine = false;
         return false;
       }
       return items[d].valid != 0;
     };
     bool have = next_item(0);
+    ok = !named_sync_or(xid, xcount, !mine);
     for (int seq = 0; ok && have; ++seq) {
       const int d = seq & 1;
       const PrefillItem& it = items[d];
@@ -612,10 +633,7 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
         for (int pg = first; pg <= last; ++pg, ++i) {
           const int tb = t * C::kSBufs + i % C::kSBufs;
           const uint32_t scol = C::kSCol + tb * kPage;
-          if (!all_ok(wait(&s_full[tb], (i / C::kSBufs) & 1))) {
-            ok = false;
-            break;
-          }
+          if (!all_ok(wait(&s_full[tb], (i / C::kSBufs) & 1))) mine = false;
           tc_fence_after_sync();
           float sv[kHalf];
 #pragma unroll
@@ -659,8 +677,7 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
           {
             const int sl = xn & 1;
             xval[t][sl][h][m] = mxh;
-            mbar_arrive(&xbar[t * 2 + sl]);
-            if (!all_ok(wait(&xbar[t * 2 + sl], (xn >> 1) & 1))) {
+            if (named_sync_or(xid, xcount, !mine)) {
               ok = false;
               break;
             }
@@ -709,34 +726,36 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
           if (__any_sync(0xffffffffu, rose)) {
             // O_t holds P V up to page i - 1, which must be done (with one
             // buffer it was, before S_t of this page was issued)
+            bool done = true;
             if (C::kSBufs > 1) {
               const int tp = t * C::kSBufs + (i - 1) % C::kSBufs;
-              if (!all_ok(wait(&o_done[tp], ((i - 1) / C::kSBufs) & 1))) {
-                ok = false;
-                break;
-              }
-              tc_fence_after_sync();
+              done = all_ok(wait(&o_done[tp], ((i - 1) / C::kSBufs) & 1));
+              if (done) tc_fence_after_sync();
+              else mine = false;
             }
+            if (done) {
 #pragma unroll
-            for (int j = 0; j < D / 32; ++j) {  // this half's O columns
-              const int q16 = h * (D / 32) + j;
-              float ov[16];
-              tmem_ld16(lane_base + C::kOCol + t * D + 16 * q16, ov);
-              tmem_wait_ld();
+              for (int j = 0; j < D / 32; ++j) {  // this half's O columns
+                const int q16 = h * (D / 32) + j;
+                float ov[16];
+                tmem_ld16(lane_base + C::kOCol + t * D + 16 * q16, ov);
+                tmem_wait_ld();
 #pragma unroll
-              for (int k = 0; k < 16; ++k) ov[k] *= alpha;
-              tmem_st16(lane_base + C::kOCol + t * D + 16 * q16, ov);
+                for (int k = 0; k < 16; ++k) ov[k] *= alpha;
+                tmem_st16(lane_base + C::kOCol + t * D + 16 * q16, ov);
+              }
             }
           }
           // V rows outside the run's key range on a boundary page -> zero
           // (warpgroup 0; both tiles' products read them after its P)
           const int rlo = max(lo_run - pos0, 0), rhi = min(pos_last - pos0, kPage - 1);
-          if (t == 0 && h == 0 && (rlo > 0 || rhi < kPage - 1)) {
+          bool zero = t == 0 && h == 0 && (rlo > 0 || rhi < kPage - 1);
+          if (zero && !all_ok(wait(&v_full[i % RV], (i / RV) & 1))) {
+            mine = false;
+            zero = false;
+          }
+          if (zero) {
             const int s = i % RV;
-            if (!all_ok(wait(&v_full[s], (i / RV) & 1))) {
-              ok = false;
-              break;
-            }
             unsigned char* vt = v_slots + s * C::kTileBytes;
             for (int e = m; e < kPage * (D / 8); e += C::kRows) {
               const int k = e / (D / 8), ch = e % (D / 8);
@@ -754,16 +773,14 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
 
         // end of run: the O_t row once P V of the last page is done
         const int il = i - 1;
-        if (!all_ok(wait(&o_done[t * C::kSBufs + il % C::kSBufs], (il / C::kSBufs) & 1))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
+        if (all_ok(wait(&o_done[t * C::kSBufs + il % C::kSBufs], (il / C::kSBufs) & 1)))
+          tc_fence_after_sync();
+        else
+          mine = false;
         {  // the row sum: this half's plus the other half's
           const int sl = xn & 1;
           xval[t][sl][h][m] = l;
-          mbar_arrive(&xbar[t * 2 + sl]);
-          if (!all_ok(wait(&xbar[t * 2 + sl], (xn >> 1) & 1))) {
+          if (named_sync_or(xid, xcount, !mine)) {
             ok = false;
             break;
           }
@@ -804,6 +821,7 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
       // waiting for the next item
       mbar_arrive(&item_free[d]);
       have = next_item(seq + 1);
+      ok = !named_sync_or(xid, xcount, !mine);
     }
   }
 
