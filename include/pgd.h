@@ -223,7 +223,8 @@ PGD_API size_t pgd_paged_decode_workspace_bytes(const pgd_dims* dims, const pgd_
  *               pgd_paged_prefill_attention (> 0) for a prefill call.
  *   window, opts  as passed to that call.
  *   count       out: 0 when dims->rows == 0; 1 for AUTO with a window of
- *               1..128 positions (the window kernel); for PREFILL_UMMA 2 without a
+ *               1..128 positions (the window kernel); for PREFILL_UMMA and
+ *               PREFILL_PAIR 2 without a
  *               window when the tokens form at most 4096 blocks of
  *               2 x (128 / group) (a pass that orders the blocks longest
  *               first, then the prefill kernel), else 1 (the kernel, after
@@ -306,14 +307,16 @@ PGD_API int pgd_paged_decode_step(const pgd_dims* dims, const void* q, const voi
  * Kernels (opts->kernel): AUTO chooses PREFILL_UMMA (tokens in blocks of
  * 2 x 128 / (Hq / Hkv), two query tiles, share every page load; persistent,
  * one CTA per SM; each item's Q copied in with TMA; without a window the
- * blocks are taken longest first) when P >= 8 * table_rows, else the
- * per-token decode kernels (the window kernel for windows of 1..128
- * positions, the TENSOR_CORE split kernel otherwise).
+ * blocks are taken longest first) when P >= 8 * table_rows -- at head_dim
+ * 128 PREFILL_PAIR instead (the same blocks, two SMs each) when the blocks
+ * x Hkv are at most the device's SM count -- else the per-token decode
+ * kernels (the window kernel for windows of 1..128 positions, the
+ * TENSOR_CORE split kernel otherwise).
  * Device errors: rows[p] outside [0, table_rows), plus those of
  * pgd_paged_decode_attention; the token's output is zero.  After
  * PGD_EDEVICE_TIMEOUT (a pipeline wait gave up) the outputs of the tokens
- * whose work was abandoned are unspecified: the PREFILL_TILED and
- * PREFILL_UMMA kernels stop without writing them.
+ * whose work was abandoned are unspecified: the PREFILL_TILED,
+ * PREFILL_UMMA and PREFILL_PAIR kernels stop without writing them.
  */
 PGD_API int pgd_paged_prefill_attention(const pgd_dims* dims, int32_t table_rows, const void* q,
                                         const void* k_pool, const void* v_pool,
@@ -336,9 +339,9 @@ PGD_API int pgd_paged_prefill_attention(const pgd_dims* dims, int32_t table_rows
  *   k_new, v_new  bf16 [P][Hkv][D] device pointers, 16-byte aligned.
  *   k_pool, v_pool  written (the tokens' slots) and read.
  *   Others as for pgd_paged_prefill_attention.
- * Launches: one kernel writes the tokens (with PREFILL_UMMA its first CTA
- * also prepares the attention kernel's work counter and block order in the
- * workspace), then the attention kernels; pgd_prefill_step_kernel_count
+ * Launches: one kernel writes the tokens (with PREFILL_UMMA or PREFILL_PAIR
+ * its first CTA also prepares the attention kernel's work counter and block
+ * order in the workspace), then the attention kernels; pgd_prefill_step_kernel_count
  * gives the number.  Two tokens with the same slot race, as with
  * pgd_kv_write_slots.
  * Device errors: a token whose row, page index or page is out of range is
@@ -355,8 +358,8 @@ PGD_API int pgd_paged_prefill_step(const pgd_dims* dims, int32_t table_rows, con
 
 /* Kernels one pgd_paged_prefill_step call with these arguments launches on
  * the current device: the write launch plus the attention kernels (for
- * PREFILL_UMMA the attention kernel alone, its counter and order prepared by
- * the write launch).  table_rows > 0; count 0 when dims->rows == 0.  Returns
+ * PREFILL_UMMA and PREFILL_PAIR the attention kernel alone, its counter and
+ * order prepared by the write launch).  table_rows > 0; count 0 when dims->rows == 0.  Returns
  * PGD_EINVAL for a NULL count or table_rows <= 0, else as
  * pgd_attention_kernel_count. */
 PGD_API int pgd_prefill_step_kernel_count(const pgd_dims* dims, int32_t table_rows,
