@@ -102,6 +102,7 @@ struct UmmaPrefillCfg {
   static_assert(D == 64 || D == 128, "head_dim");
   static_assert(kSCol + kTiles * kSBufs * kPage <= kTmemCols, "TMEM columns");
   static_assert(RK == RV, "the K and V rings are streamed by one helper");
+  static_assert(kSBufs <= RV, "a V slot is freed when S of the page kSBufs later is issued");
   static_assert(kSmemBytes + 8 * 1024 <= 227 * 1024, "shared memory");
 };
 
@@ -202,9 +203,9 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
   unsigned char* v_slots = base + C::kVOff;
   unsigned char* q_smem = base + C::kQOff;  // [tile] Q rows (head_dim 128)
   uint64_t* k_full = reinterpret_cast<uint64_t*>(base + C::kBarOff);  // TMA landed
-  uint64_t* k_empty = k_full + RK;         // S of the page done (MMA commit)
+  uint64_t* k_empty = k_full + RK;         // S of the page read (P V issuer, on the last P)
   uint64_t* v_full = k_empty + RK;
-  uint64_t* v_empty = v_full + RV;         // P V of the page done (MMA commit)
+  uint64_t* v_empty = v_full + RV;         // P V of the page done (S issuer, on o_done)
   // per (tile t, buffer b = page % kSBufs) at t * kSBufs + b:
   uint64_t* s_full = v_empty + RV;         // S of the page in TMEM (MMA commit)
   uint64_t* p_full = s_full + C::kTiles * C::kSBufs;  // P in TMEM (and boundary V rows zeroed)
@@ -495,9 +496,15 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
           for (int t = 0; t < C::kTiles; ++t) {
             // the buffer holds P_t of page i - kSBufs until P V has read it
             const int tb = t * C::kSBufs + b;
-            if (i >= C::kSBufs && !wait(&o_done[tb], ((i / C::kSBufs) - 1) & 1)) {
-              ok = false;
-              break;
+            if (i >= C::kSBufs) {
+              if (!wait(&o_done[tb], ((i / C::kSBufs) - 1) & 1)) {
+                ok = false;
+                break;
+              }
+              // the last tile's P V of page i - kSBufs done (its commit
+              // covers every product issued before it): that page's V slot
+              // is free -- one thread arrival in place of a commit a page
+              if (t == C::kTiles - 1) mbar_arrive(&v_empty[(i - C::kSBufs) % RV]);
             }
             tc_fence_after_sync();
             const uint32_t sb = tmem + C::kSCol + tb * kPage;
@@ -510,7 +517,6 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
             umma_commit(&s_full[tb]);
           }
           if (!ok) break;
-          umma_commit(&k_empty[i % RK]);
           issued = true;
         }
         if (ok) umma_commit(q_free);  // this item's S products done: Q may be replaced
@@ -551,6 +557,9 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
               ok = false;
               break;
             }
+            // the last tile's softmax has read its S, whose commit covers
+            // both tiles' S products: page i's K slot is free
+            if (t == C::kTiles - 1) mbar_arrive(&k_empty[i % RK]);
             tc_fence_after_sync();
             const uint32_t pb = tmem + C::kSCol + tb * kPage;
             const uint32_t od = tmem + C::kOCol + t * D;
@@ -567,7 +576,6 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
             umma_commit(&o_done[tb]);
           }
           if (!ok) break;
-          umma_commit(&v_empty[i % RV]);
           first = false;
           issued = true;
         }
