@@ -120,8 +120,6 @@ __global__ void __cluster_dims__(2, 1, 1)
                                   int* item_counter, const int* block_order) {
   using C = PairPrefillCfg<RK, RV, SB>;
   constexpr int D = C::D;
-  pdl_wait();
-  pdl_allow_dependents();
   const int G = p.group;
   const int T = C::kRows / G;  // tokens per tile
   const int tokens = 2 * T;
@@ -212,6 +210,10 @@ __global__ void __cluster_dims__(2, 1, 1)
   cluster_sync_all();
   tc_fence_after_sync();
   const uint32_t tmem = tmem_slot;
+  // the set-up above touches only this CTA's shared memory and TMEM, so it
+  // overlaps the kernel before; everything from here may read its writes
+  pdl_wait();
+  pdl_allow_dependents();
   const uint32_t peer_abort = cluster_map(smem_addr(const_cast<int*>(&abort_flag)), rank ^ 1u);
   // Bounded wait that also gives up when either CTA has; a CTA that gives up
   // tells the other.  `remote`: the phase is completed by an arrival from
@@ -873,8 +875,8 @@ cudaError_t launch_prefill_pair(const DecodeParams& p, const CUtensorMap& k_map,
   if (prepared)
     e = cudaSuccess;
   else if (order)
-    e = launch_pdl(prefill_block_order_kernel<128>, dim3(1), dim3(1024), 0, stream, p, tokens,
-                   n_blocks, counter, order);
+    e = launch_pdl(prefill_block_order_kernel<128>, dim3(1), dim3(block_order_threads(n_blocks)),
+                   0, stream, p, tokens, n_blocks, counter, order);
   else
     e = cudaMemsetAsync(counter, 0, sizeof(int), stream);
   if (e != cudaSuccess) return e;

@@ -185,8 +185,6 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
                               const __grid_constant__ CUtensorMap q_map, const DecodeParams p,
                               int* item_counter, const int* block_order) {
   using C = UmmaPrefillCfg<D, RK, RV>;
-  pdl_wait();
-  pdl_allow_dependents();
   const int G = p.group;
   const int T = C::kRows / G;  // tokens per tile
   const int tokens = C::kTiles * T;
@@ -266,6 +264,10 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = tmem_slot;
+  // the set-up above touches only this CTA's shared memory and TMEM, so it
+  // overlaps the kernel before; everything from here may read its writes
+  pdl_wait();
+  pdl_allow_dependents();
   auto wait = [&](uint64_t* bar, uint32_t parity) {
     return mbar_wait_abortable(bar, parity, p.err, &abort_flag);
   };
@@ -849,6 +851,16 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
 // ms), take them in token order, last block first.
 constexpr int kMaxSortedBlocks = 4096;
 
+// Threads of the block-order pass: one per key of the padded sort, so that
+// each thread makes one round trip for its block's tokens, and no more (the
+// sort's steps meet at a CTA barrier, which costs more the more warps wait
+// at it); at least a warp and at most 1024.
+inline int block_order_threads(int n_blocks) {
+  int n2 = 32;
+  while (n2 < n_blocks && n2 < 1024) n2 <<= 1;
+  return n2;
+}
+
 // Before the prefill kernel (one CTA): zeroes its item counter and writes
 // order[0 .. n_blocks) = the token blocks, longest key span first, so that
 // the persistent CTAs take the long items first and finish together.  A
@@ -996,8 +1008,8 @@ cudaError_t launch_prefill_umma(const DecodeParams& p, const CUtensorMap& k_map,
   if (prepared)
     e = cudaSuccess;
   else if (order)
-    e = launch_pdl(prefill_block_order_kernel<D>, dim3(1), dim3(1024), 0, stream, p, tokens,
-                   n_blocks, counter, order);
+    e = launch_pdl(prefill_block_order_kernel<D>, dim3(1), dim3(block_order_threads(n_blocks)), 0,
+                   stream, p, tokens, n_blocks, counter, order);
   else
     e = cudaMemsetAsync(counter, 0, sizeof(int), stream);
   if (e != cudaSuccess) return e;
