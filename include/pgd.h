@@ -107,9 +107,12 @@ enum {
                                    mma.sync products; no splits), anything else to
                                    TENSOR_CORE; prefill: when the tokens average
                                    at least 8 per table row (prompt chunks),
-                                   PREFILL_PAIR at head_dim 128 if its blocks x
-                                   kv heads are at most the device's SMs, else
-                                   PREFILL_UMMA; otherwise as decode, per token */
+                                   PREFILL_UMMA, whose blocks x kv heads, when
+                                   at most half the device's SMs, are cut into
+                                   key parts (see pgd_paged_prefill_attention)
+                                   or, where too short to cut, at head_dim 128
+                                   go to PREFILL_PAIR; otherwise as decode,
+                                   per token */
   PGD_KERNEL_TENSOR_CORE = 1,   /* mma.sync bf16 products, fp32 accumulate, per token,
                                    key range split over CTAs + combine */
   PGD_KERNEL_CUDA_CORE = 2,     /* fp32 FMA products on the CUDA cores, per token */
@@ -117,8 +120,9 @@ enum {
                                    load (mma.sync tensor cores, no key splits) */
   PGD_KERNEL_PREFILL_UMMA = 4,  /* prefill only: persistent, two tiles of 128
                                    query rows per block on the tcgen05 tensor
-                                   cores (TMEM accumulators), no key splits;
-                                   uses the start of the workspace for its work
+                                   cores (TMEM accumulators), no key splits
+                                   when named (AUTO may add key parts); uses
+                                   the start of the workspace for its work
                                    counter and block order */
   PGD_KERNEL_PREFILL_PAIR = 5   /* prefill only, head_dim 128: the same blocks
                                    on pairs of SMs (clusters of two CTAs, one
@@ -211,7 +215,9 @@ PGD_API int pgd_rope_append_paged(const pgd_dims* dims, float theta, void* q,
 /*
  * Bytes of device workspace pgd_paged_decode_attention needs for these dims
  * and options on the current device: split partials (m, l and an unnormalised
- * fp32 accumulator per row, query head and split).  0 if dims are invalid.
+ * fp32 accumulator per row, query head and split), with room as well for the
+ * key parts a prefill call of these dims may be cut into (one more split's
+ * worth than their number).  0 if dims are invalid.
  */
 PGD_API size_t pgd_paged_decode_workspace_bytes(const pgd_dims* dims, const pgd_decode_options* opts);
 
@@ -228,7 +234,8 @@ PGD_API size_t pgd_paged_decode_workspace_bytes(const pgd_dims* dims, const pgd_
  *               window when the tokens form at most 4096 blocks of
  *               2 x (128 / group) (a pass that orders the blocks longest
  *               first, then the prefill kernel), else 1 (the kernel, after
- *               one 4-byte cudaMemsetAsync); 1 for PREFILL_TILED and for
+ *               one 4-byte cudaMemsetAsync), plus 1 (the combine) when AUTO
+ *               cuts the blocks into key parts; 1 for PREFILL_TILED and for
  *               split kernels whose rows all fit one split (it writes every
  *               output); 2 when a row can span several splits (split kernel
  *               + combine kernel).
@@ -307,11 +314,18 @@ PGD_API int pgd_paged_decode_step(const pgd_dims* dims, const void* q, const voi
  * Kernels (opts->kernel): AUTO chooses PREFILL_UMMA (tokens in blocks of
  * 2 x 128 / (Hq / Hkv), two query tiles, share every page load; persistent,
  * one CTA per SM; each item's Q copied in with TMA; without a window the
- * blocks are taken longest first) when P >= 8 * table_rows -- at head_dim
- * 128 PREFILL_PAIR instead (the same blocks, two SMs each) when the blocks
- * x Hkv are at most the device's SM count -- else the per-token decode
- * kernels (the window kernel for windows of 1..128 positions, the
- * TENSOR_CORE split kernel otherwise).
+ * blocks are taken longest first) when P >= 8 * table_rows, else the
+ * per-token decode kernels (the window kernel for windows of 1..128
+ * positions, the TENSOR_CORE split kernel otherwise).  When the blocks x
+ * Hkv (the work items) are at most half the device's SM count, AUTO cuts
+ * each item's pages into key parts -- min(8, SMs / items, L / 8) of them,
+ * L the table width in pages (with a window, the pages a block's keys can
+ * span), if that is 2 or more -- each a work unit of its own that writes
+ * partials (m, l and an unnormalised fp32 accumulator per token, head and
+ * part) into the workspace, which a combine launch merges with the sink;
+ * the results then differ from PREFILL_UMMA's by rounding only.  Where the
+ * items are too short to cut, at head_dim 128 such calls go to
+ * PREFILL_PAIR (the same blocks, two SMs each).
  * Device errors: rows[p] outside [0, table_rows), plus those of
  * pgd_paged_decode_attention; the token's output is zero.  After
  * PGD_EDEVICE_TIMEOUT (a pipeline wait gave up) the outputs of the tokens
@@ -359,7 +373,7 @@ PGD_API int pgd_paged_prefill_step(const pgd_dims* dims, int32_t table_rows, con
 /* Kernels one pgd_paged_prefill_step call with these arguments launches on
  * the current device: the write launch plus the attention kernels (for
  * PREFILL_UMMA and PREFILL_PAIR the attention kernel alone, its counter and
- * order prepared by the write launch).  table_rows > 0; count 0 when dims->rows == 0.  Returns
+ * order prepared by the write launch, and the combine with key parts).  table_rows > 0; count 0 when dims->rows == 0.  Returns
  * PGD_EINVAL for a NULL count or table_rows <= 0, else as
  * pgd_attention_kernel_count. */
 PGD_API int pgd_prefill_step_kernel_count(const pgd_dims* dims, int32_t table_rows,

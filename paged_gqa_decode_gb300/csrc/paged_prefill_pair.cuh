@@ -92,7 +92,7 @@ struct PairPrefillCfg {
   static constexpr uint32_t kIdescS = umma_idesc_bf16(256, kSCols, 0, 0);
   static constexpr uint32_t kIdescPV = umma_idesc_bf16(256, D, 0, 1);
   static_assert(kSCol + SB * kSCols <= kTmemCols, "TMEM columns");
-  static_assert(kSmemBytes + 12 * 1024 <= 227 * 1024, "shared memory");
+  static_assert(kSmemBytes + 20 * 1024 <= 227 * 1024, "shared memory (dynamic + static)");
 };
 
 // Pair walk of an item's runs: c.pg is the first page of the current pair.
@@ -386,6 +386,8 @@ __global__ void __cluster_dims__(2, 1, 1)
         it.t_begin = t_begin;
         it.t_end = t_end;
         it.kvh = kvh;
+        it.part = 0;  // every page of the item
+        it.parts = 1;
       }
       __syncwarp();
       for (int r = 0; r < it.runs; ++r) {

@@ -7,14 +7,14 @@ namespace pgd {
 // paged_prefill_umma_d64.cu
 cudaError_t launch_prefill_umma_d64(const DecodeParams& p, const CUtensorMap& k_map,
                                     const CUtensorMap& v_map, const CUtensorMap& q_map,
-                                    int sm_count, bool prepared, cudaStream_t stream);
+                                    int sm_count, bool prepared, int parts, cudaStream_t stream);
 
 cudaError_t launch_prefill_umma(const DecodeParams& p, const CUtensorMap& k_map,
                                 const CUtensorMap& v_map, const CUtensorMap& q_map, int head_dim,
-                                int sm_count, bool prepared, cudaStream_t stream) {
+                                int sm_count, bool prepared, int parts, cudaStream_t stream) {
   return head_dim == 64
-             ? launch_prefill_umma_d64(p, k_map, v_map, q_map, sm_count, prepared, stream)
-             : launch_prefill_umma<128, 4, 4>(p, k_map, v_map, q_map, sm_count, prepared,
+             ? launch_prefill_umma_d64(p, k_map, v_map, q_map, sm_count, prepared, parts, stream)
+             : launch_prefill_umma<128, 4, 4>(p, k_map, v_map, q_map, sm_count, prepared, parts,
                                               stream);
 }
 
@@ -35,12 +35,12 @@ cudaError_t launch_prefill_write(const DecodeParams& p, int head_dim, bool umma,
                           n_blocks, counter, order);
 }
 
-int prefill_umma_launches(int rows, int group, int window) {
+int prefill_umma_launches(int rows, int group, int window, int parts) {
   if (rows <= 0) return 0;
   using C = UmmaPrefillCfg<128, 4, 4>;  // the block geometry is the same at head_dim 64
   const int tokens = C::kTiles * (C::kRows / group);
   const int n_blocks = (rows + tokens - 1) / tokens;
-  return window <= 0 && n_blocks <= kMaxSortedBlocks ? 2 : 1;
+  return (window <= 0 && n_blocks <= kMaxSortedBlocks ? 2 : 1) + (parts > 1 ? 1 : 0);
 }
 
 }  // namespace pgd

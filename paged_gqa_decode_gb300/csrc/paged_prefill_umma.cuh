@@ -103,7 +103,7 @@ struct UmmaPrefillCfg {
   static_assert(kSCol + kTiles * kSBufs * kPage <= kTmemCols, "TMEM columns");
   static_assert(RK == RV, "the K and V rings are streamed by one helper");
   static_assert(kSBufs <= RV, "a V slot is freed when S of the page kSBufs later is issued");
-  static_assert(kSmemBytes + 8 * 1024 <= 227 * 1024, "shared memory");
+  static_assert(kSmemBytes + 20 * 1024 <= 227 * 1024, "shared memory (dynamic + static)");
 };
 
 // Slack of the lazy running max, in log2 units: P values stay below 2^8.
@@ -148,8 +148,13 @@ __device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t count, bool 
 struct PrefillItem {
   int valid;  // 0: no more items
   int t_begin, t_end, kvh, runs;
+  // key part `part` of `parts`: each run's pages are cut into `parts`
+  // consecutive ranges and this unit takes range `part` (parts 1: all),
+  // pages run_pg[r] .. run_last[r] of run r (written for key-part kernels)
+  int part, parts;
   int run_end[257];
   int tok_row[256], tok_pos[256], run_bad[256];
+  int run_pg[256], run_last[256];
 };
 
 // Page sequence of one item: run by run (inactive and bad runs skipped),
@@ -158,38 +163,66 @@ struct ItemCursor {
   int r, pg, last, row, rs, re;
 };
 
+// The item's key part of a run's pages first..last (in place): range `part`
+// of `parts` near-equal consecutive ranges; false when it is empty.
+__device__ __forceinline__ bool part_pages(const PrefillItem& it, int& first, int& last) {
+  const int64_t n = last - first + 1;
+  const int lo = first + (int)(n * it.part / it.parts);
+  const int hi = first + (int)(n * (it.part + 1) / it.parts) - 1;
+  first = lo;
+  last = hi;
+  return lo <= hi;
+}
+
+// kParts: the item is one key part of its pages (kernels built for key
+// parts: each run's range as the producer wrote it in the descriptor);
+// otherwise every page of every run.
+template <bool kParts = false>
 __device__ __forceinline__ bool item_next_run(const PrefillItem& it, int window, ItemCursor& c) {
   for (++c.r; c.r < it.runs; ++c.r) {
     c.rs = c.r == 0 ? 0 : it.run_end[c.r - 1];
     c.re = it.run_end[c.r];
     c.row = it.tok_row[c.rs];
     if (c.row < 0 || it.run_bad[c.r]) continue;
-    const int lo = window > 0 ? max(it.tok_pos[c.rs] - window + 1, 0) : 0;
-    c.pg = lo / kPage;
-    c.last = it.tok_pos[c.re - 1] / kPage;
+    if constexpr (kParts) {
+      c.pg = it.run_pg[c.r];
+      c.last = it.run_last[c.r];
+      if (c.pg > c.last) continue;  // no page of this run in the part
+    } else {
+      const int lo = window > 0 ? max(it.tok_pos[c.rs] - window + 1, 0) : 0;
+      c.pg = lo / kPage;
+      c.last = it.tok_pos[c.re - 1] / kPage;
+    }
     return true;
   }
   return false;
 }
 
 // Next page of the item; false at its end.
+template <bool kParts = false>
 __device__ __forceinline__ bool item_advance(const PrefillItem& it, int window, ItemCursor& c) {
   if (++c.pg <= c.last) return true;
-  return item_next_run(it, window, c);
+  return item_next_run<kParts>(it, window, c);
 }
 
-template <int D, int RK, int RV>
+// kParts: built for key parts (`parts` units per item, partials to
+// part_acc / part_ml for the combine launch); otherwise parts is 1 and each
+// item's outputs are written directly.  Two builds, so that the direct one
+// carries none of the key-part code.
+template <int D, int RK, int RV, bool kParts>
 __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
     paged_prefill_umma_kernel(const __grid_constant__ CUtensorMap k_map,
                               const __grid_constant__ CUtensorMap v_map,
                               const __grid_constant__ CUtensorMap q_map, const DecodeParams p,
-                              int* item_counter, const int* block_order) {
+                              int* item_counter, const int* block_order, int parts,
+                              float* part_acc, float* part_ml) {
   using C = UmmaPrefillCfg<D, RK, RV>;
   const int G = p.group;
   const int T = C::kRows / G;  // tokens per tile
   const int tokens = C::kTiles * T;
   const int n_blocks = (p.rows + tokens - 1) / tokens;
   const int n_items = n_blocks * p.hkv;
+  const int n_units = kParts ? n_items * parts : n_items;  // work units: (item, key part)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -293,13 +326,13 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
     int n_pages = 0;
     {
       ItemCursor cc{-1, 0, -1, -1, 0, 0};
-      for (bool more = item_next_run(it, p.window, cc); more;
-           more = item_next_run(it, p.window, cc))
+      for (bool more = item_next_run<kParts>(it, p.window, cc); more;
+           more = item_next_run<kParts>(it, p.window, cc))
         n_pages += cc.last - cc.pg + 1;
     }
     const int i_end = i + n_pages;
     ItemCursor fc{-1, 0, -1, -1, 0, 0};
-    bool f_more = item_next_run(it, p.window, fc);
+    bool f_more = item_next_run<kParts>(it, p.window, fc);
     int i_fetch = i, ip = i;
     for (; i < i_end; ++i) {
       while (f_more && i_fetch < i + 16) {
@@ -312,7 +345,7 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
         __syncwarp();
         i_fetch += n;
         fc.pg += n - 1;
-        f_more = item_advance(it, p.window, fc);
+        f_more = item_advance<kParts>(it, p.window, fc);
       }
       if (prefetch && lane == 0) {
         for (; ip < min(i + kL2PrefetchPages, i_fetch); ++ip) {
@@ -352,15 +385,18 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
       j = __shfl_sync(0xffffffffu, j, 0);
       // the descriptor slot holds item seq - 2 until both consumers are done
       if (seq >= 2 && !__all_sync(0xffffffffu, wait(&item_free[d], ((seq >> 1) - 1) & 1))) break;
-      if (j >= n_items) {
+      if (j >= n_units) {
         if (lane == 0) {
           it.valid = 0;
           mbar_arrive(&item_ready[d]);
         }
         break;
       }
-      const int blk = block_order ? block_order[j / p.hkv] : n_blocks - 1 - j / p.hkv;
-      const int kvh = j % p.hkv;
+      // a unit's key parts are taken one after another, so an item's parts
+      // run side by side on different SMs
+      const int item = kParts ? j / parts : j;
+      const int blk = block_order ? block_order[item / p.hkv] : n_blocks - 1 - item / p.hkv;
+      const int kvh = item % p.hkv;
       const int t_begin = blk * tokens, t_end = min(t_begin + tokens, p.rows);
       const int h0 = kvh * G;
       // tokens of the item: rows and positions; bad ones are reported and
@@ -400,6 +436,8 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
         it.t_begin = t_begin;
         it.t_end = t_end;
         it.kvh = kvh;
+        it.part = kParts ? j % parts : 0;
+        it.parts = kParts ? parts : 1;
       }
       __syncwarp();
       // a table entry outside the pool marks its run bad (zero outputs,
@@ -420,6 +458,17 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
         if (lane == 0) {
           it.run_bad[r] = bad;
           if (bad) record_error(p.err, PGD_EDEVICE_BOUNDS);
+        }
+      }
+      if constexpr (kParts) {
+        // each run's pages in this unit's key part, for every role's walk
+        for (int r = lane; r < it.runs; r += 32) {
+          const int rs = r == 0 ? 0 : it.run_end[r - 1], re = it.run_end[r];
+          const int lo = p.window > 0 ? max(it.tok_pos[rs] - p.window + 1, 0) : 0;
+          int first = lo / kPage, last = max(it.tok_pos[re - 1], 0) / kPage;
+          part_pages(it, first, last);
+          it.run_pg[r] = first;
+          it.run_last[r] = last;
         }
       }
       __syncwarp();
@@ -487,8 +536,8 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
           q_pending = false;
         }
         ItemCursor cur{-1, 0, -1, -1, 0, 0};
-        for (bool more = item_next_run(it, p.window, cur); more && ok;
-             more = item_advance(it, p.window, cur), ++i) {
+        for (bool more = item_next_run<kParts>(it, p.window, cur); more && ok;
+             more = item_advance<kParts>(it, p.window, cur), ++i) {
           if (!wait(&k_full[i % RK], (i / RK) & 1)) {
             ok = false;
             break;
@@ -545,8 +594,8 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
         if (!it.valid) break;
         ItemCursor cur{-1, 0, -1, -1, 0, 0};
         bool first = true;  // O restarts with each item
-        for (bool more = item_next_run(it, p.window, cur); more && ok;
-             more = item_advance(it, p.window, cur), ++i) {
+        for (bool more = item_next_run<kParts>(it, p.window, cur); more && ok;
+             more = item_advance<kParts>(it, p.window, cur), ++i) {
           if (!wait(&v_full[i % RV], (i / RV) & 1)) {
             ok = false;
             break;
@@ -628,7 +677,23 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
       for (int r = 0; r < it.runs && ok; ++r) {
         const int re = it.run_end[r];
         const int row = it.tok_row[rs];
+        // with key parts, a row's partial of this part: (m, l) and its O
+        // columns, at [token][head][part] (from the descriptor in shared
+        // memory where it is written, so that no part of it is held in
+        // registers through the page loop)
+        auto unit_of = [&]() {
+          return ((size_t)(it.t_begin + tl) * p.hq + it.kvh * G + g) * it.parts + it.part;
+        };
         if (row < 0 || it.run_bad[r]) {
+          // no pass covers these tokens (their outputs are zeroed): the
+          // combine leaves them as they are
+          if constexpr (kParts) {
+            if (h == 0 && row_ok && tl >= rs && tl < re) {
+              const size_t u = unit_of();
+              part_ml[2 * u] = -INFINITY;
+              part_ml[2 * u + 1] = -1.f;
+            }
+          }
           rs = re;
           continue;
         }
@@ -637,7 +702,22 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
         const int lo = p.window > 0 ? pos - p.window + 1 : 0;
         const int lo_run = p.window > 0 ? max(it.tok_pos[rs] - p.window + 1, 0) : 0;
         const int pos_last = it.tok_pos[re - 1];
-        const int first = lo_run / kPage, last = pos_last / kPage;
+        int first = lo_run / kPage, last = pos_last / kPage;
+        if constexpr (kParts) {
+          // a key part without pages of this run: the rows' partials are
+          // empty (the same for every thread of the tile)
+          first = it.run_pg[r];
+          last = it.run_last[r];
+          if (first > last) {
+            if (h == 0 && live) {
+              const size_t u = unit_of();
+              part_ml[2 * u] = -INFINITY;
+              part_ml[2 * u + 1] = 0.f;
+            }
+            rs = re;
+            continue;
+          }
+        }
         float m_run = -INFINITY;  // running (lazy) max of the row, log2 units
         float l = 0.f;            // row sum relative to m_run
         for (int pg = first; pg <= last; ++pg, ++i) {
@@ -798,6 +878,32 @@ __global__ void __launch_bounds__(UmmaPrefillCfg<D, RK, RV>::kThreads, 1)
           ++xn;
         }
         const int hh = h0 + g;
+        if constexpr (kParts) {
+          // the row's partial over this part's keys, unnormalised (the sink
+          // and the other parts are merged by the combine launch)
+          const size_t u = unit_of();
+          if (h == 0 && live) {
+            part_ml[2 * u] = m_run;
+            part_ml[2 * u + 1] = l;
+          }
+          float* arow = part_acc + u * D;
+#pragma unroll
+          for (int j = 0; j < D / 32; ++j) {  // this half's O columns
+            const int q16 = h * (D / 32) + j;
+            float ov[16];
+            tmem_ld16(lane_base + C::kOCol + t * D + 16 * q16, ov);
+            tmem_wait_ld();
+            if (live) {
+              float4* dst = reinterpret_cast<float4*>(arow + 16 * q16);
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                dst[k] = make_float4(ov[4 * k], ov[4 * k + 1], ov[4 * k + 2], ov[4 * k + 3]);
+            }
+          }
+          tc_fence_before_sync();
+          rs = re;
+          continue;
+        }
         float inv = 0.f;
         if (live) {
           const float sk = p.sinks ? p.sinks[hh] * kLog2e : -INFINITY;
@@ -979,23 +1085,113 @@ __global__ void __launch_bounds__(1024) prefill_write_kernel(const DecodeParams 
   }
 }
 
+// Merge of the key parts of the tcgen05 prefill (a call split into `parts`
+// units per item): for token t and query head h, with the partials (m_s, l_s,
+// O_s) of parts s (m in log2 units, O unnormalised) and the sink logit
+// sigma (log2 units here, or none),
+//   M = max(max_s m_s, sigma),  L = sum_s l_s 2^(m_s - M) + 2^(sigma - M),
+//   out = sum_s O_s 2^(m_s - M) / L,
+// the split softmax of the attention step over all of the token's keys, the
+// sink in the denominator only (GPT-OSS 20B model files, src/attention.linnet,
+// SinkAttention).  A part without keys (m = -inf) adds nothing; a token whose
+// partial carries l < 0 was covered by no pass, and its output, already
+// zeroed, is left.  One warp per (token, query head), 32 lanes over D.
+template <int D>
+__global__ void __launch_bounds__(128) prefill_part_combine_kernel(const DecodeParams p,
+                                                                   int parts,
+                                                                   const float* part_acc,
+                                                                   const float* part_ml) {
+  constexpr int kDims = D / 32;
+  const int t = blockIdx.y;
+  const int h = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  // the sinks are an input of the attention kernel as well, which reads them
+  // after its own dependency wait; this grid starts once every CTA of it
+  // has passed that wait, so they are final here
+  const float sk = (p.sinks && h < p.hq) ? p.sinks[h] * kLog2e : -INFINITY;
+  pdl_wait();
+  pdl_allow_dependents();
+  if (h >= p.hq) return;
+  const size_t u0 = ((size_t)t * p.hq + h) * parts;
+  float mx = sk;
+  bool covered = true;
+  for (int s = 0; s < parts; ++s) {
+    const float ms = part_ml[2 * (u0 + s)], ls = part_ml[2 * (u0 + s) + 1];
+    covered = covered && ls >= 0.f;
+    mx = fmaxf(mx, ms);
+  }
+  if (!covered) return;
+  uint16_t* o = p.out + ((size_t)t * p.hq + h) * D + lane * kDims;
+  float acc[kDims];
+#pragma unroll
+  for (int j = 0; j < kDims; ++j) acc[j] = 0.f;
+  float total = 0.f;
+  if (mx != -INFINITY) {
+    if (sk != -INFINITY) total = exp2_approx(sk - mx);
+    for (int s = 0; s < parts; ++s) {
+      const float ms = part_ml[2 * (u0 + s)];
+      if (ms == -INFINITY) continue;
+      const float w = exp2_approx(ms - mx);
+      total = fmaf(part_ml[2 * (u0 + s) + 1], w, total);
+      const float* a = part_acc + (u0 + s) * D + lane * kDims;
+#pragma unroll
+      for (int j = 0; j < kDims; j += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(a + j);
+        acc[j] = fmaf(v.x, w, acc[j]);
+        acc[j + 1] = fmaf(v.y, w, acc[j + 1]);
+        acc[j + 2] = fmaf(v.z, w, acc[j + 2]);
+        acc[j + 3] = fmaf(v.w, w, acc[j + 3]);
+      }
+    }
+  }
+  const float inv = total > 0.f ? 1.f / total : 0.f;
+  uint32_t w2[kDims / 2];
+#pragma unroll
+  for (int j = 0; j < kDims / 2; ++j) w2[j] = pack_bf16x2(acc[2 * j] * inv, acc[2 * j + 1] * inv);
+  if constexpr (kDims == 4) {
+    *reinterpret_cast<uint2*>(o) = make_uint2(w2[0], w2[1]);
+  } else {
+    *reinterpret_cast<uint4*>(o) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+  }
+}
+
+// Where the key parts' partials live in the caller's workspace: after the
+// work counter and the block order in p.ws_acc, the O partials
+// [token][head][part][D]; the (m, l) pairs [token][head][part][2] in p.ws_ml.
+// The workspace holds p.max_splits partials a token and head, so up to
+// p.max_splits - 1 parts fit beside the counter and the order.
+inline float* prefill_part_acc(const DecodeParams& p, int n_blocks) {
+  return p.ws_acc + ((4 + n_blocks + 3) / 4) * 4;
+}
+
 // `prepared`: the step's write launch has already zeroed the work counter and
-// written the block order (prefill_write_kernel).
-template <int D, int RK, int RV>
-cudaError_t launch_prefill_umma(const DecodeParams& p, const CUtensorMap& k_map,
-                                const CUtensorMap& v_map, const CUtensorMap& q_map, int sm_count,
-                                bool prepared, cudaStream_t stream) {
+// written the block order (prefill_write_kernel).  `parts` > 1: each item's
+// pages are cut into that many key parts, one work unit each, and a combine
+// launch merges their partials.
+template <int D, int RK, int RV, bool kParts>
+cudaError_t configure_prefill_umma() {
   using C = UmmaPrefillCfg<D, RK, RV>;
   static std::atomic<bool> configured[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(paged_prefill_umma_kernel<D, RK, RV>,
+    e = cudaFuncSetAttribute(paged_prefill_umma_kernel<D, RK, RV, kParts>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev].store(true, std::memory_order_release);
   }
+  return cudaSuccess;
+}
+
+template <int D, int RK, int RV>
+cudaError_t launch_prefill_umma(const DecodeParams& p, const CUtensorMap& k_map,
+                                const CUtensorMap& v_map, const CUtensorMap& q_map, int sm_count,
+                                bool prepared, int parts, cudaStream_t stream) {
+  using C = UmmaPrefillCfg<D, RK, RV>;
+  cudaError_t e = parts > 1 ? configure_prefill_umma<D, RK, RV, true>()
+                            : configure_prefill_umma<D, RK, RV, false>();
+  if (e != cudaSuccess) return e;
   if (p.rows == 0) return cudaSuccess;
   const int tokens = C::kTiles * (C::kRows / p.group);
   const int items = ((p.rows + tokens - 1) / tokens) * p.hkv;
@@ -1013,10 +1209,24 @@ cudaError_t launch_prefill_umma(const DecodeParams& p, const CUtensorMap& k_map,
   else
     e = cudaMemsetAsync(counter, 0, sizeof(int), stream);
   if (e != cudaSuccess) return e;
-  const int ctas = items < sm_count ? items : sm_count;
-  return launch_pdl(paged_prefill_umma_kernel<D, RK, RV>, dim3(ctas), dim3(C::kThreads),
-                    C::kSmemBytes, stream, k_map, v_map, q_map, p, counter,
-                    static_cast<const int*>(order));
+  // the combine grid has a row of CTAs per token
+  if (parts < 1 || (parts > 1 && (parts > p.max_splits - 1 || p.rows > 65535)))
+    return cudaErrorInvalidValue;
+  float* part_acc = parts > 1 ? prefill_part_acc(p, n_blocks) : nullptr;
+  float* part_ml = parts > 1 ? p.ws_ml : nullptr;
+  const int units = items * parts;
+  const int ctas = units < sm_count ? units : sm_count;
+  if (parts == 1)
+    return launch_pdl(paged_prefill_umma_kernel<D, RK, RV, false>, dim3(ctas), dim3(C::kThreads),
+                      C::kSmemBytes, stream, k_map, v_map, q_map, p, counter,
+                      static_cast<const int*>(order), 1, part_acc, part_ml);
+  e = launch_pdl(paged_prefill_umma_kernel<D, RK, RV, true>, dim3(ctas), dim3(C::kThreads),
+                 C::kSmemBytes, stream, k_map, v_map, q_map, p, counter,
+                 static_cast<const int*>(order), parts, part_acc, part_ml);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(prefill_part_combine_kernel<D>, dim3((p.hq + 3) / 4, p.rows), dim3(128), 0,
+                    stream, p, parts, static_cast<const float*>(part_acc),
+                    static_cast<const float*>(part_ml));
 }
 
 }  // namespace pgd

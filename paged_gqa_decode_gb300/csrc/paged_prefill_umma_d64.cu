@@ -6,8 +6,8 @@ namespace pgd {
 
 cudaError_t launch_prefill_umma_d64(const DecodeParams& p, const CUtensorMap& k_map,
                                     const CUtensorMap& v_map, const CUtensorMap& q_map,
-                                    int sm_count, bool prepared, cudaStream_t stream) {
-  return launch_prefill_umma<64, 8, 8>(p, k_map, v_map, q_map, sm_count, prepared, stream);
+                                    int sm_count, bool prepared, int parts, cudaStream_t stream) {
+  return launch_prefill_umma<64, 8, 8>(p, k_map, v_map, q_map, sm_count, prepared, parts, stream);
 }
 
 }  // namespace pgd

@@ -75,6 +75,30 @@ struct Plan {
   int max_splits;
 };
 
+// Key parts of the one-SM tcgen05 prefill (AUTO only) for a call of these
+// dims: with at most half as many work items (blocks of 2 x 128 / group
+// tokens, times the kv heads) as SMs, each item's pages are cut into parts,
+// each a work unit of its own, so that the units fill the SMs.  At most 8,
+// and at least 8 pages a part on the longest item the table allows (a
+// window bounds it): parts of a few pages cost more in partials and the
+// combine than they gain.  1: no parts.
+constexpr int kMaxKeyParts = 8;
+constexpr int kMinPartPages = 8;
+int prefill_key_parts(const pgd_dims* d, int sm_count, int32_t window) {
+  const int64_t block = 2 * (128 / (d->num_q_heads / d->num_kv_heads));
+  const int64_t items = (d->rows + block - 1) / block * d->num_kv_heads;
+  if (sm_count <= 0 || items <= 0 || items * 2 > sm_count) return 1;
+  int64_t pages = d->max_pages_per_row;
+  if (window > 0) {
+    const int64_t span = ((int64_t)window + block - 2) / kPageSize + 2;  // window + block - 1 keys
+    if (span < pages) pages = span;
+  }
+  int64_t parts = sm_count / items;
+  if (parts > kMaxKeyParts) parts = kMaxKeyParts;
+  if (parts > pages / kMinPartPages) parts = pages / kMinPartPages;
+  return parts >= 2 ? (int)parts : 1;
+}
+
 // Pages per split: enough CTAs for several waves of 2 CTAs per SM when rows
 // are about half full, but at least 24 pages (sweeps over 1..64 on GB300
 // found every workload fastest at 24 or more: a split's fixed costs --
@@ -94,6 +118,10 @@ Plan make_plan(const pgd_dims* d, const pgd_decode_options* opts, int sm_count) 
   if (pps > d->max_pages_per_row) pps = d->max_pages_per_row;
   pl.pages_per_split = pps;
   pl.max_splits = (d->max_pages_per_row + pps - 1) / pps;
+  // the same workspace serves a prefill call of these dims: its key parts'
+  // partials take one split's room each, beside the work counter
+  const int parts = prefill_key_parts(d, sm_count, 0);  // the most any window allows
+  if (parts > 1 && parts + 1 > pl.max_splits) pl.max_splits = parts + 1;
   return pl;
 }
 
@@ -103,11 +131,13 @@ size_t workspace_bytes(const pgd_dims* d, const Plan& pl) {
 
 // The kernel a call runs: opts->kernel, or for AUTO the per-token split
 // kernel, except that prefill with tokens in runs goes to a tcgen05 kernel:
-// at head_dim 128 the paired one when its work items are no more than the
-// SMs (`sm_count`; 0 = unknown), since it puts two SMs on each item, else
-// the one-SM kernel.
+// the one-SM kernel, with key parts (`key_parts` > 1) when its work items
+// are at most half the SMs (`sm_count`; 0 = unknown) and long enough to
+// cut, else for such calls at head_dim 128 the paired one, which puts two
+// SMs on each item.  `window` bounds the items' length.
 int resolve_kernel(const pgd_dims* dims, int32_t table_rows, bool prefill,
-                   const pgd_decode_options* opts, int* kernel, int sm_count = 0) {
+                   const pgd_decode_options* opts, int* kernel, int sm_count = 0,
+                   int* key_parts = nullptr, int32_t window = 0) {
   int k = opts ? opts->kernel : PGD_KERNEL_AUTO;
   if (k < PGD_KERNEL_AUTO || k > PGD_KERNEL_PREFILL_PAIR) return PGD_EINVAL;
   if ((k == PGD_KERNEL_PREFILL_TILED || k == PGD_KERNEL_PREFILL_UMMA ||
@@ -118,14 +148,23 @@ int resolve_kernel(const pgd_dims* dims, int32_t table_rows, bool prefill,
   // Prefill: the tcgen05 kernel shares each page load among the tokens of a
   // block, which pays when they come in runs (prompt chunks); tokens that are
   // mostly one per table row (decode steps) go to the per-token split kernel.
+  // Calls with at most half as many work items as SMs: key parts on one SM
+  // per unit when the items are long enough to cut, else at head_dim 128 a
+  // pair of SMs per item (measured on GB300: key parts 41-99 us against
+  // 43-109 us for pairs on one Mistral-shaped chunk of 256-512 tokens; with
+  // 128 items, pairs 102 us against 96-98 us for one SM per item).
+  int parts = 1;
   if (prefill && k == PGD_KERNEL_AUTO && dims->rows >= 8ll * table_rows) {
     k = PGD_KERNEL_PREFILL_UMMA;
     const int group = dims->num_q_heads / dims->num_kv_heads;
     const int64_t block = 2 * (128 / group);  // tokens per work item
     const int64_t items = (dims->rows + block - 1) / block * dims->num_kv_heads;
-    if (dims->head_dim == 128 && sm_count > 0 && items <= sm_count) k = PGD_KERNEL_PREFILL_PAIR;
+    parts = prefill_key_parts(dims, sm_count, window);
+    if (parts == 1 && dims->head_dim == 128 && sm_count > 0 && items * 2 <= sm_count)
+      k = PGD_KERNEL_PREFILL_PAIR;
   }
   *kernel = k;
+  if (key_parts) *key_parts = parts;
   return PGD_OK;
 }
 
@@ -406,14 +445,16 @@ int pgd_attention_kernel_count(const pgd_dims* dims, int32_t table_rows, int32_t
   if ((rc = resolve_kernel(dims, table_rows, table_rows > 0, opts, &kernel)) != PGD_OK) return rc;
   DeviceInfo* dev = nullptr;
   if ((rc = current_device(&dev)) != PGD_OK) return rc;
-  if ((rc = resolve_kernel(dims, table_rows, table_rows > 0, opts, &kernel, dev->sm_count)) !=
-      PGD_OK)
+  int parts = 1;
+  if ((rc = resolve_kernel(dims, table_rows, table_rows > 0, opts, &kernel, dev->sm_count,
+                           &parts, window)) != PGD_OK)
     return rc;
   const Plan pl = make_plan(dims, opts, dev->sm_count);
   if (dims->rows == 0) {
     *count = 0;
   } else if (kernel == PGD_KERNEL_PREFILL_UMMA || kernel == PGD_KERNEL_PREFILL_PAIR) {
-    *count = prefill_umma_launches(dims->rows, dims->num_q_heads / dims->num_kv_heads, window);
+    *count = prefill_umma_launches(dims->rows, dims->num_q_heads / dims->num_kv_heads, window,
+                                   parts);
   } else if (kernel == PGD_KERNEL_PREFILL_TILED) {
     *count = 1;
   } else if (kernel == PGD_KERNEL_AUTO && window > 0 && window <= kMaxWindowKernel) {
@@ -454,9 +495,9 @@ static int decode_impl(const pgd_dims* dims, int32_t table_rows, const int32_t* 
   if (workspace_size < need) return PGD_EWORKSPACE;
   if (!workspace || !aligned16(workspace)) return PGD_EINVAL;
 
-  int kernel = 0;
-  if ((rc = resolve_kernel(dims, table_rows, row_of != nullptr, opts, &kernel, dev->sm_count)) !=
-      PGD_OK)
+  int kernel = 0, parts = 1;
+  if ((rc = resolve_kernel(dims, table_rows, row_of != nullptr, opts, &kernel, dev->sm_count,
+                           &parts, window)) != PGD_OK)
     return rc;
   const int padded = padded_group(dims->num_q_heads / dims->num_kv_heads);
   // the tcgen05 prefills copy a head_dim-128 K page tile with one 3-D box;
@@ -523,7 +564,7 @@ static int decode_impl(const pgd_dims* dims, int32_t table_rows, const int32_t* 
                : PGD_ECUDA;
   if (kernel == PGD_KERNEL_PREFILL_UMMA)
     return launch_prefill_umma(p, k_map, v_map, q_map, dims->head_dim, dev->sm_count,
-                               prefill_write, st) == cudaSuccess
+                               prefill_write, parts, st) == cudaSuccess
                ? PGD_OK
                : PGD_ECUDA;
   if (kernel == PGD_KERNEL_PREFILL_TILED)
@@ -596,12 +637,18 @@ int pgd_prefill_step_kernel_count(const pgd_dims* dims, int32_t table_rows, int3
     *count = 0;
     return PGD_OK;
   }
-  int kernel = 0;
-  if ((rc = resolve_kernel(dims, table_rows, true, opts, &kernel)) != PGD_OK) return rc;
+  DeviceInfo* dev = nullptr;
+  if ((rc = current_device(&dev)) != PGD_OK) return rc;
+  int kernel = 0, parts = 1;
+  if ((rc = resolve_kernel(dims, table_rows, true, opts, &kernel, dev->sm_count, &parts,
+                           window)) != PGD_OK)
+    return rc;
   // the write launch, then the attention kernels (the tcgen05 kernel alone:
-  // the write launch prepared its counter and order)
-  *count = 1 + (kernel == PGD_KERNEL_PREFILL_UMMA || kernel == PGD_KERNEL_PREFILL_PAIR ? 1
-                                                                                      : attention);
+  // the write launch prepared its counter and order; then the combine when
+  // there are key parts)
+  *count = 1 + (kernel == PGD_KERNEL_PREFILL_UMMA || kernel == PGD_KERNEL_PREFILL_PAIR
+                    ? 1 + (parts > 1 ? 1 : 0)
+                    : attention);
   return PGD_OK;
 }
 

@@ -127,9 +127,12 @@ int prefill_block_tokens(int padded);
 // (128 / group), 128-byte swizzle: the kernel copies each item's Q with it.
 // `prepared`: launch_prefill_write (with umma) has already prepared the
 // work counter and block order in p.ws_acc, so only the kernel is launched.
+// `parts` > 1: each item's pages are cut into that many key parts (work
+// units of their own) whose partials (at most p.max_splits - 1 a token and
+// head fit the workspace) a combine launch then merges.
 cudaError_t launch_prefill_umma(const DecodeParams& p, const CUtensorMap& k_map,
                                 const CUtensorMap& v_map, const CUtensorMap& q_map, int head_dim,
-                                int sm_count, bool prepared, cudaStream_t stream);
+                                int sm_count, bool prepared, int parts, cudaStream_t stream);
 // Prefill at head_dim 128 on pairs of SMs (clusters of two CTAs sharing
 // cta_group::2 tcgen05 products); the same work items, counter, block order
 // and `prepared` convention as launch_prefill_umma.  k_map: the K pool in
@@ -138,8 +141,8 @@ cudaError_t launch_prefill_pair(const DecodeParams& p, const CUtensorMap& k_map,
                                 const CUtensorMap& v_map, const CUtensorMap& q_map, int sm_count,
                                 bool prepared, cudaStream_t stream);
 // Kernels that launch issues for `rows` tokens (the block-order pass and the
-// kernel, or the kernel alone).
-int prefill_umma_launches(int rows, int group, int window);
+// kernel, or the kernel alone; then the combine when there are key parts).
+int prefill_umma_launches(int rows, int group, int window, int parts);
 // The prefill step's write launch: each token's p.k_new / p.v_new at its slot
 // in p.k_pool / p.v_pool (table row p.row_of[t], position p.positions[t]);
 // with `umma`, its first CTA also prepares the tcgen05 kernel's work counter

@@ -222,13 +222,16 @@ def test_pair_kernel_count_and_head_dim_64_refused():
         pgd.attention_kernel_count(d64, 8, kernel=PAIR)
 
 
-@pytest.mark.parametrize("rows,kernel", [(1, PAIR), (8, pgd.KERNEL_PREFILL_UMMA)])
-def test_auto_takes_the_pair_kernel_when_items_fit_the_sms(rows, kernel):
-    """AUTO runs the paired kernel when blocks x kv heads are at most the SM
-    count (one 512-token Mistral-shaped chunk: 64 items), the one-SM kernel
-    otherwise (eight chunks: 512 items): its outputs equal that kernel's."""
+@pytest.mark.parametrize("rows,prefix,kernel", [(1, 0, PAIR), (2, None, pgd.KERNEL_PREFILL_UMMA),
+                                                (8, None, pgd.KERNEL_PREFILL_UMMA)])
+def test_auto_takes_the_pair_kernel_for_few_short_items(rows, prefix, kernel):
+    """AUTO runs the paired kernel when blocks x kv heads are at most half
+    the SM count and too short to cut into key parts (one 512-token
+    Mistral-shaped chunk from position 0: 64 items of at most 8 pages), the
+    one-SM kernel when they are more (two chunks: 128 items; eight: 512):
+    its outputs equal that kernel's."""
     wl = PREFILL_WORKLOADS["mistral_prefill"].replace(rows=rows)
-    b = make_prefill_batch(wl, 2200 + rows, DEV)
+    b = make_prefill_batch(wl, 2200 + rows, DEV, prefix=None if prefix is None else [prefix] * rows)
     kw = dict(num_kv_heads=wl.kv_heads)
     args = (b.q, b.k_pool, b.v_pool, b.table, b.rows, b.positions, b.sinks, 0, wl.scale)
     auto = pgd.paged_prefill_attention(*args, **kw)
