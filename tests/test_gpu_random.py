@@ -110,3 +110,28 @@ def test_random_prefill_pair(seed):
     prefill_check(b, window=window, layout=layout, kernel=pgd.KERNEL_PREFILL_PAIR,
                   what=f"seed {seed}: {hq}/{hkv} w{window} layout{layout} prefix {prefix} "
                        f"chunks {chunks}")
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_prefill_key_parts(seed):
+    """AUTO's key parts (few work items, tables of 16 pages or more) on seeded
+    random groups, prefixes, chunks, windows, sinks and layouts."""
+    rng = np.random.default_rng(9800 + seed)
+    hq, hkv = heads(rng)
+    d = int(rng.choice([64, 128]))
+    rows = int(rng.integers(1, 4))
+    prefix = [int(rng.integers(0, 3000)) for _ in range(rows)]
+    prefix[0] = int(rng.integers(1100, 3000))  # a table of 16 pages or more
+    chunks = [int(rng.choice([int(rng.integers(8, 70)), int(rng.integers(60, 300))]))
+              for _ in range(rows)]
+    window = int(rng.choice([0, 0, int(rng.integers(600, 2500))]))
+    wl = PrefillWorkload("random_parts", rows=rows, q_heads=hq, kv_heads=hkv, head_dim=d,
+                         prefix_lo=0, prefix_hi=3000, chunk=0, window=window,
+                         sinks=bool(rng.integers(0, 2)))
+    b = make_prefill_batch(wl, 9850 + seed, DEV, prefix=prefix, chunks=chunks)
+    b.v_pool.mul_(0.25)
+    b.v_new = b.v_new * 0.25
+    layout = int(rng.choice([pgd.PAGE_MAJOR, pgd.HEAD_MAJOR]))
+    prefill_check(b, window=window, layout=layout, fused=bool(rng.integers(0, 2)),
+                  what=f"seed {seed}: {hq}/{hkv} d{d} w{window} layout{layout} prefix {prefix} "
+                       f"chunks {chunks}")
