@@ -1101,7 +1101,8 @@ __global__ void __launch_bounds__(128) prefill_part_combine_kernel(const DecodeP
                                                                    int parts,
                                                                    const float* part_acc,
                                                                    const float* part_ml) {
-  constexpr int kDims = D / 32;
+  constexpr int kDims = D / 32;  // dims of a lane: 2 or 4
+  static_assert(kDims == 2 || kDims == 4, "head_dim");
   const int t = blockIdx.y;
   const int h = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -1135,12 +1136,10 @@ __global__ void __launch_bounds__(128) prefill_part_combine_kernel(const DecodeP
       total = fmaf(part_ml[2 * (u0 + s) + 1], w, total);
       const float* a = part_acc + (u0 + s) * D + lane * kDims;
 #pragma unroll
-      for (int j = 0; j < kDims; j += 4) {
-        const float4 v = *reinterpret_cast<const float4*>(a + j);
+      for (int j = 0; j < kDims; j += 2) {
+        const float2 v = *reinterpret_cast<const float2*>(a + j);
         acc[j] = fmaf(v.x, w, acc[j]);
         acc[j + 1] = fmaf(v.y, w, acc[j + 1]);
-        acc[j + 2] = fmaf(v.z, w, acc[j + 2]);
-        acc[j + 3] = fmaf(v.w, w, acc[j + 3]);
       }
     }
   }
@@ -1149,9 +1148,9 @@ __global__ void __launch_bounds__(128) prefill_part_combine_kernel(const DecodeP
 #pragma unroll
   for (int j = 0; j < kDims / 2; ++j) w2[j] = pack_bf16x2(acc[2 * j] * inv, acc[2 * j + 1] * inv);
   if constexpr (kDims == 4) {
-    *reinterpret_cast<uint2*>(o) = make_uint2(w2[0], w2[1]);
+    *reinterpret_cast<uint2*>(o) = make_uint2(w2[0], w2[1]);  // 4 values
   } else {
-    *reinterpret_cast<uint4*>(o) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+    *reinterpret_cast<uint32_t*>(o) = w2[0];  // 2 values
   }
 }
 

@@ -222,3 +222,24 @@ def test_short_windows_and_short_tables_take_no_parts():
     short = pgd.make_dims(rows=256, num_q_heads=wl.q_heads, num_kv_heads=wl.kv_heads,
                           head_dim=wl.head_dim, num_pages=2000, max_pages_per_row=15)
     assert pgd.attention_kernel_count(short, 1) == 2  # block order, kernel
+
+
+@pytest.mark.parametrize("d,hq,hkv", [(128, 32, 8), (64, 64, 8), (64, 14, 2)])
+def test_parts_write_only_their_outputs(d, hq, hkv):
+    """The combine writes each token's rows and nothing past them: the call's
+    output is the first P rows of a larger buffer whose last row holds a
+    sentinel, which stays; every output close to the kernel without parts."""
+    wl = PrefillWorkload("parts_guard", rows=2, q_heads=hq, kv_heads=hkv, head_dim=d,
+                         prefix_lo=0, prefix_hi=2500, chunk=0, window=0, sinks=True)
+    b = make_prefill_batch(wl, 87 + d + hq, DEV, prefix=[2400, 1100], chunks=[77, 50])
+    assert_parts(b, 0)
+    tokens = len(b.rows_np)
+    buf = torch.full((tokens + 1, hq, d), 7.0, dtype=torch.bfloat16, device=DEV)
+    out = buf[:tokens]
+    kw = dict(num_kv_heads=hkv)
+    args = (b.q, b.k_pool, b.v_pool, b.table, b.rows, b.positions, b.sinks, 0, wl.scale)
+    pgd.paged_prefill_attention(*args, out=out, **kw)
+    want = pgd.paged_prefill_attention(*args, kernel=pgd.KERNEL_PREFILL_UMMA, **kw)
+    assert pgd.get_device_error() == pgd.OK
+    assert torch.all(buf[tokens] == 7.0), "a write past the call's outputs"
+    compare(out, want.float().cpu().numpy().astype(np.float64), f"parts guard d{d} {hq}/{hkv}")
