@@ -1188,6 +1188,10 @@ cudaError_t launch_prefill_umma(const DecodeParams& p, const CUtensorMap& k_map,
                                 const CUtensorMap& v_map, const CUtensorMap& q_map, int sm_count,
                                 bool prepared, int parts, cudaStream_t stream) {
   using C = UmmaPrefillCfg<D, RK, RV>;
+  // the partials' room in the workspace; the combine grid has a row of CTAs
+  // per token
+  if (parts < 1 || (parts > 1 && (parts > p.max_splits - 1 || p.rows > 65535)))
+    return cudaErrorInvalidValue;
   cudaError_t e = parts > 1 ? configure_prefill_umma<D, RK, RV, true>()
                             : configure_prefill_umma<D, RK, RV, false>();
   if (e != cudaSuccess) return e;
@@ -1208,9 +1212,6 @@ cudaError_t launch_prefill_umma(const DecodeParams& p, const CUtensorMap& k_map,
   else
     e = cudaMemsetAsync(counter, 0, sizeof(int), stream);
   if (e != cudaSuccess) return e;
-  // the combine grid has a row of CTAs per token
-  if (parts < 1 || (parts > 1 && (parts > p.max_splits - 1 || p.rows > 65535)))
-    return cudaErrorInvalidValue;
   float* part_acc = parts > 1 ? prefill_part_acc(p, n_blocks) : nullptr;
   float* part_ml = parts > 1 ? p.ws_ml : nullptr;
   const int units = items * parts;
