@@ -16,7 +16,8 @@
 // takes B split along N between the two CTAs; if each CTA holds one whole
 // page, one S product covers two pages (N 128) without any rearrangement of
 // the page tiles, and each SM copies every other page.  Each work item then
-// has two SMs, which is what pays when a call has fewer items than SMs.
+// has two SMs, which is what pays when a call has at most half as many
+// items as SMs and they are too short for the one-SM kernel's key parts.
 //
 // Work items are the one-SM kernel's: (block of 2 x 128 / G consecutive
 // packed tokens, kv head), two query tiles of 128 rows (token, head).  A pair

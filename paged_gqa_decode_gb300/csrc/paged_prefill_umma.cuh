@@ -59,6 +59,11 @@
 // works on this one; P per chunk of 32 keys: the bf16 head in the chunk's
 // first 16 columns, the residual in the next 16, as packed pairs).  At
 // head_dim 128 that is all 512 columns.
+// Key parts (a separate build, for calls with few items): each item's runs
+// are cut into `parts` consecutive page ranges, one work unit each; a unit
+// ends each run by writing the row's partial -- lazy maximum, row sum and
+// the O row, unnormalised, fp32 -- to the workspace, and a combine launch
+// merges the parts with the sink (the split softmax, as the decode combine).
 // Every wait is bounded; a timeout records PGD_EDEVICE_TIMEOUT, stops all
 // roles, drains in-flight copies and MMAs and frees TMEM before the CTA exits.
 #pragma once
