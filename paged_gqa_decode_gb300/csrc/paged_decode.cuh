@@ -891,7 +891,9 @@ struct WindowCfg {
   static constexpr int kSmemBytes = UNITS * kUnitSmem;
   static constexpr int kMinBlocks = UNITS == 1 ? (228 * 1024) / (kUnitSmem + 1024) : 1;
   static constexpr int kHeads = MmaConsumer<D>::kHeads;
-  static constexpr int kPerThread = kHeads * D / kUnitThreads;  // output dims per thread
+  // output dims per thread (at least 4: with many warps, threads past
+  // kHeads * D / 4 have no output run and only copy and compute)
+  static constexpr int kPerThread = kHeads * D / kUnitThreads >= 4 ? kHeads * D / kUnitThreads : 4;
   static constexpr int kRun = kPerThread >= 8 ? 8 : 4;          // dims per store
   static_assert(kPerThread % kRun == 0 && D % kPerThread == 0, "output runs");
   static_assert(kWarps * kHeads * (D + 2) * 4 <= kBytes, "merge buffer");
@@ -1160,10 +1162,29 @@ constexpr int kShortStages3 = 3;
 template <int D>
 cudaError_t launch_decode_for_dim(const DecodeParams& p, const CUtensorMap& k_map,
                                   const CUtensorMap& v_map, int padded, int kernel,
-                                  int grid_splits, int pages_per_cta, cudaStream_t stream) {
+                                  int grid_splits, int pages_per_cta, bool short_rows,
+                                  cudaStream_t stream) {
   constexpr int kStages = D == 128 ? 3 : 6;
   if (kernel == PGD_KERNEL_AUTO && p.window > 0 && p.window <= kMaxWindowKernel)
     return p.window <= kPage ? launch_window<D, 1>(p, stream) : launch_window<D, 2>(p, stream);
+  if (short_rows && p.window == 0) {
+    // Full attention over a table of a few pages: the window kernel with the
+    // whole table as its window (every row's positions 0 .. n are then in
+    // it: n < 64 x the table width, which the kernel checks).
+    DecodeParams q = p;
+    switch (short_row_tiles(D, p.maxp)) {
+      case 1: q.window = kPage; return launch_window<D, 1>(q, stream);
+      case 2: q.window = 2 * kPage; return launch_window<D, 2>(q, stream);
+      case 4: q.window = 4 * kPage; return launch_window<D, 4>(q, stream);
+      case 10:
+        if constexpr (D == 64) {
+          q.window = 10 * kPage;
+          return launch_window<D, 10>(q, stream);
+        }
+        break;
+      default: break;
+    }
+  }
   if (kernel != PGD_KERNEL_CUDA_CORE) {
     // A ring no deeper than the pages a split can stream: shallower rings let
     // more CTAs share an SM when splits are short (windows, small contexts).

@@ -5,9 +5,9 @@ namespace pgd {
 
 cudaError_t launch_decode_d64(const DecodeParams& p, const CUtensorMap& k_map,
                               const CUtensorMap& v_map, int padded, int kernel, int grid_splits,
-                              int pages_per_cta, cudaStream_t stream) {
+                              int pages_per_cta, bool short_rows, cudaStream_t stream) {
   return launch_decode_for_dim<64>(p, k_map, v_map, padded, kernel, grid_splits, pages_per_cta,
-                                    stream);
+                                    short_rows, stream);
 }
 
 // Self-test of failure handling.  Thread 0 waits on an mbarrier phase that

@@ -168,6 +168,23 @@ int resolve_kernel(const pgd_dims* dims, int32_t table_rows, bool prefill,
   return PGD_OK;
 }
 
+// AUTO decode with full attention over a table of a few pages runs the
+// window kernel, the whole table its window (every row's rows copied at
+// once, one warp per 32 positions, no splits), when the split size is the
+// library's choice and the batch has between half as many and as many
+// (row, kv head) units as SMs: one round of units, each on an SM of its own.
+// Outside that range the split kernel measured faster (GB300, per step
+// between L2 flushes: Qwen2.5 shapes, 64 rows (128 units) 12.4 against 13.0
+// us with the window kernel, 4 rows (8 units) 10.8 against 10.3 us; 64
+// dense gpt-oss rows of 640 positions (512 units) 35.3 against 24.3 us).
+bool short_row_kernel(const pgd_dims* d, int32_t window, const pgd_decode_options* opts,
+                      int kernel, int sm_count) {
+  const int64_t units = (int64_t)d->rows * d->num_kv_heads;
+  return kernel == PGD_KERNEL_AUTO && window <= 0 && !(opts && opts->pages_per_split > 0) &&
+         sm_count > 0 && units * 2 >= sm_count && units <= sm_count &&
+         short_row_tiles(d->head_dim, d->max_pages_per_row) > 0;
+}
+
 // Pages the split grid must cover per row: the table width, or with a
 // window at most ceil((window - 1) / 64) + 1 pages.
 int span_pages(const pgd_dims* dims, int32_t window) {
@@ -457,7 +474,8 @@ int pgd_attention_kernel_count(const pgd_dims* dims, int32_t table_rows, int32_t
                                    parts);
   } else if (kernel == PGD_KERNEL_PREFILL_TILED) {
     *count = 1;
-  } else if (kernel == PGD_KERNEL_AUTO && window > 0 && window <= kMaxWindowKernel) {
+  } else if ((kernel == PGD_KERNEL_AUTO && window > 0 && window <= kMaxWindowKernel) ||
+             short_row_kernel(dims, window, opts, kernel, dev->sm_count)) {
     *count = 1;  // the window kernel
   } else {
     const int pages = span_pages(dims, window > 0 ? window : 0);
@@ -543,6 +561,7 @@ static int decode_impl(const pgd_dims* dims, int32_t table_rows, const int32_t* 
   const int grid_pages = span_pages(dims, p.window);
   const int grid_splits = (grid_pages + pl.pages_per_split - 1) / pl.pages_per_split;
   const int pages_per_cta = grid_pages < pl.pages_per_split ? grid_pages : pl.pages_per_split;
+  const bool short_rows = short_row_kernel(dims, window, opts, kernel, dev->sm_count);
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // prefill step: the tokens' K and V are written by a launch of their own
@@ -573,8 +592,10 @@ static int decode_impl(const pgd_dims* dims, int32_t table_rows, const int32_t* 
                : PGD_ECUDA;
   cudaError_t e =
       dims->head_dim == 64
-          ? launch_decode_d64(p, k_map, v_map, padded, kernel, grid_splits, pages_per_cta, st)
-          : launch_decode_d128(p, k_map, v_map, padded, kernel, grid_splits, pages_per_cta, st);
+          ? launch_decode_d64(p, k_map, v_map, padded, kernel, grid_splits, pages_per_cta,
+                              short_rows, st)
+          : launch_decode_d128(p, k_map, v_map, padded, kernel, grid_splits, pages_per_cta,
+                               short_rows, st);
   return e == cudaSuccess ? PGD_OK : PGD_ECUDA;
 }
 

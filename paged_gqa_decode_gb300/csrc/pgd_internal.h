@@ -72,6 +72,18 @@ struct DecodeParams {
 // to the window kernel (a unit of warps per row and kv head, no splits).
 constexpr int kMaxWindowKernel = 128;
 
+// Tiles of the window kernel for full attention over a table of max_pages
+// pages, its window the whole table: 64 positions a tile, TILES in {1, 2, 4}
+// (and 10 at head_dim 64), so that a unit's rows fit its shared memory.
+// 0: the table is too wide.
+inline int short_row_tiles(int head_dim, int max_pages) {
+  if (max_pages <= 1) return 1;
+  if (max_pages <= 2) return 2;
+  if (max_pages <= 4) return 4;
+  if (head_dim == 64 && max_pages <= 10) return 10;
+  return 0;
+}
+
 // Padded query-group sizes that have a decode kernel instantiation.
 int padded_group(int group);  // 0 if unsupported
 
@@ -104,15 +116,16 @@ cudaError_t launch_page_slots(const SlotParams& p, cudaStream_t stream);
 cudaError_t launch_bounded_wait_selftest(unsigned int* err, int* outcome, cudaStream_t stream);
 
 // Decode kernels for one head_dim: the window kernel (AUTO, windows of at
-// most kMaxWindowKernel positions) or the split kernel + combine kernel;
-// `padded` is the padded group size, `kernel` a PGD_KERNEL_* choice.
+// most kMaxWindowKernel positions; with `short_rows`, full attention over a
+// table of short_row_tiles pages or fewer) or the split kernel + combine
+// kernel; `padded` is the padded group size, `kernel` a PGD_KERNEL_* choice.
 // `pages_per_cta` bounds the pages one split streams (it picks the ring depth).
 cudaError_t launch_decode_d64(const DecodeParams& p, const CUtensorMap& k_map,
                               const CUtensorMap& v_map, int padded, int kernel, int grid_splits,
-                              int pages_per_cta, cudaStream_t stream);
+                              int pages_per_cta, bool short_rows, cudaStream_t stream);
 cudaError_t launch_decode_d128(const DecodeParams& p, const CUtensorMap& k_map,
                                const CUtensorMap& v_map, int padded, int kernel, int grid_splits,
-                               int pages_per_cta, cudaStream_t stream);
+                               int pages_per_cta, bool short_rows, cudaStream_t stream);
 
 // Tiled prefill (tokens of a block share each page load); no key splits.
 cudaError_t launch_prefill_tiled(const DecodeParams& p, const CUtensorMap& k_map,
