@@ -104,8 +104,13 @@ enum {
   PGD_KERNEL_AUTO = 0,          /* decode: windows of 1..128 positions go to the
                                    window kernel (the warps given each row and
                                    kv head copy exactly the window's K/V rows;
-                                   mma.sync products; no splits), anything else to
-                                   TENSOR_CORE; prefill: when the tokens average
+                                   mma.sync products; no splits), and so does
+                                   full attention over a table of at most 10
+                                   pages (head_dim 64) or 4 (128) when the
+                                   rows x kv heads are between half and all of
+                                   the device's SMs and opts->pages_per_split
+                                   is 0 (the whole table its window); anything
+                                   else to TENSOR_CORE; prefill: when the tokens average
                                    at least 8 per table row (prompt chunks),
                                    PREFILL_UMMA, whose blocks x kv heads, when
                                    at most half the device's SMs, are cut into
@@ -229,7 +234,8 @@ PGD_API size_t pgd_paged_decode_workspace_bytes(const pgd_dims* dims, const pgd_
  *               pgd_paged_prefill_attention (> 0) for a prefill call.
  *   window, opts  as passed to that call.
  *   count       out: 0 when dims->rows == 0; 1 for AUTO with a window of
- *               1..128 positions (the window kernel); for PREFILL_UMMA and
+ *               1..128 positions or on a table the window kernel takes
+ *               whole (see PGD_KERNEL_AUTO); for PREFILL_UMMA and
  *               PREFILL_PAIR 2 without a
  *               window when the tokens form at most 4096 blocks of
  *               2 x (128 / group) (a pass that orders the blocks longest
