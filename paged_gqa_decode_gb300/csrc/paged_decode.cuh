@@ -855,9 +855,7 @@ __device__ __forceinline__ void cp_async_wait_all() {
 
 // Sliding-window decode for windows of at most 64 * TILES positions
 // (GPT-OSS 20B model files, src/attention.linnet, SinkAttention.decode_rows:
-// key s is seen when n - window < s <= n); also full attention over a table
-// of at most TILES pages, launched with the whole table (64 * TILES) as its
-// window, which then holds every row's positions 0 .. n.  A unit of 2 * TILES warps per
+// key s is seen when n - window < s <= n).  A unit of 2 * TILES warps per
 // (row, kv head) attends over exactly the window's positions, wherever they
 // fall in the row's pages, so no byte outside the window is read and no split
 // or combine is needed.  A CTA holds UNITS units, each on its own shared
